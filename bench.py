@@ -1,0 +1,497 @@
+"""Decode benchmark of the River-LLM KV-shared exit river on GB300.
+
+One bench step = one decode step of the whole hot path (embedding, every
+layer on the backbone or the exit river with its KV append and attention,
+layer-end similarity / exit decision, LM head, argmax) for one batch.
+
+Default workload: Llama-3.2-1B shape (random init N(0, 0.02), seed 0), batch 1,
+prompt of 512 uniform-random ids (seed 1), a 256-step generation under the
+seeded forced exit schedule (mean exit layer 3.8 of 16, 5% full-depth steps,
+seed 2); the timed steps cycle through that generation (positions 512..767).
+Also timed: the same library with no exit (tau = 1.01) and with tau = 0.5.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl river|reference]
+                  [--config 1b-b1|tiny|1b-b32|8b-b1|8b-b64] [--no-cpu-baseline]
+
+Under torchrun (N > 1) every rank runs an independent replica (the batch-min
+rule couples the sequences of a batch, so a batch does not shard; see the
+design notes): value = all ranks' tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s at Llama-1B/8B shapes; achieved HBM GB/s vs GB300 peak"
+
+CONFIGS = {
+    # name: (shape, batch, prompt, generation steps, forced-schedule mean, taus, kv fill)
+    "tiny": ("tiny", 1, 32, 16, 2.0, (0.5, 1.01), "prefill"),
+    "1b-b1": ("llama-3.2-1b", 1, 512, 256, 3.8, (0.5,), "prefill"),
+    "1b-b32": ("llama-3.2-1b", 32, 1024, 512, 3.8, (0.3, 0.5, 0.7), "prefill"),
+    "8b-b1": ("llama-3.1-8b", 1, 2048, 512, 8.0, (0.5,), "prefill"),
+    "8b-b64": ("llama-3.1-8b", 64, 4096, 256, 8.0, (0.3, 0.5, 0.7), "random"),
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], "measured"
+    return 6800.0, "fallback"
+
+
+def workload_desc(name, shape, B, T, G, mean):
+    return (f"{shape.name} shape, random init N(0,0.02) seed 0, batch {B}, prompt {T} uniform ids "
+            f"(seed 1), {G}-step generation under a forced exit schedule (geometric, target mean "
+            f"exit layer {mean} of {shape.n_layers}, 5% full-depth steps, seed 2)")
+
+
+# ------------------------------------------------------------------- algorithmic bytes
+
+def layer_bytes(S, w4):
+    d, hq, hkv, hd, f = S.d_model, S.n_q_heads, S.n_kv_heads, S.head_dim, S.ffn_dim
+    shapes = [(hq * hd, d), (hkv * hd, d), (hkv * hd, d), (d, hq * hd), (f, d), (f, d), (d, f)]
+    tot = 0.0
+    for n, k in shapes:
+        tot += n * k / 2 + n * ((k + 127) // 128) * 4 if w4 else n * k * 2
+    return tot
+
+
+def step_bytes(S, B, e, pos):
+    """Weights of layers <= e in bf16, layers > e in W4 (+ fp16 scale/zero),
+    the LM head, K/V rows 0..pos of every layer (read) and slot pos (write)."""
+    w = e * layer_bytes(S, False) + (S.n_layers - e) * layer_bytes(S, True)
+    w += S.vocab * S.d_model * 2
+    kv = S.n_layers * B * S.n_kv_heads * S.head_dim * 2 * 2 * (pos + 1 + 1)
+    return w + kv
+
+
+# ---------------------------------------------------------------------- clocks
+
+class Clocks:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_id):
+        self.proc = None
+        self.out = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.out), exist_ok=True)
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", dev_id, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.out):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) >= 8:
+                try:
+                    rows.append((float(p[0]), float(p[1]), p[4], p[5], p[6], p[7]))
+                except ValueError:
+                    pass
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), r[2:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------- the library arm
+
+def run_river(args, rank, world, dev):
+    import torch
+    import synth
+    import early_exit_decoding_gb300 as river
+
+    shape_name, B, T, G, mean, taus, kvfill = CONFIGS[args.config]
+    S = synth.SHAPES[shape_name]
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream()
+    t0 = time.time()
+    w = synth.gen_weights(S, seed=0, device="cuda", gains="ones")
+    with torch.cuda.stream(stream):
+        model = river.Model(S, w, stream)
+        model.quantize_exit_layers(stream)
+    stream.synchronize()
+    del w
+    torch.cuda.empty_cache()
+    max_seq = T + G + 1
+    kv = model.kv_cache_alloc(B, max_seq)
+    sched_np = synth.gen_schedule(S.n_layers, G, mean, seed=2)
+    sched = torch.from_numpy(sched_np).cuda()
+    prompt = torch.from_numpy(synth.gen_tokens(S.vocab, (B, T), seed=1)).cuda()
+    dec_tokens = torch.from_numpy(synth.gen_tokens(S.vocab, (G, B), seed=4)).cuda()
+    out = {"logits": torch.empty((B, S.vocab), dtype=torch.float32, device="cuda"),
+           "next_token": torch.empty((B,), dtype=torch.int32, device="cuda"),
+           "exit_layer": torch.empty((1,), dtype=torch.int32, device="cuda"),
+           "min_cos": torch.empty((S.n_layers,), dtype=torch.float32, device="cuda")}
+    with torch.cuda.stream(stream):
+        if kvfill == "prefill":
+            river.prefill(model, kv, prompt, river.Policy.tau_(1.01), out=out, stream=stream)
+        else:  # timing-only fill of the cache at the target context
+            for l in range(S.n_layers):
+                k, v = kv.view(l)
+                k[:B, :, :T].normal_()
+                v[:B, :, :T].normal_()
+            kv.set_position(T, 0, stream)
+        kv.sync(stream)
+    log(f"[rank {rank}] setup {time.time() - t0:.1f}s ({S.name}, B={B}, prompt {T})")
+
+    tok_slices = [dec_tokens[i].contiguous() for i in range(G)]
+    state = {"i": 0}
+
+    def one_step(policy):
+        i = state["i"]
+        if i % G == 0 and i > 0:
+            kv.set_position(T, 0, stream)
+        river.decode_step(model, kv, tok_slices[i % G], policy, out=out, stream=stream)
+        state["i"] = i + 1
+
+    def timed(policy, K, W, flush_clocks=None):
+        state["i"] = 0
+        kv.set_position(T, 0, stream)
+        with torch.cuda.stream(stream):
+            for _ in range(W):
+                one_step(policy)
+            kv.sync(stream)
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            clocks = Clocks(args.smi_id) if flush_clocks else None
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            resets = 0
+            e0.record(stream)
+            for _ in range(K):
+                if state["i"] % G == 0 and state["i"] > 0:
+                    resets += 1
+                one_step(policy)
+            e1.record(stream)
+            e1.synchronize()
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            ck = clocks.stop() if clocks else None
+            kv.sync(stream)
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms, ck, resets
+
+    forced = river.Policy.forced(sched)
+    K, W = args.steps, args.warmup
+    ms_forced, clocks, resets = timed(forced, K, W, flush_clocks=True)
+    res = {"ms_forced": ms_forced, "clocks": clocks, "resets": resets}
+    res["ms_full"], _, _ = timed(river.Policy.tau_(1.01), K, W)
+    res["tau"] = {}
+    for tau in taus:
+        ms_t, _, _ = timed(river.Policy.tau_(tau), min(K, 4 * G), W)
+        # exit layers of one pass through the generation
+        state["i"] = 0
+        kv.set_position(T, 0, stream)
+        exits = []
+        with torch.cuda.stream(stream):
+            for _ in range(min(G, 64)):
+                one_step(river.Policy.tau_(tau))
+                exits.append(int(out["exit_layer"].item()))
+        res["tau"][tau] = (ms_t / min(K, 4 * G), sum(exits) / len(exits))
+
+    # live per-kernel timing inside the graph (separate pass)
+    prof_rows = []
+    river.rl_kv_set_profiling(kv.handle, True)
+    state["i"] = 0
+    kv.set_position(T, 0, stream)
+    with torch.cuda.stream(stream):
+        for i in range(min(G, 64) + 2):
+            one_step(forced)
+            rows = river.rl_kv_profile(kv.handle, stream)
+            if i >= 2:
+                prof_rows.extend(rows)
+    river.rl_kv_set_profiling(kv.handle, False)
+
+    # end to end: host buffers through rl_decode_step_host, copies inside the timed region
+    import numpy as np
+    ht = torch.zeros((B,), dtype=torch.int32).pin_memory()
+    hn = torch.zeros((B,), dtype=torch.int32).pin_memory()
+    he = torch.zeros((1,), dtype=torch.int32).pin_memory()
+    host_tokens = dec_tokens.cpu().numpy()
+    Ke = min(K, G)
+    state["i"] = 0
+    kv.set_position(T, 0, stream)
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            ht.copy_(torch.from_numpy(host_tokens[i % G]))
+            river.rl_decode_step_host(model.handle, kv.handle, ht, B, forced.c(), None, hn, he, None,
+                                      stream)
+        kv.set_position(T, 0, stream)
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        t1 = time.perf_counter()
+        for i in range(Ke):
+            ht.numpy()[:] = host_tokens[i % G]
+            river.rl_decode_step_host(model.handle, kv.handle, ht, B, forced.c(), None, hn, he,
+                                      None, stream)
+        e2e_s = time.perf_counter() - t1
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    res["e2e"] = (Ke, e2e_s)
+    res["prof"] = prof_rows
+    res["kernels_per_step"] = model.kernel_count(B)
+    res["shape"], res["B"], res["T"], res["G"], res["mean"] = S, B, T, G, mean
+    res["sched_mean"] = float(sched_np.mean())
+    res["sched"] = sched_np
+    return res
+
+
+def gemv_traffic_note():
+    """Per-launch DRAM traffic of the GEMV kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "gemv_dram_traffic.txt")
+    src = os.path.join(ROOT, "early_exit_decoding_gb300", "csrc", "gemv.cu")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if kv.get("gemv_source_sha256_16") != h:
+        return None
+    try:
+        return float(kv["traffic_bytes_per_avg_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------- the oracle (CPU)
+
+def oracle_setup(args, need_exit=True):
+    import numpy as np
+    import torch
+    import synth
+    from oracle.model import OracleModel, Policy as OPolicy, KVState
+
+    shape_name, B, T, G, mean, taus, kvfill = CONFIGS[args.config]
+    S = synth.SHAPES[shape_name]
+    t0 = time.time()
+    dev = "cuda" if (S.name != "tiny" and torch.cuda.is_available()) else "cpu"
+    w = synth.gen_weights(S, seed=0, device=dev, gains="ones")
+    wn = synth.weights_to_numpy(w)
+    del w
+    om = OracleModel(S, wn)
+    if need_exit:
+        om.quantize_exit_layers()
+    st = KVState(S, B, T + G + 1)
+    prompt = synth.gen_tokens(S.vocab, (B, T), seed=1)
+    if kvfill == "prefill":
+        om.prefill(prompt, st, OPolicy.tau_(1.01))
+    else:
+        rng = np.random.default_rng(3)
+        for l in range(S.n_layers):
+            st.K[l][:, :, :T] = rng.standard_normal(st.K[l][:, :, :T].shape, dtype=np.float32)
+            st.V[l][:, :, :T] = rng.standard_normal(st.V[l][:, :, :T].shape, dtype=np.float32)
+        st.pos = T
+    sched = synth.gen_schedule(S.n_layers, G, mean, seed=2)
+    dec = synth.gen_tokens(S.vocab, (G, B), seed=4)
+    log(f"oracle setup {time.time() - t0:.1f}s")
+    return om, st, sched, dec, OPolicy, (S, B, T, G)
+
+
+def run_oracle_steps(om, st, sched, dec, OPolicy, dims, n, budget_s):
+    S, B, T, G = dims
+    done, t = 0, 0.0
+    for i in range(n):
+        if st.pos >= T + G:
+            st.pos = T
+        t1 = time.perf_counter()
+        om.decode_step(dec[i % G], st, OPolicy.forced(int(sched[i % G])))
+        t += time.perf_counter() - t1
+        done += 1
+        if t > budget_s:
+            break
+    return done, t
+
+
+def threads_used():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
+def cpu_baseline(args):
+    om, st, sched, dec, OPolicy, dims = oracle_setup(args)
+    S, B, T, G = dims
+    n, t = run_oracle_steps(om, st, sched, dec, OPolicy, dims, 64, 15.0)
+    return {"value": n * B / t, "unit": "tokens/s", "cores": threads_used(), "kind": "oracle",
+            "sample": f"{n} decode steps of the same workload (after the full {T}-token prefill, "
+                      f"untimed), NumPy fp32 oracle on the host CPU"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="river", choices=("river", "reference"))
+    ap.add_argument("--config", default="1b-b1", choices=sorted(CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    shape_name, B, T, G, mean, taus, kvfill = CONFIGS[args.config]
+    import synth
+    S = synth.SHAPES[shape_name]
+    hbm_peak, peak_src = load_peaks()
+
+    if args.impl == "reference":
+        # The reference arm is the oracle, timed as it stands on the host cores.
+        if rank != 0:
+            return
+        om, st, sched, dec, OPolicy, dims = oracle_setup(args)
+        run_oracle_steps(om, st, sched, dec, OPolicy, dims, args.warmup, 60.0)
+        n, t = run_oracle_steps(om, st, sched, dec, OPolicy, dims, args.steps, 120.0)
+        v = n * B / t
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+                "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * t / n,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic",
+                "config": {"workload": workload_desc(args.config, S, B, T, G, mean), "batch": B,
+                           "prompt": T, "decode_steps": G},
+                "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads_used(),
+                                 "kind": "oracle",
+                                 "sample": f"{n} decode steps (bounded to ~120 s) of the workload"},
+                "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = local
+    props = torch.cuda.get_device_properties(dev)
+    args.smi_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else str(dev)
+    res = run_river(args, rank, world, dev)
+    K = args.steps
+    ms_step = res["ms_forced"] / K
+    tok_s = world * B * K / (res["ms_forced"] / 1e3)
+    full_ms_step = res["ms_full"] / K
+
+    # algorithmic bytes of the timed steps: the schedule's exit layers, positions T..T+G-1
+    sched = res["sched"]
+    tot_bytes = 0.0
+    for i in range(K):
+        tot_bytes += step_bytes(S, B, int(sched[i % G]), T + (i % G))
+    gbs = tot_bytes / (res["ms_forced"] / 1e3) / 1e9
+    full_bytes = sum(step_bytes(S, B, S.n_layers, T + (i % G)) for i in range(K))
+    full_gbs = full_bytes / (res["ms_full"] / 1e3) / 1e9
+
+    # roofline of the dominant kernel (the dual-path GEMV), from the live profile
+    prof = res["prof"]
+    gemv = [r for r in prof if r[0] in ("qkv", "o_proj", "gate_up", "down", "lm_head")]
+    g_ms = sum(r[3] for r in gemv)
+    g_bytes = sum(r[4] for r in gemv)
+    all_ms = sum(r[3] for r in prof)
+    per_launch_bytes = g_bytes / max(1, len(gemv))
+    per_launch_ms = g_ms / max(1, len(gemv))
+    achieved = per_launch_bytes / (per_launch_ms / 1e3) / 1e9 if gemv else 0.0
+    traffic = gemv_traffic_note()
+    shares = {}
+    for r in prof:
+        shares[r[0]] = shares.get(r[0], 0.0) + r[3]
+    shares = {k: round(v / all_ms, 4) for k, v in sorted(shares.items(), key=lambda kv: -kv[1])}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            cpu = cpu_baseline(args)
+        except Exception as ex:  # the baseline is reported, never required
+            cpu = {"value": None, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": f"failed: {ex!r}"}
+
+    Ke, e2e_s = res["e2e"]
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (random-init weights, uniform token ids)",
+        "config": {"workload": workload_desc(args.config, S, B, T, G, mean), "batch": B,
+                   "prompt": T, "decode_steps": G, "policy": "forced exit schedule",
+                   "schedule_mean_exit_layer": res["sched_mean"],
+                   "l2": "inputs larger than L2: every step streams >= 1.4 GB of weights (L2 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "hbm": {"algorithmic_bytes_per_step": tot_bytes / K, "achieved_gbs": gbs,
+                "peak_gbs": hbm_peak, "frac": gbs / hbm_peak, "peak_source": peak_src},
+        "roofline": {"kernel": "k_gemv (dual-path bf16 / W4 GEMV, all projections + LM head)",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic,
+                     "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
+                     "launches_profiled": len(gemv), "peak_source": f"{peak_src} (copy test)",
+                     "time_share_in_step": round(g_ms / all_ms, 4) if all_ms else None},
+        "kernel_time_shares": shares,
+        "variants": {
+            "no_exit": {"tokens_per_s": world * B / (full_ms_step / 1e3), "ms_per_step": full_ms_step,
+                        "hbm_frac": full_gbs / hbm_peak},
+            "forced_over_no_exit": full_ms_step / ms_step,
+            **{f"tau_{t}": {"tokens_per_s": world * B / (v[0] / 1e3), "ms_per_step": v[0],
+                            "mean_exit_layer": v[1]} for t, v in res["tau"].items()},
+        },
+        "e2e": {"value": world * B * Ke / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
+                "d2h_bytes_per_step": 4 * B + 4,
+                "note": "rl_decode_step_host: pinned host tokens in, next tokens + exit layer out"},
+        "gpu_launches": K * res["kernels_per_step"] + res["resets"],
+        "clocks": res["clocks"],
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,1077 @@
+// Host runtime of libriver.so: the C ABI declared in include/river.h.
+//
+// Owns the model (weights in the kernels' layouts), the exit river, the
+// shared KV cache with its per-step device state, and the CUDA graph that
+// replays one decode step with a single launch.  Every step of the path runs
+// in the kernels of this library; the host only validates arguments and
+// enqueues launches.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using namespace river;
+
+namespace {
+
+thread_local std::string g_err;
+
+rl_status fail(rl_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+#define RL_CUDA(call)                                                                    \
+  do {                                                                                   \
+    cudaError_t e_ = (call);                                                             \
+    if (e_ != cudaSuccess) return fail(RL_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+#define RL_LAUNCHED()                                                                    \
+  do {                                                                                   \
+    cudaError_t e_ = cudaGetLastError();                                                 \
+    if (e_ != cudaSuccess) return fail(RL_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e_)); \
+  } while (0)
+
+struct Linear {
+  bf16* w = nullptr;        // [N][Kp]
+  uint32_t* qw = nullptr;   // [N][Kp/8]
+  __half2* sz = nullptr;    // [N][Kp/128]
+  int N = 0, K = 0, Kp = 0;
+  int view_base = 0;        // first rl linear index this fused matrix maps to
+  const int2* rowmap = nullptr;
+};
+
+struct Layer {
+  Linear qkv, o, gu, dn;
+  float* g_attn = nullptr;
+  float* g_ffn = nullptr;
+};
+
+}  // namespace
+
+struct rl_model {
+  rl_config cfg;
+  int L, d, Hq, Hkv, hd, F, V;
+  int Kd, Ko, Kf, Nqkv;
+  std::vector<Layer> layers;
+  bf16* embed = nullptr;
+  bf16* lm_head = nullptr;  // [V][Kd]
+  float* g_final = nullptr;
+  float* inv_freq = nullptr;
+  int2* map_qkv = nullptr;
+  int2* map_gu = nullptr;
+  int2* map_id = nullptr;
+  bool quantized = false;
+  std::vector<NSView> views;  // [L][7]
+  NSView* d_views = nullptr;
+  std::vector<void*> allocs;
+  int sm_count = 0;
+  size_t bytes = 0;
+
+  template <typename T>
+  rl_status alloc(T** p, size_t n) {
+    void* q = nullptr;
+    if (n == 0) n = 1;
+    cudaError_t e = cudaMalloc(&q, n * sizeof(T));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(RL_ERR_OOM, "cudaMalloc(%zu bytes): %s", n * sizeof(T), cudaGetErrorString(e));
+    }
+    allocs.push_back(q);
+    bytes += n * sizeof(T);
+    *p = static_cast<T*>(q);
+    return RL_OK;
+  }
+  ~rl_model() {
+    for (void* p : allocs) cudaFree(p);
+  }
+};
+
+namespace {
+
+struct GraphKey {
+  int B = -1, mode = -1;
+  float tau = 0.f;
+  const int* sched = nullptr;
+  int sched_len = 0;
+  const int* tokens = nullptr;
+  float* logits = nullptr;
+  int* next = nullptr;
+  int* exit = nullptr;
+  float* min_cos = nullptr;
+  float* trace = nullptr;
+  bool prof = false;
+  bool operator==(const GraphKey& o) const {
+    return B == o.B && mode == o.mode && tau == o.tau && sched == o.sched &&
+           sched_len == o.sched_len && tokens == o.tokens && logits == o.logits &&
+           next == o.next && exit == o.exit && min_cos == o.min_cos && trace == o.trace &&
+           prof == o.prof;
+  }
+};
+
+// One profiled launch: kind, layer, algorithmic bytes of either path.
+struct ProfRec {
+  int kind = 0, layer = 0;
+  bool gemv = false, attn = false;
+  double bytes_bf = 0, bytes_w4 = 0;
+};
+
+}  // namespace
+
+struct rl_kv {
+  rl_model* m = nullptr;
+  int maxB = 0, Tmax = 0;
+  std::vector<bf16*> K, V;
+  DevState* st = nullptr;
+  int host_pos = 0, host_step = 0;
+  // decode workspace
+  float* h[3] = {nullptr, nullptr, nullptr};
+  bf16 *x_attn = nullptr, *x_ffn = nullptr, *o = nullptr, *u = nullptr;
+  float *xs_attn = nullptr, *xs_ffn = nullptr, *xs_o = nullptr, *xs_u = nullptr;
+  float* q = nullptr;
+  float* part = nullptr;
+  int nchunks_cap = 1;
+  float* cosbuf = nullptr;
+  // buffers of the host-pointer entry point
+  int* d_tok = nullptr;
+  int* d_next = nullptr;
+  int* d_exit = nullptr;
+  float* d_logits = nullptr;
+  float* d_mincos = nullptr;
+  float* trace = nullptr;
+  // decode graph
+  cudaGraphExec_t exec = nullptr;
+  GraphKey key;
+  // live profiling
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev;
+  std::vector<ProfRec> recs;
+  int nrec = 0;
+  int* d_paths = nullptr;
+  int prof_pos = 0, prof_B = 1;
+  std::vector<void*> allocs;
+
+  template <typename T>
+  rl_status alloc(T** p, size_t n) {
+    void* q = nullptr;
+    if (n == 0) n = 1;
+    cudaError_t e = cudaMalloc(&q, n * sizeof(T));
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(RL_ERR_OOM, "cudaMalloc(%zu bytes): %s", n * sizeof(T), cudaGetErrorString(e));
+    }
+    e = cudaMemset(q, 0, n * sizeof(T));
+    if (e != cudaSuccess) return fail(RL_ERR_CUDA, "cudaMemset: %s", cudaGetErrorString(e));
+    allocs.push_back(q);
+    *p = static_cast<T*>(q);
+    return RL_OK;
+  }
+  ~rl_kv() {
+    if (exec) cudaGraphExecDestroy(exec);
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    for (void* p : allocs) cudaFree(p);
+  }
+};
+
+namespace {
+
+#define RL_TRY(expr)                  \
+  do {                                \
+    rl_status s_ = (expr);            \
+    if (s_ != RL_OK) return s_;       \
+  } while (0)
+
+cudaStream_t as_stream(rl_stream_t s) { return static_cast<cudaStream_t>(s); }
+
+// Internal row order of the fused QKV matrix: per head, 16-row tile j holds
+// dims 8j..8j+7 and hd/2+8j..hd/2+8j+7, so each RoPE pair (i, i + hd/2)
+// lands in one tile.  Source 0/1/2 = wq/wk/wv.
+std::vector<int2> qkv_rowmap(int Hq, int Hkv, int hd) {
+  std::vector<int2> m;
+  const int heads = Hq + 2 * Hkv;
+  for (int r = 0; r < heads * hd; ++r) {
+    const int head = r / hd, i = r % hd, j = i / 16, rr = i % 16;
+    const int dim = rr < 8 ? 8 * j + rr : hd / 2 + 8 * j + rr - 8;
+    if (head < Hq)
+      m.push_back(make_int2(0, head * hd + dim));
+    else if (head < Hq + Hkv)
+      m.push_back(make_int2(1, (head - Hq) * hd + dim));
+    else
+      m.push_back(make_int2(2, (head - Hq - Hkv) * hd + dim));
+  }
+  return m;
+}
+
+// Internal row order of the fused gate/up matrix: tile j = gate rows
+// 8j..8j+7 then up rows 8j..8j+7 (SwiGLU pairs in one tile).
+std::vector<int2> gu_rowmap(int F) {
+  std::vector<int2> m;
+  for (int r = 0; r < 2 * F; ++r) {
+    const int j = r / 16, rr = r % 16;
+    m.push_back(rr < 8 ? make_int2(0, 8 * j + rr) : make_int2(1, 8 * j + rr - 8));
+  }
+  return m;
+}
+
+rl_status upload_map(rl_model* m, const std::vector<int2>& h, int2** d) {
+  RL_TRY(m->alloc(d, h.size()));
+  RL_CUDA(cudaMemcpy(*d, h.data(), h.size() * sizeof(int2), cudaMemcpyHostToDevice));
+  return RL_OK;
+}
+
+rl_status validate_config(const rl_config* c) {
+  if (!c) return fail(RL_ERR_INVALID_ARG, "config is NULL");
+  if (c->n_layers < 1 || c->d_model < 16 || c->n_q_heads < 1 || c->n_kv_heads < 1 ||
+      c->ffn_dim < 8 || c->vocab < 16)
+    return fail(RL_ERR_INVALID_ARG, "non-positive or too small dimension in config");
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(RL_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", c->head_dim);
+  if (c->n_q_heads % c->n_kv_heads != 0 || c->n_q_heads / c->n_kv_heads > 8)
+    return fail(RL_ERR_UNSUPPORTED, "n_q_heads must be a multiple (<= 8x) of n_kv_heads");
+  if (c->d_model % 16 || c->ffn_dim % 8 || c->vocab % 16)
+    return fail(RL_ERR_UNSUPPORTED, "d_model and vocab must be multiples of 16, ffn_dim of 8");
+  if (c->d_model > 12288) return fail(RL_ERR_UNSUPPORTED, "d_model > 12288");
+  if (c->group_size != kGroup) return fail(RL_ERR_UNSUPPORTED, "group_size must be 128");
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f))
+    return fail(RL_ERR_INVALID_ARG, "rms_eps and rope_theta must be positive");
+  return RL_OK;
+}
+
+int decode_nchunks(const rl_model* m, int B, int Tmax) {
+  int n = (2 * m->sm_count + B * m->Hkv - 1) / (B * m->Hkv);
+  const int cap = (Tmax + 63) / 64;
+  if (n > cap) n = cap;
+  if (n > 64) n = 64;
+  if (n < 1) n = 1;
+  return n;
+}
+
+GemvArgs gemv_base(const rl_model* m, const Linear& lin, int w4_mode, const DevState* st,
+                   int layer_no) {
+  GemvArgs a;
+  memset(&a, 0, sizeof(a));
+  a.w = lin.w;
+  a.qw = lin.qw;
+  a.sz = lin.sz;
+  a.N = lin.N;
+  a.Kp = lin.Kp;
+  a.w4_mode = w4_mode;
+  a.exit_layer = st ? &st->exit_layer : nullptr;
+  a.layer_no = layer_no;
+  return a;
+}
+
+struct StepIO {
+  const int* tokens;
+  int B, T;  // T = 1 for decode
+  const rl_exit_policy* pol;
+  float* logits;
+  int* next;
+  int* exit;
+  float* min_cos;
+  bool prefill;  // rows are B sequences of T prompt tokens at positions 0..T-1
+};
+
+// Event records around launches when the cache has profiling switched on.
+struct Prof {
+  rl_kv* kv;
+  cudaStream_t s;
+  bool on;
+  int n = 0;
+  void begin() {
+    if (on && n < (int)kv->recs.size()) cudaEventRecord(kv->ev[2 * n], s);
+  }
+  int* slot() { return (on && n < (int)kv->recs.size()) ? kv->d_paths + n : nullptr; }
+  void end(int kind, int layer, double bytes_bf, double bytes_w4, bool gemv, bool attn = false) {
+    if (!on || n >= (int)kv->recs.size()) return;
+    cudaEventRecord(kv->ev[2 * n + 1], s);
+    ProfRec& r = kv->recs[n];
+    r.kind = kind;
+    r.layer = layer;
+    r.gemv = gemv;
+    r.attn = attn;
+    r.bytes_bf = bytes_bf;
+    r.bytes_w4 = bytes_w4;
+    ++n;
+  }
+};
+
+double bytes_bf16(const Linear& l) { return (double)l.N * l.K * 2.0; }
+double bytes_w4(const Linear& l) {
+  return (double)l.N * l.K / 2.0 + (double)l.N * ((l.K + kGroup - 1) / kGroup) * 4.0;
+}
+
+// Enqueue one full pass of the decode path (T == 1) or of the prefill
+// (T > 1, buffers passed in `ws`).
+struct Work {
+  float* h[3];
+  bf16 *x_attn, *x_ffn, *o, *u;
+  float *xs_attn, *xs_ffn, *xs_o, *xs_u;
+  float* q;
+  float* part;
+  int nchunks;
+  float* cosbuf;
+};
+
+rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, cudaStream_t s) {
+  const int L = m->L, d = m->d;
+  Prof pf{kv, s, kv->profiling && !io.prefill};
+  const bool prefill = io.prefill;
+  const int T = io.T;
+  const int M = prefill ? io.B * io.T : io.B;  // rows (tokens) in this pass
+  const int Gd = m->Kd / kGroup, Go = m->Ko / kGroup, Gf = m->Kf / kGroup;
+  const int w4mode = m->quantized ? W4_BY_LAYER : W4_OFF;
+  const int mode = io.pol->mode;
+  const float tau = io.pol->tau;
+
+  RowNormArgs emb;
+  memset(&emb, 0, sizeof(emb));
+  emb.tokens = io.tokens;
+  emb.embed = m->embed;
+  emb.vocab = m->V;
+  emb.h_out = w.h[0];
+  emb.rows = M;
+  emb.d = d;
+  emb.g = m->layers[0].g_attn;
+  emb.eps = m->cfg.rms_eps;
+  emb.x = w.x_attn;
+  emb.ldx = m->Kd;
+  emb.xsum = w.xs_attn;
+  emb.ldxs = Gd;
+  emb.L = L;
+  emb.mode = mode;
+  emb.tau = tau;
+  emb.st = kv->st;
+  emb.schedule = io.pol->d_schedule;
+  emb.schedule_len = io.pol->schedule_len > 0 ? io.pol->schedule_len : 1;
+  emb.use_step_index = prefill ? 0 : 1;
+  emb.trace = kv->trace;
+  emb.trace_layer = 0;
+  emb.trace_maxB = kv->maxB;
+  emb.trace_T = prefill ? T : 0;
+  pf.begin();
+  launch_rownorm(emb, s);
+  RL_LAUNCHED();
+  pf.end(RL_K_EMBED, 0, 0, 0, false);
+
+  const int colstep = prefill ? kMaxBatch : M;
+  int cur = 0;
+  for (int l = 0; l < L; ++l) {
+    const Layer& ly = m->layers[l];
+    const int mid = (cur + 1) % 3, nxt = (cur + 2) % 3;
+    // QKV + RoPE + KV append
+    for (int cb = 0; cb < M; cb += colstep) {
+      GemvArgs a = gemv_base(m, ly.qkv, w4mode, kv->st, l + 1);
+      a.x = w.x_attn + (size_t)cb * m->Kd;
+      a.ldx = m->Kd;
+      a.xsum = w.xs_attn + (size_t)cb * Gd;
+      a.ldxs = Gd;
+      a.B = std::min(colstep, M - cb);
+      a.epi = EPI_QKV_ROPE;
+      a.q_out = w.q;
+      a.kc = kv->K[l];
+      a.vc = kv->V[l];
+      a.maxB = kv->maxB;
+      a.Tmax = kv->Tmax;
+      a.Hq = m->Hq;
+      a.Hkv = m->Hkv;
+      a.hd = m->hd;
+      a.pos_ptr = &kv->st->pos;
+      a.T_prefill = prefill ? T : 0;
+      a.col_base = cb;
+      a.inv_freq = m->inv_freq;
+      a.err = &kv->st->err;
+      pf.begin();
+      a.path_out = pf.slot();
+      launch_gemv(a, m->sm_count, s);
+      RL_LAUNCHED();
+      pf.end(RL_K_QKV, l + 1, bytes_bf16(ly.qkv), bytes_w4(ly.qkv), true);
+    }
+    // attention over the shared cache
+    AttnArgs at;
+    memset(&at, 0, sizeof(at));
+    at.q = w.q;
+    at.kc = kv->K[l];
+    at.vc = kv->V[l];
+    at.maxB = kv->maxB;
+    at.Tmax = kv->Tmax;
+    at.Hq = m->Hq;
+    at.Hkv = m->Hkv;
+    at.hd = m->hd;
+    at.nq = M;
+    at.T_prefill = prefill ? T : 0;
+    at.pos_ptr = &kv->st->pos;
+    at.nchunks = w.nchunks;
+    at.part = w.part;
+    at.o = w.o;
+    at.ldo = m->Ko;
+    pf.begin();
+    launch_attention(at, s);
+    RL_LAUNCHED();
+    pf.end(RL_K_ATTN, l + 1, 0, 0, false, true);
+    pf.begin();
+    launch_group_sums(w.o, m->Ko, m->Ko, M, w.xs_o, Go, s);
+    RL_LAUNCHED();
+    pf.end(RL_K_GSUM, l + 1, 0, 0, false);
+    // O projection + residual
+    for (int cb = 0; cb < M; cb += colstep) {
+      GemvArgs a = gemv_base(m, ly.o, w4mode, kv->st, l + 1);
+      a.x = w.o + (size_t)cb * m->Ko;
+      a.ldx = m->Ko;
+      a.xsum = w.xs_o + (size_t)cb * Go;
+      a.ldxs = Go;
+      a.B = std::min(colstep, M - cb);
+      a.epi = EPI_RESID;
+      a.out = w.h[mid] + (size_t)cb * d;
+      a.ldo = d;
+      a.resid = w.h[cur] + (size_t)cb * d;
+      a.ldr = d;
+      pf.begin();
+      a.path_out = pf.slot();
+      launch_gemv(a, m->sm_count, s);
+      RL_LAUNCHED();
+      pf.end(RL_K_O, l + 1, bytes_bf16(ly.o), bytes_w4(ly.o), true);
+    }
+    // pre-FFN RMSNorm
+    RowNormArgs n2;
+    memset(&n2, 0, sizeof(n2));
+    n2.h_out = w.h[mid];
+    n2.rows = M;
+    n2.d = d;
+    n2.g = ly.g_ffn;
+    n2.eps = m->cfg.rms_eps;
+    n2.x = w.x_ffn;
+    n2.ldx = m->Kd;
+    n2.xsum = w.xs_ffn;
+    n2.ldxs = Gd;
+    n2.st = kv->st;
+    pf.begin();
+    launch_rownorm(n2, s);
+    RL_LAUNCHED();
+    pf.end(RL_K_NORM, l + 1, 0, 0, false);
+    // gate/up + SwiGLU
+    for (int cb = 0; cb < M; cb += colstep) {
+      GemvArgs a = gemv_base(m, ly.gu, w4mode, kv->st, l + 1);
+      a.x = w.x_ffn + (size_t)cb * m->Kd;
+      a.ldx = m->Kd;
+      a.xsum = w.xs_ffn + (size_t)cb * Gd;
+      a.ldxs = Gd;
+      a.B = std::min(colstep, M - cb);
+      a.epi = EPI_SWIGLU;
+      a.out_h = w.u + (size_t)cb * m->Kf;
+      a.ldoh = m->Kf;
+      pf.begin();
+      a.path_out = pf.slot();
+      launch_gemv(a, m->sm_count, s);
+      RL_LAUNCHED();
+      pf.end(RL_K_GU, l + 1, bytes_bf16(ly.gu), bytes_w4(ly.gu), true);
+    }
+    pf.begin();
+    launch_group_sums(w.u, m->Kf, m->Kf, M, w.xs_u, Gf, s);
+    RL_LAUNCHED();
+    pf.end(RL_K_GSUM, l + 1, 0, 0, false);
+    // down + residual
+    for (int cb = 0; cb < M; cb += colstep) {
+      GemvArgs a = gemv_base(m, ly.dn, w4mode, kv->st, l + 1);
+      a.x = w.u + (size_t)cb * m->Kf;
+      a.ldx = m->Kf;
+      a.xsum = w.xs_u + (size_t)cb * Gf;
+      a.ldxs = Gf;
+      a.B = std::min(colstep, M - cb);
+      a.epi = EPI_RESID;
+      a.out = w.h[nxt] + (size_t)cb * d;
+      a.ldo = d;
+      a.resid = w.h[mid] + (size_t)cb * d;
+      a.ldr = d;
+      pf.begin();
+      a.path_out = pf.slot();
+      launch_gemv(a, m->sm_count, s);
+      RL_LAUNCHED();
+      pf.end(RL_K_DOWN, l + 1, bytes_bf16(ly.dn), bytes_w4(ly.dn), true);
+    }
+    // layer end: cosine, batch-min, tau compare, next RMSNorm
+    RowNormArgs le;
+    memset(&le, 0, sizeof(le));
+    le.h_in = w.h[cur];
+    le.h_out = w.h[nxt];
+    le.rows = M;
+    le.d = d;
+    le.g = (l + 1 < L) ? m->layers[l + 1].g_attn : m->g_final;
+    le.eps = m->cfg.rms_eps;
+    le.x = w.x_attn;
+    le.ldx = m->Kd;
+    le.xsum = w.xs_attn;
+    le.ldxs = Gd;
+    le.cosbuf = w.cosbuf;
+    le.layer_no = l + 1;
+    le.L = L;
+    le.mode = mode;
+    le.tau = tau;
+    le.min_cos_out = io.min_cos;
+    le.exit_out = io.exit;
+    le.st = kv->st;
+    le.set_pos = prefill ? T : -1;
+    le.set_step = prefill ? 0 : -1;
+    le.trace = kv->trace;
+    le.trace_layer = l + 1;
+    le.trace_maxB = kv->maxB;
+    le.trace_T = prefill ? T : 0;
+    pf.begin();
+    launch_rownorm(le, s);
+    RL_LAUNCHED();
+    pf.end(RL_K_LAYER_END, l + 1, 0, 0, false);
+    cur = nxt;
+  }
+  // final RMSNorm was applied by the last layer end (gain g_final) into x_attn.
+  {
+    GemvArgs a = gemv_base(m, Linear(), W4_OFF, nullptr, 0);
+    a.w = m->lm_head;
+    a.N = m->V;
+    a.Kp = m->Kd;
+    const int last = prefill ? T - 1 : 0;
+    const int stride = prefill ? T : 1;
+    a.x = w.x_attn + (size_t)last * m->Kd;
+    a.ldx = m->Kd * stride;
+    a.B = io.B;
+    a.epi = EPI_STORE;
+    a.out = io.logits;
+    a.ldo = m->V;
+    pf.begin();
+    a.path_out = pf.slot();
+    launch_gemv(a, m->sm_count, s);
+    RL_LAUNCHED();
+    const double lm = (double)m->V * m->d * 2.0;
+    pf.end(RL_K_LM_HEAD, 0, lm, lm, true);
+  }
+  if (io.next) {
+    pf.begin();
+    launch_argmax(io.logits, m->V, m->V, io.B, io.next, s);
+    RL_LAUNCHED();
+    pf.end(RL_K_ARGMAX, 0, 0, 0, false);
+  }
+  if (pf.on) kv->nrec = pf.n;
+  return RL_OK;
+}
+
+Work decode_work(rl_kv* kv, int B) {
+  Work w;
+  for (int i = 0; i < 3; ++i) w.h[i] = kv->h[i];
+  w.x_attn = kv->x_attn;
+  w.x_ffn = kv->x_ffn;
+  w.o = kv->o;
+  w.u = kv->u;
+  w.xs_attn = kv->xs_attn;
+  w.xs_ffn = kv->xs_ffn;
+  w.xs_o = kv->xs_o;
+  w.xs_u = kv->xs_u;
+  w.q = kv->q;
+  w.part = kv->part;
+  w.nchunks = decode_nchunks(kv->m, B, kv->Tmax);
+  w.cosbuf = kv->cosbuf;
+  return w;
+}
+
+rl_status check_policy(const rl_model* m, const rl_exit_policy* p) {
+  if (!p) return fail(RL_ERR_INVALID_ARG, "policy is NULL");
+  if (p->mode == RL_EXIT_TAU) {
+    if (!(p->tau == p->tau)) return fail(RL_ERR_INVALID_ARG, "tau is NaN");
+    if (p->tau <= 1.0f && !m->quantized)
+      return fail(RL_ERR_STATE, "tau <= 1 can exit: call rl_quantize_exit_layers first");
+    return RL_OK;
+  }
+  if (p->mode == RL_EXIT_FORCED) {
+    if (!p->d_schedule || p->schedule_len < 1)
+      return fail(RL_ERR_INVALID_ARG, "forced policy needs d_schedule and schedule_len >= 1");
+    if (!m->quantized)
+      return fail(RL_ERR_STATE, "forced exits need the exit river: call rl_quantize_exit_layers");
+    return RL_OK;
+  }
+  return fail(RL_ERR_INVALID_ARG, "unknown policy mode %d", p->mode);
+}
+
+bool is_capturable(cudaStream_t s) {
+  return s != nullptr && s != cudaStreamLegacy && s != cudaStreamPerThread;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rl_version(void) { return "libriver 0.1 (sm_103a)"; }
+
+const char* rl_last_error(void) { return g_err.c_str(); }
+
+rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream_t stream,
+                          rl_model** out) {
+  if (!out) return fail(RL_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  RL_TRY(validate_config(cfg));
+  if (!wts || !wts->embed || !wts->lm_head || !wts->g_final || !wts->layers)
+    return fail(RL_ERR_INVALID_ARG, "weights: NULL pointer");
+  for (int l = 0; l < cfg->n_layers; ++l) {
+    const rl_layer_weights& lw = wts->layers[l];
+    if (!lw.wq || !lw.wk || !lw.wv || !lw.wo || !lw.wg || !lw.wu || !lw.wd || !lw.g_attn || !lw.g_ffn)
+      return fail(RL_ERR_INVALID_ARG, "weights of layer %d: NULL pointer", l);
+  }
+  cudaStream_t s = as_stream(stream);
+  rl_model* m = new rl_model();
+  m->cfg = *cfg;
+  m->L = cfg->n_layers;
+  m->d = cfg->d_model;
+  m->Hq = cfg->n_q_heads;
+  m->Hkv = cfg->n_kv_heads;
+  m->hd = cfg->head_dim;
+  m->F = cfg->ffn_dim;
+  m->V = cfg->vocab;
+  m->Kd = round_up(m->d, kGroup);
+  m->Ko = round_up(m->Hq * m->hd, kGroup);
+  m->Kf = round_up(m->F, kGroup);
+  m->Nqkv = (m->Hq + 2 * m->Hkv) * m->hd;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&m->sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (m->sm_count < 1) m->sm_count = 1;
+
+  auto bail = [&](rl_status st) {
+    delete m;
+    return st;
+  };
+#define M_TRY(expr)                     \
+  do {                                  \
+    rl_status s_ = (expr);              \
+    if (s_ != RL_OK) return bail(s_);   \
+  } while (0)
+#define M_CUDA(call)                                                                      \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess)                                                                \
+      return bail(fail(RL_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_)));            \
+  } while (0)
+
+  M_TRY(upload_map(m, qkv_rowmap(m->Hq, m->Hkv, m->hd), &m->map_qkv));
+  M_TRY(upload_map(m, gu_rowmap(m->F), &m->map_gu));
+  {
+    const int n = std::max(m->d, m->V);
+    std::vector<int2> id(n);
+    for (int i = 0; i < n; ++i) id[i] = make_int2(0, i);
+    M_TRY(upload_map(m, id, &m->map_id));
+  }
+
+  auto make_linear = [&](Linear& lin, int N, int K, int view_base, const int2* map,
+                         GatherSrcs src) -> rl_status {
+    lin.N = N;
+    lin.K = K;
+    lin.Kp = round_up(K, kGroup);
+    lin.view_base = view_base;
+    lin.rowmap = map;
+    RL_TRY(m->alloc(&lin.w, (size_t)N * lin.Kp));
+    launch_gather_rows(lin.w, lin.Kp, N, K, map, src, K, s);
+    RL_LAUNCHED();
+    return RL_OK;
+  };
+
+  m->layers.resize(m->L);
+  for (int l = 0; l < m->L; ++l) {
+    const rl_layer_weights& lw = wts->layers[l];
+    Layer& ly = m->layers[l];
+    GatherSrcs qkv = {{(const bf16*)lw.wq, (const bf16*)lw.wk, (const bf16*)lw.wv}};
+    GatherSrcs o = {{(const bf16*)lw.wo, nullptr, nullptr}};
+    GatherSrcs gu = {{(const bf16*)lw.wg, (const bf16*)lw.wu, nullptr}};
+    GatherSrcs dn = {{(const bf16*)lw.wd, nullptr, nullptr}};
+    M_TRY(make_linear(ly.qkv, m->Nqkv, m->d, RL_WQ, m->map_qkv, qkv));
+    M_TRY(make_linear(ly.o, m->d, m->Hq * m->hd, RL_WO, m->map_id, o));
+    M_TRY(make_linear(ly.gu, 2 * m->F, m->d, RL_WG, m->map_gu, gu));
+    M_TRY(make_linear(ly.dn, m->d, m->F, RL_WD, m->map_id, dn));
+    M_TRY(m->alloc(&ly.g_attn, m->d));
+    M_TRY(m->alloc(&ly.g_ffn, m->d));
+    launch_bf16_to_f32((const bf16*)lw.g_attn, ly.g_attn, m->d, s);
+    launch_bf16_to_f32((const bf16*)lw.g_ffn, ly.g_ffn, m->d, s);
+  }
+  M_TRY(m->alloc(&m->embed, (size_t)m->V * m->d));
+  M_CUDA(cudaMemcpyAsync(m->embed, wts->embed, (size_t)m->V * m->d * sizeof(bf16),
+                         cudaMemcpyDeviceToDevice, s));
+  M_TRY(m->alloc(&m->lm_head, (size_t)m->V * m->Kd));
+  launch_gather_rows(m->lm_head, m->Kd, m->V, m->d, m->map_id,
+                     GatherSrcs{{(const bf16*)wts->lm_head, nullptr, nullptr}}, m->d, s);
+  M_TRY(m->alloc(&m->g_final, m->d));
+  launch_bf16_to_f32((const bf16*)wts->g_final, m->g_final, m->d, s);
+  {
+    std::vector<float> inv(m->hd / 2);
+    for (int i = 0; i < m->hd / 2; ++i)
+      inv[i] = (float)std::pow((double)m->cfg.rope_theta, -2.0 * i / (double)m->hd);
+    M_TRY(m->alloc(&m->inv_freq, inv.size()));
+    M_CUDA(cudaMemcpyAsync(m->inv_freq, inv.data(), inv.size() * sizeof(float),
+                           cudaMemcpyHostToDevice, s));
+  }
+  M_CUDA(cudaGetLastError());
+  M_CUDA(cudaStreamSynchronize(s));
+#undef M_TRY
+#undef M_CUDA
+  *out = m;
+  return RL_OK;
+}
+
+void rl_model_destroy(rl_model* m) { delete m; }
+
+rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream) {
+  if (!m) return fail(RL_ERR_INVALID_ARG, "model is NULL");
+  if (m->quantized) return RL_OK;
+  cudaStream_t s = as_stream(stream);
+  const int L = m->L;
+  // interchange views, original row order
+  m->views.assign((size_t)L * 7, NSView{});
+  const int outs[7] = {m->Hq * m->hd, m->Hkv * m->hd, m->Hkv * m->hd, m->d, m->F, m->F, m->d};
+  const int ins[7] = {m->d, m->d, m->d, m->Hq * m->hd, m->d, m->d, m->F};
+  for (int l = 0; l < L; ++l)
+    for (int i = 0; i < 7; ++i) {
+      NSView& v = m->views[(size_t)l * 7 + i];
+      v.N = outs[i];
+      v.K = ins[i];
+      const int G = (ins[i] + kGroup - 1) / kGroup;
+      RL_TRY(m->alloc(&v.q, (size_t)v.N * (v.K / 8)));
+      RL_TRY(m->alloc(&v.s, (size_t)v.N * G));
+      RL_TRY(m->alloc(&v.z, (size_t)v.N * G));
+    }
+  RL_TRY(m->alloc(&m->d_views, m->views.size()));
+  RL_CUDA(cudaMemcpyAsync(m->d_views, m->views.data(), m->views.size() * sizeof(NSView),
+                          cudaMemcpyHostToDevice, s));
+  for (int l = 0; l < L; ++l) {
+    Layer& ly = m->layers[l];
+    Linear* lins[4] = {&ly.qkv, &ly.o, &ly.gu, &ly.dn};
+    for (Linear* lin : lins) {
+      RL_TRY(m->alloc(&lin->qw, (size_t)lin->N * (lin->Kp / 8)));
+      RL_TRY(m->alloc(&lin->sz, (size_t)lin->N * (lin->Kp / kGroup)));
+      launch_quantize(lin->w, lin->N, lin->K, lin->Kp, lin->qw, lin->sz, lin->rowmap,
+                      m->d_views + (size_t)l * 7 + lin->view_base, s);
+      RL_LAUNCHED();
+    }
+  }
+  RL_CUDA(cudaStreamSynchronize(s));
+  m->quantized = true;
+  return RL_OK;
+}
+
+rl_status rl_exit_layer_view(const rl_model* m, int32_t layer, int32_t which,
+                             const uint32_t** qweight, const uint16_t** scales,
+                             const uint16_t** zeros, int32_t* n_rows, int32_t* n_cols) {
+  if (!m) return fail(RL_ERR_INVALID_ARG, "model is NULL");
+  if (!m->quantized) return fail(RL_ERR_STATE, "exit river not built");
+  if (layer < 0 || layer >= m->L || which < 0 || which > 6)
+    return fail(RL_ERR_INVALID_ARG, "layer %d / linear %d out of range", layer, which);
+  const NSView& v = m->views[(size_t)layer * 7 + which];
+  if (qweight) *qweight = v.q;
+  if (scales) *scales = v.s;
+  if (zeros) *zeros = v.z;
+  if (n_rows) *n_rows = v.N;
+  if (n_cols) *n_cols = v.K;
+  return RL_OK;
+}
+
+rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_seq, rl_kv** out) {
+  if (!mc || !out) return fail(RL_ERR_INVALID_ARG, "NULL argument");
+  *out = nullptr;
+  if (max_batch < 1 || max_batch > 1024 || max_seq < 1)
+    return fail(RL_ERR_INVALID_ARG, "max_batch must be in [1, 1024] and max_seq >= 1");
+  rl_model* m = const_cast<rl_model*>(mc);
+  rl_kv* kv = new rl_kv();
+  kv->m = m;
+  kv->maxB = max_batch;
+  kv->Tmax = max_seq;
+  auto bail = [&](rl_status st) {
+    delete kv;
+    return st;
+  };
+#define K_TRY(expr)                   \
+  do {                                \
+    rl_status s_ = (expr);            \
+    if (s_ != RL_OK) return bail(s_); \
+  } while (0)
+  const size_t per_layer = (size_t)max_batch * m->Hkv * max_seq * m->hd;
+  kv->K.resize(m->L);
+  kv->V.resize(m->L);
+  for (int l = 0; l < m->L; ++l) {
+    K_TRY(kv->alloc(&kv->K[l], per_layer));
+    K_TRY(kv->alloc(&kv->V[l], per_layer));
+  }
+  K_TRY(kv->alloc(&kv->st, 1));
+  const int B = max_batch;
+  for (int i = 0; i < 3; ++i) K_TRY(kv->alloc(&kv->h[i], (size_t)B * m->d));
+  K_TRY(kv->alloc(&kv->x_attn, (size_t)B * m->Kd));
+  K_TRY(kv->alloc(&kv->x_ffn, (size_t)B * m->Kd));
+  K_TRY(kv->alloc(&kv->o, (size_t)B * m->Ko));
+  K_TRY(kv->alloc(&kv->u, (size_t)B * m->Kf));
+  K_TRY(kv->alloc(&kv->xs_attn, (size_t)B * (m->Kd / kGroup)));
+  K_TRY(kv->alloc(&kv->xs_ffn, (size_t)B * (m->Kd / kGroup)));
+  K_TRY(kv->alloc(&kv->xs_o, (size_t)B * (m->Ko / kGroup)));
+  K_TRY(kv->alloc(&kv->xs_u, (size_t)B * (m->Kf / kGroup)));
+  K_TRY(kv->alloc(&kv->q, (size_t)B * m->Hq * m->hd));
+  int ncap = 1;
+  for (int b = 1; b <= B; ++b) ncap = std::max(ncap, b * decode_nchunks(m, b, max_seq));
+  kv->nchunks_cap = ncap;
+  K_TRY(kv->alloc(&kv->part, (size_t)ncap * m->Hq * (m->hd + 2)));
+  K_TRY(kv->alloc(&kv->cosbuf, (size_t)B));
+  K_TRY(kv->alloc(&kv->d_tok, (size_t)B));
+  K_TRY(kv->alloc(&kv->d_next, (size_t)B));
+  K_TRY(kv->alloc(&kv->d_exit, 1));
+  K_TRY(kv->alloc(&kv->d_logits, (size_t)B * m->V));
+  K_TRY(kv->alloc(&kv->d_mincos, (size_t)m->L));
+#undef K_TRY
+  *out = kv;
+  return RL_OK;
+}
+
+rl_status rl_kv_cache_free(rl_kv* kv) {
+  delete kv;
+  return RL_OK;
+}
+
+rl_status rl_kv_view(const rl_kv* kv, int32_t layer, const void** d_k, const void** d_v) {
+  if (!kv) return fail(RL_ERR_INVALID_ARG, "kv is NULL");
+  if (layer < 0 || layer >= kv->m->L) return fail(RL_ERR_INVALID_ARG, "layer out of range");
+  if (d_k) *d_k = kv->K[layer];
+  if (d_v) *d_v = kv->V[layer];
+  return RL_OK;
+}
+
+rl_status rl_kv_position(const rl_kv* kv, int32_t* pos, int32_t* decode_step) {
+  if (!kv) return fail(RL_ERR_INVALID_ARG, "kv is NULL");
+  if (pos) *pos = kv->host_pos;
+  if (decode_step) *decode_step = kv->host_step;
+  return RL_OK;
+}
+
+rl_status rl_kv_set_position(rl_kv* kv, int32_t pos, int32_t decode_step, rl_stream_t stream) {
+  if (!kv) return fail(RL_ERR_INVALID_ARG, "kv is NULL");
+  if (pos < 0 || pos > kv->Tmax || decode_step < 0)
+    return fail(RL_ERR_INVALID_ARG, "position %d outside [0, %d] or negative step", pos, kv->Tmax);
+  launch_set_state(kv->st, pos, decode_step, as_stream(stream));
+  RL_LAUNCHED();
+  kv->host_pos = pos;
+  kv->host_step = decode_step;
+  return RL_OK;
+}
+
+rl_status rl_kv_set_trace(rl_kv* kv, float* d_hidden) {
+  if (!kv) return fail(RL_ERR_INVALID_ARG, "kv is NULL");
+  kv->trace = d_hidden;
+  return RL_OK;
+}
+
+rl_status rl_prefill(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_t B, int32_t T,
+                     const rl_exit_policy* policy, float* d_logits, int32_t* d_next_token,
+                     int32_t* d_exit_layer, float* d_min_cos, rl_stream_t stream) {
+  if (!m || !kv || !d_tokens || !d_logits || !d_exit_layer)
+    return fail(RL_ERR_INVALID_ARG, "NULL argument");
+  if (kv->m != m) return fail(RL_ERR_INVALID_ARG, "kv cache belongs to another model");
+  if (B < 1 || T < 1) return fail(RL_ERR_INVALID_ARG, "B and T must be >= 1");
+  if (B > kv->maxB || T > kv->Tmax)
+    return fail(RL_ERR_CAPACITY, "B=%d > max_batch=%d or T=%d > max_seq=%d", B, kv->maxB, T,
+                kv->Tmax);
+  RL_TRY(check_policy(m, policy));
+  cudaStream_t s = as_stream(stream);
+  const size_t M = (size_t)B * T;
+  const int Gd = m->Kd / kGroup, Go = m->Ko / kGroup, Gf = m->Kf / kGroup;
+  // stream-ordered workspace for the B*T token rows
+  const size_t n_h = M * m->d, n_xd = M * m->Kd, n_xo = M * m->Ko, n_xf = M * m->Kf;
+  const size_t bytes = 3 * n_h * 4 + 2 * n_xd * 2 + n_xo * 2 + n_xf * 2 +
+                       M * (2 * Gd + Go + Gf) * 4 + M * m->Hq * m->hd * 4 +
+                       M * m->Hq * (m->hd + 2) * 4 + M * 4 + 1024;
+  char* base = nullptr;
+  RL_CUDA(cudaMallocAsync((void**)&base, bytes, s));
+  RL_CUDA(cudaMemsetAsync(base, 0, bytes, s));
+  char* p = base;
+  auto take = [&](size_t nbytes) {
+    char* r = p;
+    p += (nbytes + 255) / 256 * 256;
+    return r;
+  };
+  Work w;
+  for (int i = 0; i < 3; ++i) w.h[i] = (float*)take(n_h * 4);
+  w.x_attn = (bf16*)take(n_xd * 2);
+  w.x_ffn = (bf16*)take(n_xd * 2);
+  w.o = (bf16*)take(n_xo * 2);
+  w.u = (bf16*)take(n_xf * 2);
+  w.xs_attn = (float*)take(M * Gd * 4);
+  w.xs_ffn = (float*)take(M * Gd * 4);
+  w.xs_o = (float*)take(M * Go * 4);
+  w.xs_u = (float*)take(M * Gf * 4);
+  w.q = (float*)take(M * m->Hq * m->hd * 4);
+  w.part = (float*)take(M * m->Hq * (m->hd + 2) * 4);
+  w.nchunks = 1;
+  w.cosbuf = (float*)take(M * 4);
+  if ((size_t)(p - base) > bytes) return fail(RL_ERR_CUDA, "prefill workspace sizing");
+  StepIO io{d_tokens, B, T, policy, d_logits, d_next_token, d_exit_layer, d_min_cos, true};
+  rl_status st = enqueue_pass(m, kv, io, w, s);
+  cudaFreeAsync(base, s);
+  if (st != RL_OK) return st;
+  kv->host_pos = T;
+  kv->host_step = 0;
+  return RL_OK;
+}
+
+rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_t B,
+                         const rl_exit_policy* policy, float* d_logits, int32_t* d_next_token,
+                         int32_t* d_exit_layer, float* d_min_cos, rl_stream_t stream) {
+  if (!m || !kv || !d_tokens || !d_logits || !d_exit_layer)
+    return fail(RL_ERR_INVALID_ARG, "NULL argument");
+  if (kv->m != m) return fail(RL_ERR_INVALID_ARG, "kv cache belongs to another model");
+  if (B < 1) return fail(RL_ERR_INVALID_ARG, "B must be >= 1");
+  if (B > kv->maxB || B > kMaxBatch)
+    return fail(RL_ERR_CAPACITY, "B=%d > max_batch=%d (or > %d)", B, kv->maxB, kMaxBatch);
+  if (kv->host_pos + 1 > kv->Tmax)
+    return fail(RL_ERR_CAPACITY, "KV cache full: position %d, max_seq %d", kv->host_pos, kv->Tmax);
+  RL_TRY(check_policy(m, policy));
+  cudaStream_t s = as_stream(stream);
+  StepIO io{d_tokens, B, 1, policy, d_logits, d_next_token, d_exit_layer, d_min_cos, false};
+  const Work w = decode_work(kv, B);
+  kv->prof_pos = kv->host_pos;
+  kv->prof_B = B;
+  if (!is_capturable(s)) {
+    RL_TRY(enqueue_pass(m, kv, io, w, s));
+  } else {
+    GraphKey key;
+    key.B = B;
+    key.mode = policy->mode;
+    key.tau = policy->tau;
+    key.sched = policy->d_schedule;
+    key.sched_len = policy->schedule_len;
+    key.tokens = d_tokens;
+    key.logits = d_logits;
+    key.next = d_next_token;
+    key.exit = d_exit_layer;
+    key.min_cos = d_min_cos;
+    key.trace = kv->trace;
+    key.prof = kv->profiling;
+    if (!kv->exec || !(key == kv->key)) {
+      cudaGraph_t g = nullptr;
+      RL_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
+      rl_status st = enqueue_pass(m, kv, io, w, s);
+      cudaError_t e = cudaStreamEndCapture(s, &g);
+      if (st != RL_OK) {
+        if (g) cudaGraphDestroy(g);
+        return st;
+      }
+      if (e != cudaSuccess) return fail(RL_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
+      if (kv->exec) {
+        cudaGraphExecUpdateResultInfo info;
+        if (cudaGraphExecUpdate(kv->exec, g, &info) != cudaSuccess) {
+          cudaGetLastError();
+          cudaGraphExecDestroy(kv->exec);
+          kv->exec = nullptr;
+        }
+      }
+      if (!kv->exec) {
+        e = cudaGraphInstantiate(&kv->exec, g, 0);
+        if (e != cudaSuccess) {
+          cudaGraphDestroy(g);
+          kv->exec = nullptr;
+          return fail(RL_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
+        }
+      }
+      cudaGraphDestroy(g);
+      kv->key = key;
+    }
+    RL_CUDA(cudaGraphLaunch(kv->exec, s));
+  }
+  kv->host_pos += 1;
+  kv->host_step += 1;
+  return RL_OK;
+}
+
+rl_status rl_decode_step_host(rl_model* m, rl_kv* kv, const int32_t* h_tokens, int32_t B,
+                              const rl_exit_policy* policy, float* h_logits,
+                              int32_t* h_next_token, int32_t* h_exit_layer, float* h_min_cos,
+                              rl_stream_t stream) {
+  if (!m || !kv || !h_tokens || !h_next_token || !h_exit_layer)
+    return fail(RL_ERR_INVALID_ARG, "NULL argument");
+  if (B < 1 || B > kv->maxB) return fail(RL_ERR_CAPACITY, "B=%d outside [1, max_batch]", B);
+  cudaStream_t s = as_stream(stream);
+  RL_CUDA(cudaMemcpyAsync(kv->d_tok, h_tokens, (size_t)B * 4, cudaMemcpyHostToDevice, s));
+  RL_TRY(rl_decode_step(m, kv, kv->d_tok, B, policy, kv->d_logits, kv->d_next, kv->d_exit,
+                        kv->d_mincos, stream));
+  RL_CUDA(cudaMemcpyAsync(h_next_token, kv->d_next, (size_t)B * 4, cudaMemcpyDeviceToHost, s));
+  RL_CUDA(cudaMemcpyAsync(h_exit_layer, kv->d_exit, 4, cudaMemcpyDeviceToHost, s));
+  if (h_logits)
+    RL_CUDA(cudaMemcpyAsync(h_logits, kv->d_logits, (size_t)B * m->V * 4, cudaMemcpyDeviceToHost, s));
+  if (h_min_cos)
+    RL_CUDA(cudaMemcpyAsync(h_min_cos, kv->d_mincos, (size_t)m->L * 4, cudaMemcpyDeviceToHost, s));
+  RL_CUDA(cudaStreamSynchronize(s));
+  return RL_OK;
+}
+
+rl_status rl_sync(rl_model* m, rl_kv* kv, rl_stream_t stream) {
+  (void)m;
+  RL_CUDA(cudaStreamSynchronize(as_stream(stream)));
+  RL_CUDA(cudaGetLastError());
+  if (kv) {
+    int err = 0;
+    RL_CUDA(cudaMemcpy(&err, &kv->st->err, sizeof(int), cudaMemcpyDeviceToHost));
+    if (err) {
+      RL_CUDA(cudaMemset(&kv->st->err, 0, sizeof(int)));
+      return fail(RL_ERR_DEVICE, "device error word 0x%x (%s%s%s)", err,
+                  (err & RL_DEVERR_TOKEN) ? "token id out of range " : "",
+                  (err & RL_DEVERR_CAPACITY) ? "kv capacity " : "",
+                  (err & RL_DEVERR_SCHEDULE) ? "schedule entry out of range" : "");
+    }
+  }
+  return RL_OK;
+}
+
+rl_status rl_kv_set_profiling(rl_kv* kv, int32_t enable) {
+  if (!kv) return fail(RL_ERR_INVALID_ARG, "kv is NULL");
+  if (enable && kv->ev.empty()) {
+    const int cap = 12 * kv->m->L + 8;
+    kv->recs.assign(cap, ProfRec());
+    kv->ev.assign(2 * cap, nullptr);
+    for (auto& e : kv->ev) RL_CUDA(cudaEventCreate(&e));
+    RL_TRY(kv->alloc(&kv->d_paths, (size_t)cap));
+  }
+  kv->profiling = enable != 0;
+  return RL_OK;
+}
+
+rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32_t* kinds,
+                        int32_t* layers, int32_t* paths, float* ms, double* bytes, int32_t* n) {
+  if (!kv || !n) return fail(RL_ERR_INVALID_ARG, "NULL argument");
+  RL_CUDA(cudaStreamSynchronize(as_stream(stream)));
+  const int cnt = std::min(kv->nrec, (int)cap);
+  std::vector<int> hp(kv->nrec > 0 ? kv->nrec : 1, 0);
+  if (kv->nrec > 0)
+    RL_CUDA(cudaMemcpy(hp.data(), kv->d_paths, kv->nrec * sizeof(int), cudaMemcpyDeviceToHost));
+  const rl_model* m = kv->m;
+  for (int i = 0; i < cnt; ++i) {
+    const ProfRec& r = kv->recs[i];
+    float t = 0.f;
+    RL_CUDA(cudaEventElapsedTime(&t, kv->ev[2 * i], kv->ev[2 * i + 1]));
+    const int path = r.gemv ? hp[i] : -1;
+    double b = path == 1 ? r.bytes_w4 : r.bytes_bf;
+    if (r.attn)  // K and V rows 0..p of every sequence
+      b = 2.0 * kv->prof_B * m->Hkv * (double)(kv->prof_pos + 1) * m->hd * 2.0;
+    if (kinds) kinds[i] = r.kind;
+    if (layers) layers[i] = r.layer;
+    if (paths) paths[i] = path;
+    if (ms) ms[i] = t;
+    if (bytes) bytes[i] = b;
+  }
+  *n = cnt;
+  return RL_OK;
+}
+
+int32_t rl_decode_kernel_count(const rl_model* m, int32_t B) {
+  if (!m || B < 1) return 0;
+  // per layer: QKV, attention (2), group sums, O, RMSNorm, gate/up, group sums, down, layer end
+  return 1 + m->L * 10 + 1 + 1;
+}
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// Internal declarations shared by the kernels and the host runtime of
+// libriver.so.  Nothing here is part of the C ABI (see include/river.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "river.h"
+
+namespace river {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kGroup = 128;     // quantization group along K
+constexpr int kMaxBatch = 64;   // decode batch handled by one GEMV launch
+
+inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// ---------------------------------------------------------------------------
+// Per-cache device state.  All kernels of one step read/write it; it never
+// returns to the host during a step.
+// ---------------------------------------------------------------------------
+struct DevState {
+  int pos;          // next KV slot to write (shared by all sequences)
+  int step;         // decode-step counter since the last prefill (forced schedules)
+  int exit_layer;   // exit layer e of the current step: layers l > e use the exit river
+  int err;          // RL_DEVERR_* bits, sticky until rl_sync
+  unsigned int ticket;  // last-arriver counter of the row-norm kernel (reset by the last CTA)
+  unsigned int pad[3];
+};
+
+// ---------------------------------------------------------------------------
+// GEMV / small-batch GEMM: y[b][n] = sum_k x[b][k] * W[n][k] on bf16 weights
+// or on W4 weights (q - z) * s, chosen on the device per layer.
+// ---------------------------------------------------------------------------
+enum GemvEpilogue {
+  EPI_STORE = 0,     // out[b][n] = y
+  EPI_RESID = 1,     // out[b][n] = resid[b][n] + y
+  EPI_SWIGLU = 2,    // rows interleaved per 16-row tile (8 gate, 8 up): out_h[b][j] = silu(g) * u
+  EPI_QKV_ROPE = 3,  // rows permuted per head (RoPE pairs in one tile); RoPE + KV append
+};
+
+enum W4Mode { W4_OFF = 0, W4_ON = 1, W4_BY_LAYER = 2 };
+
+struct GemvArgs {
+  const bf16* w;          // bf16 [N][Kp] row-major (K zero-padded to Kp)
+  const uint32_t* qw;     // W4 [N][Kp/8], nibble for k at bits 4*(k%8)
+  const __half2* sz;      // W4 (scale, zero) per (row, group) [N][Kp/128]
+  int N, Kp;              // N % 16 == 0, Kp % 128 == 0
+  int w4_mode;            // W4Mode
+  const int* exit_layer;  // W4_BY_LAYER: W4 path iff layer_no > *exit_layer
+  int layer_no;           // 1-based
+  const bf16* x;          // activations [B][ldx] bf16 (zero beyond K)
+  int ldx;
+  const float* xsum;      // per (b, group) sum of x, [B][ldxs] (W4 path only)
+  int ldxs;
+  int B;                  // columns in this launch (<= 64)
+  int epi;
+  float* out; int ldo;            // STORE / RESID
+  const float* resid; int ldr;    // RESID
+  bf16* out_h; int ldoh;          // SWIGLU
+  // EPI_QKV_ROPE
+  float* q_out;           // [tokens][Hq*hd] fp32
+  bf16* kc; bf16* vc;     // layer cache base, [maxB][Hkv][Tmax][hd]
+  int maxB, Tmax, Hq, Hkv, hd;
+  const int* pos_ptr;     // decode: slot for every column
+  int T_prefill;          // >0: column c is token (col_base + c) = seq*T + t at position t
+  int col_base;
+  const float* inv_freq;  // [hd/2]
+  int* err;
+  int* path_out;          // nullable: CTA 0 records the path taken (0 bf16, 1 W4)
+};
+
+void launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Row kernels: embedding, RMSNorm, cosine, batch-min exit decision.
+// ---------------------------------------------------------------------------
+struct RowNormArgs {
+  // embedding mode (tokens != nullptr): h_out[r] = embed[tokens[r]]
+  const int* tokens; const bf16* embed; int vocab;
+  const float* h_in;      // residual entering the layer (cosine), nullable
+  float* h_out;           // residual leaving the layer [rows][d]
+  int rows, d;
+  const float* g;         // gain of the next RMSNorm [d], nullable (no x written)
+  float eps;
+  bf16* x; int ldx;       // normalized bf16 output
+  float* xsum; int ldxs;  // per-group sums of x
+  // decision (when h_in != nullptr)
+  float* cosbuf;          // [rows]
+  int layer_no, L;
+  int mode; float tau;    // RL_EXIT_TAU / RL_EXIT_FORCED
+  float* min_cos_out;     // [L], nullable
+  int* exit_out;          // written at layer L, nullable
+  DevState* st;
+  int set_pos;            // at layer L: st->pos = set_pos (>= 0) or st->pos + 1 (< 0)
+  int set_step;           // at layer L: st->step = set_step (>= 0) or st->step + 1 (< 0)
+  // step begin (embedding mode, CTA 0): initialize st->exit_layer
+  const int* schedule; int schedule_len; int use_step_index;
+  // trace of the last position of each sequence
+  float* trace; int trace_layer; int trace_maxB; int trace_T;
+};
+
+void launch_rownorm(const RowNormArgs& a, cudaStream_t s);
+
+void launch_group_sums(const bf16* x, int ldx, int Kp, int B, float* xsum, int ldxs,
+                       cudaStream_t s);
+
+void launch_argmax(const float* logits, int ld, int V, int B, int* out, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Attention over the shared KV cache.
+// ---------------------------------------------------------------------------
+struct AttnArgs {
+  const float* q;         // [nq][Hq*hd] (RoPE applied)
+  const bf16* kc; const bf16* vc;  // [maxB][Hkv][Tmax][hd]
+  int maxB, Tmax, Hq, Hkv, hd;
+  int nq;                 // query rows
+  int T_prefill;          // >0: row r is sequence r/T at position r%T; else row b at *pos_ptr
+  const int* pos_ptr;
+  int nchunks;            // context split per (row, kv head)
+  float* part;            // [nq][Hq][nchunks][hd + 2]
+  bf16* o; int ldo;       // [nq][ldo] output, head h at h*hd
+};
+
+void launch_attention(const AttnArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Weight preparation and quantization.
+// ---------------------------------------------------------------------------
+// Up to three source matrices [rows][src_ld]; rowmap[r] = (source, source row).
+struct GatherSrcs { const bf16* p[3]; };
+
+void launch_gather_rows(bf16* dst, int ldd, int N, int K, const int2* rowmap, GatherSrcs srcs,
+                        int src_ld, cudaStream_t s);
+void launch_set_state(DevState* st, int pos, int step, cudaStream_t s);
+void launch_bf16_to_f32(const bf16* src, float* dst, int n, cudaStream_t s);
+
+struct NSView { uint32_t* q; uint16_t* s; uint16_t* z; int N; int K; };
+
+// Quantize the library's bf16 copy w [N][Kp] (K real inputs) into the
+// internal W4 layout (qw, sz) and the interchange views: row r goes to
+// views[rowmap[r].x] at row rowmap[r].y.
+void launch_quantize(const bf16* w, int N, int K, int Kp, uint32_t* qw, __half2* sz,
+                     const int2* rowmap, const NSView* views, cudaStream_t s);
+
+}  // namespace river

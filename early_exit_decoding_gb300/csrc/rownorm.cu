@@ -1,0 +1,300 @@
+// Row kernels of the decode/prefill path.
+//
+// k_rownorm is the layer-end kernel: for every token it computes the
+// state-transition similarity of the layer (cosine of the residual entering
+// vs leaving it, River-LLM explainer section 四), the next RMSNorm (bf16
+// activations plus their per-group sums for the W4 path), and -- in the last
+// CTA to finish, chosen by an atomic ticket, so no CTA ever waits -- the
+// minimum over all tokens processed together and the tau compare that sets
+// the step's exit layer on the device.  Once the exit layer is below L no
+// later layer is checked (section 四: similarity rises with depth).
+#include <float.h>
+
+#include "internal.h"
+
+namespace river {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide sum of three values (fixed order: per warp, then warp 0).
+__device__ __forceinline__ void block_sum3(float& a, float& b, float& c) {
+  __shared__ float sh[3][kThreads / 32];
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  c = warp_sum(c);
+  if (l == 0) {
+    sh[0][w] = a;
+    sh[1][w] = b;
+    sh[2][w] = c;
+  }
+  __syncthreads();
+  if (w == 0) {
+    a = l < kThreads / 32 ? sh[0][l] : 0.f;
+    b = l < kThreads / 32 ? sh[1][l] : 0.f;
+    c = l < kThreads / 32 ? sh[2][l] : 0.f;
+    a = warp_sum(a);
+    b = warp_sum(b);
+    c = warp_sum(c);
+    if (l == 0) {
+      sh[0][0] = a;
+      sh[1][0] = b;
+      sh[2][0] = c;
+    }
+  }
+  __syncthreads();
+  a = sh[0][0];
+  b = sh[1][0];
+  c = sh[2][0];
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads) k_rownorm(RowNormArgs a) {
+  extern __shared__ float hrow[];  // d fp32 values of this row
+  __shared__ int s_last;
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int d = a.d;
+  float* hout = a.h_out + (size_t)r * d;
+
+  if (a.tokens != nullptr) {
+    int tok = a.tokens[r];
+    if (tok < 0 || tok >= a.vocab) {
+      if (tid == 0) atomicOr(&a.st->err, RL_DEVERR_TOKEN);
+      tok = 0;
+    }
+    const bf16* e = a.embed + (size_t)tok * d;
+    for (int k = tid; k < d; k += kThreads) {
+      const float v = __bfloat162float(e[k]);
+      hrow[k] = v;
+      hout[k] = v;
+    }
+    if (r == 0 && tid == 0) {
+      // Step begin: the exit layer of this call.
+      int e_l = a.L;
+      if (a.mode == RL_EXIT_FORCED) {
+        const int idx = a.use_step_index ? (a.st->step % a.schedule_len) : 0;
+        e_l = a.schedule[idx];
+        if (e_l < 0 || e_l > a.L) {
+          atomicOr(&a.st->err, RL_DEVERR_SCHEDULE);
+          e_l = e_l < 0 ? 0 : a.L;
+        }
+      }
+      a.st->exit_layer = e_l;
+    }
+  } else {
+    for (int k = tid; k < d; k += kThreads) hrow[k] = hout[k];
+  }
+  __syncthreads();
+
+  float ss_out = 0.f, dot = 0.f, ss_in = 0.f;
+  const float* hin = a.h_in ? a.h_in + (size_t)r * d : nullptr;
+  for (int k = tid; k < d; k += kThreads) {
+    const float v = hrow[k];
+    ss_out += v * v;
+    if (hin) {
+      const float u = hin[k];
+      dot += u * v;
+      ss_in += u * u;
+    }
+  }
+  block_sum3(ss_out, dot, ss_in);
+
+  if (a.g != nullptr) {
+    const float den = sqrtf(ss_out / (float)d + a.eps);
+    bf16* x = a.x + (size_t)r * a.ldx;
+    for (int k = tid; k < d; k += kThreads) {
+      const bf16 xb = __float2bfloat16_rn(hrow[k] / den * a.g[k]);
+      x[k] = xb;
+      hrow[k] = __bfloat162float(xb);  // keep the rounded value for the group sums
+    }
+    __syncthreads();
+    const int w = tid >> 5, l = tid & 31;
+    const int G = (d + kGroup - 1) / kGroup;
+    for (int gi = w; gi < G; gi += kThreads / 32) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = gi * kGroup + 4 * l + i;
+        if (k < d) s += hrow[k];
+      }
+      s = warp_sum(s);
+      if (l == 0) a.xsum[(size_t)r * a.ldxs + gi] = s;
+    }
+    __syncthreads();
+    // restore the residual values for the trace below
+    if (a.trace) {
+      for (int k = tid; k < d; k += kThreads) hrow[k] = hout[k];
+      __syncthreads();
+    }
+  }
+
+  if (a.trace != nullptr) {
+    const bool last_pos = a.trace_T <= 0 || (r % a.trace_T) == a.trace_T - 1;
+    if (last_pos) {
+      const int seq = a.trace_T > 0 ? r / a.trace_T : r;
+      float* tr = a.trace + ((size_t)a.trace_layer * a.trace_maxB + seq) * d;
+      for (int k = tid; k < d; k += kThreads) tr[k] = hout[k];
+    }
+  }
+
+  if (hin == nullptr) return;
+
+  if (tid == 0) {
+    const float den = fmaxf(sqrtf(ss_in) * sqrtf(ss_out), 1e-12f);
+    a.cosbuf[r] = dot / den;
+  }
+  // Last-arriver reduction: no CTA waits for another.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned int t = atomicAdd(&a.st->ticket, 1u);
+    s_last = (t == (unsigned int)(a.rows - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  float m = FLT_MAX;
+  for (int i = tid; i < a.rows; i += kThreads) m = fminf(m, __ldcg(a.cosbuf + i));
+  m = warp_min(m);
+  __shared__ float sm[kThreads / 32];
+  if ((tid & 31) == 0) sm[tid >> 5] = m;
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < kThreads / 32; ++w) m = fminf(m, sm[w]);
+    m = fminf(m, sm[0]);
+    if (a.min_cos_out) a.min_cos_out[a.layer_no - 1] = m;
+    DevState* st = a.st;
+    if (a.mode == RL_EXIT_TAU && st->exit_layer == a.L && a.layer_no < a.L && m > a.tau)
+      st->exit_layer = a.layer_no;
+    if (a.layer_no == a.L) {
+      if (a.exit_out) a.exit_out[0] = st->exit_layer;
+      st->pos = a.set_pos >= 0 ? a.set_pos : st->pos + 1;
+      st->step = a.set_step >= 0 ? a.set_step : st->step + 1;
+    }
+    st->ticket = 0u;
+    __threadfence();
+  }
+}
+
+__global__ void k_group_sums(const bf16* __restrict__ x, int ldx, int Kp, int B,
+                             float* __restrict__ xsum, int ldxs) {
+  const int G = Kp / kGroup;
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int l = threadIdx.x & 31;
+  if (wid >= B * G) return;
+  const int b = wid / G, gi = wid % G;
+  const bf16* p = x + (size_t)b * ldx + gi * kGroup + 4 * l;
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s += __bfloat162float(p[i]);
+  s = warp_sum(s);
+  if (l == 0) xsum[(size_t)b * ldxs + gi] = s;
+}
+
+__global__ void __launch_bounds__(1024) k_argmax(const float* __restrict__ logits, int ld, int V,
+                                                 int* __restrict__ out) {
+  const int b = blockIdx.x;
+  const float* p = logits + (size_t)b * ld;
+  float best = -FLT_MAX;
+  int bi = 0x7fffffff;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const float v = p[i];
+    if (v > best || (v == best && i < bi)) {
+      best = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) {
+      best = ov;
+      bi = oi;
+    }
+  }
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    sv[w] = best;
+    si[w] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int nw = blockDim.x / 32;
+    for (int i = 1; i < nw; ++i)
+      if (sv[i] > best || (sv[i] == best && si[i] < bi)) {
+        best = sv[i];
+        bi = si[i];
+      }
+    out[b] = bi == 0x7fffffff ? 0 : bi;
+  }
+}
+
+__global__ void k_gather_rows(bf16* __restrict__ dst, int ldd, int K, const int2* __restrict__ map,
+                              GatherSrcs srcs, int src_ld) {
+  const int r = blockIdx.x;
+  const int2 m = map[r];
+  const bf16* s = srcs.p[m.x] + (size_t)m.y * src_ld;
+  bf16* o = dst + (size_t)r * ldd;
+  const bf16 zero = __float2bfloat16_rn(0.f);
+  for (int k = threadIdx.x; k < ldd; k += blockDim.x) o[k] = k < K ? s[k] : zero;
+}
+
+__global__ void k_set_state(DevState* st, int pos, int step) {
+  st->pos = pos;
+  st->step = step;
+}
+
+__global__ void k_bf16_to_f32(const bf16* __restrict__ s, float* __restrict__ d, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) d[i] = __bfloat162float(s[i]);
+}
+
+}  // namespace
+
+void launch_rownorm(const RowNormArgs& a, cudaStream_t s) {
+  k_rownorm<<<a.rows, kThreads, a.d * sizeof(float), s>>>(a);
+}
+
+void launch_group_sums(const bf16* x, int ldx, int Kp, int B, float* xsum, int ldxs,
+                       cudaStream_t s) {
+  const int warps = B * (Kp / kGroup);
+  const int blocks = (warps * 32 + 255) / 256;
+  k_group_sums<<<blocks, 256, 0, s>>>(x, ldx, Kp, B, xsum, ldxs);
+}
+
+void launch_argmax(const float* logits, int ld, int V, int B, int* out, cudaStream_t s) {
+  k_argmax<<<B, 1024, 0, s>>>(logits, ld, V, out);
+}
+
+void launch_gather_rows(bf16* dst, int ldd, int N, int K, const int2* rowmap, GatherSrcs srcs,
+                        int src_ld, cudaStream_t s) {
+  k_gather_rows<<<N, 256, 0, s>>>(dst, ldd, K, rowmap, srcs, src_ld);
+}
+
+void launch_set_state(DevState* st, int pos, int step, cudaStream_t s) {
+  k_set_state<<<1, 1, 0, s>>>(st, pos, step);
+}
+
+void launch_bf16_to_f32(const bf16* src, float* dst, int n, cudaStream_t s) {
+  k_bf16_to_f32<<<(n + 255) / 256, 256, 0, s>>>(src, dst, n);
+}
+
+}  // namespace river

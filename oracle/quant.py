@@ -73,15 +73,20 @@ def unpack_nibbles(qweight: np.ndarray, K: int) -> np.ndarray:
     """Inverse of the packing: ``q [N][K]`` uint8 with q[n][k] at bits 4*(k%8)."""
     qweight = np.asarray(qweight, dtype=np.uint32)
     N = qweight.shape[0]
-    q = np.empty((N, K), dtype=np.uint8)
-    for i in range(8):
-        q[:, i::8] = ((qweight >> np.uint32(4 * i)) & np.uint32(0xF)).astype(np.uint8)
-    return q
+    shifts = (np.arange(8, dtype=np.uint32) * np.uint32(4))[None, None, :]
+    q = (qweight[:, :, None] >> shifts) & np.uint32(0xF)          # [N][K/8][8]
+    return q.reshape(N, K).astype(np.uint8)
 
 
 def dequantize_linear(qweight, scales, zeros, K: int, group: int = 128) -> np.ndarray:
     """``w_hat[n][k] = (q - z) * s`` in fp32, group of k = k // group."""
     q = unpack_nibbles(qweight, K).astype(F32)
-    s = np.repeat(np.asarray(scales).astype(F32), group, axis=1)[:, :K]
-    z = np.repeat(np.asarray(zeros).astype(F32), group, axis=1)[:, :K]
-    return ((q - z).astype(F32) * s).astype(F32)
+    N = q.shape[0]
+    s = np.asarray(scales).astype(F32)
+    z = np.asarray(zeros).astype(F32)
+    G = s.shape[1]
+    qg = np.zeros((N, G * group), F32)
+    qg[:, :K] = q
+    qg = qg.reshape(N, G, group)
+    w = ((qg - z[:, :, None]).astype(F32) * s[:, :, None]).astype(F32)
+    return w.reshape(N, G * group)[:, :K].copy()

@@ -1,0 +1,303 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+River-LLM explainer: section 三 (W4A16 exit layers that share the backbone's
+KV slots), 四 (batch-min state-transition similarity vs tau), 五 (one exit
+decision for the prompt in prefill, one per generation step).
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle.model import Policy as OPolicy, KVState
+from oracle.quant import quantize_linear
+from tests.harness import build_pair, check_step, tau_band_ok
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TINY = synth.TINY
+
+
+@pytest.fixture(scope="module")
+def river():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    import early_exit_decoding_gb300 as r
+    return r
+
+
+@pytest.fixture(scope="module")
+def stream(river):
+    return torch.cuda.Stream()
+
+
+@pytest.fixture(scope="module")
+def tiny(river, stream):
+    with torch.cuda.stream(stream):
+        m, om, w = build_pair(TINY, seed=0, gains="random", stream=stream)
+    return m, om, w
+
+
+def _run_sequence(river, m, om, stream, policies, B=1, prompt=32, steps=16, seed=1, trace=True,
+                  max_seq=128):
+    """Prefill + decode with teacher forcing on the oracle's greedy tokens.
+    ``policies``: (gpu Policy, oracle Policy) for prefill, then per decode step."""
+    S = m.shape
+    toks = synth.gen_tokens(S.vocab, (B, prompt), seed=seed)
+    kv = m.kv_cache_alloc(B, max_seq)
+    st = KVState(S, B, max_seq)
+    tr = None
+    if trace:
+        tr = torch.zeros((S.n_layers + 1, B, S.d_model), dtype=torch.float32, device="cuda")
+        kv.set_trace(tr)
+    results = []
+    with torch.cuda.stream(stream):
+        gp, op = policies[0]
+        out = river.prefill(m, kv, torch.from_numpy(toks).cuda(), gp, stream=stream)
+        kv.sync(stream)
+        ref = om.prefill(toks, st, op)
+        assert int(out["exit_layer"].item()) == ref.exit_layer or \
+            (op.mode == "tau" and tau_band_ok(ref, op.tau, int(out["exit_layer"].item())))
+        if int(out["exit_layer"].item()) == ref.exit_layer:
+            check_step(out, ref, tr, B, "prefill")
+        results.append((out, ref))
+        nxt = ref.logits.argmax(-1).astype(np.int32)
+        for i in range(steps):
+            gp, op = policies[1 + i]
+            p, s_idx = kv.position()
+            tin = torch.from_numpy(nxt.copy()).cuda()
+            out = river.decode_step(m, kv, tin, gp, stream=stream)
+            kv.sync(stream)
+            ref = om.decode_step(nxt, st, op)
+            e = int(out["exit_layer"].item())
+            if e != ref.exit_layer:
+                assert op.mode == "tau" and tau_band_ok(ref, op.tau, e), \
+                    f"step {i}: exit layer {e} vs oracle {ref.exit_layer}, min_cos {ref.min_cos}"
+                # teacher-force the oracle's decision: the step rewrites the same slots
+                kv.set_position(p, 0, stream)
+                sched = torch.tensor([ref.exit_layer], dtype=torch.int32, device="cuda")
+                out = river.decode_step(m, kv, tin, river.Policy.forced(sched), stream=stream)
+                kv.sync(stream)
+                kv.set_position(p + 1, s_idx + 1, stream)
+            check_step(out, ref, tr, B, f"decode step {i}")
+            results.append((out, ref))
+            nxt = ref.logits.argmax(-1).astype(np.int32)
+    kv.set_trace(None)
+    return results, kv
+
+
+def test_quantizer_is_bit_exact(river, tiny):
+    m, om, w = tiny
+    for l in range(TINY.n_layers):
+        for i, name in enumerate(river.LINEAR_NAMES):
+            qt, st, zt = m.exit_layer_view(l, i)
+            q_ref, s_ref, z_ref = om.quant[l][name]
+            assert np.array_equal(qt.cpu().numpy().view(np.uint32), q_ref), (l, name)
+            assert np.array_equal(st.cpu().numpy().view(np.uint16), s_ref.view(np.uint16)), (l, name)
+            assert np.array_equal(zt.cpu().numpy().view(np.uint16), z_ref.view(np.uint16)), (l, name)
+
+
+def test_full_depth_matches_oracle(river, tiny, stream):
+    """tau = 1.01 > 1 >= cos: never exits; prompt 32, 16 greedy steps."""
+    m, om, _ = tiny
+    pol = [(river.Policy.tau_(1.01), OPolicy.tau_(1.01))] * 17
+    res, _ = _run_sequence(river, m, om, stream, pol)
+    assert all(int(o["exit_layer"].item()) == TINY.n_layers for o, _ in res)
+
+
+def test_tau_half_matches_oracle(river, tiny, stream):
+    m, om, _ = tiny
+    pol = [(river.Policy.tau_(0.5), OPolicy.tau_(0.5))] * 17
+    _run_sequence(river, m, om, stream, pol)
+
+
+def test_forced_schedule_exit_layers_bit_exact(river, tiny, stream):
+    m, om, _ = tiny
+    L = TINY.n_layers
+    sched = [L, 1, 0, 2, 3, 4, 1, 1, 2, 0, 4, 3, 2, 1, 0, 1, 2]
+    d_sched = torch.tensor(sched[1:], dtype=torch.int32, device="cuda")
+    d_pre = torch.tensor([sched[0]], dtype=torch.int32, device="cuda")
+    pol = [(river.Policy.forced(d_pre), OPolicy.forced(sched[0]))]
+    pol += [(river.Policy.forced(d_sched), OPolicy.forced(e)) for e in sched[1:]]
+    res, _ = _run_sequence(river, m, om, stream, pol)
+    assert [int(o["exit_layer"].item()) for o, _ in res] == sched
+
+
+def test_batch_min_rule_batch3(river, tiny, stream):
+    """Batch of 3: the minimum over the batch decides (section 四)."""
+    m, om, _ = tiny
+    for tau in (0.3, 0.5, 0.7):
+        pol = [(river.Policy.tau_(tau), OPolicy.tau_(tau))] * 7
+        _run_sequence(river, m, om, stream, pol, B=3, prompt=12, steps=6, seed=4)
+
+
+def test_batch_forced_and_ragged_shapes(river, stream):
+    """B = 5 and 13 (several n-tiles, ragged), forced exits, prompt 7."""
+    S = synth.scaled(TINY, n_layers=3)
+    with torch.cuda.stream(stream):
+        m, om, _ = build_pair(S, seed=3, stream=stream)
+    for B in (5, 13):
+        sched = [3, 0, 1, 2, 3]
+        d_pre = torch.tensor([sched[0]], dtype=torch.int32, device="cuda")
+        d_sched = torch.tensor(sched[1:], dtype=torch.int32, device="cuda")
+        pol = [(river.Policy.forced(d_pre), OPolicy.forced(sched[0]))]
+        pol += [(river.Policy.forced(d_sched), OPolicy.forced(e)) for e in sched[1:]]
+        _run_sequence(river, m, om, stream, pol, B=B, prompt=7, steps=4, seed=5 + B)
+
+
+def test_exit_writes_slot_p_of_every_layer(river, tiny, stream):
+    """Exit layers write their K/V into the backbone's own slot p (section 三);
+    nothing else in any layer's cache changes."""
+    m, om, _ = tiny
+    S = TINY
+    kv = m.kv_cache_alloc(2, 64)
+    toks = torch.from_numpy(synth.gen_tokens(S.vocab, (2, 10), seed=6)).cuda()
+    with torch.cuda.stream(stream):
+        river.prefill(m, kv, toks[:, :6].contiguous(), river.Policy.tau_(1.01), stream=stream)
+        for e in (0, 1, S.n_layers):
+            stream.synchronize()
+            before = [tuple(t.clone() for t in kv.view(l)) for l in range(S.n_layers)]
+            p, _ = kv.position()
+            sched = torch.tensor([e], dtype=torch.int32, device="cuda")
+            kv.set_position(p, 0, stream)
+            out = river.decode_step(m, kv, toks[:, p].contiguous(), river.Policy.forced(sched),
+                                    stream=stream)
+            kv.sync(stream)
+            assert int(out["exit_layer"].item()) == e
+            for l in range(S.n_layers):
+                for new, old in zip(kv.view(l), before[l]):
+                    changed = (new[:2] != old[:2]).any(dim=3).any(dim=1).any(dim=0)
+                    idx = torch.nonzero(changed).flatten().tolist()
+                    assert idx == [p], (e, l, idx)
+                    assert not (new[2:] != old[2:]).any() if new.shape[0] > 2 else True
+
+
+def test_grid_aligned_exit_river_equals_backbone(river, stream):
+    """Weights on the W4 grid (each group holds nibbles 0 and 15, power-of-two
+    scale, integer zero) quantize exactly, so the exit river must reproduce the
+    backbone: the W4 kernels are then checked against the bf16 ones."""
+    S = synth.scaled(TINY, n_layers=2, vocab=512)
+    w = synth.gen_weights(S, seed=9, device="cpu", gains="random")
+    rng = np.random.default_rng(0)
+    for lw in w["layers"]:
+        for name in synth.LINEARS:
+            N, K = lw[name].shape
+            Gn = (K + 127) // 128
+            q = rng.integers(0, 16, size=(N, K))
+            for g in range(Gn):
+                q[:, g * 128] = 0
+                q[:, min(g * 128 + 1, K - 1)] = 15
+            z = np.repeat(rng.integers(0, 16, size=(N, Gn)), 128, axis=1)[:, :K]
+            lw[name] = torch.from_numpy(((q - z) * 2.0 ** -7).astype(np.float32)).to(torch.bfloat16)
+    import early_exit_decoding_gb300 as r
+    from tests.harness import to_cuda
+    m = r.Model(S, to_cuda(w), stream)
+    m.quantize_exit_layers(stream)
+    toks = torch.from_numpy(synth.gen_tokens(S.vocab, (2, 9), seed=7)).cuda()
+    outs = []
+    for e in (S.n_layers, 0):
+        kv = m.kv_cache_alloc(2, 32)
+        sched = torch.tensor([e], dtype=torch.int32, device="cuda")
+        with torch.cuda.stream(stream):
+            r.prefill(m, kv, toks[:, :8].contiguous(), r.Policy.forced(sched), stream=stream)
+            o = r.decode_step(m, kv, toks[:, 8].contiguous(), r.Policy.forced(sched), stream=stream)
+            kv.sync(stream)
+        outs.append(o["logits"].cpu().numpy())
+    scale = np.abs(outs[0]).max()
+    assert np.abs(outs[0] - outs[1]).max() <= 2e-3 * max(1.0, scale)
+
+
+def test_graph_replay_is_deterministic_and_matches_eager(river, tiny, stream):
+    m, om, _ = tiny
+    S = TINY
+    toks = torch.from_numpy(synth.gen_tokens(S.vocab, (1, 20), seed=8)).cuda()
+    sched = torch.tensor([2, 0, 4, 1], dtype=torch.int32, device="cuda")
+
+    def run(use_stream):
+        kv = m.kv_cache_alloc(1, 64)
+        outs = []
+        ctx = torch.cuda.stream(use_stream) if use_stream is not None else torch.cuda.stream(
+            torch.cuda.default_stream())
+        with ctx:
+            river.prefill(m, kv, toks[:, :12].contiguous(), river.Policy.tau_(1.01), stream=use_stream)
+            for i in range(8):
+                o = river.decode_step(m, kv, toks[:, 12 + i].contiguous(),
+                                      river.Policy.forced(sched), stream=use_stream)
+                outs.append(o["logits"].clone())
+            kv.sync(use_stream)
+        return torch.stack(outs)
+
+    a = run(stream)
+    b = run(stream)
+    c = run(torch.cuda.default_stream())
+    assert torch.equal(a, b)
+    assert torch.equal(a, c)
+
+
+def test_error_paths(river, tiny, stream):
+    m, om, _ = tiny
+    S = TINY
+    kv = m.kv_cache_alloc(2, 8)
+    toks = torch.zeros((2, 8), dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        river.prefill(m, kv, toks, river.Policy.tau_(1.01), stream=stream)
+        with pytest.raises(river.RiverError) as e:
+            river.decode_step(m, kv, toks[:, 0].contiguous(), river.Policy.tau_(1.01), stream=stream)
+        assert e.value.status == river.RL_ERR_CAPACITY
+        with pytest.raises(river.RiverError) as e:
+            river.prefill(m, kv, torch.zeros((3, 4), dtype=torch.int32, device="cuda"),
+                          river.Policy.tau_(1.01), stream=stream)
+        assert e.value.status == river.RL_ERR_CAPACITY
+        bad = torch.full((2, 4), S.vocab + 5, dtype=torch.int32, device="cuda")
+        river.prefill(m, kv, bad, river.Policy.tau_(1.01), stream=stream)
+        with pytest.raises(river.RiverError) as e:
+            kv.sync(stream)
+        assert e.value.status == river.RL_ERR_DEVICE
+        sched = torch.tensor([S.n_layers + 3], dtype=torch.int32, device="cuda")
+        river.decode_step(m, kv, toks[:, 0].contiguous(), river.Policy.forced(sched), stream=stream)
+        with pytest.raises(river.RiverError) as e:
+            kv.sync(stream)
+        assert e.value.status == river.RL_ERR_DEVICE
+        kv.sync(stream)  # cleared
+    import early_exit_decoding_gb300 as r
+    m2 = r.Model(S, __import__("tests.harness", fromlist=["to_cuda"]).to_cuda(
+        synth.gen_weights(S, seed=1, device="cpu")), stream)
+    kv2 = m2.kv_cache_alloc(1, 16)
+    with pytest.raises(river.RiverError) as e:
+        river.prefill(m2, kv2, toks[:1, :4].contiguous(),
+                      river.Policy.forced(torch.tensor([1], dtype=torch.int32, device="cuda")),
+                      stream=stream)
+    assert e.value.status == river.RL_ERR_STATE
+
+
+def test_host_buffer_entry_point(river, tiny, stream):
+    """rl_decode_step_host (host buffers, copies inside) equals rl_decode_step."""
+    m, om, _ = tiny
+    S = TINY
+    toks = synth.gen_tokens(S.vocab, (2, 10), seed=11)
+    sched = torch.tensor([1, 3], dtype=torch.int32, device="cuda")
+    res = []
+    for host in (False, True):
+        kv = m.kv_cache_alloc(2, 32)
+        with torch.cuda.stream(stream):
+            river.prefill(m, kv, torch.from_numpy(toks[:, :8]).cuda(), river.Policy.tau_(1.01),
+                          stream=stream)
+            for i in range(2):
+                if host:
+                    ht = torch.from_numpy(toks[:, 8 + i].copy()).pin_memory()
+                    lg = torch.empty((2, S.vocab), dtype=torch.float32).pin_memory()
+                    nt = torch.empty((2,), dtype=torch.int32).pin_memory()
+                    ex = torch.empty((1,), dtype=torch.int32).pin_memory()
+                    river.rl_decode_step_host(m.handle, kv.handle, ht, 2,
+                                              river.Policy.forced(sched).c(), lg, nt, ex, None,
+                                              stream)
+                    res.append((lg.clone(), nt.clone(), int(ex.item())))
+                else:
+                    o = river.decode_step(m, kv, torch.from_numpy(toks[:, 8 + i].copy()).cuda(),
+                                          river.Policy.forced(sched), stream=stream)
+                    kv.sync(stream)
+                    res.append((o["logits"].cpu(), o["next_token"].cpu(), int(o["exit_layer"].item())))
+    for a, b in zip(res[:2], res[2:]):
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and a[2] == b[2]
