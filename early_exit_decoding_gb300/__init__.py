@@ -229,11 +229,11 @@ def rl_kv_profile(kv, stream=None, cap=1024):
 # --------------------------------------------------------------- conveniences
 
 class _DevArray:
-    """Wraps a library-owned device buffer for torch.as_tensor (read-only view)."""
+    """Wraps a library-owned device buffer for torch.as_tensor (no copy)."""
 
-    def __init__(self, ptr, shape, typestr, readonly=True):
+    def __init__(self, ptr, shape, typestr):
         self.__cuda_array_interface__ = {
-            "shape": tuple(shape), "typestr": typestr, "data": (ptr, readonly), "version": 3,
+            "shape": tuple(shape), "typestr": typestr, "data": (ptr, False), "version": 3,
             "strides": None,
         }
 
@@ -334,8 +334,8 @@ class KVCache:
         S = self.model.shape
         k, v = rl_kv_view(self.handle, layer)
         shp = (self.max_batch, S.n_kv_heads, self.max_seq, S.head_dim)
-        kt = torch.as_tensor(_DevArray(k, shp, "<i2", False), device="cuda").view(torch.bfloat16)
-        vt = torch.as_tensor(_DevArray(v, shp, "<i2", False), device="cuda").view(torch.bfloat16)
+        kt = torch.as_tensor(_DevArray(k, shp, "<i2"), device="cuda").view(torch.bfloat16)
+        vt = torch.as_tensor(_DevArray(v, shp, "<i2"), device="cuda").view(torch.bfloat16)
         return kt, vt
 
     def position(self):

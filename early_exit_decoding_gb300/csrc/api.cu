@@ -47,6 +47,7 @@ struct Linear {
   bf16* w = nullptr;        // [N][Kp]
   uint32_t* qw = nullptr;   // [N][Kp/8]
   __half2* sz = nullptr;    // [N][Kp/128]
+  unsigned char* qwt = nullptr;  // W4 + (s, z) in the fused kernel's unit-tiled layout
   int N = 0, K = 0, Kp = 0;
   int view_base = 0;        // first rl linear index this fused matrix maps to
   const int2* rowmap = nullptr;
@@ -112,11 +113,12 @@ struct GraphKey {
   float* min_cos = nullptr;
   float* trace = nullptr;
   bool prof = false;
+  bool fused = false;
   bool operator==(const GraphKey& o) const {
     return B == o.B && mode == o.mode && tau == o.tau && sched == o.sched &&
            sched_len == o.sched_len && tokens == o.tokens && logits == o.logits &&
            next == o.next && exit == o.exit && min_cos == o.min_cos && trace == o.trace &&
-           prof == o.prof;
+           prof == o.prof && fused == o.fused;
   }
 };
 
@@ -143,6 +145,16 @@ struct rl_kv {
   float* part = nullptr;
   int nchunks_cap = 1;
   float* cosbuf = nullptr;
+  // fused small-batch decode workspace (stream-K partials, tickets, argmax)
+  float* ws = nullptr;
+  unsigned* tile_ticket = nullptr;
+  unsigned* cta_ticket = nullptr;
+  unsigned* attn_ticket = nullptr;
+  float* am_val = nullptr;
+  int* am_idx = nullptr;
+  float* st_mid = nullptr;  // per-tile |h_mid|^2 of the O projection's output [d/16][8]
+  float* st_end = nullptr;  // per-tile (|h_out|^2, <h_in,h_out>, |h_in|^2) of the layer [d/16][8][3]
+  bool use_fused = true;
   // buffers of the host-pointer entry point
   int* d_tok = nullptr;
   int* d_next = nullptr;
@@ -290,12 +302,14 @@ struct Prof {
   bool on;
   int n = 0;
   void begin() {
-    if (on && n < (int)kv->recs.size()) cudaEventRecord(kv->ev[2 * n], s);
+    if (on && n < (int)kv->recs.size())
+      cudaEventRecordWithFlags(kv->ev[2 * n], s, cudaEventRecordExternal);
   }
   int* slot() { return (on && n < (int)kv->recs.size()) ? kv->d_paths + n : nullptr; }
   void end(int kind, int layer, double bytes_bf, double bytes_w4, bool gemv, bool attn = false) {
     if (!on || n >= (int)kv->recs.size()) return;
-    cudaEventRecord(kv->ev[2 * n + 1], s);
+    // External records become event-record nodes when the step is captured.
+    cudaEventRecordWithFlags(kv->ev[2 * n + 1], s, cudaEventRecordExternal);
     ProfRec& r = kv->recs[n];
     r.kind = kind;
     r.layer = layer;
@@ -564,6 +578,212 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
   return RL_OK;
 }
 
+// Fused small-batch decode pass (B <= 8): five kernels per layer plus the
+// LM head, chained with programmatic dependent launch.
+rl_status enqueue_decode_fused(rl_model* m, rl_kv* kv, const StepIO& io, int nchunks,
+                               cudaStream_t s) {
+  const int L = m->L, d = m->d, B = io.B;
+  Prof pf{kv, s, kv->profiling};
+  const bool pdl = !pf.on;  // event records between kernels would break the programmatic edges
+  const int w4mode = m->quantized ? W4_BY_LAYER : W4_OFF;
+  const int tiles_d = d / 16;
+  auto base = [&](const Linear& lin, int layer_no) {
+    FusedArgs a;
+    memset(&a, 0, sizeof(a));
+    a.w = lin.w;
+    a.qwt = lin.qwt;
+    a.N = lin.N;
+    a.Kp = lin.Kp;
+    a.w4_mode = w4mode;
+    a.layer_no = layer_no;
+    a.st = kv->st;
+    a.B = B;
+    a.d = d;
+    a.eps = m->cfg.rms_eps;
+    a.L = L;
+    a.mode = io.pol->mode;
+    a.tau = io.pol->tau;
+    a.schedule = io.pol->d_schedule;
+    a.schedule_len = io.pol->schedule_len > 0 ? io.pol->schedule_len : 1;
+    a.trace_maxB = kv->maxB;
+    a.ws = kv->ws;
+    a.tile_ticket = kv->tile_ticket;
+    a.cta_ticket = kv->cta_ticket;
+    return a;
+  };
+  int cur = 0;
+  for (int l = 0; l < L; ++l) {
+    const Layer& ly = m->layers[l];
+    const int mid = (cur + 1) % 3, nxt = (cur + 2) % 3;
+    // QKV: exit decision of layer l (l >= 1), RMSNorm scale, projection, RoPE, KV append
+    {
+      FusedArgs a = base(ly.qkv, l + 1);
+      if (l == 0) {
+        a.xmode = X_EMBED;
+        a.tokens = io.tokens;
+        a.embed = m->embed;
+        a.vocab = m->V;
+        a.gain_embed = ly.g_attn;
+        a.h_store = kv->h[0];
+        a.step_begin = 1;
+        a.trace = kv->trace;
+        a.trace_layer = 0;
+      } else {
+        a.xmode = X_SCALED;
+        a.xg = kv->x_attn;
+        a.ldxg = m->Kd;
+        a.stats_in = kv->st_end;
+        a.stats_tiles = tiles_d;
+        a.stats_k = 3;
+        a.dec_layer = l;
+        a.min_cos_out = io.min_cos;
+      }
+      a.epi = EPI_QKV_ROPE;
+      a.q_out = kv->q;
+      a.kc = kv->K[l];
+      a.vc = kv->V[l];
+      a.maxB = kv->maxB;
+      a.Tmax = kv->Tmax;
+      a.Hq = m->Hq;
+      a.Hkv = m->Hkv;
+      a.hd = m->hd;
+      a.inv_freq = m->inv_freq;
+      pf.begin();
+      a.path_out = pf.slot();
+      RL_CUDA(launch_gemv_fused(a, m->sm_count, pdl && l > 0, s));
+      pf.end(RL_K_QKV, l + 1, bytes_bf16(ly.qkv), bytes_w4(ly.qkv), true);
+    }
+    {
+      AttnArgs at;
+      memset(&at, 0, sizeof(at));
+      at.q = kv->q;
+      at.kc = kv->K[l];
+      at.vc = kv->V[l];
+      at.maxB = kv->maxB;
+      at.Tmax = kv->Tmax;
+      at.Hq = m->Hq;
+      at.Hkv = m->Hkv;
+      at.hd = m->hd;
+      at.nq = B;
+      at.pos_ptr = &kv->st->pos;
+      at.nchunks = nchunks;
+      at.part = kv->part;
+      at.o = kv->o;
+      at.ldo = m->Ko;
+      at.ticket = kv->attn_ticket;
+      pf.begin();
+      RL_CUDA(launch_attention_fused(at, pdl, s));
+      pf.end(RL_K_ATTN, l + 1, 0, 0, false, true);
+    }
+    {  // O projection + residual; x' and |h_mid|^2 partials for the FFN norm
+      FusedArgs a = base(ly.o, l + 1);
+      a.xmode = X_COPY;
+      a.xg = kv->o;
+      a.ldxg = m->Ko;
+      a.epi = EPI_RESID;
+      a.out = kv->h[mid];
+      a.ldo = d;
+      a.resid = kv->h[cur];
+      a.ldr = d;
+      a.gnext = ly.g_ffn;
+      a.xnext = kv->x_ffn;
+      a.ldxnext = m->Kd;
+      a.stats_out = kv->st_mid;
+      a.stats_k_out = 1;
+      pf.begin();
+      a.path_out = pf.slot();
+      RL_CUDA(launch_gemv_fused(a, m->sm_count, pdl, s));
+      pf.end(RL_K_O, l + 1, bytes_bf16(ly.o), bytes_w4(ly.o), true);
+    }
+    {  // gate/up + SwiGLU
+      FusedArgs a = base(ly.gu, l + 1);
+      a.xmode = X_SCALED;
+      a.xg = kv->x_ffn;
+      a.ldxg = m->Kd;
+      a.stats_in = kv->st_mid;
+      a.stats_tiles = tiles_d;
+      a.stats_k = 1;
+      a.epi = EPI_SWIGLU;
+      a.out_h = kv->u;
+      a.ldoh = m->Kf;
+      pf.begin();
+      a.path_out = pf.slot();
+      RL_CUDA(launch_gemv_fused(a, m->sm_count, pdl, s));
+      pf.end(RL_K_GU, l + 1, bytes_bf16(ly.gu), bytes_w4(ly.gu), true);
+    }
+    {  // down + residual; x' and layer-end partials for the next layer
+      FusedArgs a = base(ly.dn, l + 1);
+      a.xmode = X_COPY;
+      a.xg = kv->u;
+      a.ldxg = m->Kf;
+      a.epi = EPI_RESID;
+      a.out = kv->h[nxt];
+      a.ldo = d;
+      a.resid = kv->h[mid];
+      a.ldr = d;
+      a.gnext = (l + 1 < L) ? m->layers[l + 1].g_attn : m->g_final;
+      a.xnext = kv->x_attn;
+      a.ldxnext = m->Kd;
+      a.stats_out = kv->st_end;
+      a.stats_k_out = 3;
+      a.h_in = kv->h[cur];
+      a.trace = kv->trace;
+      a.trace_layer = l + 1;
+      pf.begin();
+      a.path_out = pf.slot();
+      RL_CUDA(launch_gemv_fused(a, m->sm_count, pdl, s));
+      pf.end(RL_K_DOWN, l + 1, bytes_bf16(ly.dn), bytes_w4(ly.dn), true);
+    }
+    cur = nxt;
+  }
+  {
+    // LM head: min cosine of layer L, final RMSNorm scale, logits, argmax, end of step
+    Linear lm;
+    lm.w = m->lm_head;
+    lm.N = m->V;
+    lm.K = m->d;
+    lm.Kp = m->Kd;
+    FusedArgs a = base(lm, 0);
+    a.w4_mode = W4_OFF;
+    a.xmode = X_SCALED;
+    a.xg = kv->x_attn;
+    a.ldxg = m->Kd;
+    a.stats_in = kv->st_end;
+    a.stats_tiles = tiles_d;
+    a.stats_k = 3;
+    a.dec_layer = L;
+    a.min_cos_out = io.min_cos;
+    a.epi = EPI_LMHEAD;
+    a.out = io.logits;
+    a.ldo = m->V;
+    a.am_val = kv->am_val;
+    a.am_idx = kv->am_idx;
+    a.next_token = io.next;
+    a.exit_out = io.exit;
+    pf.begin();
+    a.path_out = pf.slot();
+    RL_CUDA(launch_gemv_fused(a, m->sm_count, pdl, s));
+    const double lmb = (double)m->V * m->d * 2.0;
+    pf.end(RL_K_LM_HEAD, 0, lmb, lmb, true);
+  }
+  if (pf.on) kv->nrec = pf.n;
+  return RL_OK;
+}
+
+// The fused path holds each projection's activations in shared memory.
+bool fused_fits(const rl_model* m, int B) {
+  if (B > kFusedMaxB || m->d % 16) return false;
+  FusedArgs a;
+  memset(&a, 0, sizeof(a));
+  a.B = B;
+  const int kps[3] = {m->Kd, m->Ko, m->Kf};
+  for (int kp : kps) {
+    a.Kp = kp;
+    if (fused_smem_bytes(a) > 220 * 1024) return false;
+  }
+  return true;
+}
+
 Work decode_work(rl_kv* kv, int B) {
   Work w;
   for (int i = 0; i < 3; ++i) w.h[i] = kv->h[i];
@@ -642,6 +862,8 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&m->sm_count, cudaDevAttrMultiProcessorCount, dev);
   if (m->sm_count < 1) m->sm_count = 1;
+  gemv_fused_setup();
+  attention_setup();
 
   auto bail = [&](rl_status st) {
     delete m;
@@ -755,6 +977,9 @@ rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream) {
       launch_quantize(lin->w, lin->N, lin->K, lin->Kp, lin->qw, lin->sz, lin->rowmap,
                       m->d_views + (size_t)l * 7 + lin->view_base, s);
       RL_LAUNCHED();
+      RL_TRY(m->alloc(&lin->qwt, w4_tiled_bytes(lin->N, lin->Kp)));
+      launch_w4_tile_layout(lin->qw, lin->sz, lin->N, lin->Kp, lin->qwt, s);
+      RL_LAUNCHED();
     }
   }
   RL_CUDA(cudaStreamSynchronize(s));
@@ -817,10 +1042,27 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
   K_TRY(kv->alloc(&kv->xs_u, (size_t)B * (m->Kf / kGroup)));
   K_TRY(kv->alloc(&kv->q, (size_t)B * m->Hq * m->hd));
   int ncap = 1;
-  for (int b = 1; b <= B; ++b) ncap = std::max(ncap, b * decode_nchunks(m, b, max_seq));
+  for (int b = 1; b <= B; ++b) {
+    ncap = std::max(ncap, b * decode_nchunks(m, b, max_seq));
+    ncap = std::max(ncap, b * decode_attention_chunks(b, m->Hkv, max_seq, m->sm_count));
+  }
+  if (decode_attention_chunks(1, m->Hkv, max_seq, m->sm_count) > 256)
+    return bail(fail(RL_ERR_UNSUPPORTED, "max_seq %d exceeds the decode attention limit (32768)", max_seq));
   kv->nchunks_cap = ncap;
   K_TRY(kv->alloc(&kv->part, (size_t)ncap * m->Hq * (m->hd + 2)));
   K_TRY(kv->alloc(&kv->cosbuf, (size_t)B));
+  {
+    const int sm = m->sm_count;
+    const int max_tiles = std::max(std::max(m->Nqkv, 2 * m->F), std::max(m->d, m->V)) / 16 + 1;
+    K_TRY(kv->alloc(&kv->ws, (size_t)sm * 2 * 128));
+    K_TRY(kv->alloc(&kv->tile_ticket, (size_t)max_tiles));
+    K_TRY(kv->alloc(&kv->cta_ticket, 1));
+    K_TRY(kv->alloc(&kv->attn_ticket, (size_t)B * m->Hkv));
+    K_TRY(kv->alloc(&kv->am_val, (size_t)sm * kFusedMaxB));
+    K_TRY(kv->alloc(&kv->am_idx, (size_t)sm * kFusedMaxB));
+    K_TRY(kv->alloc(&kv->st_mid, (size_t)(m->d / 16) * 8));
+    K_TRY(kv->alloc(&kv->st_end, (size_t)(m->d / 16) * 8 * 3));
+  }
   K_TRY(kv->alloc(&kv->d_tok, (size_t)B));
   K_TRY(kv->alloc(&kv->d_next, (size_t)B));
   K_TRY(kv->alloc(&kv->d_exit, 1));
@@ -886,7 +1128,7 @@ rl_status rl_prefill(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_t B,
   const size_t n_h = M * m->d, n_xd = M * m->Kd, n_xo = M * m->Ko, n_xf = M * m->Kf;
   const size_t bytes = 3 * n_h * 4 + 2 * n_xd * 2 + n_xo * 2 + n_xf * 2 +
                        M * (2 * Gd + Go + Gf) * 4 + M * m->Hq * m->hd * 4 +
-                       M * m->Hq * (m->hd + 2) * 4 + M * 4 + 1024;
+                       M * m->Hq * (m->hd + 2) * 4 + M * 4 + 32 * 256;  // + alignment slack of the carve-up
   char* base = nullptr;
   RL_CUDA(cudaMallocAsync((void**)&base, bytes, s));
   RL_CUDA(cudaMemsetAsync(base, 0, bytes, s));
@@ -937,8 +1179,13 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
   const Work w = decode_work(kv, B);
   kv->prof_pos = kv->host_pos;
   kv->prof_B = B;
+  const bool fused = kv->use_fused && fused_fits(m, B);
+  auto enqueue = [&]() -> rl_status {
+    if (fused) return enqueue_decode_fused(m, kv, io, decode_attention_chunks(B, m->Hkv, kv->Tmax, m->sm_count), s);
+    return enqueue_pass(m, kv, io, w, s);
+  };
   if (!is_capturable(s)) {
-    RL_TRY(enqueue_pass(m, kv, io, w, s));
+    RL_TRY(enqueue());
   } else {
     GraphKey key;
     key.B = B;
@@ -953,10 +1200,11 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
     key.min_cos = d_min_cos;
     key.trace = kv->trace;
     key.prof = kv->profiling;
+    key.fused = fused;
     if (!kv->exec || !(key == kv->key)) {
       cudaGraph_t g = nullptr;
       RL_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
-      rl_status st = enqueue_pass(m, kv, io, w, s);
+      rl_status st = enqueue();
       cudaError_t e = cudaStreamEndCapture(s, &g);
       if (st != RL_OK) {
         if (g) cudaGraphDestroy(g);
@@ -1070,6 +1318,8 @@ rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32_t* kin
 
 int32_t rl_decode_kernel_count(const rl_model* m, int32_t B) {
   if (!m || B < 1) return 0;
+  if (fused_fits(m, B))  // fused path: QKV, attention, O, gate/up, down; LM head
+    return m->L * 5 + 1;
   // per layer: QKV, attention (2), group sums, O, RMSNorm, gate/up, group sums, down, layer end
   return 1 + m->L * 10 + 1 + 1;
 }

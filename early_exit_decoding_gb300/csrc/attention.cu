@@ -19,7 +19,7 @@ constexpr int kThreads = 128;
 constexpr int kMaxRep = 8;
 
 template <int HD>
-__global__ void __launch_bounds__(kThreads) k_attn_partial(AttnArgs a) {
+__device__ __forceinline__ void attn_partial_body(const AttnArgs& a) {
   const int c = blockIdx.x, hk = blockIdx.y, row = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rep = a.Hq / a.Hkv;
@@ -43,9 +43,18 @@ __global__ void __launch_bounds__(kThreads) k_attn_partial(AttnArgs a) {
   __shared__ float red[kMaxRep][kThreads / 32];
 
   const float scale = rsqrtf((float)HD);
-  for (int i = tid; i < rep * HD; i += kThreads) {
-    const int h = i / HD, dd = i % HD;
-    qs[h][dd] = a.q[(size_t)row * a.Hq * HD + (hk * rep + h) * HD + dd] * scale;
+  {
+    float qv[kMaxRep * HD / kThreads];  // all loads first, then the stores
+#pragma unroll
+    for (int q = 0; q < kMaxRep * HD / kThreads; ++q) {
+      const int i = tid + q * kThreads;
+      qv[q] = i < rep * HD ? a.q[(size_t)row * a.Hq * HD + hk * rep * HD + i] : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < kMaxRep * HD / kThreads; ++q) {
+      const int i = tid + q * kThreads;
+      if (i < rep * HD) qs[i / HD][i % HD] = qv[q] * scale;
+    }
   }
   __syncthreads();
 
@@ -72,9 +81,12 @@ __global__ void __launch_bounds__(kThreads) k_attn_partial(AttnArgs a) {
     for (int h = 0; h < kMaxRep; ++h) sc[h] = 0.f;
     if (valid) {
       const uint4* kr = reinterpret_cast<const uint4*>(kbase + (size_t)j * HD);
-#pragma unroll 4
+      uint4 kw[HD / 8];  // the whole K row in flight at once
+#pragma unroll
+      for (int v = 0; v < HD / 8; ++v) kw[v] = kr[v];
+#pragma unroll
       for (int v = 0; v < HD / 8; ++v) {
-        const uint4 w = kr[v];
+        const uint4 w = kw[v];
         const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -97,6 +109,8 @@ __global__ void __launch_bounds__(kThreads) k_attn_partial(AttnArgs a) {
     }
     __syncthreads();
     float alpha[kMaxRep];
+#pragma unroll
+    for (int h = 0; h < kMaxRep; ++h) alpha[h] = 1.f;
 #pragma unroll
     for (int h = 0; h < kMaxRep; ++h) {
       if (h >= rep) break;
@@ -127,29 +141,45 @@ __global__ void __launch_bounds__(kThreads) k_attn_partial(AttnArgs a) {
       for (int w = 0; w < kThreads / 32; ++w) bs += red[h][w];
       l_run[h] = l_run[h] * alpha[h] + bs;
     }
-    // P V
+    // P V: eight positions per batch, all their V loads in flight together
     const int nvalid = min(kThreads, end - sb);
+    constexpr int NS = (kSlotsMax > 0 ? kSlotsMax : 1);
+    int sh[NS];
 #pragma unroll
-    for (int si = 0; si < (kSlotsMax > 0 ? kSlotsMax : 1); ++si) {
+    for (int si = 0; si < NS; ++si) {
       const int s = tid + si * kThreads;
-      if (s >= nslots) break;
-      const int h = s / (HD / 2), dp = s % (HD / 2);
-      float2 o = acc[si];
-      float al = 1.f;
+      sh[si] = s < nslots ? s / (HD / 2) : -1;
+      if (sh[si] >= 0) {
+        float al = 1.f;
 #pragma unroll
-      for (int hh = 0; hh < kMaxRep; ++hh)
-        if (hh == h) al = alpha[hh];
-      o.x *= al;
-      o.y *= al;
-      const __nv_bfloat162* vp =
-          reinterpret_cast<const __nv_bfloat162*>(vbase + (size_t)sb * HD) + dp;
-      for (int i = 0; i < nvalid; ++i) {
-        const float p = ps[h][i];
-        const float2 v = __bfloat1622float2(vp[(size_t)i * (HD / 2)]);
-        o.x += p * v.x;
-        o.y += p * v.y;
+        for (int hh = 0; hh < kMaxRep; ++hh)
+          if (hh == sh[si]) al = alpha[hh];
+        acc[si].x *= al;
+        acc[si].y *= al;
       }
-      acc[si] = o;
+    }
+    const __nv_bfloat162* vrow = reinterpret_cast<const __nv_bfloat162*>(vbase + (size_t)sb * HD);
+    for (int i0 = 0; i0 < nvalid; i0 += 8) {
+      __nv_bfloat162 vv[NS][8];
+#pragma unroll
+      for (int si = 0; si < NS; ++si)
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (sh[si] >= 0 && i0 + q < nvalid)
+            vv[si][q] = vrow[(size_t)(i0 + q) * (HD / 2) + (tid + si * kThreads) % (HD / 2)];
+#pragma unroll
+      for (int si = 0; si < NS; ++si) {
+        if (sh[si] < 0) continue;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (i0 + q < nvalid) {
+            const float p = ps[sh[si]][i0 + q];
+            const float2 v = __bfloat1622float2(vv[si][q]);
+            acc[si].x += p * v.x;
+            acc[si].y += p * v.y;
+          }
+        }
+      }
     }
     __syncthreads();
   }
@@ -180,6 +210,230 @@ __global__ void __launch_bounds__(kThreads) k_attn_partial(AttnArgs a) {
 }
 
 template <int HD>
+__global__ void __launch_bounds__(kThreads) k_attn_partial(AttnArgs a) {
+  attn_partial_body<HD>(a);
+}
+
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// Decode attention in one kernel.  CTA (chunk c, KV head, sequence) owns
+// context positions [start, end).  Rows before the current position are
+// final before the projection kernel that precedes this one finishes (only
+// row `pos` is being written), so they are copied into shared memory with
+// cp.async BEFORE the programmatic-dependent-launch wait; after the wait only
+// q and row `pos` are fetched.  Each K/V row is read once for all Hq/Hkv query
+// heads of the group.  The last CTA of each (sequence, KV head) to finish
+// merges the chunks (split-context "flash decoding"); no CTA waits on another.
+constexpr int kCH = 128;  // max positions per CTA
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads) k_attn_decode(AttnArgs a) {
+  constexpr int RSK = HD * 2 + 16;  // padded smem row: conflict-free row-per-thread reads
+  extern __shared__ __align__(16) unsigned char kvs[];  // K rows, then V rows
+  unsigned char* Ks = kvs;
+  unsigned char* Vs = kvs + kCH * RSK;
+  __shared__ float qs[kMaxRep][HD];
+  __shared__ float ps[kMaxRep][kCH];
+  __shared__ float red[kMaxRep][kThreads / 32];
+  __shared__ float mstat[kMaxRep][2];
+  __shared__ int s_last;
+
+  const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rep = a.Hq / a.Hkv;
+  const int nch = a.nchunks;
+  const int pos = *a.pos_ptr;  // set by the previous step: stable before the wait
+  int ctx = pos + 1;
+  if (ctx > a.Tmax) ctx = a.Tmax;
+  const int clen = (ctx + nch - 1) / nch;  // <= kCH by the chunk-count rule
+  const int start = c * clen;
+  const int end = min(start + clen, ctx);
+  const int n = end > start ? end - start : 0;
+  const size_t head_base = ((size_t)b * a.Hkv + hk) * a.Tmax;
+  const bf16* kb = a.kc + head_base * HD;
+  const bf16* vb = a.vc + head_base * HD;
+
+  // ---- before the wait: rows start .. min(end, pos) - 1 -----------------------
+  const int npre = max(0, min(end, pos) - start);
+  for (int idx = tid; idx < npre * (HD / 8); idx += kThreads) {
+    const int r = idx / (HD / 8), ch = idx % (HD / 8);
+    const uint32_t dk = (uint32_t)__cvta_generic_to_shared(Ks + r * RSK + ch * 16);
+    const uint32_t dv = (uint32_t)__cvta_generic_to_shared(Vs + r * RSK + ch * 16);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dk),
+                 "l"(kb + (size_t)(start + r) * HD + ch * 8) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dv),
+                 "l"(vb + (size_t)(start + r) * HD + ch * 8) : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  grid_dep_wait();
+  grid_dep_launch();
+
+  // ---- after the wait: q and the row being written this step ------------------
+  const float scale = rsqrtf((float)HD);
+  {
+    float qv[kMaxRep * HD / kThreads];
+#pragma unroll
+    for (int q = 0; q < kMaxRep * HD / kThreads; ++q) {
+      const int i = tid + q * kThreads;
+      qv[q] = i < rep * HD ? a.q[(size_t)b * a.Hq * HD + hk * rep * HD + i] : 0.f;
+    }
+    if (pos >= start && pos < end && tid < HD / 8) {
+      const int r = pos - start;
+      *reinterpret_cast<uint4*>(Ks + r * RSK + tid * 16) =
+          *reinterpret_cast<const uint4*>(kb + (size_t)pos * HD + tid * 8);
+      *reinterpret_cast<uint4*>(Vs + r * RSK + tid * 16) =
+          *reinterpret_cast<const uint4*>(vb + (size_t)pos * HD + tid * 8);
+    }
+#pragma unroll
+    for (int q = 0; q < kMaxRep * HD / kThreads; ++q) {
+      const int i = tid + q * kThreads;
+      if (i < rep * HD) qs[i / HD][i % HD] = qv[q] * scale;
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+
+  // ---- scores: one position per thread ------------------------------------------
+  float sc[kMaxRep];
+#pragma unroll
+  for (int h = 0; h < kMaxRep; ++h) sc[h] = -FLT_MAX;
+  if (tid < n) {
+#pragma unroll
+    for (int h = 0; h < kMaxRep; ++h) sc[h] = 0.f;
+#pragma unroll 4
+    for (int v = 0; v < HD / 8; ++v) {
+      const uint4 w = *reinterpret_cast<const uint4*>(Ks + tid * RSK + v * 16);
+      const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(e[i]);
+#pragma unroll
+        for (int h = 0; h < kMaxRep; ++h)
+          if (h < rep) sc[h] += f.x * qs[h][8 * v + 2 * i] + f.y * qs[h][8 * v + 2 * i + 1];
+      }
+    }
+  }
+  // block max and sum per head
+#pragma unroll
+  for (int h = 0; h < kMaxRep; ++h) {
+    if (h >= rep) break;
+    float v = sc[h];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) red[h][warp] = v;
+  }
+  __syncthreads();
+  if (tid < rep) {
+    float m = red[tid][0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, red[tid][w]);
+    mstat[tid][0] = m;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < kMaxRep; ++h) {
+    if (h >= rep) break;
+    const float p = tid < n ? __expf(sc[h] - mstat[h][0]) : 0.f;
+    if (tid < kCH) ps[h][tid] = p;
+    float v = p;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[h][warp] = v;
+  }
+  __syncthreads();
+  if (tid < rep) {
+    float l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) l += red[tid][w];
+    mstat[tid][1] = l;
+  }
+  // ---- P V: thread owns (head, dim pair) slots ----------------------------------
+  constexpr int NS = kMaxRep * HD / 2 / kThreads;
+  float2 acc[NS];
+#pragma unroll
+  for (int si = 0; si < NS; ++si) acc[si] = make_float2(0.f, 0.f);
+  const int nslots = rep * HD / 2;
+  for (int j = 0; j < n; ++j) {
+#pragma unroll
+    for (int si = 0; si < NS; ++si) {
+      const int s2 = tid + si * kThreads;
+      if (s2 < nslots) {
+        const int h = s2 / (HD / 2), dp = s2 % (HD / 2);
+        const float p = ps[h][j];
+        const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Vs + j * RSK + dp * 4));
+        acc[si].x += p * v.x;
+        acc[si].y += p * v.y;
+      }
+    }
+  }
+  __syncthreads();
+  // ---- partials: o (unnormalised), running max, sum ------------------------------
+  float* part = a.part + ((size_t)b * a.Hq + hk * rep) * nch * (HD + 2);
+#pragma unroll
+  for (int si = 0; si < NS; ++si) {
+    const int s2 = tid + si * kThreads;
+    if (s2 < nslots) {
+      const int h = s2 / (HD / 2), dp = s2 % (HD / 2);
+      float* p = part + ((size_t)h * nch + c) * (HD + 2);
+      p[2 * dp] = acc[si].x;
+      p[2 * dp + 1] = acc[si].y;
+    }
+  }
+  if (tid < rep) {
+    float* p = part + ((size_t)tid * nch + c) * (HD + 2);
+    p[HD] = n > 0 ? mstat[tid][0] : -FLT_MAX;
+    p[HD + 1] = n > 0 ? mstat[tid][1] : 0.f;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0)
+    s_last = atomicAdd(&a.ticket[(size_t)b * a.Hkv + hk], 1u) == (unsigned int)(nch - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // ---- merge (last CTA of this sequence and KV head) ----------------------------
+  float2* ml = reinterpret_cast<float2*>(kvs);           // [rep][nch]
+  float* wc = reinterpret_cast<float*>(kvs) + 2 * kMaxRep * 256;  // [rep][nch]
+  for (int i = tid; i < rep * nch; i += kThreads) {
+    const int h = i / nch, cc = i % nch;
+    const float* p = a.part + (((size_t)b * a.Hq + hk * rep + h) * nch + cc) * (HD + 2);
+    ml[i] = make_float2(__ldcg(p + HD), __ldcg(p + HD + 1));
+  }
+  __syncthreads();
+  if (tid < rep) {
+    float M = -FLT_MAX, den = 0.f;
+    for (int cc = 0; cc < nch; ++cc)
+      if (ml[tid * nch + cc].y > 0.f) M = fmaxf(M, ml[tid * nch + cc].x);
+    for (int cc = 0; cc < nch; ++cc) {
+      const float2 v = ml[tid * nch + cc];
+      const float w = v.y > 0.f ? __expf(v.x - M) : 0.f;
+      wc[tid * nch + cc] = w;
+      den += w * v.y;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int cc = 0; cc < nch; ++cc) wc[tid * nch + cc] *= inv;
+  }
+  __syncthreads();
+  for (int i = tid; i < rep * HD; i += kThreads) {
+    const int h = i / HD, dd = i % HD;
+    const float* p = a.part + ((size_t)b * a.Hq + hk * rep + h) * nch * (HD + 2) + dd;
+    float num = 0.f;
+    for (int c0 = 0; c0 < nch; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        v[q] = (c0 + q < nch && wc[h * nch + c0 + q] != 0.f) ? __ldcg(p + (size_t)(c0 + q) * (HD + 2)) : 0.f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q)
+        if (c0 + q < nch) num += wc[h * nch + c0 + q] * v[q];
+    }
+    a.o[(size_t)b * a.ldo + (hk * rep + h) * HD + dd] = __float2bfloat16_rn(num);
+  }
+  if (tid == 0) a.ticket[(size_t)b * a.Hkv + hk] = 0u;
+}
+
+template <int HD>
 __global__ void __launch_bounds__(HD) k_attn_combine(AttnArgs a) {
   const int hq = blockIdx.x, row = blockIdx.y, dd = threadIdx.x;
   const float* part = a.part + ((size_t)row * a.Hq + hq) * a.nchunks * (HD + 2);
@@ -203,6 +457,43 @@ __global__ void __launch_bounds__(HD) k_attn_combine(AttnArgs a) {
 }
 
 }  // namespace
+
+void attention_setup() {
+  cudaFuncSetAttribute(k_attn_decode<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       2 * kCH * (128 * 2 + 16));
+  cudaFuncSetAttribute(k_attn_decode<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       2 * kCH * (64 * 2 + 16));
+}
+
+int decode_attention_chunks(int B, int Hkv, int Tmax, int sm_count) {
+  // at most kCH positions per CTA; otherwise about two CTAs per SM, >= 32 positions each
+  const int need = (Tmax + kCH - 1) / kCH;
+  int n = (2 * sm_count + B * Hkv - 1) / (B * Hkv);
+  const int cap32 = (Tmax + 31) / 32;
+  if (n > cap32) n = cap32;
+  if (n < need) n = need;
+  if (n < 1) n = 1;
+  return n;
+}
+
+cudaError_t launch_attention_fused(const AttnArgs& a, bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nchunks, a.Hkv, a.nq);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (a.hd == 64) {
+    cfg.dynamicSmemBytes = 2 * kCH * (64 * 2 + 16);
+    return cudaLaunchKernelEx(&cfg, k_attn_decode<64>, a);
+  }
+  cfg.dynamicSmemBytes = 2 * kCH * (128 * 2 + 16);
+  return cudaLaunchKernelEx(&cfg, k_attn_decode<128>, a);
+}
 
 void launch_attention(const AttnArgs& a, cudaStream_t s) {
   dim3 g1(a.nchunks, a.Hkv, a.nq);

@@ -40,6 +40,7 @@ enum GemvEpilogue {
   EPI_RESID = 1,     // out[b][n] = resid[b][n] + y
   EPI_SWIGLU = 2,    // rows interleaved per 16-row tile (8 gate, 8 up): out_h[b][j] = silu(g) * u
   EPI_QKV_ROPE = 3,  // rows permuted per head (RoPE pairs in one tile); RoPE + KV append
+  EPI_LMHEAD = 4,    // logits + argmax (fused decode path only)
 };
 
 enum W4Mode { W4_OFF = 0, W4_ON = 1, W4_BY_LAYER = 2 };
@@ -74,6 +75,52 @@ struct GemvArgs {
 };
 
 void launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Fused small-batch decode GEMV (B <= 8): norm / exit decision / embedding in
+// the prologue, stream-K main loop, fused epilogues (see gemv_fused.cu).
+// ---------------------------------------------------------------------------
+// Activations of a fused projection: X_COPY = bf16 rows copied as they are;
+// X_SCALED = bf16 rows x' = h * gain written by the producing epilogue, scaled
+// per column by 1/sqrt(mean(h^2) + eps) from per-tile partial sums (and, with
+// three partials per tile, the previous layer's exit decision);
+// X_EMBED = the token embedding gathered and normalised in the prologue.
+enum XMode { X_COPY = 1, X_SCALED = 2, X_EMBED = 3 };
+constexpr int kFusedMaxB = 8;
+
+struct FusedArgs {
+  const bf16* w;          // bf16 [N][Kp] row-major
+  const void* qwt;        // W4 in the unit-tiled layout (w4_tiled_bytes)
+  int N, Kp;
+  int w4_mode; int layer_no;
+  DevState* st;
+  int B;
+  int xmode;
+  const bf16* xg; int ldxg;                 // activations [B][ldxg], zero beyond K
+  const float* stats_in; int stats_tiles; int stats_k;  // X_SCALED: [tiles][8][stats_k]
+  int d; float eps;
+  int dec_layer;                            // layer whose exit decision is taken here (0: none)
+  int L; int mode; float tau; const int* schedule; int schedule_len; int step_begin;
+  float* min_cos_out;
+  const int* tokens; const bf16* embed; int vocab; const float* gain_embed; float* h_store;
+  int epi;
+  float* out; int ldo; const float* resid; int ldr; bf16* out_h; int ldoh;
+  const float* gnext; bf16* xnext; int ldxnext;          // RESID: x' = h * gnext for the next norm
+  float* stats_out; int stats_k_out; const float* h_in;  // RESID: per-tile partial sums
+  float* trace; int trace_layer; int trace_maxB;
+  float* q_out; bf16* kc; bf16* vc; int maxB, Tmax, Hq, Hkv, hd; const float* inv_freq;
+  float* am_val; int* am_idx; int* next_token; int* exit_out;
+  float* ws; unsigned* tile_ticket; unsigned* cta_ticket;
+  int* path_out;
+};
+
+size_t fused_smem_bytes(const FusedArgs& a);
+size_t w4_tiled_bytes(int N, int Kp);
+void launch_w4_tile_layout(const uint32_t* qw, const __half2* sz, int N, int Kp, void* out,
+                           cudaStream_t s);
+int fused_grid(const FusedArgs& a, int sm_count);
+void gemv_fused_setup();
+cudaError_t launch_gemv_fused(const FusedArgs& a, int sm_count, bool pdl, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Row kernels: embedding, RMSNorm, cosine, batch-min exit decision.
@@ -123,9 +170,16 @@ struct AttnArgs {
   int nchunks;            // context split per (row, kv head)
   float* part;            // [nq][Hq][nchunks][hd + 2]
   bf16* o; int ldo;       // [nq][ldo] output, head h at h*hd
+  unsigned* ticket;       // fused kernel: [nq][Hkv] last-arriver counters (zero between launches)
 };
 
 void launch_attention(const AttnArgs& a, cudaStream_t s);
+// Single-kernel decode attention: partials + combine by the last CTA per (row, KV head).
+cudaError_t launch_attention_fused(const AttnArgs& a, bool pdl, cudaStream_t s);
+void attention_setup();
+// Context chunks per (sequence, KV head) of the fused decode attention (<= 256
+// supported by its merge; <= 128 positions per chunk).
+int decode_attention_chunks(int B, int Hkv, int Tmax, int sm_count);
 
 // ---------------------------------------------------------------------------
 // Weight preparation and quantization.

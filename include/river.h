@@ -67,7 +67,8 @@ typedef enum {
 enum {
   RL_DEVERR_TOKEN = 1,    /* a token id was outside [0, vocab); row 0 used instead */
   RL_DEVERR_CAPACITY = 2, /* KV position >= max_seq; K/V write skipped */
-  RL_DEVERR_SCHEDULE = 4  /* forced schedule entry outside [0, L]; clamped */
+  RL_DEVERR_SCHEDULE = 4, /* forced schedule entry outside [0, L]; clamped */
+  RL_DEVERR_TIMEOUT = 8   /* a bounded wait inside a kernel gave up; outputs invalid */
 };
 
 /* Decoder shape (Llama-style).  Requirements: head_dim in {64, 128};

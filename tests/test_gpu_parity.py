@@ -196,17 +196,24 @@ def test_grid_aligned_exit_river_equals_backbone(river, stream):
     m = r.Model(S, to_cuda(w), stream)
     m.quantize_exit_layers(stream)
     toks = torch.from_numpy(synth.gen_tokens(S.vocab, (2, 9), seed=7)).cuda()
-    outs = []
+    outs, hid = [], []
     for e in (S.n_layers, 0):
         kv = m.kv_cache_alloc(2, 32)
+        tr = torch.zeros((S.n_layers + 1, 2, S.d_model), dtype=torch.float32, device="cuda")
+        kv.set_trace(tr)
         sched = torch.tensor([e], dtype=torch.int32, device="cuda")
         with torch.cuda.stream(stream):
             r.prefill(m, kv, toks[:, :8].contiguous(), r.Policy.forced(sched), stream=stream)
             o = r.decode_step(m, kv, toks[:, 8].contiguous(), r.Policy.forced(sched), stream=stream)
             kv.sync(stream)
         outs.append(o["logits"].cpu().numpy())
+        hid.append(tr.cpu().numpy())
+    # Same weight values on both paths: only fp32 summation order differs,
+    # which can flip a bf16 activation rounding by one ulp (2^-8 relative).
     scale = np.abs(outs[0]).max()
-    assert np.abs(outs[0] - outs[1]).max() <= 2e-3 * max(1.0, scale)
+    assert np.abs(outs[0] - outs[1]).max() <= 1e-2 * max(1.0, scale)
+    from tests.harness import cos_rows
+    assert cos_rows(hid[0], hid[1]).min() >= 0.99999
 
 
 def test_graph_replay_is_deterministic_and_matches_eager(river, tiny, stream):
