@@ -285,7 +285,7 @@ def gemv_traffic_note():
     """Per-launch DRAM traffic of the GEMV kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "gemv_dram_traffic.txt")
-    src = os.path.join(ROOT, "early_exit_decoding_gb300", "csrc", "gemv.cu")
+    src = os.path.join(ROOT, "early_exit_decoding_gb300", "csrc", "gemv_fused.cu")
     if not os.path.exists(p):
         return None
     kv = {}

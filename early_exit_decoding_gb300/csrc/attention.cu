@@ -415,20 +415,40 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode(AttnArgs a) {
     for (int cc = 0; cc < nch; ++cc) wc[tid * nch + cc] *= inv;
   }
   __syncthreads();
-  for (int i = tid; i < rep * HD; i += kThreads) {
-    const int h = i / HD, dd = i % HD;
-    const float* p = a.part + ((size_t)b * a.Hq + hk * rep + h) * nch * (HD + 2) + dd;
-    float num = 0.f;
-    for (int c0 = 0; c0 < nch; c0 += 16) {
-      float v[16];
+  // every thread owns OPT outputs and issues the loads of all of them for a
+  // batch of chunks at once
+  constexpr int OPT = kMaxRep * HD / kThreads;
+  constexpr int CB = OPT <= 4 ? 16 : 8;
+  float num[OPT];
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        v[q] = (c0 + q < nch && wc[h * nch + c0 + q] != 0.f) ? __ldcg(p + (size_t)(c0 + q) * (HD + 2)) : 0.f;
+  for (int o = 0; o < OPT; ++o) num[o] = 0.f;
+  for (int c0 = 0; c0 < nch; c0 += CB) {
+    float v[OPT][CB];
 #pragma unroll
-      for (int q = 0; q < 16; ++q)
-        if (c0 + q < nch) num += wc[h * nch + c0 + q] * v[q];
+    for (int o = 0; o < OPT; ++o) {
+      const int i = tid + o * kThreads;
+      const int h = i / HD, dd = i % HD;
+      const float* p = a.part + ((size_t)b * a.Hq + hk * rep + h) * nch * (HD + 2) + dd;
+#pragma unroll
+      for (int q = 0; q < CB; ++q)
+        v[o][q] = (i < rep * HD && c0 + q < nch) ? __ldcg(p + (size_t)(c0 + q) * (HD + 2)) : 0.f;
     }
-    a.o[(size_t)b * a.ldo + (hk * rep + h) * HD + dd] = __float2bfloat16_rn(num);
+#pragma unroll
+    for (int o = 0; o < OPT; ++o) {
+      const int i = tid + o * kThreads;
+      const int h = i < rep * HD ? i / HD : 0;
+#pragma unroll
+      for (int q = 0; q < CB; ++q)
+        if (c0 + q < nch) num[o] += wc[h * nch + c0 + q] * v[o][q];
+    }
+  }
+#pragma unroll
+  for (int o = 0; o < OPT; ++o) {
+    const int i = tid + o * kThreads;
+    if (i < rep * HD) {
+      const int h = i / HD, dd = i % HD;
+      a.o[(size_t)b * a.ldo + (hk * rep + h) * HD + dd] = __float2bfloat16_rn(num[o]);
+    }
   }
   if (tid == 0) a.ticket[(size_t)b * a.Hkv + hk] = 0u;
 }
@@ -463,6 +483,10 @@ void attention_setup() {
                        2 * kCH * (128 * 2 + 16));
   cudaFuncSetAttribute(k_attn_decode<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        2 * kCH * (64 * 2 + 16));
+  cudaFuncSetAttribute(k_attn_decode<128>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+  cudaFuncSetAttribute(k_attn_decode<64>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
 }
 
 int decode_attention_chunks(int B, int Hkv, int Tmax, int sm_count) {

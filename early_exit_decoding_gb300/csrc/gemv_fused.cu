@@ -116,10 +116,12 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ int chunk_owner(long long x, long long U, int grid) {
-  int c = (int)((x * grid) / U);
-  while (c + 1 < grid && ((long long)(c + 1) * U) / grid <= x) ++c;
-  while (c > 0 && ((long long)c * U) / grid > x) --c;
+// CTA owning unit x under the tile partition c0(c) = floor(ntiles*c/grid)*UPT.
+__device__ __forceinline__ int chunk_owner(long long x, long long ntiles, int UPT, int grid) {
+  const long long tile = x / UPT;
+  int c = (int)((tile * grid) / ntiles);
+  while (c + 1 < grid && (ntiles * (c + 1)) / grid <= tile) ++c;
+  while (c > 0 && (ntiles * c) / grid > tile) --c;
   return c;
 }
 
@@ -144,7 +146,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_fused(FusedArgs a) {
   const int ntiles = a.N >> 4;
   const long long U = (long long)ntiles * UPT;
   const int grid = gridDim.x, cta = blockIdx.x;
-  const long long c0 = (U * cta) / grid, c1 = (U * (cta + 1)) / grid;
+  // Whole 16-row tiles per CTA, spread evenly: no tile is shared between CTAs,
+  // so no tile ever needs a cross-CTA merge (the stream-K merge below then
+  // never triggers; it stays for grids that split tiles).
+  const long long c0 = ((long long)ntiles * cta / grid) * UPT;
+  const long long c1 = ((long long)ntiles * (cta + 1) / grid) * UPT;
   const int nunits = (int)(c1 - c0);
   const int first_tile = (int)(c0 / UPT);
   const int ntl = nunits > 0 ? (int)((c1 - 1) / UPT) - first_tile + 1 : 0;  // tiles touched
@@ -393,7 +399,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_fused(FusedArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) y[j][i] = 0.f;
     int tcount = 0;
-    const unsigned char* xrow = xs + (size_t)g * RSX;
+    // column g of the MMA reads activation row min(g, B-1): columns >= B are
+    // computed on a duplicate row and discarded, with no divergent branch
+    const unsigned char* xrow = xs + (size_t)(g < B ? g : B - 1) * RSX;
 
     for (int i = 0; i < nunits; ++i) {
       const int slot = i % S;
@@ -426,8 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_fused(FusedArgs a) {
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const uint32_t va = u4get(wa, m), vb = u4get(wb, m);
-            const uint4 X = g < B ? *reinterpret_cast<const uint4*>(xrow + (gi * 128 + 32 * m + 8 * t) * 2)
-                                  : make_uint4(0, 0, 0, 0);
+            const uint4 X = *reinterpret_cast<const uint4*>(xrow + (gi * 128 + 32 * m + 8 * t) * 2);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const uint32_t A0 = ((va >> (4 * h)) & 0x000F000Fu) | 0x43004300u;
@@ -460,8 +467,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_fused(FusedArgs a) {
             const int cb = warp * 16 + 4 * i4 + t;  // 16-byte chunk within the unit row
             const uint4 wa = *reinterpret_cast<const uint4*>(st + g * RSB + cb * 16);
             const uint4 wb = *reinterpret_cast<const uint4*>(st + (g + 8) * RSB + cb * 16);
-            const uint4 X = g < B ? *reinterpret_cast<const uint4*>(xrow + (uk * KU + cb * 8) * 2)
-                                  : make_uint4(0, 0, 0, 0);
+            const uint4 X = *reinterpret_cast<const uint4*>(xrow + (uk * KU + cb * 8) * 2);
 #pragma unroll
             for (int e = 0; e < 2; ++e)
               mma_bf16(y[i4], u4get(wa, 2 * e), u4get(wb, 2 * e), u4get(wa, 2 * e + 1),
@@ -539,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_fused(FusedArgs a) {
         for (int k = 0; k < 4; ++k) wsp[lane + 32 * k] = tv[k];
         __threadfence();
         __syncwarp();
-        const int oa = chunk_owner(tc0, U, grid), ob = chunk_owner(tc1 - 1, U, grid);
+        const int oa = chunk_owner(tc0, ntiles, UPT, grid), ob = chunk_owner(tc1 - 1, ntiles, UPT, grid);
         unsigned int last = 0;
         if (lane == 0) last = atomicAdd(&a.tile_ticket[tl], 1u) == (unsigned int)(ob - oa);
         last = __shfl_sync(0xffffffffu, last, 0);
@@ -549,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_fused(FusedArgs a) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) tv[k] = 0.f;
           for (int o = oa; o <= ob; ++o) {
-            const int ft = (int)((((long long)o * U) / grid) / UPT);
+            const int ft = (int)(((long long)ntiles * o) / grid);
             const float* p = a.ws + ((size_t)o * 2 + (tl == ft ? 0 : 1)) * 128;
 #pragma unroll
             for (int k = 0; k < 4; ++k) tv[k] += __ldcg(p + lane + 32 * k);
@@ -734,8 +740,8 @@ size_t fused_smem_bytes(const FusedArgs& a) {
 }
 
 int fused_grid(const FusedArgs& a, int sm_count) {
-  const long long U = (long long)(a.N / 16) * ((a.Kp + KU - 1) / KU);
-  return (int)(U < sm_count ? U : sm_count);
+  const int ntiles = a.N / 16;
+  return ntiles < sm_count ? ntiles : sm_count;
 }
 
 size_t w4_tiled_bytes(int N, int Kp) {
@@ -744,6 +750,10 @@ size_t w4_tiled_bytes(int N, int Kp) {
 
 void gemv_fused_setup() {
   cudaFuncSetAttribute(k_gemv_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+  // one shared-memory carveout for every decode kernel: switching the L1 /
+  // shared split between consecutive kernels would drain the SMs
+  cudaFuncSetAttribute(k_gemv_fused, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
 }
 
 cudaError_t launch_gemv_fused(const FusedArgs& a, int sm_count, bool pdl, cudaStream_t s) {
