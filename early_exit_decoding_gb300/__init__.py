@@ -28,7 +28,7 @@ EXPORTS = (
     "rl_quantize_exit_layers", "rl_exit_layer_view", "rl_kv_cache_alloc", "rl_kv_cache_free",
     "rl_kv_view", "rl_kv_position", "rl_kv_set_position", "rl_kv_set_trace", "rl_prefill",
     "rl_decode_step", "rl_decode_step_host", "rl_sync", "rl_decode_kernel_count",
-    "rl_kv_set_profiling", "rl_kv_profile",
+    "rl_kv_set_profiling", "rl_kv_profile", "rl_lm_head_static",
 )
 KERNEL_KINDS = ("embed", "qkv", "attention", "group_sums", "o_proj", "norm", "gate_up", "down",
                 "layer_end", "lm_head", "argmax")
@@ -90,6 +90,7 @@ def _load():
         "rl_kv_set_profiling": (I, [P, I]),
         "rl_kv_profile": (I, [P, P, I, PI, PI, PI, ctypes.POINTER(ctypes.c_float),
                               ctypes.POINTER(ctypes.c_double), PI]),
+        "rl_lm_head_static": (I, [P, P, I, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -207,6 +208,13 @@ def rl_sync(model, kv, stream=None):
 
 def rl_decode_kernel_count(model, B):
     return int(_lib.rl_decode_kernel_count(model, B))
+
+
+def rl_lm_head_static(model, d_h, B, d_logits, d_next_token=None, d_err=None, stream=None):
+    """Final RMSNorm + LM head + greedy argmax of ``d_h [B][d]`` using only the
+    library's static scratch (allocates nothing)."""
+    _check(_lib.rl_lm_head_static(model, _ptr(d_h), B, _ptr(d_logits), _ptr(d_next_token),
+                                  _ptr(d_err), _stream(stream)))
 
 
 def rl_kv_set_profiling(kv, enable):

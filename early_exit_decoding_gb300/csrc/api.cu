@@ -1325,3 +1325,22 @@ int32_t rl_decode_kernel_count(const rl_model* m, int32_t B) {
 }
 
 }  // extern "C"
+
+namespace river {
+
+LmHeadView lm_head_view(const rl_model* m) {
+  LmHeadView v;
+  v.w = m->lm_head;
+  v.g_final = m->g_final;
+  v.V = m->V;
+  v.d = m->d;
+  v.Kd = m->Kd;
+  v.L = m->L;
+  v.sm_count = m->sm_count;
+  v.eps = m->cfg.rms_eps;
+  return v;
+}
+
+rl_status set_error(rl_status s, const char* msg) { return fail(s, "%s", msg); }
+
+}  // namespace river

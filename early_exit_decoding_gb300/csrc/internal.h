@@ -200,4 +200,18 @@ struct NSView { uint32_t* q; uint16_t* s; uint16_t* z; int N; int K; };
 void launch_quantize(const bf16* w, int N, int K, int Kp, uint32_t* qw, __half2* sz,
                      const int2* rowmap, const NSView* views, cudaStream_t s);
 
+
+// ---------------------------------------------------------------------------
+// What the allocation-free LM-head entry point needs from the model, and the
+// runtime's error message setter (both defined in api.cu).
+// ---------------------------------------------------------------------------
+struct LmHeadView {
+  const bf16* w;          // LM head [V][Kd]
+  const float* g_final;   // final RMSNorm gain [d]
+  int V, d, Kd, L, sm_count;
+  float eps;
+};
+LmHeadView lm_head_view(const rl_model* m);
+rl_status set_error(rl_status s, const char* msg);
+
 }  // namespace river

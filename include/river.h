@@ -233,6 +233,29 @@ RL_API rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32
  * accounting); 0 on bad arguments. */
 RL_API int32_t rl_decode_kernel_count(const rl_model* m, int32_t B);
 
+/* rl_lm_head_static: final RMSNorm + LM head + greedy argmax of B residual
+ * rows, for callers that must not allocate device memory.  The pages have no
+ * counterpart to this call: it is the decode step's last kernel offered on
+ * its own, with all of its working memory in one fixed static device array
+ * inside the library (about 209 KiB), so the call allocates nothing and needs
+ * no rl_kv.  Callers that cannot allocate: code running while another
+ * framework captures a CUDA graph (an allocation is not capturable), serving
+ * loops with a fixed memory pool, and latency-critical paths where
+ * cudaMalloc / cudaFree would synchronise the device.
+ *   d_h          [B][d_model] fp32 residual rows (device, caller-owned)
+ *   d_logits     [B][vocab] fp32 out (device, caller-owned)
+ *   d_next_token [B] int32 out, ties to the lowest id (device; may be NULL)
+ *   d_err        [1] int32 out: RL_DEVERR_* bits of this call (device; may be NULL)
+ * Limits: 1 <= B <= 8, d_model <= 8192, vocab and d_model multiples of 16;
+ * beyond them the call returns RL_ERR_UNSUPPORTED and enqueues nothing.
+ * The first call on each device resolves the array's device address with that
+ * device current; make that first call before any stream capture on the
+ * device.  Every call shares the one array: calls that overlap on the GPU
+ * (different streams or threads) race on it; calls on one stream are safe. */
+RL_API rl_status rl_lm_head_static(const rl_model* m, const float* d_h, int32_t B,
+                                   float* d_logits, int32_t* d_next_token, int32_t* d_err,
+                                   rl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
