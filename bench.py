@@ -282,8 +282,8 @@ def run_river(args, rank, world, dev):
 
 
 def gemv_traffic_note():
-    """Per-launch DRAM traffic of the GEMV kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    """DRAM bytes over algorithmic bytes of the fused GEMV kernel from the
+    committed ncu summary, if it was taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "gemv_dram_traffic.txt")
     src = os.path.join(ROOT, "early_exit_decoding_gb300", "csrc", "gemv_fused.cu")
     if not os.path.exists(p):
@@ -297,7 +297,7 @@ def gemv_traffic_note():
     if kv.get("gemv_source_sha256_16") != h:
         return None
     try:
-        return float(kv["traffic_bytes_per_avg_launch"])
+        return float(kv["read_over_algorithmic"])
     except (KeyError, ValueError):
         return None
 
@@ -438,7 +438,8 @@ def main():
     per_launch_bytes = g_bytes / max(1, len(gemv))
     per_launch_ms = g_ms / max(1, len(gemv))
     achieved = per_launch_bytes / (per_launch_ms / 1e3) / 1e9 if gemv else 0.0
-    traffic = gemv_traffic_note()
+    ratio = gemv_traffic_note()
+    traffic = ratio * per_launch_bytes if ratio is not None else None
     shares = {}
     for r in prof:
         shares[r[0]] = shares.get(r[0], 0.0) + r[3]
@@ -465,7 +466,7 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "hbm": {"algorithmic_bytes_per_step": tot_bytes / K, "achieved_gbs": gbs,
                 "peak_gbs": hbm_peak, "frac": gbs / hbm_peak, "peak_source": peak_src},
-        "roofline": {"kernel": "k_gemv (dual-path bf16 / W4 GEMV, all projections + LM head)",
+        "roofline": {"kernel": "k_gemv_fused (bf16 / W4 projections + LM head, B <= 8)",
                      "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
