@@ -31,7 +31,7 @@ EXPORTS = (
     "rl_kv_set_profiling", "rl_kv_profile", "rl_lm_head_static",
 )
 KERNEL_KINDS = ("embed", "qkv", "attention", "group_sums", "o_proj", "norm", "gate_up", "down",
-                "layer_end", "lm_head", "argmax")
+                "layer_end", "lm_head", "argmax", "decode_step")
 
 
 class rl_config(ctypes.Structure):

@@ -45,6 +45,7 @@ rl_status fail(rl_status s, const char* fmt, ...) {
 
 struct Linear {
   bf16* w = nullptr;        // [N][Kp]
+  bf16* wt = nullptr;       // the same weights unit-tiled for the persistent step kernel
   uint32_t* qw = nullptr;   // [N][Kp/8]
   __half2* sz = nullptr;    // [N][Kp/128]
   unsigned char* qwt = nullptr;  // W4 + (s, z) in the fused kernel's unit-tiled layout
@@ -68,6 +69,8 @@ struct rl_model {
   std::vector<Layer> layers;
   bf16* embed = nullptr;
   bf16* lm_head = nullptr;  // [V][Kd]
+  bf16* lm_head_t = nullptr;  // unit-tiled copy
+  bool step_ok = false;       // the persistent step kernel can be launched cooperatively
   float* g_final = nullptr;
   float* inv_freq = nullptr;
   int2* map_qkv = nullptr;
@@ -114,11 +117,12 @@ struct GraphKey {
   float* trace = nullptr;
   bool prof = false;
   bool fused = false;
+  bool step = false;
   bool operator==(const GraphKey& o) const {
     return B == o.B && mode == o.mode && tau == o.tau && sched == o.sched &&
            sched_len == o.sched_len && tokens == o.tokens && logits == o.logits &&
            next == o.next && exit == o.exit && min_cos == o.min_cos && trace == o.trace &&
-           prof == o.prof && fused == o.fused;
+           prof == o.prof && fused == o.fused && step == o.step;
   }
 };
 
@@ -127,6 +131,7 @@ struct ProfRec {
   int kind = 0, layer = 0;
   bool gemv = false, attn = false;
   double bytes_bf = 0, bytes_w4 = 0;
+  int phase = -1;      // >= 0: a phase of the persistent step kernel (timeline record)
 };
 
 }  // namespace
@@ -155,6 +160,17 @@ struct rl_kv {
   float* st_mid = nullptr;  // per-tile |h_mid|^2 of the O projection's output [d/16][8]
   float* st_end = nullptr;  // per-tile (|h_out|^2, <h_in,h_out>, |h_in|^2) of the layer [d/16][8][3]
   bool use_fused = true;
+  // persistent step kernel
+  bool use_step = true;
+  unsigned* bars = nullptr;           // phase arrival counters [nph_cap]
+  PhaseDesc* d_ph = nullptr;          // phase descriptors [nph_cap]
+  std::vector<PhaseDesc> h_ph;        // host copy of what d_ph holds
+  int nph_cap = 0;
+  float* part_s = nullptr;            // attention partials [min(maxB,8)][Hq][part_cap][hd+2]
+  int part_cap = 0;
+  unsigned long long* tl = nullptr;   // per-phase timeline (profiling) [2][nph_cap]
+  int nph_last = 0;
+  int n_tile_ticket = 0;
   // buffers of the host-pointer entry point
   int* d_tok = nullptr;
   int* d_next = nullptr;
@@ -770,6 +786,243 @@ rl_status enqueue_decode_fused(rl_model* m, rl_kv* kv, const StepIO& io, int nch
   return RL_OK;
 }
 
+// Zero the cross-CTA counters of the decode kernels (after an aborted step,
+// or when the position is rewound).
+rl_status reset_sync_words(rl_kv* kv, cudaStream_t s) {
+  RL_CUDA(cudaMemsetAsync(kv->bars, 0, (size_t)kv->nph_cap * sizeof(unsigned), s));
+  RL_CUDA(cudaMemsetAsync(kv->tile_ticket, 0, (size_t)kv->n_tile_ticket * sizeof(unsigned), s));
+  RL_CUDA(cudaMemsetAsync(kv->attn_ticket, 0, (size_t)kv->maxB * kv->m->Hkv * sizeof(unsigned), s));
+  RL_CUDA(cudaMemsetAsync(kv->cta_ticket, 0, sizeof(unsigned), s));
+  return RL_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Persistent step kernel: phase descriptors, fit test, launch.
+// ---------------------------------------------------------------------------
+int step_kmax(const rl_model* m) { return std::max(std::max(m->Kd, m->Ko), m->Kf); }
+
+// Stream-K split of a projection with `ntiles` 16-row tiles over `grid` CTAs:
+// used when whole tiles would leave the CTAs unevenly loaded.
+int step_split(int ntiles, int grid) { return (ntiles % grid != 0 && ntiles < 8 * grid) ? 1 : 0; }
+
+bool step_fits_model(const rl_model* m, int B) {
+  if (!m->step_ok || B < 1 || B > kFusedMaxB || m->d % 16) return false;
+  if (m->Hq / m->Hkv > 8 || m->hd > 128) return false;
+  int ns = 0;
+  const size_t smem = step_smem_bytes(B, step_kmax(m), step_kmax(m) / kGroup, &ns);
+  return smem && decode_step_occupancy(smem) >= 1;
+}
+
+bool step_fits(const rl_model* m, const rl_kv* kv, int B) {
+  if (!m->step_ok || !kv->part_s || B < 1 || B > kFusedMaxB || B > kv->maxB || m->d % 16) return false;
+  if (m->Hq / m->Hkv > 8 || m->hd > 128) return false;
+  if (5 * m->L + 1 > kv->nph_cap) return false;
+  int ns = 0;
+  const size_t smem = step_smem_bytes(B, step_kmax(m), step_kmax(m) / kGroup, &ns);
+  if (!smem) return false;
+  return decode_step_occupancy(smem) >= 1;
+}
+
+std::vector<PhaseDesc> build_step_phases(rl_model* m, rl_kv* kv, const StepIO& io) {
+  const int L = m->L, d = m->d, grid = m->sm_count;
+  const int tiles_d = d / 16;
+  std::vector<PhaseDesc> ph;
+  auto gemv = [&](const Linear& lin, int layer_no) {
+    PhaseDesc p;
+    memset(&p, 0, sizeof(p));
+    p.kind = PH_GEMV;
+    p.layer_no = layer_no;
+    p.wt = lin.wt;
+    p.qwt = m->quantized ? lin.qwt : nullptr;
+    p.N = lin.N;
+    p.Kp = lin.Kp;
+    p.split = step_split(lin.N / 16, grid);
+    return p;
+  };
+  int cur = 0;
+  for (int l = 0; l < L; ++l) {
+    const Layer& ly = m->layers[l];
+    const int mid = (cur + 1) % 3, nxt = (cur + 2) % 3;
+    {  // QKV: exit decision of layer l, RMSNorm scale, projection, RoPE, KV append
+      PhaseDesc p = gemv(ly.qkv, l + 1);
+      if (l == 0) {
+        p.xmode = X_EMBED;
+        p.trace = kv->trace;
+        p.trace_layer = 0;
+      } else {
+        p.xmode = X_SCALED;
+        p.xg = kv->x_attn;
+        p.ldxg = m->Kd;
+        p.stats_in = kv->st_end;
+        p.stats_tiles = tiles_d;
+        p.stats_k = 3;
+        p.dec_layer = l;
+      }
+      p.epi = EPI_QKV_ROPE;
+      p.q_out = kv->q;
+      p.kc = kv->K[l];
+      p.vc = kv->V[l];
+      ph.push_back(p);
+    }
+    {  // attention
+      PhaseDesc p;
+      memset(&p, 0, sizeof(p));
+      p.kind = PH_ATTN;
+      p.layer_no = l + 1;
+      p.q_out = kv->q;
+      p.kc = kv->K[l];
+      p.vc = kv->V[l];
+      p.o_out = kv->o;
+      p.ldo_attn = m->Ko;
+      ph.push_back(p);
+    }
+    {  // O + residual; x' and |h_mid|^2 partials for the FFN norm
+      PhaseDesc p = gemv(ly.o, l + 1);
+      p.xmode = X_COPY;
+      p.xg = kv->o;
+      p.ldxg = m->Ko;
+      p.epi = EPI_RESID;
+      p.out = kv->h[mid];
+      p.ldo = d;
+      p.resid = kv->h[cur];
+      p.ldr = d;
+      p.gnext = ly.g_ffn;
+      p.xnext = kv->x_ffn;
+      p.ldxnext = m->Kd;
+      p.stats_out = kv->st_mid;
+      p.stats_k_out = 1;
+      ph.push_back(p);
+    }
+    {  // gate/up + SwiGLU
+      PhaseDesc p = gemv(ly.gu, l + 1);
+      p.xmode = X_SCALED;
+      p.xg = kv->x_ffn;
+      p.ldxg = m->Kd;
+      p.stats_in = kv->st_mid;
+      p.stats_tiles = tiles_d;
+      p.stats_k = 1;
+      p.epi = EPI_SWIGLU;
+      p.out_h = kv->u;
+      p.ldoh = m->Kf;
+      ph.push_back(p);
+    }
+    {  // down + residual; x' and layer-end partials for the next layer
+      PhaseDesc p = gemv(ly.dn, l + 1);
+      p.xmode = X_COPY;
+      p.xg = kv->u;
+      p.ldxg = m->Kf;
+      p.epi = EPI_RESID;
+      p.out = kv->h[nxt];
+      p.ldo = d;
+      p.resid = kv->h[mid];
+      p.ldr = d;
+      p.gnext = (l + 1 < L) ? m->layers[l + 1].g_attn : m->g_final;
+      p.xnext = kv->x_attn;
+      p.ldxnext = m->Kd;
+      p.stats_out = kv->st_end;
+      p.stats_k_out = 3;
+      p.h_in = kv->h[cur];
+      p.trace = kv->trace;
+      p.trace_layer = l + 1;
+      ph.push_back(p);
+    }
+    cur = nxt;
+  }
+  {  // LM head: min cosine of layer L, final RMSNorm scale, logits, argmax
+    Linear lm;
+    lm.wt = m->lm_head_t;
+    lm.N = m->V;
+    lm.K = m->d;
+    lm.Kp = m->Kd;
+    PhaseDesc p = gemv(lm, 0);
+    p.qwt = nullptr;
+    p.split = 0;
+    p.xmode = X_SCALED;
+    p.xg = kv->x_attn;
+    p.ldxg = m->Kd;
+    p.stats_in = kv->st_end;
+    p.stats_tiles = tiles_d;
+    p.stats_k = 3;
+    p.dec_layer = L;
+    p.epi = EPI_LMHEAD;
+    p.out = io.logits;
+    p.ldo = m->V;
+    ph.push_back(p);
+  }
+  return ph;
+}
+
+// Make the device descriptors match this call (synchronously, outside any
+// capture; waits for earlier work on `s` that may still read them).
+rl_status prepare_step_phases(rl_model* m, rl_kv* kv, const StepIO& io, cudaStream_t s) {
+  std::vector<PhaseDesc> ph = build_step_phases(m, kv, io);
+  if ((int)ph.size() > kv->nph_cap) return fail(RL_ERR_UNSUPPORTED, "too many phases");
+  if (ph.size() == kv->h_ph.size() && memcmp(ph.data(), kv->h_ph.data(), ph.size() * sizeof(PhaseDesc)) == 0)
+    return RL_OK;
+  RL_CUDA(cudaStreamSynchronize(s));
+  RL_CUDA(cudaMemcpy(kv->d_ph, ph.data(), ph.size() * sizeof(PhaseDesc), cudaMemcpyHostToDevice));
+  kv->h_ph.swap(ph);
+  return RL_OK;
+}
+
+rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStream_t s) {
+  const int B = io.B;
+  StepArgs a;
+  memset(&a, 0, sizeof(a));
+  a.ph = kv->d_ph;
+  a.nph = (int)kv->h_ph.size();
+  a.st = kv->st;
+  a.B = B;
+  a.L = m->L;
+  a.d = m->d;
+  a.Hq = m->Hq;
+  a.Hkv = m->Hkv;
+  a.hd = m->hd;
+  a.Tmax = kv->Tmax;
+  a.vocab = m->V;
+  a.eps = m->cfg.rms_eps;
+  a.mode = io.pol->mode;
+  a.tau = io.pol->tau;
+  a.schedule = io.pol->d_schedule;
+  a.schedule_len = io.pol->schedule_len > 0 ? io.pol->schedule_len : 1;
+  a.tokens = io.tokens;
+  a.embed = m->embed;
+  a.gain_embed = m->layers[0].g_attn;
+  a.h_store = kv->h[0];
+  a.trace_maxB = kv->maxB;
+  a.inv_freq = m->inv_freq;
+  a.min_cos_out = io.min_cos;
+  a.next_token = io.next;
+  a.exit_out = io.exit;
+  a.am_val = kv->am_val;
+  a.am_idx = kv->am_idx;
+  a.cta_ticket = kv->cta_ticket;
+  a.bars = kv->bars;
+  a.ws = kv->ws;
+  a.tile_ticket = kv->tile_ticket;
+  a.part = kv->part_s;
+  a.attn_ticket = kv->attn_ticket;
+  a.part_cap = kv->part_cap;
+  a.xs_row_bytes = step_kmax(m) * 2 + 64;
+  a.gmax = step_kmax(m) / kGroup;
+  const size_t smem = step_smem_bytes(B, step_kmax(m), a.gmax, &a.nslot);
+  if (!smem) return fail(RL_ERR_UNSUPPORTED, "step kernel does not fit");
+  const bool prof = kv->profiling;
+  if (prof) {
+    a.tl = kv->tl;
+    RL_CUDA(cudaMemsetAsync(kv->tl, 0xff, (size_t)a.nph * 8, s));
+    RL_CUDA(cudaMemsetAsync(kv->tl + a.nph, 0, (size_t)a.nph * 8, s));
+    cudaEventRecordWithFlags(kv->ev[0], s, cudaEventRecordExternal);
+  }
+  RL_CUDA(launch_decode_step(a, m->sm_count, smem, s));
+  if (prof) {
+    cudaEventRecordWithFlags(kv->ev[1], s, cudaEventRecordExternal);
+    kv->nph_last = a.nph;
+    kv->nrec = -1;  // marks a step-kernel profile
+  }
+  return RL_OK;
+}
+
 // The fused path holds each projection's activations in shared memory.
 bool fused_fits(const rl_model* m, int B) {
   if (B > kFusedMaxB || m->d % 16) return false;
@@ -864,6 +1117,12 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
   if (m->sm_count < 1) m->sm_count = 1;
   gemv_fused_setup();
   attention_setup();
+  decode_step_setup();
+  {
+    int coop = 0;
+    cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    m->step_ok = coop != 0;
+  }
 
   auto bail = [&](rl_status st) {
     delete m;
@@ -900,6 +1159,9 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
     RL_TRY(m->alloc(&lin.w, (size_t)N * lin.Kp));
     launch_gather_rows(lin.w, lin.Kp, N, K, map, src, K, s);
     RL_LAUNCHED();
+    RL_TRY(m->alloc(&lin.wt, (size_t)N * lin.Kp));
+    launch_bf16_tile_layout(lin.w, N, lin.Kp, lin.wt, s);
+    RL_LAUNCHED();
     return RL_OK;
   };
 
@@ -926,6 +1188,8 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
   M_TRY(m->alloc(&m->lm_head, (size_t)m->V * m->Kd));
   launch_gather_rows(m->lm_head, m->Kd, m->V, m->d, m->map_id,
                      GatherSrcs{{(const bf16*)wts->lm_head, nullptr, nullptr}}, m->d, s);
+  M_TRY(m->alloc(&m->lm_head_t, (size_t)m->V * m->Kd));
+  launch_bf16_tile_layout(m->lm_head, m->V, m->Kd, m->lm_head_t, s);
   M_TRY(m->alloc(&m->g_final, m->d));
   launch_bf16_to_f32((const bf16*)wts->g_final, m->g_final, m->d, s);
   {
@@ -1056,12 +1320,28 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
     const int max_tiles = std::max(std::max(m->Nqkv, 2 * m->F), std::max(m->d, m->V)) / 16 + 1;
     K_TRY(kv->alloc(&kv->ws, (size_t)sm * 2 * 128));
     K_TRY(kv->alloc(&kv->tile_ticket, (size_t)max_tiles));
+    kv->n_tile_ticket = max_tiles;
     K_TRY(kv->alloc(&kv->cta_ticket, 1));
     K_TRY(kv->alloc(&kv->attn_ticket, (size_t)B * m->Hkv));
     K_TRY(kv->alloc(&kv->am_val, (size_t)sm * kFusedMaxB));
     K_TRY(kv->alloc(&kv->am_idx, (size_t)sm * kFusedMaxB));
     K_TRY(kv->alloc(&kv->st_mid, (size_t)(m->d / 16) * 8));
     K_TRY(kv->alloc(&kv->st_end, (size_t)(m->d / 16) * 8 * 3));
+  }
+  {
+    // persistent step kernel: phase counters, descriptors, attention partials
+    kv->nph_cap = 5 * m->L + 2;
+    K_TRY(kv->alloc(&kv->bars, (size_t)kv->nph_cap));
+    K_TRY(kv->alloc(&kv->d_ph, (size_t)kv->nph_cap));
+    const int CH = 128;  // positions per attention chunk
+    const int need = (max_seq + CH - 1) / CH;
+    kv->part_cap = std::min(256, need + m->sm_count + 1);
+    if (need <= 256) {
+      const int bs = std::min(B, kFusedMaxB);
+      K_TRY(kv->alloc(&kv->part_s, (size_t)bs * m->Hq * kv->part_cap * (m->hd + 2)));
+    } else {
+      kv->part_cap = 0;  // context too long for the step kernel's chunking: fused path
+    }
   }
   K_TRY(kv->alloc(&kv->d_tok, (size_t)B));
   K_TRY(kv->alloc(&kv->d_next, (size_t)B));
@@ -1099,6 +1379,7 @@ rl_status rl_kv_set_position(rl_kv* kv, int32_t pos, int32_t decode_step, rl_str
     return fail(RL_ERR_INVALID_ARG, "position %d outside [0, %d] or negative step", pos, kv->Tmax);
   launch_set_state(kv->st, pos, decode_step, as_stream(stream));
   RL_LAUNCHED();
+  RL_TRY(reset_sync_words(kv, as_stream(stream)));
   kv->host_pos = pos;
   kv->host_step = decode_step;
   return RL_OK;
@@ -1154,6 +1435,7 @@ rl_status rl_prefill(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_t B,
   w.cosbuf = (float*)take(M * 4);
   if ((size_t)(p - base) > bytes) return fail(RL_ERR_CUDA, "prefill workspace sizing");
   StepIO io{d_tokens, B, T, policy, d_logits, d_next_token, d_exit_layer, d_min_cos, true};
+  RL_TRY(reset_sync_words(kv, s));
   rl_status st = enqueue_pass(m, kv, io, w, s);
   cudaFreeAsync(base, s);
   if (st != RL_OK) return st;
@@ -1179,8 +1461,11 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
   const Work w = decode_work(kv, B);
   kv->prof_pos = kv->host_pos;
   kv->prof_B = B;
-  const bool fused = kv->use_fused && fused_fits(m, B);
+  const bool step = kv->use_step && step_fits(m, kv, B);
+  const bool fused = !step && kv->use_fused && fused_fits(m, B);
+  if (step) RL_TRY(prepare_step_phases(m, kv, io, s));
   auto enqueue = [&]() -> rl_status {
+    if (step) return enqueue_decode_step(m, kv, io, s);
     if (fused) return enqueue_decode_fused(m, kv, io, decode_attention_chunks(B, m->Hkv, kv->Tmax, m->sm_count), s);
     return enqueue_pass(m, kv, io, w, s);
   };
@@ -1201,6 +1486,7 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
     key.trace = kv->trace;
     key.prof = kv->profiling;
     key.fused = fused;
+    key.step = step;
     if (!kv->exec || !(key == kv->key)) {
       cudaGraph_t g = nullptr;
       RL_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
@@ -1267,10 +1553,13 @@ rl_status rl_sync(rl_model* m, rl_kv* kv, rl_stream_t stream) {
     RL_CUDA(cudaMemcpy(&err, &kv->st->err, sizeof(int), cudaMemcpyDeviceToHost));
     if (err) {
       RL_CUDA(cudaMemset(&kv->st->err, 0, sizeof(int)));
-      return fail(RL_ERR_DEVICE, "device error word 0x%x (%s%s%s)", err,
+      RL_TRY(reset_sync_words(kv, as_stream(stream)));
+      RL_CUDA(cudaStreamSynchronize(as_stream(stream)));
+      return fail(RL_ERR_DEVICE, "device error word 0x%x (%s%s%s%s)", err,
                   (err & RL_DEVERR_TOKEN) ? "token id out of range " : "",
                   (err & RL_DEVERR_CAPACITY) ? "kv capacity " : "",
-                  (err & RL_DEVERR_SCHEDULE) ? "schedule entry out of range" : "");
+                  (err & RL_DEVERR_SCHEDULE) ? "schedule entry out of range " : "",
+                  (err & RL_DEVERR_TIMEOUT) ? "a bounded wait in a kernel timed out" : "");
     }
   }
   return RL_OK;
@@ -1284,6 +1573,7 @@ rl_status rl_kv_set_profiling(rl_kv* kv, int32_t enable) {
     kv->ev.assign(2 * cap, nullptr);
     for (auto& e : kv->ev) RL_CUDA(cudaEventCreate(&e));
     RL_TRY(kv->alloc(&kv->d_paths, (size_t)cap));
+    RL_TRY(kv->alloc(&kv->tl, (size_t)2 * kv->nph_cap));
   }
   kv->profiling = enable != 0;
   return RL_OK;
@@ -1293,6 +1583,56 @@ rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32_t* kin
                         int32_t* layers, int32_t* paths, float* ms, double* bytes, int32_t* n) {
   if (!kv || !n) return fail(RL_ERR_INVALID_ARG, "NULL argument");
   RL_CUDA(cudaStreamSynchronize(as_stream(stream)));
+  if (kv->nrec == -1) {
+    // persistent step kernel: one record per phase (first start .. last end
+    // over CTAs, from the in-kernel timeline), then the whole kernel (events)
+    const rl_model* m = kv->m;
+    const int nph = kv->nph_last;
+    std::vector<unsigned long long> tl((size_t)2 * nph);
+    RL_CUDA(cudaMemcpy(tl.data(), kv->tl, tl.size() * 8, cudaMemcpyDeviceToHost));
+    DevState hs;
+    RL_CUDA(cudaMemcpy(&hs, kv->st, sizeof(hs), cudaMemcpyDeviceToHost));
+    const int e = hs.exit_layer;
+    int cnt = 0;
+    double total = 0;
+    for (int p = 0; p < nph && cnt < cap; ++p, ++cnt) {
+      const PhaseDesc& d = kv->h_ph[p];
+      int kind = RL_K_LM_HEAD;
+      double b = 0;
+      int path = -1;
+      if (d.kind == PH_ATTN) {
+        kind = RL_K_ATTN;
+        b = 2.0 * kv->prof_B * m->Hkv * (double)(kv->prof_pos + 1) * m->hd * 2.0;
+      } else {
+        if (d.layer_no > 0) {
+          const int r = p % 5;
+          kind = r == 0 ? RL_K_QKV : (r == 2 ? RL_K_O : (r == 3 ? RL_K_GU : RL_K_DOWN));
+        }
+        path = (d.qwt && d.layer_no > e) ? 1 : 0;
+        b = path ? (double)d.N * d.Kp / 2.0 + (double)d.N * (d.Kp / kGroup) * 4.0
+                 : (double)d.N * d.Kp * 2.0;
+      }
+      total += b;
+      const double t = tl[(size_t)nph + p] > tl[p] ? (double)(tl[(size_t)nph + p] - tl[p]) * 1e-6 : 0.0;
+      if (kinds) kinds[cnt] = kind;
+      if (layers) layers[cnt] = d.layer_no;
+      if (paths) paths[cnt] = path;
+      if (ms) ms[cnt] = (float)t;
+      if (bytes) bytes[cnt] = b;
+    }
+    if (cnt < cap) {
+      float t = 0.f;
+      RL_CUDA(cudaEventElapsedTime(&t, kv->ev[0], kv->ev[1]));
+      if (kinds) kinds[cnt] = RL_K_STEP;
+      if (layers) layers[cnt] = 0;
+      if (paths) paths[cnt] = -1;
+      if (ms) ms[cnt] = t;
+      if (bytes) bytes[cnt] = total;
+      ++cnt;
+    }
+    *n = cnt;
+    return RL_OK;
+  }
   const int cnt = std::min(kv->nrec, (int)cap);
   std::vector<int> hp(kv->nrec > 0 ? kv->nrec : 1, 0);
   if (kv->nrec > 0)
@@ -1318,6 +1658,7 @@ rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32_t* kin
 
 int32_t rl_decode_kernel_count(const rl_model* m, int32_t B) {
   if (!m || B < 1) return 0;
+  if (step_fits_model(m, B)) return 1;  // one persistent kernel per step
   if (fused_fits(m, B))  // fused path: QKV, attention, O, gate/up, down; LM head
     return m->L * 5 + 1;
   // per layer: QKV, attention (2), group sums, O, RMSNorm, gate/up, group sums, down, layer end

@@ -1,0 +1,1115 @@
+// Persistent decode step for small batches (B <= 8): ONE cooperative kernel
+// per decode step runs every phase -- for each layer QKV (+ exit decision,
+// RoPE, KV append), attention, O (+ residual), gate/up (+ SwiGLU), down (+
+// residual, next RMSNorm input, cosine partials); then the LM head (+ greedy
+// argmax).  River-LLM explainer, section 四: the batch-minimum cosine of a
+// layer's input and output residual decides, once, that the remaining layers
+// run on the W4A16 exit river; section 三: those layers write K/V into the
+// backbone's own cache slot.
+//
+// One CTA per SM, warp-specialised:
+//   * producer warp: streams, through a ring of shared-memory slots, every
+//     weight unit (16 rows x 1024 inputs bf16, or four 16 x 1024 W4 units with
+//     their scales/zeros, one bulk copy each) and every K/V chunk this CTA will
+//     consume in the whole step, in consumption order.  None of that depends on
+//     this step's activations, so the stream runs ahead across phase
+//     boundaries; it only waits for free slots and -- in tau mode, before the
+//     exit -- for this CTA's exit decision of the previous layer, which picks
+//     bf16 or W4 weights for the next one;
+//   * eight consumer warps: wait for the previous phase (grid-wide arrival
+//     counter), fetch the phase's activation rows, then run mma.sync on the
+//     staged weights (or the attention math on staged K/V);
+//   * reducer warp: sums the consumer warps' partial tiles and runs the
+//     epilogues.
+// Tiles of the small projections are split across CTAs in (tile, unit) order
+// (stream-K); the last CTA to finish a split tile merges it (ticket, partials
+// summed in CTA order: deterministic).  Every wait is bounded: on timeout the
+// kernel sets RL_DEVERR_TIMEOUT and winds down without touching more memory.
+#include "dev_common.cuh"
+
+namespace river {
+
+namespace {
+
+using namespace dev;
+
+constexpr int NC = 8;                     // consumer warps
+constexpr int WP = NC;                    // producer warp
+constexpr int WR = NC + 1;                // reducer warp
+constexpr int kThreads = (NC + 2) * 32;
+constexpr int KU = 1024;                  // inputs per unit
+constexpr int STAGE_W = 16 * 512 + 512;   // one W4 unit: 16 rows x 512 B nibbles + 16 x 8 (s, z)
+constexpr int W4U = 4;                    // W4 units per ring slot
+constexpr int SLOT_B = W4U * STAGE_W;     // 34816 bytes (>= 32 KB bf16 unit, >= K+V chunk)
+constexpr int kMaxSlots = 8;
+constexpr int kCHP = 128;                 // positions per attention chunk
+constexpr int kAttnHalf = 16384;          // V offset in a one-slot chunk (head_dim 64)
+constexpr int kMaxRep = 8;
+constexpr int kMaxHD = 128;
+constexpr long long kSpin = 1LL << 20;     // mbarrier polls
+constexpr long long kSpinBar = 1LL << 24;  // grid-barrier polls (each with a short sleep)
+constexpr int kBarCons = 1;                // named barrier: consumer warps
+constexpr int kBarPhase = 2;               // named barrier: consumers + reducer
+constexpr int kStaticSmem = 12 * 1024;     // upper bound of the kernel's static shared memory
+
+struct GRange {
+  long long c0, c1;
+  int UPT, ntiles;
+};
+
+// (tile, unit) range of CTA `cta`: whole tiles, or stream-K when `split`.
+__device__ __forceinline__ GRange gemv_range(int N, int Kp, int split, int cta, int grid) {
+  GRange r;
+  r.UPT = (Kp + KU - 1) / KU;
+  r.ntiles = N >> 4;
+  const long long U = (long long)r.ntiles * r.UPT;
+  if (split) {
+    r.c0 = U * cta / grid;
+    r.c1 = U * (cta + 1) / grid;
+  } else {
+    r.c0 = ((long long)r.ntiles * cta / grid) * r.UPT;
+    r.c1 = ((long long)r.ntiles * (cta + 1) / grid) * r.UPT;
+  }
+  return r;
+}
+
+// Position in the ring of shared-memory slots: slot index and how many times
+// the ring has wrapped (the mbarrier phase parity), advanced without divisions.
+struct RingPos {
+  int slot, round;
+  __device__ __forceinline__ void next(int ns) {
+    if (++slot == ns) {
+      slot = 0;
+      ++round;
+    }
+  }
+};
+
+// CTA whose stream-K range holds unit x.
+__device__ __forceinline__ int split_owner(long long x, long long U, int grid) {
+  int c = (int)((x * grid) / U);
+  while (c + 1 < grid && (U * (c + 1)) / grid <= x) ++c;
+  while (c > 0 && (U * c) / grid > x) --c;
+  return c;
+}
+
+// Timeline of a profiled step: tl[p] = first start of phase p over CTAs,
+// tl[nph + p] = last end.
+__device__ __forceinline__ void tl_mark(unsigned long long* tl, int nph, int p, int which) {
+  if (!tl) return;
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  if (which == 0)
+    atomicMin(tl + p, t);
+  else
+    atomicMax(tl + nph + p, t);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_constant__ StepArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ __align__(8) uint64_t full[kMaxSlots], empty[kMaxSlots], xbar, rfull[2], rempty[2];
+  __shared__ __align__(16) PhaseDesc cdesc;  // consumers' copy of the current phase
+  __shared__ __align__(16) PhaseDesc rdesc;  // reducer's copy
+  __shared__ float s_col[8][3];
+  __shared__ float s_rs[8];
+  __shared__ float s_freq[64];
+  __shared__ volatile int s_e;    // exit layer as far as this CTA knows it
+  __shared__ volatile int s_dec;  // last layer whose exit decision this CTA has taken
+  __shared__ volatile int s_abort;
+  __shared__ int s_pos, s_last, s_tick;
+  __shared__ float qs[kMaxRep][kMaxHD];
+  __shared__ float ps[kMaxRep][128];
+  __shared__ float ared[kMaxRep][NC];
+  __shared__ float mstat[kMaxRep][2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int grid = gridDim.x, cta = blockIdx.x;
+  const int B = a.B, NS = a.nslot, RSX = a.xs_row_bytes;
+  unsigned char* ring = smem;
+  unsigned char* xs = smem + (size_t)NS * SLOT_B;
+  float* xsum = reinterpret_cast<float*>(xs + (size_t)B * RSX);
+  float4* red = reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(xsum) +
+                                          ((((size_t)B * a.gmax * 4) + 15) & ~(size_t)15));
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], NC);
+    }
+    mbar_init(&xbar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&rfull[i], NC);
+      mbar_init(&rempty[i], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_abort = 0;
+    s_pos = a.st->pos;
+    int e = a.L;
+    if (a.mode == RL_EXIT_FORCED) {
+      e = a.schedule[a.st->step % a.schedule_len];
+      e = e < 0 ? 0 : (e > a.L ? a.L : e);
+    }
+    s_e = e;
+    s_dec = 0;
+  }
+  if (tid < 8) s_rs[tid] = 1.f;
+  if (tid < 64) s_freq[tid] = tid < a.hd / 2 ? a.inv_freq[tid] : 0.f;
+  __syncthreads();
+
+  if (warp == WP) {
+    // ================================ producer ===================================
+    if (lane == 0) {
+      RingPos rp{0, 0};
+      int issued = 0;
+      int e_known = s_e;
+      auto take_slot = [&]() -> bool {
+        if (rp.round == 0) return true;
+        if (s_abort) return false;
+        if (!mbar_wait(&empty[rp.slot], (uint32_t)((rp.round - 1) & 1), kSpin)) {
+          atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+          s_abort = 1;
+          return false;
+        }
+        return true;
+      };
+      for (int p = 0; p < a.nph && !s_abort; ++p) {
+        const PhaseDesc* D = a.ph + p;
+        if (D->kind == PH_GEMV) {
+          const int layer_no = D->layer_no;
+          const unsigned char* qwt = D->qwt;
+          const bf16* wt = D->wt;
+          const int N = D->N, Kp = D->Kp, split = D->split;
+          bool w4 = false;
+          if (qwt && layer_no > 0) {
+            if (a.mode == RL_EXIT_TAU && e_known >= a.L && layer_no >= 2) {
+              // the weight path of this layer waits for the exit decision of the previous one
+              long long i = 0;
+              while (s_dec < layer_no - 1 && !s_abort && i < kSpinBar) {
+                __nanosleep(64);
+                ++i;
+              }
+              if (s_dec < layer_no - 1) {
+                if (!s_abort) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+                s_abort = 1;
+                break;
+              }
+              e_known = s_e;
+            }
+            w4 = layer_no > e_known;
+          }
+          const GRange r = gemv_range(N, Kp, split, cta, grid);
+          if (w4) {
+            for (long long u = r.c0; u < r.c1; u += W4U) {
+              if (!take_slot()) break;
+              const int ns = (int)min((long long)W4U, r.c1 - u);
+              const int slot = rp.slot;
+              mbar_expect_tx(&full[slot], (uint32_t)(ns * STAGE_W));
+              bulk_g2s(ring + (size_t)slot * SLOT_B, qwt + (size_t)u * STAGE_W, (uint32_t)(ns * STAGE_W),
+                       &full[slot]);
+              rp.next(NS);
+              ++issued;
+            }
+          } else {
+            int tl = (int)(r.c0 / r.UPT), uk = (int)(r.c0 % r.UPT);
+            for (long long u = r.c0; u < r.c1; ++u) {
+              if (!take_slot()) break;
+              const int k0 = uk * KU, kn = min(KU, Kp - k0);
+              const int slot = rp.slot;
+              const uint32_t bytes = (uint32_t)(16 * kn * 2);
+              mbar_expect_tx(&full[slot], bytes);
+              bulk_g2s(ring + (size_t)slot * SLOT_B, wt + (size_t)tl * 16 * Kp + (size_t)16 * k0, bytes,
+                       &full[slot]);
+              rp.next(NS);
+              ++issued;
+              if (++uk == r.UPT) {
+                uk = 0;
+                ++tl;
+              }
+            }
+          }
+        } else {
+          // attention: K and V rows below this step's position; a chunk of up
+          // to 128 positions takes one slot (head_dim 64: K, then V at 16 KB)
+          // or two (head_dim 128: K in the first, V in the second)
+          const int pos = s_pos, hd = a.hd, Hkv = a.Hkv;
+          const int ctx = min(pos + 1, a.Tmax);
+          const int nch = step_attn_chunks(ctx, B, Hkv, hd, grid, a.part_cap);
+          const int clen = (ctx + nch - 1) / nch;
+          const int nitems = B * Hkv * nch;
+          const bool two = hd * 2 * kCHP > kAttnHalf;
+          const bf16* kc = D->kc;
+          const bf16* vc = D->vc;
+          for (int it = cta; it < nitems && !s_abort; it += grid) {
+            const int b = it / (Hkv * nch), rr = it % (Hkv * nch), hk = rr / nch, ch = rr % nch;
+            const int start = ch * clen, end = min(start + clen, ctx);
+            const int npre = min(kCHP, max(0, min(end, pos) - start));
+            const uint32_t bytes = (uint32_t)(npre * hd * 2);
+            const size_t off = (((size_t)b * Hkv + hk) * a.Tmax + start) * hd;
+            if (!take_slot()) break;
+            const int sk = rp.slot;
+            rp.next(NS);
+            ++issued;
+            if (!two) {
+              mbar_expect_tx(&full[sk], 2 * bytes);
+              if (bytes) {
+                bulk_g2s(ring + (size_t)sk * SLOT_B, kc + off, bytes, &full[sk]);
+                bulk_g2s(ring + (size_t)sk * SLOT_B + kAttnHalf, vc + off, bytes, &full[sk]);
+              }
+            } else {
+              mbar_expect_tx(&full[sk], bytes);
+              if (bytes) bulk_g2s(ring + (size_t)sk * SLOT_B, kc + off, bytes, &full[sk]);
+              if (!take_slot()) break;
+              const int sv = rp.slot;
+              rp.next(NS);
+              ++issued;
+              mbar_expect_tx(&full[sv], bytes);
+              if (bytes) bulk_g2s(ring + (size_t)sv * SLOT_B, vc + off, bytes, &full[sv]);
+            }
+          }
+        }
+      }
+      // never leave with copies in flight: wait for the last NS issued units
+      if (s_abort)
+        for (int u = issued - NS < 0 ? 0 : issued - NS; u < issued; ++u)
+          mbar_wait(&full[u % NS], (uint32_t)((u / NS) & 1), kSpin);
+    }
+  } else if (warp < NC) {
+    // ================================ consumers ==================================
+    const int ct = tid;
+    RingPos rc{0, 0};
+    int tcount = 0;
+    uint32_t xpar = 0;
+    for (int p = 0; p < a.nph; ++p) {
+      {
+        const int* src = reinterpret_cast<const int*>(a.ph + p);
+        int* dst = reinterpret_cast<int*>(&cdesc);
+        for (int i = ct; i < (int)(sizeof(PhaseDesc) / 4); i += NC * 32) dst[i] = __ldg(src + i);
+      }
+      if (p > 0 && ct == 0 && !s_abort) {
+        // every CTA has finished phase p - 1
+        const unsigned* bp = a.bars + (p - 1);
+        long long i = 0;
+        while (ld_acquire(bp) < (unsigned)grid && i < kSpinBar) {
+          __nanosleep(20);
+          ++i;
+        }
+        if (i >= kSpinBar) {
+          atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+          s_abort = 1;
+        }
+        __threadfence();
+        fence_proxy_async();
+      }
+      named_sync(kBarCons, NC * 32);
+      if (ct == 0) tl_mark(a.tl, a.nph, p, 0);
+      const PhaseDesc& D = cdesc;
+
+      if (D.kind == PH_GEMV) {
+        const int Kp = D.Kp, G = Kp >> 7;
+        const GRange r = gemv_range(D.N, Kp, D.split, cta, grid);
+        const bool scaled = D.xmode != X_COPY;
+        // ---- activation rows ----
+        if (D.xmode != X_EMBED && ct == 0 && !s_abort) {
+          mbar_expect_tx(&xbar, (uint32_t)B * Kp * 2);
+          for (int b = 0; b < B; ++b)
+            bulk_g2s(xs + (size_t)b * RSX, D.xg + (size_t)b * D.ldxg, (uint32_t)Kp * 2, &xbar);
+        }
+        if (D.xmode == X_SCALED) {
+          if (warp < B) {  // warp b sums the per-tile partials of column b
+            // all partials in one round of loads (up to 512 tiles, d_model <= 8192)
+            float acc[3] = {0.f, 0.f, 0.f};
+            for (int t0 = 0; t0 < D.stats_tiles; t0 += 32 * 16) {
+              float v[16][3];
+#pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                const int tt = t0 + q * 32 + lane;
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                  v[q][j] = (tt < D.stats_tiles && j < D.stats_k)
+                                ? __ldcg(D.stats_in + ((size_t)tt * 8 + warp) * D.stats_k + j)
+                                : 0.f;
+              }
+#pragma unroll
+              for (int q = 0; q < 16; ++q)
+#pragma unroll
+                for (int j = 0; j < 3; ++j) acc[j] += v[q][j];
+            }
+#pragma unroll
+            for (int j = 0; j < 3; ++j) acc[j] = warp_sum(acc[j]);
+            if (lane == 0) {
+              s_col[warp][0] = acc[0];
+              s_col[warp][1] = acc[1];
+              s_col[warp][2] = acc[2];
+            }
+          }
+        } else if (D.xmode == X_EMBED) {
+          // gather the token rows; x' = bf16(e * gain) into shared memory
+          const int d = a.d, nchk = d >> 3;
+          for (int b = 0; b < B; ++b) {
+            const int tok_raw = a.tokens[b];
+            const int tok = (tok_raw < 0 || tok_raw >= a.vocab) ? 0 : tok_raw;
+            if (cta == 0 && ct == 0 && (tok_raw < 0 || tok_raw >= a.vocab))
+              atomicOr(&a.st->err, RL_DEVERR_TOKEN);
+            float ss = 0.f;
+            constexpr int PER = 4;
+            for (int q0 = 0; q0 < nchk; q0 += NC * 32 * PER) {
+              uint4 e[PER];
+              float4 g0[PER], g1[PER];
+#pragma unroll
+              for (int q = 0; q < PER; ++q) {
+                const int ch = q0 + q * NC * 32 + ct;
+                if (ch < nchk) {
+                  e[q] = *reinterpret_cast<const uint4*>(a.embed + (size_t)tok * d + ch * 8);
+                  g0[q] = *reinterpret_cast<const float4*>(a.gain_embed + ch * 8);
+                  g1[q] = *reinterpret_cast<const float4*>(a.gain_embed + ch * 8 + 4);
+                }
+              }
+#pragma unroll
+              for (int q = 0; q < PER; ++q) {
+                const int ch = q0 + q * NC * 32 + ct;
+                if (ch >= nchk) continue;
+                const __nv_bfloat162* ev = reinterpret_cast<const __nv_bfloat162*>(&e[q]);
+                const float gg[8] = {g0[q].x, g0[q].y, g0[q].z, g0[q].w,
+                                     g1[q].x, g1[q].y, g1[q].z, g1[q].w};
+                float hv[8];
+                uint32_t xw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 f = __bfloat1622float2(ev[i]);
+                  hv[2 * i] = f.x;
+                  hv[2 * i + 1] = f.y;
+                  ss += f.x * f.x + f.y * f.y;
+                  const __nv_bfloat162 xb = __floats2bfloat162_rn(f.x * gg[2 * i], f.y * gg[2 * i + 1]);
+                  xw[i] = *reinterpret_cast<const uint32_t*>(&xb);
+                }
+                *reinterpret_cast<uint4*>(xs + (size_t)b * RSX + ch * 16) =
+                    make_uint4(xw[0], xw[1], xw[2], xw[3]);
+                if (cta == 0) {
+                  float* hs = a.h_store + (size_t)b * d + ch * 8;
+                  *reinterpret_cast<float4*>(hs) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                  *reinterpret_cast<float4*>(hs + 4) = make_float4(hv[4], hv[5], hv[6], hv[7]);
+                  if (D.trace) {
+                    float* tr = D.trace + ((size_t)D.trace_layer * a.trace_maxB + b) * d + ch * 8;
+                    *reinterpret_cast<float4*>(tr) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+                    *reinterpret_cast<float4*>(tr + 4) = make_float4(hv[4], hv[5], hv[6], hv[7]);
+                  }
+                }
+              }
+            }
+            for (int k = d + ct; k < Kp; k += NC * 32)
+              reinterpret_cast<bf16*>(xs + (size_t)b * RSX)[k] = __float2bfloat16_rn(0.f);
+            ss = warp_sum(ss);
+            if (lane == 0) red[warp * 32 + b] = make_float4(ss, 0.f, 0.f, 0.f);
+          }
+          named_sync(kBarCons, NC * 32);
+          if (ct < B) {
+            float sum = 0.f;
+            for (int w = 0; w < NC; ++w) sum += red[w * 32 + ct].x;
+            s_col[ct][0] = sum;
+          }
+        }
+        named_sync(kBarCons, NC * 32);
+        if (ct == 0) {
+          if (D.xmode == X_EMBED) {  // step begin
+            if (a.mode == RL_EXIT_FORCED && cta == 0) {
+              const int raw = a.schedule[a.st->step % a.schedule_len];
+              if (raw < 0 || raw > a.L) atomicOr(&a.st->err, RL_DEVERR_SCHEDULE);
+            }
+            if (cta == 0) a.st->exit_layer = s_e;
+          }
+          if (D.xmode == X_SCALED && D.dec_layer > 0 && D.stats_k == 3) {
+            float m = FLT_MAX;
+            for (int b = 0; b < B; ++b) {
+              const float ss = s_col[b][0], dot = s_col[b][1], ssp = s_col[b][2];
+              m = fminf(m, dot / fmaxf(sqrtf(ssp) * sqrtf(ss), 1e-12f));
+            }
+            int e = s_e;
+            if (a.mode == RL_EXIT_TAU && e == a.L && D.dec_layer < a.L && m > a.tau) e = D.dec_layer;
+            s_e = e;
+            if (cta == 0) {
+              if (a.min_cos_out) a.min_cos_out[D.dec_layer - 1] = m;
+              a.st->exit_layer = e;
+            }
+            __threadfence_block();
+            s_dec = D.dec_layer;
+          }
+          if (scaled)
+            for (int b = 0; b < B; ++b) s_rs[b] = 1.f / sqrtf(s_col[b][0] / (float)a.d + a.eps);
+        }
+        named_sync(kBarCons, NC * 32);
+        const bool w4 = D.qwt && D.layer_no > 0 && D.layer_no > s_e;
+        if (D.xmode != X_EMBED) {
+          if (!s_abort && !mbar_wait(&xbar, xpar, kSpin)) {
+            if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+            s_abort = 1;
+          }
+          xpar ^= 1u;
+        }
+        if (w4) {  // per-group sums of the bf16 activations
+          for (int gw = warp; gw < B * G; gw += NC) {
+            const int b = gw / G, gi = gw % G;
+            const uint2 v = *reinterpret_cast<const uint2*>(xs + (size_t)b * RSX + (gi * 128 + 4 * lane) * 2);
+            const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+            const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+            const float s2 = warp_sum((f0.x + f0.y) + (f1.x + f1.y));
+            if (lane == 0) xsum[b * G + gi] = s2;
+          }
+          named_sync(kBarCons, NC * 32);
+        }
+        float y[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) y[j][i] = 0.f;
+        // MMA column g reads activation row min(g, B-1); columns >= B are dropped
+        const unsigned char* xrow = xs + (size_t)(g < B ? g : B - 1) * RSX;
+        auto hand_off = [&]() {
+          const int buf = tcount & 1;
+          if (tcount >= 2 && !s_abort && !mbar_wait(&rempty[buf], (uint32_t)(((tcount >> 1) - 1) & 1), kSpin))
+            s_abort = 1;
+          float4 v;
+          v.x = (y[0][0] + y[1][0]) + (y[2][0] + y[3][0]);
+          v.y = (y[0][1] + y[1][1]) + (y[2][1] + y[3][1]);
+          v.z = (y[0][2] + y[1][2]) + (y[2][2] + y[3][2]);
+          v.w = (y[0][3] + y[1][3]) + (y[2][3] + y[3][3]);
+          red[(buf * NC + warp) * 32 + lane] = v;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) y[j][q] = 0.f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&rfull[buf]);
+          ++tcount;
+        };
+        const int UPT = r.UPT;
+        const int step_u = w4 ? W4U : 1;
+        const int nsub = (int)(r.c1 - r.c0);
+        int uk = (int)(r.c0 % UPT);
+        for (int i0 = 0; i0 < nsub; i0 += step_u) {
+          const int slot = rc.slot;
+          bool ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
+          if (!ok && s_abort == 0) {
+            if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+            s_abort = 1;
+          }
+          const unsigned char* sb = ring + (size_t)slot * SLOT_B;
+          const int ns = min(step_u, nsub - i0);
+          for (int s = 0; s < ns; ++s) {
+            const int gi = uk * 8 + warp;  // this warp's group
+            if (ok && gi < G) {
+              if (w4) {
+                // Lane t's word m holds the eight nibbles of input chunk 4m + t of
+                // the group; odd rows have their 64-byte halves swapped.
+                const unsigned char* st = sb + (size_t)s * STAGE_W;
+                const int cw = warp * 4 + t;
+                const uint4 wa = *reinterpret_cast<const uint4*>(st + g * 512 + ((cw ^ ((g & 1) << 2)) * 16));
+                const uint4 wb = *reinterpret_cast<const uint4*>(st + (g + 8) * 512 +
+                                                                 ((cw ^ (((g + 8) & 1) << 2)) * 16));
+                const uint32_t* szs = reinterpret_cast<const uint32_t*>(st + 16 * 512);
+                const uint32_t s0 = szs[g * 8 + (warp ^ (g >> 2))];
+                const uint32_t s1 = szs[(g + 8) * 8 + (warp ^ ((g + 8) >> 2))];
+                float acc[4][4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+#pragma unroll
+                  for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                  const uint32_t va = u4get(wa, m), vb = u4get(wb, m);
+                  const uint4 X = *reinterpret_cast<const uint4*>(xrow + (gi * 128 + 32 * m + 8 * t) * 2);
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    const uint32_t A0 = ((va >> (4 * h)) & 0x000F000Fu) | 0x43004300u;
+                    const uint32_t A1 = ((vb >> (4 * h)) & 0x000F000Fu) | 0x43004300u;
+                    const uint32_t A2 = ((va >> (4 * h + 8)) & 0x000F000Fu) | 0x43004300u;
+                    const uint32_t A3 = ((vb >> (4 * h + 8)) & 0x000F000Fu) | 0x43004300u;
+                    const uint32_t sel = h ? 0x7632u : 0x5410u;
+                    mma_bf16(acc[m], A0, A1, A2, A3, __byte_perm(X.x, X.z, sel), __byte_perm(X.y, X.w, sel));
+                  }
+                }
+                __half2 h0, h1;
+                *reinterpret_cast<uint32_t*>(&h0) = s0;
+                *reinterpret_cast<uint32_t*>(&h1) = s1;
+                const float2 sz0 = __half22float2(h0), sz1 = __half22float2(h1);
+                const float xs0 = 2 * t < B ? xsum[(2 * t) * G + gi] : 0.f;
+                const float xs1 = 2 * t + 1 < B ? xsum[(2 * t + 1) * G + gi] : 0.f;
+                const float o0 = 128.f + sz0.y, o1 = 128.f + sz1.y;
+                const float a0 = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
+                const float a1 = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
+                const float a2 = (acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2]);
+                const float a3 = (acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3]);
+                y[0][0] += sz0.x * (a0 - o0 * xs0);
+                y[0][1] += sz0.x * (a1 - o0 * xs1);
+                y[0][2] += sz1.x * (a2 - o1 * xs0);
+                y[0][3] += sz1.x * (a3 - o1 * xs1);
+              } else {
+                // bf16 unit: 16 rows of kn inputs; 16-byte chunk c of row r at
+                // c ^ 4 (r & 1): the 8 lanes of a quarter warp (rows 2q, 2q+1,
+                // chunks c0..c0+3) hit 8 different 16-byte bank groups
+                const int k0 = uk * KU, kn = min(KU, Kp - k0), RS = kn * 2;
+                const int sw = (g & 1) << 2;
+#pragma unroll
+                for (int i4 = 0; i4 < 4; ++i4) {
+                  const int cb = warp * 16 + 4 * i4 + t;
+                  const uint4 wa = *reinterpret_cast<const uint4*>(sb + g * RS + ((cb ^ sw) << 4));
+                  const uint4 wb = *reinterpret_cast<const uint4*>(sb + (g + 8) * RS + ((cb ^ sw) << 4));
+                  const uint4 X = *reinterpret_cast<const uint4*>(xrow + (k0 + cb * 8) * 2);
+#pragma unroll
+                  for (int e = 0; e < 2; ++e)
+                    mma_bf16(y[i4], u4get(wa, 2 * e), u4get(wb, 2 * e), u4get(wa, 2 * e + 1),
+                             u4get(wb, 2 * e + 1), u4get(X, 2 * e), u4get(X, 2 * e + 1));
+                }
+              }
+            }
+            if (uk + 1 == UPT || i0 + s + 1 == nsub) hand_off();
+            if (++uk == UPT) uk = 0;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+          rc.next(NS);
+        }
+      } else {
+        // ---- attention over this CTA's chunks --------------------------------------
+        const int pos = s_pos, hd = a.hd, Hkv = a.Hkv, Hq = a.Hq, rep = Hq / Hkv;
+        const int ctx = min(pos + 1, a.Tmax);
+        const int nch = step_attn_chunks(ctx, B, Hkv, hd, grid, a.part_cap);
+        const int clen = (ctx + nch - 1) / nch;
+        const int CH = kCHP;
+        const int nitems = B * Hkv * nch;
+        const bool two = hd * 2 * kCHP > kAttnHalf;
+        const int RK = hd * 2;  // K/V row bytes
+        const int hd8 = hd >> 3;
+        const float scale = rsqrtf((float)hd);
+        const int j = ct & 127, hh = ct >> 7;
+        if (clen > CH && cta == 0 && ct == 0) atomicOr(&a.st->err, RL_DEVERR_CAPACITY);
+        for (int it = cta; it < nitems; it += grid) {
+          const int b = it / (Hkv * nch), rr = it % (Hkv * nch), hk = rr / nch, ch = rr % nch;
+          const int start = ch * clen, end = min(start + clen, ctx);
+          const int n = min(CH, max(0, end - start));
+          const int slot = rc.slot;
+          bool ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
+          rc.next(NS);
+          int slot_v = slot;
+          if (two) {
+            slot_v = rc.slot;
+            ok = ok && mbar_wait(&full[slot_v], (uint32_t)(rc.round & 1), kSpin);
+            rc.next(NS);
+          }
+          if (!ok && s_abort == 0) {
+            if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+            s_abort = 1;
+          }
+          unsigned char* Ks = ring + (size_t)slot * SLOT_B;
+          unsigned char* Vs = two ? ring + (size_t)slot_v * SLOT_B : Ks + kAttnHalf;
+          const size_t head_base = ((size_t)b * Hkv + hk) * a.Tmax;
+          if (ok && pos >= start && pos < start + n && ct < hd8) {
+            // the row written by this step's QKV phase
+            const int rw = pos - start;
+            const uint4 kv = __ldcg(reinterpret_cast<const uint4*>(D.kc + (head_base + pos) * hd) + ct);
+            const uint4 vv = __ldcg(reinterpret_cast<const uint4*>(D.vc + (head_base + pos) * hd) + ct);
+            *reinterpret_cast<uint4*>(Ks + rw * RK + ct * 16) = kv;
+            *reinterpret_cast<uint4*>(Vs + rw * RK + ct * 16) = vv;
+          }
+          for (int i = ct; i < rep * hd; i += NC * 32)
+            qs[i / hd][i % hd] = __ldcg(D.q_out + (size_t)b * Hq * hd + (size_t)hk * rep * hd + i) * scale;
+          named_sync(kBarCons, NC * 32);
+          // scores: thread (j, hh) -> position j, heads hh, hh + 2, ...
+          float sc[kMaxRep / 2];
+#pragma unroll
+          for (int i = 0; i < kMaxRep / 2; ++i) sc[i] = -FLT_MAX;
+          if (ok && j < n) {
+#pragma unroll
+            for (int i = 0; i < kMaxRep / 2; ++i) sc[i] = 0.f;
+            for (int v = 0; v < hd8; ++v) {
+              const int c = (v + j) & (hd8 - 1);  // rotate chunks: conflict-free rows
+              const uint4 w = *reinterpret_cast<const uint4*>(Ks + j * RK + c * 16);
+              const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&w);
+              float kf[8];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float2 f = __bfloat1622float2(e[q]);
+                kf[2 * q] = f.x;
+                kf[2 * q + 1] = f.y;
+              }
+#pragma unroll
+              for (int i = 0; i < kMaxRep / 2; ++i) {
+                const int h = hh + 2 * i;
+                if (h < rep) {
+                  const float4 q0 = *reinterpret_cast<const float4*>(&qs[h][8 * c]);
+                  const float4 q1 = *reinterpret_cast<const float4*>(&qs[h][8 * c + 4]);
+                  sc[i] += kf[0] * q0.x + kf[1] * q0.y + kf[2] * q0.z + kf[3] * q0.w +
+                           kf[4] * q1.x + kf[5] * q1.y + kf[6] * q1.z + kf[7] * q1.w;
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kMaxRep / 2; ++i) {
+            const int h = hh + 2 * i;
+            if (h < rep) {
+              const float v = warp_max(sc[i]);
+              if (lane == 0) ared[h][warp] = v;
+            }
+          }
+          named_sync(kBarCons, NC * 32);
+          if (ct < rep) {
+            const int w0 = (ct & 1) * 4;
+            float mx = ared[ct][w0];
+            for (int w = 1; w < 4; ++w) mx = fmaxf(mx, ared[ct][w0 + w]);
+            mstat[ct][0] = mx;
+          }
+          named_sync(kBarCons, NC * 32);
+#pragma unroll
+          for (int i = 0; i < kMaxRep / 2; ++i) {
+            const int h = hh + 2 * i;
+            if (h < rep) {
+              const float pv = (ok && j < n) ? __expf(sc[i] - mstat[h][0]) : 0.f;
+              ps[h][j] = pv;
+              const float v = warp_sum(pv);
+              if (lane == 0) ared[h][warp] = v;
+            }
+          }
+          named_sync(kBarCons, NC * 32);
+          if (ct < rep) {
+            const int w0 = (ct & 1) * 4;
+            float l = 0.f;
+            for (int w = 0; w < 4; ++w) l += ared[ct][w0 + w];
+            mstat[ct][1] = l;
+          }
+          // P V: thread owns (head, dim pair) slots
+          const int nslots = rep * hd / 2;
+          float* part = a.part + ((size_t)b * Hq + (size_t)hk * rep) * a.part_cap * (hd + 2);
+          for (int s2 = ct; s2 < nslots; s2 += NC * 32) {
+            const int h = s2 / (hd / 2), dp = s2 % (hd / 2);
+            float2 acc[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+            if (ok) {
+              int jj = 0;
+              for (; jj + 4 <= n; jj += 4) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const float pj = ps[h][jj + q];
+                  const float2 v =
+                      __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Vs + (jj + q) * RK + dp * 4));
+                  acc[q].x += pj * v.x;
+                  acc[q].y += pj * v.y;
+                }
+              }
+              for (; jj < n; ++jj) {
+                const float pj = ps[h][jj];
+                const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Vs + jj * RK + dp * 4));
+                acc[0].x += pj * v.x;
+                acc[0].y += pj * v.y;
+              }
+            }
+            float* pp = part + ((size_t)h * a.part_cap + ch) * (hd + 2);
+            pp[2 * dp] = (acc[0].x + acc[1].x) + (acc[2].x + acc[3].x);
+            pp[2 * dp + 1] = (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y);
+          }
+          if (ct < rep) {
+            float* pp = part + ((size_t)ct * a.part_cap + ch) * (hd + 2);
+            pp[hd] = n > 0 ? mstat[ct][0] : -FLT_MAX;
+            pp[hd + 1] = n > 0 ? mstat[ct][1] : 0.f;
+          }
+          named_sync(kBarCons, NC * 32);
+          if (ct == 0) {
+            // release every thread's partial writes (ordered before by the barrier)
+            __threadfence();
+            s_tick = !s_abort && atomicAdd(&a.attn_ticket[(size_t)b * Hkv + hk], 1u) == (unsigned)(nch - 1);
+            if (s_tick) __threadfence();
+          }
+          named_sync(kBarCons, NC * 32);
+          if (s_tick) {
+            // ---- merge: last CTA of this (sequence, KV head); slot memory as scratch ----
+            float2* ml = reinterpret_cast<float2*>(Ks);                 // [rep][nch]
+            float* wc = reinterpret_cast<float*>(Ks) + 2 * rep * nch;   // [rep][nch]
+            for (int i = ct; i < rep * nch; i += NC * 32) {
+              const int h = i / nch, cc = i % nch;
+              const float* pp = part + ((size_t)h * a.part_cap + cc) * (hd + 2);
+              ml[i] = make_float2(__ldcg(pp + hd), __ldcg(pp + hd + 1));
+            }
+            named_sync(kBarCons, NC * 32);
+            if (ct < rep) {
+              float M = -FLT_MAX, den = 0.f;
+              for (int cc = 0; cc < nch; ++cc)
+                if (ml[ct * nch + cc].y > 0.f) M = fmaxf(M, ml[ct * nch + cc].x);
+              for (int cc = 0; cc < nch; ++cc) {
+                const float2 v = ml[ct * nch + cc];
+                const float w = v.y > 0.f ? __expf(v.x - M) : 0.f;
+                wc[ct * nch + cc] = w;
+                den += w * v.y;
+              }
+              const float inv = den > 0.f ? 1.f / den : 0.f;
+              for (int cc = 0; cc < nch; ++cc) wc[ct * nch + cc] *= inv;
+            }
+            named_sync(kBarCons, NC * 32);
+            // every thread owns up to MO outputs and loads CB chunks of all of
+            // them per round: few dependent round trips to L2
+            constexpr int MO = kMaxRep * kMaxHD / (NC * 32), CB = 8;
+            const int nout = rep * hd;
+            float num[MO];
+#pragma unroll
+            for (int o = 0; o < MO; ++o) num[o] = 0.f;
+            for (int c0 = 0; c0 < nch; c0 += CB) {
+              float v[MO][CB];
+#pragma unroll
+              for (int o = 0; o < MO; ++o) {
+                const int i = ct + o * NC * 32;
+                const int h = i / hd, dd = i % hd;
+                const float* pp = part + (size_t)h * a.part_cap * (hd + 2) + dd;
+#pragma unroll
+                for (int q = 0; q < CB; ++q)
+                  v[o][q] = (i < nout && c0 + q < nch) ? __ldcg(pp + (size_t)(c0 + q) * (hd + 2)) : 0.f;
+              }
+#pragma unroll
+              for (int o = 0; o < MO; ++o) {
+                const int i = ct + o * NC * 32;
+                const int h = i < nout ? i / hd : 0;
+#pragma unroll
+                for (int q = 0; q < CB; ++q)
+                  if (c0 + q < nch) num[o] += wc[h * nch + c0 + q] * v[o][q];
+              }
+            }
+#pragma unroll
+            for (int o = 0; o < MO; ++o) {
+              const int i = ct + o * NC * 32;
+              if (i < nout) {
+                const int h = i / hd, dd = i % hd;
+                D.o_out[(size_t)b * D.ldo_attn + (size_t)(hk * rep + h) * hd + dd] = __float2bfloat16_rn(num[o]);
+              }
+            }
+            if (ct == 0) a.attn_ticket[(size_t)b * Hkv + hk] = 0u;
+          }
+          named_sync(kBarCons, NC * 32);
+          if (lane == 0) {
+            mbar_arrive(&empty[slot]);
+            if (two) mbar_arrive(&empty[slot_v]);
+          }
+        }
+      }
+      // ---- end of phase: this CTA's writes are done; arrive ----
+      named_sync(kBarPhase, (NC + 1) * 32);
+      if (ct == 0) {
+        tl_mark(a.tl, a.nph, p, 1);
+        if (p + 1 < a.nph) {
+          __threadfence();
+          red_release_add(a.bars + p, 1u);
+        }
+      }
+    }
+  } else {
+    // ================================ reducer ====================================
+    // Lane l holds tile values (r, c) = (l/8 + 4k, l%8), k = 0..3.
+    const int c = lane & 7, rb = lane >> 3;
+    int tc_run = 0;
+    float amv = -FLT_MAX;
+    int ami = 0x7fffffff;
+    bool lm = false;
+    for (int p = 0; p < a.nph; ++p) {
+      {
+        const int* src = reinterpret_cast<const int*>(a.ph + p);
+        int* dst = reinterpret_cast<int*>(&rdesc);
+        for (int i = lane; i < (int)(sizeof(PhaseDesc) / 4); i += 32) dst[i] = __ldg(src + i);
+        __syncwarp();
+      }
+      const PhaseDesc& D = rdesc;
+      if (D.kind == PH_GEMV && !s_abort) {
+        const GRange r = gemv_range(D.N, D.Kp, D.split, cta, grid);
+        const int UPT = r.UPT;
+        const long long U = (long long)r.ntiles * UPT;
+        const int first_tile = (int)(r.c0 / UPT);
+        const int ntl = r.c1 > r.c0 ? (int)((r.c1 - 1) / UPT) - first_tile + 1 : 0;
+        if (D.epi == EPI_LMHEAD) lm = true;
+        for (int tc = 0; tc < ntl; ++tc) {
+          const int tl = first_tile + tc;
+          const int buf = tc_run & 1;
+          float res[4] = {0.f, 0.f, 0.f, 0.f}, hin[4] = {0.f, 0.f, 0.f, 0.f}, gn[4] = {0.f, 0.f, 0.f, 0.f};
+          if (D.epi == EPI_RESID && c < B) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int n = tl * 16 + rb + 4 * k;
+              res[k] = __ldcg(D.resid + (size_t)c * D.ldr + n);
+              if (D.h_in) hin[k] = __ldcg(D.h_in + (size_t)c * a.d + n);
+              if (D.gnext) gn[k] = D.gnext[n];
+            }
+          }
+          if (s_abort || !mbar_wait(&rfull[buf], (uint32_t)((tc_run >> 1) & 1), kSpin)) {
+            if (!s_abort && lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+            s_abort = 1;
+            break;
+          }
+          float tv[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = rb + 4 * k;
+            const int ln = (rr & 7) * 4 + (c >> 1);
+            const int comp = (rr >= 8 ? 2 : 0) + (c & 1);
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < NC; ++w) sum += f4get(red[(buf * NC + w) * 32 + ln], comp);
+            tv[k] = sum;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&rempty[buf]);
+          ++tc_run;
+          // tile split between CTAs: the last to arrive completes it
+          const long long tc0 = (long long)tl * UPT, tc1 = tc0 + UPT;
+          if (tc0 < r.c0 || tc1 > r.c1) {
+            const int slot = tl == first_tile ? 0 : 1;
+            float* wsp = a.ws + ((size_t)cta * 2 + slot) * 128;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) wsp[lane + 32 * k] = tv[k];
+            __threadfence();
+            __syncwarp();
+            const int oa = split_owner(tc0, U, grid), ob = split_owner(tc1 - 1, U, grid);
+            unsigned int last = 0;
+            if (lane == 0) last = atomicAdd(&a.tile_ticket[tl], 1u) == (unsigned int)(ob - oa);
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (!last) continue;
+            __threadfence();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) tv[k] = 0.f;
+            for (int o = oa; o <= ob; ++o) {
+              const int ft = (int)((U * o / grid) / UPT);
+              const float* pp = a.ws + ((size_t)o * 2 + (tl == ft ? 0 : 1)) * 128;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) tv[k] += __ldcg(pp + lane + 32 * k);
+            }
+            if (lane == 0) a.tile_ticket[tl] = 0u;
+          }
+          // ---- epilogue ----
+          if (D.epi == EPI_RESID) {
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+            if (c < B) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int n = tl * 16 + rb + 4 * k;
+                const float v = tv[k] + res[k];
+                D.out[(size_t)c * D.ldo + n] = v;
+                if (D.trace) D.trace[((size_t)D.trace_layer * a.trace_maxB + c) * D.ldo + n] = v;
+                if (D.xnext) D.xnext[(size_t)c * D.ldxnext + n] = __float2bfloat16_rn(v * gn[k]);
+                s0 += v * v;
+                s1 += v * hin[k];
+                s2 += hin[k] * hin[k];
+              }
+            }
+            if (D.stats_out) {
+#pragma unroll
+              for (int o = 8; o < 32; o <<= 1) {
+                s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+              }
+              if (lane < 8 && c < B) {
+                float* so = D.stats_out + ((size_t)tl * 8 + c) * D.stats_k_out;
+                so[0] = s0;
+                if (D.stats_k_out == 3) {
+                  so[1] = s1;
+                  so[2] = s2;
+                }
+              }
+            }
+          } else if (D.epi == EPI_SWIGLU) {
+            if (c < B) {
+              const float rs = s_rs[c];
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const float gv = tv[k] * rs, uv = tv[k + 2] * rs;
+                D.out_h[(size_t)c * D.ldoh + tl * 8 + rb + 4 * k] = __float2bfloat16_rn(silu_f(gv) * uv);
+              }
+            }
+          } else if (D.epi == EPI_QKV_ROPE) {
+            if (c < B) {
+              const int hd = a.hd, half = hd >> 1;
+              const int row0 = tl * 16;
+              const int head_all = row0 / hd;
+              const float rs = s_rs[c];
+              const int pos = s_pos;
+#pragma unroll
+              for (int k = 0; k < 2; ++k) {
+                const int rr = rb + 4 * k;
+                const int dim = 8 * ((row0 % hd) >> 4) + rr;
+                float lo = tv[k] * rs, hi = tv[k + 2] * rs;
+                if (head_all < a.Hq + a.Hkv) {
+                  float sn, cs;
+                  sincosf((float)pos * s_freq[dim], &sn, &cs);
+                  const float nlo = lo * cs - hi * sn, nhi = hi * cs + lo * sn;
+                  lo = nlo;
+                  hi = nhi;
+                }
+                if (head_all < a.Hq) {
+                  float* q = D.q_out + (size_t)c * a.Hq * hd + head_all * hd;
+                  q[dim] = lo;
+                  q[dim + half] = hi;
+                } else if (pos >= 0 && pos < a.Tmax) {
+                  const bool is_k = head_all < a.Hq + a.Hkv;
+                  const int hk = is_k ? head_all - a.Hq : head_all - a.Hq - a.Hkv;
+                  bf16* dst = (is_k ? D.kc : D.vc) + (((size_t)c * a.Hkv + hk) * a.Tmax + pos) * hd;
+                  dst[dim] = __float2bfloat16_rn(lo);
+                  dst[dim + half] = __float2bfloat16_rn(hi);
+                } else if (rr == 0 && c == 0) {
+                  atomicOr(&a.st->err, RL_DEVERR_CAPACITY);
+                }
+              }
+            }
+          } else if (D.epi == EPI_LMHEAD) {
+            if (c < B) {
+              const float rs = s_rs[c];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int n = tl * 16 + rb + 4 * k;
+                const float v = tv[k] * rs;
+                D.out[(size_t)c * D.ldo + n] = v;
+                if (v > amv || (v == amv && n < ami)) {
+                  amv = v;
+                  ami = n;
+                }
+              }
+            }
+          } else {  // EPI_STORE
+            if (c < B)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) D.out[(size_t)c * D.ldo + tl * 16 + rb + 4 * k] = tv[k] * s_rs[c];
+          }
+        }
+      }
+      named_sync(kBarPhase, (NC + 1) * 32);
+    }
+    if (lm) {
+#pragma unroll
+      for (int o = 8; o < 32; o <<= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, amv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, ami, o);
+        if (ov > amv || (ov == amv && oi < ami)) {
+          amv = ov;
+          ami = oi;
+        }
+      }
+      if (lane < 8) {
+        a.am_val[(size_t)cta * 8 + lane] = amv;
+        a.am_idx[(size_t)cta * 8 + lane] = ami;
+      }
+    }
+  }
+
+  // ---- end of step: argmax over CTAs and the state update, by the last CTA ----
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.cta_ticket, 1u) == (unsigned int)(grid - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp < B) {
+    float bv = -FLT_MAX;
+    int bi = 0x7fffffff;
+    for (int o0 = 0; o0 < grid; o0 += 32 * 8) {
+      float v[8];
+      int ix[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int o = o0 + q * 32 + lane;
+        v[q] = o < grid ? __ldcg(a.am_val + (size_t)o * 8 + warp) : -FLT_MAX;
+        ix[q] = o < grid ? __ldcg(a.am_idx + (size_t)o * 8 + warp) : 0x7fffffff;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (v[q] > bv || (v[q] == bv && ix[q] < bi)) {
+          bv = v[q];
+          bi = ix[q];
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if (lane == 0 && a.next_token) a.next_token[warp] = bi == 0x7fffffff ? 0 : bi;
+  }
+  for (int i = tid; i < a.nph; i += kThreads) a.bars[i] = 0u;
+  if (tid == 0) {
+    DevState* st = a.st;
+    if (a.exit_out) a.exit_out[0] = st->exit_layer;
+    st->pos = st->pos + 1;
+    st->step = st->step + 1;
+    *a.cta_ticket = 0u;
+  }
+  __threadfence();
+}
+
+size_t step_smem_bytes(int B, int kmax, int gmax, int* nslot) {
+  const size_t xs = (size_t)B * (kmax * 2 + 64);
+  const size_t xsum = (((size_t)B * gmax * 4) + 15) & ~(size_t)15;
+  const size_t red = (size_t)2 * NC * 32 * 16;
+  const size_t budget = 227 * 1024 - kStaticSmem;
+  const size_t fixed = xs + xsum + red;
+  if (fixed >= budget) return 0;
+  int ns = (int)((budget - fixed) / SLOT_B);
+  if (ns > 6) ns = 6;
+  if (ns < 3) return 0;
+  if (nslot) *nslot = ns;
+  return (size_t)ns * SLOT_B + fixed;
+}
+
+int decode_step_occupancy(size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode_step, kThreads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+void decode_step_setup() {
+  cudaFuncSetAttribute(k_decode_step, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       227 * 1024 - kStaticSmem);
+  cudaFuncSetAttribute(k_decode_step, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       cudaSharedmemCarveoutMaxShared);
+}
+
+cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: they wait on one another
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_decode_step, a);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 weights [N][Kp] -> unit-tiled: for 16-row tile T and 1024-input unit u
+// (kn = min(1024, Kp - 1024u) inputs), 16 rows of kn inputs stored
+// contiguously at T*16*Kp + 16*1024*u elements, 16-byte chunk c of row r at
+// chunk position c ^ (4 * (r & 1)): one bulk copy per unit, conflict-free reads.
+// ---------------------------------------------------------------------------
+__global__ void k_bf16_tile_layout(const bf16* __restrict__ w, int N, int Kp, bf16* __restrict__ out) {
+  const int UPT = (Kp + KU - 1) / KU;
+  const long long blk = blockIdx.x;
+  const int tl = (int)(blk / UPT), uk = (int)(blk % UPT);
+  const int k0 = uk * KU, kn = min(KU, Kp - k0), nch = kn / 8;
+  unsigned char* dst = reinterpret_cast<unsigned char*>(out + (size_t)tl * 16 * Kp + (size_t)16 * k0);
+  for (int idx = threadIdx.x; idx < 16 * nch; idx += blockDim.x) {
+    const int r = idx / nch, c = idx % nch;
+    const uint4 v = *reinterpret_cast<const uint4*>(w + (size_t)(tl * 16 + r) * Kp + k0 + c * 8);
+    *reinterpret_cast<uint4*>(dst + (size_t)r * kn * 2 + ((c ^ ((r & 1) << 2)) * 16)) = v;
+  }
+}
+
+void launch_bf16_tile_layout(const bf16* w, int N, int Kp, bf16* out, cudaStream_t s) {
+  const long long blocks = (long long)(N / 16) * ((Kp + KU - 1) / KU);
+  k_bf16_tile_layout<<<(unsigned)blocks, 256, 0, s>>>(w, N, Kp, out);
+}
+
+}  // namespace river

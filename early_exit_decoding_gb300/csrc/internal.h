@@ -202,6 +202,107 @@ void launch_quantize(const bf16* w, int N, int K, int Kp, uint32_t* qw, __half2*
 
 
 // ---------------------------------------------------------------------------
+// Persistent decode step (B <= 8): one cooperative kernel runs every phase of
+// a decode step -- per layer QKV (+RoPE, KV append, exit decision), attention,
+// O, gate/up, down; then the LM head -- with grid-wide phase barriers.  The
+// weight stream of a CTA runs ahead across phase boundaries: it depends only
+// on the weight path, never on this step's activations.
+// ---------------------------------------------------------------------------
+enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1 };
+
+struct PhaseDesc {
+  int kind;                   // PH_GEMV / PH_ATTN
+  int layer_no;               // 1..L; 0 = LM head (always the bf16 weights)
+  // GEMV weights
+  const bf16* wt;             // bf16 unit-tiled (see k_bf16_tile_layout)
+  const unsigned char* qwt;   // W4 unit-tiled, nullptr if there is no exit-river copy
+  int N, Kp, split;           // split: stream-K partition of the (tile, unit) pairs
+  // activations
+  int xmode;                  // X_COPY / X_SCALED / X_EMBED
+  const bf16* xg;
+  int ldxg;
+  const float* stats_in;
+  int stats_tiles, stats_k;
+  int dec_layer;              // > 0: exit decision of layer dec_layer in the prologue
+  // epilogue
+  int epi;
+  float* out;
+  int ldo;
+  const float* resid;
+  int ldr;
+  bf16* out_h;
+  int ldoh;
+  const float* gnext;
+  bf16* xnext;
+  int ldxnext;
+  float* stats_out;
+  int stats_k_out;
+  const float* h_in;
+  float* trace;
+  int trace_layer;
+  float* q_out;               // QKV output / attention input [B][Hq*hd] fp32
+  bf16* kc;                   // layer's K cache [maxB][Hkv][Tmax][hd]
+  bf16* vc;
+  bf16* o_out;                // attention output [B][ldo_attn] bf16
+  int ldo_attn;
+};
+
+struct StepArgs {
+  const PhaseDesc* ph;
+  int nph;
+  DevState* st;
+  int B, L, d, Hq, Hkv, hd, Tmax, vocab;
+  float eps;
+  int mode;
+  float tau;
+  const int* schedule;
+  int schedule_len;
+  const int* tokens;
+  const bf16* embed;
+  const float* gain_embed;
+  float* h_store;
+  int trace_maxB;
+  const float* inv_freq;
+  float* min_cos_out;
+  int* next_token;
+  int* exit_out;
+  float* am_val;
+  int* am_idx;
+  unsigned* cta_ticket;
+  unsigned* bars;             // [nph] phase arrival counters, zero at step start
+  float* ws;                  // stream-K partial tiles [grid][2][128]
+  unsigned* tile_ticket;      // [max tiles]
+  float* part;                // attention partials [B][Hq][part_cap][hd + 2]
+  unsigned* attn_ticket;      // [B][Hkv]
+  int part_cap;
+  int nslot;                  // weight ring slots
+  int xs_row_bytes;           // activation row stride in shared memory
+  int gmax;                   // max 128-input groups over the phases
+  unsigned long long* tl;     // optional timeline: [nph] first starts, then [nph] last ends
+};
+
+// Shared memory the step kernel needs (0 if it does not fit).
+size_t step_smem_bytes(int B, int kmax, int gmax, int* nslot);
+cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, cudaStream_t s);
+void decode_step_setup();
+int decode_step_occupancy(size_t smem);  // resident CTAs per SM at this shared-memory size
+// Attention chunks per (sequence, KV head) for context `ctx` (identical on host and device).
+__host__ __device__ inline int step_attn_chunks(int ctx, int B, int Hkv, int hd, int grid, int cap) {
+  const int CH = 128;  // positions per chunk
+  const int n_min = (ctx + CH - 1) / CH;
+  const int items = B * Hkv * n_min;
+  const int per = (items + grid - 1) / grid;
+  int n = (per * grid) / (B * Hkv);
+  if (n < n_min) n = n_min;
+  if (n > ctx) n = ctx;
+  if (n > cap) n = cap;
+  if (n < 1) n = 1;
+  return n;
+}
+// bf16 weights [N][Kp] -> the unit-tiled layout of the step kernel.
+void launch_bf16_tile_layout(const bf16* w, int N, int Kp, bf16* out, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // What the allocation-free LM-head entry point needs from the model, and the
 // runtime's error message setter (both defined in api.cu).
 // ---------------------------------------------------------------------------

@@ -213,7 +213,10 @@ enum {
   RL_K_DOWN = 7,       /* down projection + residual (GEMV kernel) */
   RL_K_LAYER_END = 8,  /* cosine, batch-min, tau compare, next RMSNorm */
   RL_K_LM_HEAD = 9,    /* LM head (GEMV kernel) */
-  RL_K_ARGMAX = 10
+  RL_K_ARGMAX = 10,
+  RL_K_STEP = 11       /* the whole persistent decode-step kernel (B <= 8); the
+                          phase records before it come from its in-kernel timeline:
+                          first start to last end of each phase over all CTAs */
 };
 
 /* Live per-kernel timing of decode steps: when enabled, the captured decode
