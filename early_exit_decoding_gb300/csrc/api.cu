@@ -801,9 +801,16 @@ rl_status reset_sync_words(rl_kv* kv, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 int step_kmax(const rl_model* m) { return std::max(std::max(m->Kd, m->Ko), m->Kf); }
 
-// Stream-K split of a projection with `ntiles` 16-row tiles over `grid` CTAs:
-// used when whole tiles would leave the CTAs unevenly loaded.
-int step_split(int ntiles, int grid) { return (ntiles % grid != 0 && ntiles < 8 * grid) ? 1 : 0; }
+// Stream-K split of a projection with `ntiles` 16-row tiles of `upt` units
+// over `grid` CTAs.  A split tile costs its last CTA two dependent L2 round
+// trips (ticket, partner's partial), about as long as streaming eight units;
+// split only when whole tiles leave the busiest CTA more units than that
+// above the mean.
+int step_split(int ntiles, int upt, int grid) {
+  const double mean = (double)ntiles * upt / grid;
+  const int most = (ntiles + grid - 1) / grid * upt;
+  return most - mean > 8.0 ? 1 : 0;
+}
 
 bool step_fits_model(const rl_model* m, int B) {
   if (!m->step_ok || B < 1 || B > kFusedMaxB || m->d % 16) return false;
@@ -836,7 +843,7 @@ std::vector<PhaseDesc> build_step_phases(rl_model* m, rl_kv* kv, const StepIO& i
     p.qwt = m->quantized ? lin.qwt : nullptr;
     p.N = lin.N;
     p.Kp = lin.Kp;
-    p.split = step_split(lin.N / 16, grid);
+    p.split = step_split(lin.N / 16, (lin.Kp + 1023) / 1024, grid);
     return p;
   };
   int cur = 0;

@@ -310,42 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
       if (D.kind == PH_GEMV) {
         const int Kp = D.Kp, G = Kp >> 7;
         const GRange r = gemv_range(D.N, Kp, D.split, cta, grid);
-        const bool scaled = D.xmode != X_COPY;
         // ---- activation rows ----
         if (D.xmode != X_EMBED && ct == 0 && !s_abort) {
           mbar_expect_tx(&xbar, (uint32_t)B * Kp * 2);
           for (int b = 0; b < B; ++b)
             bulk_g2s(xs + (size_t)b * RSX, D.xg + (size_t)b * D.ldxg, (uint32_t)Kp * 2, &xbar);
         }
-        if (D.xmode == X_SCALED) {
-          if (warp < B) {  // warp b sums the per-tile partials of column b
-            // all partials in one round of loads (up to 512 tiles, d_model <= 8192)
-            float acc[3] = {0.f, 0.f, 0.f};
-            for (int t0 = 0; t0 < D.stats_tiles; t0 += 32 * 16) {
-              float v[16][3];
-#pragma unroll
-              for (int q = 0; q < 16; ++q) {
-                const int tt = t0 + q * 32 + lane;
-#pragma unroll
-                for (int j = 0; j < 3; ++j)
-                  v[q][j] = (tt < D.stats_tiles && j < D.stats_k)
-                                ? __ldcg(D.stats_in + ((size_t)tt * 8 + warp) * D.stats_k + j)
-                                : 0.f;
-              }
-#pragma unroll
-              for (int q = 0; q < 16; ++q)
-#pragma unroll
-                for (int j = 0; j < 3; ++j) acc[j] += v[q][j];
-            }
-#pragma unroll
-            for (int j = 0; j < 3; ++j) acc[j] = warp_sum(acc[j]);
-            if (lane == 0) {
-              s_col[warp][0] = acc[0];
-              s_col[warp][1] = acc[1];
-              s_col[warp][2] = acc[2];
-            }
-          }
-        } else if (D.xmode == X_EMBED) {
+        if (D.xmode == X_EMBED) {
           // gather the token rows; x' = bf16(e * gain) into shared memory
           const int d = a.d, nchk = d >> 3;
           for (int b = 0; b < B; ++b) {
@@ -420,24 +391,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
             if (cta == 0) a.st->exit_layer = s_e;
           }
-          if (D.xmode == X_SCALED && D.dec_layer > 0 && D.stats_k == 3) {
-            float m = FLT_MAX;
-            for (int b = 0; b < B; ++b) {
-              const float ss = s_col[b][0], dot = s_col[b][1], ssp = s_col[b][2];
-              m = fminf(m, dot / fmaxf(sqrtf(ssp) * sqrtf(ss), 1e-12f));
-            }
-            int e = s_e;
-            if (a.mode == RL_EXIT_TAU && e == a.L && D.dec_layer < a.L && m > a.tau) e = D.dec_layer;
-            s_e = e;
-            if (cta == 0) {
-              if (a.min_cos_out) a.min_cos_out[D.dec_layer - 1] = m;
-              a.st->exit_layer = e;
-            }
-            __threadfence_block();
-            s_dec = D.dec_layer;
-          }
-          if (scaled)
+          if (D.xmode == X_EMBED)
             for (int b = 0; b < B; ++b) s_rs[b] = 1.f / sqrtf(s_col[b][0] / (float)a.d + a.eps);
+          // tau mode before the exit: this layer's weight path is the reducer's
+          // decision on the previous layer (taken concurrently with the x fetch)
+          if (a.mode == RL_EXIT_TAU && D.dec_layer > 0 && D.qwt && D.layer_no > 0 && s_e == a.L) {
+            long long i = 0;
+            while (s_dec < D.dec_layer && !s_abort && i < kSpinBar) {
+              __nanosleep(32);
+              ++i;
+            }
+            if (s_dec < D.dec_layer && !s_abort) {
+              atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+              s_abort = 1;
+            }
+          }
         }
         named_sync(kBarCons, NC * 32);
         const bool w4 = D.qwt && D.layer_no > 0 && D.layer_no > s_e;
@@ -795,13 +763,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
       named_sync(kBarPhase, (NC + 1) * 32);
       if (ct == 0) {
         tl_mark(a.tl, a.nph, p, 1);
-        if (p + 1 < a.nph) {
-          __threadfence();
-          red_release_add(a.bars + p, 1u);
-        }
+        // the release orders every write of this CTA's phase (made before the
+        // barrier above) before the arrival
+        if (p + 1 < a.nph) red_release_add(a.bars + p, 1u);
       }
     }
-  } else {
+  } else if (warp == WR) {
     // ================================ reducer ====================================
     // Lane l holds tile values (r, c) = (l/8 + 4k, l%8), k = 0..3.
     const int c = lane & 7, rb = lane >> 3;
@@ -824,6 +791,67 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         const int first_tile = (int)(r.c0 / UPT);
         const int ntl = r.c1 > r.c0 ? (int)((r.c1 - 1) / UPT) - first_tile + 1 : 0;
         if (D.epi == EPI_LMHEAD) lm = true;
+        if (D.xmode == X_SCALED) {
+          // RMSNorm scale and exit decision from the previous phase's per-tile
+          // partial sums, off the consumers' path: they only need x to start
+          if (lane == 0 && p > 0) {
+            long long i = 0;
+            while (ld_acquire(a.bars + (p - 1)) < (unsigned)grid && i < kSpinBar) {
+              __nanosleep(20);
+              ++i;
+            }
+            if (i >= kSpinBar) {
+              atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+              s_abort = 1;
+            }
+          }
+          __syncwarp();
+          float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f;  // lane b keeps column b's sums
+          for (int b = 0; b < B; ++b) {
+            float acc[3] = {0.f, 0.f, 0.f};
+            for (int t0 = 0; t0 < D.stats_tiles; t0 += 32 * 16) {
+              float v[16][3];
+#pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                const int tt = t0 + q * 32 + lane;
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                  v[q][j] = (tt < D.stats_tiles && j < D.stats_k)
+                                ? __ldcg(D.stats_in + ((size_t)tt * 8 + b) * D.stats_k + j)
+                                : 0.f;
+              }
+#pragma unroll
+              for (int q = 0; q < 16; ++q)
+#pragma unroll
+                for (int j = 0; j < 3; ++j) acc[j] += v[q][j];
+            }
+#pragma unroll
+            for (int j = 0; j < 3; ++j) acc[j] = warp_sum(acc[j]);
+            if (lane == b) {
+              cs0 = acc[0];
+              cs1 = acc[1];
+              cs2 = acc[2];
+            }
+          }
+          if (lane < B) s_rs[lane] = 1.f / sqrtf(cs0 / (float)a.d + a.eps);
+          if (D.dec_layer > 0 && D.stats_k == 3) {
+            float m = lane < B ? cs1 / fmaxf(sqrtf(cs2) * sqrtf(cs0), 1e-12f) : FLT_MAX;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) {
+              int e = s_e;
+              if (a.mode == RL_EXIT_TAU && e == a.L && D.dec_layer < a.L && m > a.tau) e = D.dec_layer;
+              s_e = e;
+              if (cta == 0) {
+                if (a.min_cos_out) a.min_cos_out[D.dec_layer - 1] = m;
+                a.st->exit_layer = e;
+              }
+              __threadfence_block();
+              s_dec = D.dec_layer;
+            }
+          }
+          __syncwarp();
+        }
         for (int tc = 0; tc < ntl; ++tc) {
           const int tl = first_tile + tc;
           const int buf = tc_run & 1;
