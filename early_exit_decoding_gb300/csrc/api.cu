@@ -163,6 +163,7 @@ struct rl_kv {
   // persistent step kernel
   bool use_step = true;
   unsigned* bars = nullptr;           // phase arrival counters [nph_cap]
+  unsigned* tctr = nullptr;           // per-phase tile counters [nph_cap]
   PhaseDesc* d_ph = nullptr;          // phase descriptors [nph_cap]
   std::vector<PhaseDesc> h_ph;        // host copy of what d_ph holds
   int nph_cap = 0;
@@ -790,6 +791,7 @@ rl_status enqueue_decode_fused(rl_model* m, rl_kv* kv, const StepIO& io, int nch
 // or when the position is rewound).
 rl_status reset_sync_words(rl_kv* kv, cudaStream_t s) {
   RL_CUDA(cudaMemsetAsync(kv->bars, 0, (size_t)kv->nph_cap * sizeof(unsigned), s));
+  RL_CUDA(cudaMemsetAsync(kv->tctr, 0, (size_t)kv->nph_cap * sizeof(unsigned), s));
   RL_CUDA(cudaMemsetAsync(kv->tile_ticket, 0, (size_t)kv->n_tile_ticket * sizeof(unsigned), s));
   RL_CUDA(cudaMemsetAsync(kv->attn_ticket, 0, (size_t)kv->maxB * kv->m->Hkv * sizeof(unsigned), s));
   RL_CUDA(cudaMemsetAsync(kv->cta_ticket, 0, sizeof(unsigned), s));
@@ -801,20 +803,18 @@ rl_status reset_sync_words(rl_kv* kv, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 int step_kmax(const rl_model* m) { return std::max(std::max(m->Kd, m->Ko), m->Kf); }
 
-// Stream-K split of a projection with `ntiles` 16-row tiles of `upt` units
-// over `grid` CTAs.  A split tile costs its last CTA two dependent L2 round
-// trips (ticket, partner's partial), about as long as streaming eight units;
-// split only when whole tiles leave the busiest CTA more units than that
-// above the mean.
+// Tile scheduling of a projection with `ntiles` 16-row tiles over `grid`
+// CTAs: claimed at run time from a shared counter when there are at least
+// four tiles per CTA (the faster CTAs take more), else assigned round-robin.
 int step_split(int ntiles, int upt, int grid) {
-  const double mean = (double)ntiles * upt / grid;
-  const int most = (ntiles + grid - 1) / grid * upt;
-  return most - mean > 8.0 ? 1 : 0;
+  (void)upt;
+  return ntiles >= 4 * grid ? 1 : 0;
 }
 
 bool step_fits_model(const rl_model* m, int B) {
   if (!m->step_ok || B < 1 || B > kFusedMaxB || m->d % 16) return false;
-  if (m->Hq / m->Hkv > 8 || m->hd > 128) return false;
+  const int rep = m->Hq / m->Hkv;
+  if ((rep != 1 && rep != 2 && rep != 4) || (m->hd != 64 && m->hd != 128)) return false;
   int ns = 0;
   const size_t smem = step_smem_bytes(B, step_kmax(m), step_kmax(m) / kGroup, &ns);
   return smem && decode_step_occupancy(smem) >= 1;
@@ -822,8 +822,9 @@ bool step_fits_model(const rl_model* m, int B) {
 
 bool step_fits(const rl_model* m, const rl_kv* kv, int B) {
   if (!m->step_ok || !kv->part_s || B < 1 || B > kFusedMaxB || B > kv->maxB || m->d % 16) return false;
-  if (m->Hq / m->Hkv > 8 || m->hd > 128) return false;
-  if (5 * m->L + 1 > kv->nph_cap) return false;
+  const int rep = m->Hq / m->Hkv;
+  if ((rep != 1 && rep != 2 && rep != 4) || (m->hd != 64 && m->hd != 128)) return false;
+  if (6 * m->L + 1 > kv->nph_cap) return false;
   int ns = 0;
   const size_t smem = step_smem_bytes(B, step_kmax(m), step_kmax(m) / kGroup, &ns);
   if (!smem) return false;
@@ -881,6 +882,8 @@ std::vector<PhaseDesc> build_step_phases(rl_model* m, rl_kv* kv, const StepIO& i
       p.vc = kv->V[l];
       p.o_out = kv->o;
       p.ldo_attn = m->Ko;
+      ph.push_back(p);
+      p.kind = PH_MERGE;  // the chunks' partials merged, spread over all CTAs
       ph.push_back(p);
     }
     {  // O + residual; x' and |h_mid|^2 partials for the FFN norm
@@ -1005,6 +1008,7 @@ rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStre
   a.am_idx = kv->am_idx;
   a.cta_ticket = kv->cta_ticket;
   a.bars = kv->bars;
+  a.tctr = kv->tctr;
   a.ws = kv->ws;
   a.tile_ticket = kv->tile_ticket;
   a.part = kv->part_s;
@@ -1337,8 +1341,9 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
   }
   {
     // persistent step kernel: phase counters, descriptors, attention partials
-    kv->nph_cap = 5 * m->L + 2;
+    kv->nph_cap = 6 * m->L + 2;
     K_TRY(kv->alloc(&kv->bars, (size_t)kv->nph_cap));
+    K_TRY(kv->alloc(&kv->tctr, (size_t)kv->nph_cap));
     K_TRY(kv->alloc(&kv->d_ph, (size_t)kv->nph_cap));
     const int CH = 128;  // positions per attention chunk
     const int need = (max_seq + CH - 1) / CH;
@@ -1610,11 +1615,14 @@ rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32_t* kin
       if (d.kind == PH_ATTN) {
         kind = RL_K_ATTN;
         b = 2.0 * kv->prof_B * m->Hkv * (double)(kv->prof_pos + 1) * m->hd * 2.0;
+      } else if (d.kind == PH_MERGE) {
+        kind = RL_K_ATTN;
       } else {
-        if (d.layer_no > 0) {
-          const int r = p % 5;
-          kind = r == 0 ? RL_K_QKV : (r == 2 ? RL_K_O : (r == 3 ? RL_K_GU : RL_K_DOWN));
-        }
+        if (d.layer_no > 0)
+          kind = d.epi == EPI_QKV_ROPE ? RL_K_QKV
+                 : d.epi == EPI_SWIGLU ? RL_K_GU
+                 : d.stats_k_out == 3  ? RL_K_DOWN
+                                       : RL_K_O;
         path = (d.qwt && d.layer_no > e) ? 1 : 0;
         b = path ? (double)d.N * d.Kp / 2.0 + (double)d.N * (d.Kp / kGroup) * 4.0
                  : (double)d.N * d.Kp * 2.0;

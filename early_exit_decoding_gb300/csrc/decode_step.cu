@@ -44,12 +44,11 @@ constexpr int SLOT_B = W4U * STAGE_W;     // 34816 bytes (>= 32 KB bf16 unit, >=
 constexpr int kMaxSlots = 8;
 constexpr int kCHP = 128;                 // positions per attention chunk
 constexpr int kAttnHalf = 16384;          // V offset in a one-slot chunk (head_dim 64)
-constexpr int kMaxRep = 8;
-constexpr int kMaxHD = 128;
 constexpr long long kSpin = 1LL << 20;     // mbarrier polls
 constexpr long long kSpinBar = 1LL << 24;  // grid-barrier polls (each with a short sleep)
 constexpr int kBarCons = 1;                // named barrier: consumer warps
 constexpr int kBarPhase = 2;               // named barrier: consumers + reducer
+constexpr int kTileList = 16;              // circular list of the tiles a CTA took
 constexpr int kStaticSmem = 12 * 1024;     // upper bound of the kernel's static shared memory
 
 struct GRange {
@@ -85,14 +84,6 @@ struct RingPos {
   }
 };
 
-// CTA whose stream-K range holds unit x.
-__device__ __forceinline__ int split_owner(long long x, long long U, int grid) {
-  int c = (int)((x * grid) / U);
-  while (c + 1 < grid && (U * (c + 1)) / grid <= x) ++c;
-  while (c > 0 && (U * c) / grid > x) --c;
-  return c;
-}
-
 // Timeline of a profiled step: tl[p] = first start of phase p over CTAs,
 // tl[nph + p] = last end.
 __device__ __forceinline__ void tl_mark(unsigned long long* tl, int nph, int p, int which) {
@@ -103,6 +94,137 @@ __device__ __forceinline__ void tl_mark(unsigned long long* tl, int nph, int p, 
     atomicMin(tl + p, t);
   else
     atomicMax(tl + nph + p, t);
+}
+
+// Sum 32 values over the 32 lanes of a warp, leaving the total of value i
+// in lane i (31 shuffles: each step halves the values a lane carries).
+__device__ __forceinline__ float butterfly32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = upper ? v[i] : v[i + s];
+      const float keep = upper ? v[i + s] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
+// One warp's share of an attention chunk: positions 16*warp .. 16*warp+15
+// (those below n) against the REP query heads of one KV head.  Lane l holds
+// dims [DPL*l, DPL*(l+1)) of q (pre-scaled by 1/sqrt(hd)) and of each K / V
+// row.  Scores come 32 at a time from the butterfly (P positions x REP heads,
+// output i in lane i); the warp keeps its own running max / sum per head and
+// its P V partial.  After a barrier of the consumer warps (every warp is
+// done reading K and V) writes, per head, (max, sum, o[hd]) to wb, which may
+// overlay the chunk's K / V rows.
+template <int REP, int DPL>
+__device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigned char* Vs, int n,
+                                          const float* qg, float scale, int warp, int lane, float* wb) {
+  constexpr int HD = 32 * DPL, RK = HD * 2, P = 32 / REP, NB = (16 + P - 1) / P, WS = 2 + HD;
+  float qr[REP][DPL];
+#pragma unroll
+  for (int h = 0; h < REP; ++h)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) qr[h][d] = __ldcg(qg + h * HD + DPL * lane + d) * scale;
+  float sc[NB];
+  float mloc = -FLT_MAX;
+#pragma unroll
+  for (int bb = 0; bb < NB; ++bb) {
+    float vals[32];
+#pragma unroll
+    for (int jj = 0; jj < P; ++jj) {
+      const int jw = bb * P + jj, j = warp * 16 + jw;
+      float kf[DPL];
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) kf[d] = 0.f;
+      if (jw < 16 && j < n) {
+        if (DPL == 4) {
+          const uint2 w = *reinterpret_cast<const uint2*>(Ks + j * RK + lane * 8);
+          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+          const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+          kf[0] = f0.x;
+          kf[1] = f0.y;
+          kf[DPL > 2 ? 2 : 0] = f1.x;
+          kf[DPL > 3 ? 3 : 0] = f1.y;
+        } else {
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(Ks + j * RK + lane * 4);
+          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+          kf[0] = f0.x;
+          kf[1] = f0.y;
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < REP; ++h) {
+        float acc = 0.f;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc += qr[h][d] * kf[d];
+        vals[jj * REP + h] = acc;
+      }
+    }
+    const float s = butterfly32(vals, lane);
+    const int jw = bb * P + lane / REP, j = warp * 16 + jw;
+    sc[bb] = (jw < 16 && j < n) ? s : -FLT_MAX;
+    mloc = fmaxf(mloc, sc[bb]);
+  }
+  // lanes with the same head (lane % REP) share max and sum
+#pragma unroll
+  for (int o = 16; o >= REP; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+  float pv[NB];
+  float lloc = 0.f;
+#pragma unroll
+  for (int bb = 0; bb < NB; ++bb) {
+    pv[bb] = sc[bb] > -FLT_MAX ? __expf(sc[bb] - mloc) : 0.f;
+    lloc += pv[bb];
+  }
+#pragma unroll
+  for (int o = 16; o >= REP; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
+  float o[REP][DPL];
+#pragma unroll
+  for (int h = 0; h < REP; ++h)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) o[h][d] = 0.f;
+#pragma unroll
+  for (int bb = 0; bb < NB; ++bb) {
+#pragma unroll
+    for (int jj = 0; jj < P; ++jj) {
+      const int jw = bb * P + jj, j = warp * 16 + jw;
+      if (!(jw < 16 && j < n)) continue;  // uniform over the warp
+      float vf[DPL];
+      if (DPL == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(Vs + j * RK + lane * 8);
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+        vf[0] = f0.x;
+        vf[1] = f0.y;
+        vf[DPL > 2 ? 2 : 0] = f1.x;
+        vf[DPL > 3 ? 3 : 0] = f1.y;
+      } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + j * RK + lane * 4);
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+        vf[0] = f0.x;
+        vf[1] = f0.y;
+      }
+#pragma unroll
+      for (int h = 0; h < REP; ++h) {
+        const float pj = __shfl_sync(0xffffffffu, pv[bb], jj * REP + h);
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) o[h][d] += pj * vf[d];
+      }
+    }
+  }
+  dev::named_sync(1, 8 * 32);
+  float* w0 = wb + (size_t)warp * REP * WS;
+  if (lane < REP) {
+    w0[lane * WS] = mloc;
+    w0[lane * WS + 1] = lloc;
+  }
+#pragma unroll
+  for (int h = 0; h < REP; ++h)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) w0[h * WS + 2 + DPL * lane + d] = o[h][d];
 }
 
 }  // namespace
@@ -118,11 +240,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
   __shared__ volatile int s_e;    // exit layer as far as this CTA knows it
   __shared__ volatile int s_dec;  // last layer whose exit decision this CTA has taken
   __shared__ volatile int s_abort;
-  __shared__ int s_pos, s_last, s_tick;
-  __shared__ float qs[kMaxRep][kMaxHD];
-  __shared__ float ps[kMaxRep][128];
-  __shared__ float ared[kMaxRep][NC];
-  __shared__ float mstat[kMaxRep][2];
+  // Tiles this CTA took, in ring order (circular; the producer is at most a few
+  // tiles ahead of the consumers, the reducer at most two behind them); -1
+  // closes a phase.  s_tcount = entries written so far.
+  __shared__ volatile int s_tl[kTileList];
+  __shared__ volatile int s_tcount, s_cseq, s_rseq;  // written / read by consumers / by reducer
+  __shared__ int s_pos, s_last;
+  __shared__ __align__(16) float s_mrg[1024];  // attention merge: chunk (max, sum), weights, partial sums
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -154,6 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
     }
     s_e = e;
     s_dec = 0;
+    s_tcount = 0;
+    s_cseq = 0;
+    s_rseq = 0;
   }
   if (tid < 8) s_rs[tid] = 1.f;
   if (tid < 64) s_freq[tid] = tid < a.hd / 2 ? a.inv_freq[tid] : 0.f;
@@ -164,6 +291,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
     if (lane == 0) {
       RingPos rp{0, 0};
       int issued = 0;
+      int tseq = 0;
+      // append to the tile list once both readers are less than a list length behind
+      auto publish = [&](int v) -> bool {
+        long long i = 0;
+        while (tseq - min(s_cseq, s_rseq) >= kTileList - 1 && !s_abort && i < kSpinBar) {
+          __nanosleep(32);
+          ++i;
+        }
+        if (tseq - min(s_cseq, s_rseq) >= kTileList - 1) {
+          if (!s_abort) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+          s_abort = 1;
+          return false;
+        }
+        s_tl[tseq % kTileList] = v;
+        __threadfence_block();
+        s_tcount = ++tseq;
+        return true;
+      };
       int e_known = s_e;
       auto take_slot = [&]() -> bool {
         if (rp.round == 0) return true;
@@ -200,37 +345,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
             w4 = layer_no > e_known;
           }
-          const GRange r = gemv_range(N, Kp, split, cta, grid);
-          if (w4) {
-            for (long long u = r.c0; u < r.c1; u += W4U) {
-              if (!take_slot()) break;
-              const int ns = (int)min((long long)W4U, r.c1 - u);
-              const int slot = rp.slot;
-              mbar_expect_tx(&full[slot], (uint32_t)(ns * STAGE_W));
-              bulk_g2s(ring + (size_t)slot * SLOT_B, qwt + (size_t)u * STAGE_W, (uint32_t)(ns * STAGE_W),
-                       &full[slot]);
-              rp.next(NS);
-              ++issued;
-            }
-          } else {
-            int tl = (int)(r.c0 / r.UPT), uk = (int)(r.c0 % r.UPT);
-            for (long long u = r.c0; u < r.c1; ++u) {
-              if (!take_slot()) break;
-              const int k0 = uk * KU, kn = min(KU, Kp - k0);
-              const int slot = rp.slot;
-              const uint32_t bytes = (uint32_t)(16 * kn * 2);
-              mbar_expect_tx(&full[slot], bytes);
-              bulk_g2s(ring + (size_t)slot * SLOT_B, wt + (size_t)tl * 16 * Kp + (size_t)16 * k0, bytes,
-                       &full[slot]);
-              rp.next(NS);
-              ++issued;
-              if (++uk == r.UPT) {
-                uk = 0;
-                ++tl;
+          // Whole 16-row tiles.  Large projections (D->split != 0): taken from
+          // the phase's shared counter, so CTAs that stream faster take more
+          // (the next claim overlaps the current tile's copies).  Small ones:
+          // tiles cta, cta + grid, ... -- a claim made early, while the ring
+          // prefetches ahead, would pile several tiles onto one CTA.
+          const bool dyn = split != 0;
+          const int UPT = (Kp + KU - 1) / KU, ntiles = N >> 4;
+          int tl = dyn ? (int)atomicAdd(a.tctr + p, 1u) : cta;
+          while (tl < ntiles && !s_abort) {
+            const int nxt = dyn ? (int)atomicAdd(a.tctr + p, 1u) : tl + grid;
+            if (!publish(tl)) break;
+            if (w4) {
+              for (int s0 = 0; s0 < UPT; s0 += W4U) {
+                if (!take_slot()) break;
+                const int ns = min(W4U, UPT - s0);
+                const int slot = rp.slot;
+                mbar_expect_tx(&full[slot], (uint32_t)(ns * STAGE_W));
+                bulk_g2s(ring + (size_t)slot * SLOT_B, qwt + ((size_t)tl * UPT + s0) * STAGE_W,
+                         (uint32_t)(ns * STAGE_W), &full[slot]);
+                rp.next(NS);
+                ++issued;
+              }
+            } else {
+              for (int uk = 0; uk < UPT; ++uk) {
+                if (!take_slot()) break;
+                const int k0 = uk * KU, kn = min(KU, Kp - k0);
+                const int slot = rp.slot;
+                const uint32_t bytes = (uint32_t)(16 * kn * 2);
+                mbar_expect_tx(&full[slot], bytes);
+                bulk_g2s(ring + (size_t)slot * SLOT_B, wt + (size_t)tl * 16 * Kp + (size_t)16 * k0, bytes,
+                         &full[slot]);
+                rp.next(NS);
+                ++issued;
               }
             }
+            tl = nxt;
           }
-        } else {
+          if (!publish(-1)) break;  // end of this CTA's tiles in the phase
+        } else if (D->kind == PH_ATTN) {
           // attention: K and V rows below this step's position; a chunk of up
           // to 128 positions takes one slot (head_dim 64: K, then V at 16 KB)
           // or two (head_dim 128: K in the first, V in the second)
@@ -281,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
     const int ct = tid;
     RingPos rc{0, 0};
     int tcount = 0;
+    int cseq = 0;  // position in the tile list
     uint32_t xpar = 0;
     for (int p = 0; p < a.nph; ++p) {
       {
@@ -454,9 +608,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         };
         const int UPT = r.UPT;
         const int step_u = w4 ? W4U : 1;
-        const int nsub = (int)(r.c1 - r.c0);
-        int uk = (int)(r.c0 % UPT);
-        for (int i0 = 0; i0 < nsub; i0 += step_u) {
+        for (;;) {
+          // next tile this CTA took (the producer publishes it before its copies)
+          long long spin = 0;
+          while (s_tcount <= cseq && !s_abort && spin < kSpinBar) {
+            __nanosleep(20);
+            ++spin;
+          }
+          if (s_tcount <= cseq) {
+            if (!s_abort && lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+            s_abort = 1;
+            break;
+          }
+          const int tile = s_tl[cseq % kTileList];
+          ++cseq;
+          named_sync(kBarCons, NC * 32);  // every consumer warp has read the entry
+          if (ct == 0) s_cseq = cseq;
+          if (tile < 0) break;
+          int uk = 0;
+        for (int i0 = 0; i0 < UPT; i0 += step_u) {
           const int slot = rc.slot;
           bool ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
           if (!ok && s_abort == 0) {
@@ -464,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             s_abort = 1;
           }
           const unsigned char* sb = ring + (size_t)slot * SLOT_B;
-          const int ns = min(step_u, nsub - i0);
+          const int ns = min(step_u, UPT - i0);
           for (int s = 0; s < ns; ++s) {
             const int gi = uk * 8 + warp;  // this warp's group
             if (ok && gi < G) {
@@ -532,31 +702,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 }
               }
             }
-            if (uk + 1 == UPT || i0 + s + 1 == nsub) hand_off();
-            if (++uk == UPT) uk = 0;
+            if (uk + 1 == UPT) hand_off();
+            ++uk;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[slot]);
           rc.next(NS);
         }
-      } else {
-        // ---- attention over this CTA's chunks --------------------------------------
+        }
+      } else if (D.kind == PH_ATTN) {
+        // ---- attention over this CTA's chunks: partial (max, sum, o) per chunk ----
         const int pos = s_pos, hd = a.hd, Hkv = a.Hkv, Hq = a.Hq, rep = Hq / Hkv;
         const int ctx = min(pos + 1, a.Tmax);
         const int nch = step_attn_chunks(ctx, B, Hkv, hd, grid, a.part_cap);
         const int clen = (ctx + nch - 1) / nch;
-        const int CH = kCHP;
         const int nitems = B * Hkv * nch;
         const bool two = hd * 2 * kCHP > kAttnHalf;
         const int RK = hd * 2;  // K/V row bytes
-        const int hd8 = hd >> 3;
         const float scale = rsqrtf((float)hd);
-        const int j = ct & 127, hh = ct >> 7;
-        if (clen > CH && cta == 0 && ct == 0) atomicOr(&a.st->err, RL_DEVERR_CAPACITY);
+        const int WS = 2 + hd;
+        if (clen > kCHP && cta == 0 && ct == 0) atomicOr(&a.st->err, RL_DEVERR_CAPACITY);
         for (int it = cta; it < nitems; it += grid) {
           const int b = it / (Hkv * nch), rr = it % (Hkv * nch), hk = rr / nch, ch = rr % nch;
           const int start = ch * clen, end = min(start + clen, ctx);
-          const int n = min(CH, max(0, end - start));
+          const int n = min(kCHP, max(0, end - start));
           const int slot = rc.slot;
           bool ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
           rc.next(NS);
@@ -573,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           unsigned char* Ks = ring + (size_t)slot * SLOT_B;
           unsigned char* Vs = two ? ring + (size_t)slot_v * SLOT_B : Ks + kAttnHalf;
           const size_t head_base = ((size_t)b * Hkv + hk) * a.Tmax;
-          if (ok && pos >= start && pos < start + n && ct < hd8) {
+          if (ok && pos >= start && pos < start + n && ct < hd / 8) {
             // the row written by this step's QKV phase
             const int rw = pos - start;
             const uint4 kv = __ldcg(reinterpret_cast<const uint4*>(D.kc + (head_base + pos) * hd) + ct);
@@ -581,182 +750,112 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             *reinterpret_cast<uint4*>(Ks + rw * RK + ct * 16) = kv;
             *reinterpret_cast<uint4*>(Vs + rw * RK + ct * 16) = vv;
           }
-          for (int i = ct; i < rep * hd; i += NC * 32)
-            qs[i / hd][i % hd] = __ldcg(D.q_out + (size_t)b * Hq * hd + (size_t)hk * rep * hd + i) * scale;
           named_sync(kBarCons, NC * 32);
-          // scores: thread (j, hh) -> position j, heads hh, hh + 2, ...
-          float sc[kMaxRep / 2];
-#pragma unroll
-          for (int i = 0; i < kMaxRep / 2; ++i) sc[i] = -FLT_MAX;
-          if (ok && j < n) {
-#pragma unroll
-            for (int i = 0; i < kMaxRep / 2; ++i) sc[i] = 0.f;
-            for (int v = 0; v < hd8; ++v) {
-              const int c = (v + j) & (hd8 - 1);  // rotate chunks: conflict-free rows
-              const uint4 w = *reinterpret_cast<const uint4*>(Ks + j * RK + c * 16);
-              const __nv_bfloat162* e = reinterpret_cast<const __nv_bfloat162*>(&w);
-              float kf[8];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float2 f = __bfloat1622float2(e[q]);
-                kf[2 * q] = f.x;
-                kf[2 * q + 1] = f.y;
-              }
-#pragma unroll
-              for (int i = 0; i < kMaxRep / 2; ++i) {
-                const int h = hh + 2 * i;
-                if (h < rep) {
-                  const float4 q0 = *reinterpret_cast<const float4*>(&qs[h][8 * c]);
-                  const float4 q1 = *reinterpret_cast<const float4*>(&qs[h][8 * c + 4]);
-                  sc[i] += kf[0] * q0.x + kf[1] * q0.y + kf[2] * q0.z + kf[3] * q0.w +
-                           kf[4] * q1.x + kf[5] * q1.y + kf[6] * q1.z + kf[7] * q1.w;
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < kMaxRep / 2; ++i) {
-            const int h = hh + 2 * i;
-            if (h < rep) {
-              const float v = warp_max(sc[i]);
-              if (lane == 0) ared[h][warp] = v;
-            }
+          // per-warp scores, softmax and P V; the warps' partials overlay the K rows
+          float* wb = reinterpret_cast<float*>(Ks);
+          const float* qg = D.q_out + (size_t)b * Hq * hd + (size_t)hk * rep * hd;
+          const int nn = ok ? n : 0;
+          const int key = rep * 8 + (hd >> 5);
+          switch (key) {
+            case 1 * 8 + 2: attn_warp<1, 2>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
+            case 2 * 8 + 2: attn_warp<2, 2>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
+            case 4 * 8 + 2: attn_warp<4, 2>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
+            case 1 * 8 + 4: attn_warp<1, 4>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
+            case 2 * 8 + 4: attn_warp<2, 4>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
+            default: attn_warp<4, 4>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
           }
           named_sync(kBarCons, NC * 32);
-          if (ct < rep) {
-            const int w0 = (ct & 1) * 4;
-            float mx = ared[ct][w0];
-            for (int w = 1; w < 4; ++w) mx = fmaxf(mx, ared[ct][w0 + w]);
-            mstat[ct][0] = mx;
-          }
-          named_sync(kBarCons, NC * 32);
-#pragma unroll
-          for (int i = 0; i < kMaxRep / 2; ++i) {
-            const int h = hh + 2 * i;
-            if (h < rep) {
-              const float pv = (ok && j < n) ? __expf(sc[i] - mstat[h][0]) : 0.f;
-              ps[h][j] = pv;
-              const float v = warp_sum(pv);
-              if (lane == 0) ared[h][warp] = v;
-            }
-          }
-          named_sync(kBarCons, NC * 32);
-          if (ct < rep) {
-            const int w0 = (ct & 1) * 4;
-            float l = 0.f;
-            for (int w = 0; w < 4; ++w) l += ared[ct][w0 + w];
-            mstat[ct][1] = l;
-          }
-          // P V: thread owns (head, dim pair) slots
-          const int nslots = rep * hd / 2;
+          // combine the eight warps (online-softmax rescale) into this chunk's partial
           float* part = a.part + ((size_t)b * Hq + (size_t)hk * rep) * a.part_cap * (hd + 2);
-          for (int s2 = ct; s2 < nslots; s2 += NC * 32) {
-            const int h = s2 / (hd / 2), dp = s2 % (hd / 2);
-            float2 acc[4];
+          for (int i = ct; i < rep * hd; i += NC * 32) {
+            const int h = i / hd, dd = i % hd;
+            float M = -FLT_MAX;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
-            if (ok) {
-              int jj = 0;
-              for (; jj + 4 <= n; jj += 4) {
+            for (int w = 0; w < NC; ++w) M = fmaxf(M, wb[(w * rep + h) * WS]);
+            float num = 0.f, den = 0.f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  const float pj = ps[h][jj + q];
-                  const float2 v =
-                      __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Vs + (jj + q) * RK + dp * 4));
-                  acc[q].x += pj * v.x;
-                  acc[q].y += pj * v.y;
-                }
-              }
-              for (; jj < n; ++jj) {
-                const float pj = ps[h][jj];
-                const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Vs + jj * RK + dp * 4));
-                acc[0].x += pj * v.x;
-                acc[0].y += pj * v.y;
-              }
+            for (int w = 0; w < NC; ++w) {
+              const float* ww = wb + (w * rep + h) * WS;
+              const float f = ww[1] > 0.f ? __expf(ww[0] - M) : 0.f;
+              num += f * ww[2 + dd];
+              den += f * ww[1];
             }
             float* pp = part + ((size_t)h * a.part_cap + ch) * (hd + 2);
-            pp[2 * dp] = (acc[0].x + acc[1].x) + (acc[2].x + acc[3].x);
-            pp[2 * dp + 1] = (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y);
-          }
-          if (ct < rep) {
-            float* pp = part + ((size_t)ct * a.part_cap + ch) * (hd + 2);
-            pp[hd] = n > 0 ? mstat[ct][0] : -FLT_MAX;
-            pp[hd + 1] = n > 0 ? mstat[ct][1] : 0.f;
-          }
-          named_sync(kBarCons, NC * 32);
-          if (ct == 0) {
-            // release every thread's partial writes (ordered before by the barrier)
-            __threadfence();
-            s_tick = !s_abort && atomicAdd(&a.attn_ticket[(size_t)b * Hkv + hk], 1u) == (unsigned)(nch - 1);
-            if (s_tick) __threadfence();
-          }
-          named_sync(kBarCons, NC * 32);
-          if (s_tick) {
-            // ---- merge: last CTA of this (sequence, KV head); slot memory as scratch ----
-            float2* ml = reinterpret_cast<float2*>(Ks);                 // [rep][nch]
-            float* wc = reinterpret_cast<float*>(Ks) + 2 * rep * nch;   // [rep][nch]
-            for (int i = ct; i < rep * nch; i += NC * 32) {
-              const int h = i / nch, cc = i % nch;
-              const float* pp = part + ((size_t)h * a.part_cap + cc) * (hd + 2);
-              ml[i] = make_float2(__ldcg(pp + hd), __ldcg(pp + hd + 1));
+            pp[dd] = num;
+            if (dd == 0) {
+              pp[hd] = den > 0.f ? M : -FLT_MAX;
+              pp[hd + 1] = den;
             }
-            named_sync(kBarCons, NC * 32);
-            if (ct < rep) {
-              float M = -FLT_MAX, den = 0.f;
-              for (int cc = 0; cc < nch; ++cc)
-                if (ml[ct * nch + cc].y > 0.f) M = fmaxf(M, ml[ct * nch + cc].x);
-              for (int cc = 0; cc < nch; ++cc) {
-                const float2 v = ml[ct * nch + cc];
-                const float w = v.y > 0.f ? __expf(v.x - M) : 0.f;
-                wc[ct * nch + cc] = w;
-                den += w * v.y;
-              }
-              const float inv = den > 0.f ? 1.f / den : 0.f;
-              for (int cc = 0; cc < nch; ++cc) wc[ct * nch + cc] *= inv;
-            }
-            named_sync(kBarCons, NC * 32);
-            // every thread owns up to MO outputs and loads CB chunks of all of
-            // them per round: few dependent round trips to L2
-            constexpr int MO = kMaxRep * kMaxHD / (NC * 32), CB = 8;
-            const int nout = rep * hd;
-            float num[MO];
-#pragma unroll
-            for (int o = 0; o < MO; ++o) num[o] = 0.f;
-            for (int c0 = 0; c0 < nch; c0 += CB) {
-              float v[MO][CB];
-#pragma unroll
-              for (int o = 0; o < MO; ++o) {
-                const int i = ct + o * NC * 32;
-                const int h = i / hd, dd = i % hd;
-                const float* pp = part + (size_t)h * a.part_cap * (hd + 2) + dd;
-#pragma unroll
-                for (int q = 0; q < CB; ++q)
-                  v[o][q] = (i < nout && c0 + q < nch) ? __ldcg(pp + (size_t)(c0 + q) * (hd + 2)) : 0.f;
-              }
-#pragma unroll
-              for (int o = 0; o < MO; ++o) {
-                const int i = ct + o * NC * 32;
-                const int h = i < nout ? i / hd : 0;
-#pragma unroll
-                for (int q = 0; q < CB; ++q)
-                  if (c0 + q < nch) num[o] += wc[h * nch + c0 + q] * v[o][q];
-              }
-            }
-#pragma unroll
-            for (int o = 0; o < MO; ++o) {
-              const int i = ct + o * NC * 32;
-              if (i < nout) {
-                const int h = i / hd, dd = i % hd;
-                D.o_out[(size_t)b * D.ldo_attn + (size_t)(hk * rep + h) * hd + dd] = __float2bfloat16_rn(num[o]);
-              }
-            }
-            if (ct == 0) a.attn_ticket[(size_t)b * Hkv + hk] = 0u;
           }
           named_sync(kBarCons, NC * 32);
           if (lane == 0) {
             mbar_arrive(&empty[slot]);
             if (two) mbar_arrive(&empty[slot_v]);
           }
+        }
+      } else {
+        // ---- merge of the attention chunks, spread over all CTAs ------------------------
+        // item = (sequence, query head, slice of head dims); threads split the chunks
+        const int pos = s_pos, hd = a.hd, Hkv = a.Hkv, Hq = a.Hq;
+        const int ctx = min(pos + 1, a.Tmax);
+        const int nch = step_attn_chunks(ctx, B, Hkv, hd, grid, a.part_cap);
+        const int nheads = B * Hq;
+        const int spl = max(1, min(hd / 8, grid / nheads));  // slices per head
+        const int sl = (hd + spl - 1) / spl;                    // outputs per slice
+        const int S = (NC * 32) / sl;                           // threads per output
+        float* ml = s_mrg;                                       // [nch][2]
+        float* wc = ml + 2 * 256;                                // [nch]
+        float* rd = wc + 256;                                    // [NC * 32]
+        for (int item = cta; item < nheads * spl; item += grid) {
+          const int gh = item / spl, sc0 = (item % spl) * sl;
+          const float* hp = a.part + (size_t)gh * a.part_cap * (hd + 2);
+          const int k = ct / S, sidx = ct % S;
+          const int dd = sc0 + k;
+          const bool act = k < sl && dd < hd;
+          float v[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int c = sidx + q * S;
+            v[q] = (act && c < nch) ? __ldcg(hp + (size_t)c * (hd + 2) + dd) : 0.f;
+          }
+          for (int c = ct; c < nch; c += NC * 32) {
+            ml[2 * c] = __ldcg(hp + (size_t)c * (hd + 2) + hd);
+            ml[2 * c + 1] = __ldcg(hp + (size_t)c * (hd + 2) + hd + 1);
+          }
+          named_sync(kBarCons, NC * 32);
+          if (warp == 0) {
+            float M = -FLT_MAX;
+            for (int c = lane; c < nch; c += 32)
+              if (ml[2 * c + 1] > 0.f) M = fmaxf(M, ml[2 * c]);
+            M = warp_max(M);
+            float den = 0.f;
+            for (int c = lane; c < nch; c += 32) {
+              const float w = ml[2 * c + 1] > 0.f ? __expf(ml[2 * c] - M) : 0.f;
+              wc[c] = w;
+              den += w * ml[2 * c + 1];
+            }
+            den = warp_sum(den);
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            __syncwarp();
+            for (int c = lane; c < nch; c += 32) wc[c] *= inv;
+          }
+          named_sync(kBarCons, NC * 32);
+          float acc = 0.f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int c = sidx + q * S;
+            if (act && c < nch) acc += wc[c] * v[q];
+          }
+          for (int c = sidx + 8 * S; act && c < nch; c += S) acc += wc[c] * __ldcg(hp + (size_t)c * (hd + 2) + dd);
+          rd[ct] = acc;
+          named_sync(kBarCons, NC * 32);
+          if (act && sidx == 0) {
+            float sum = 0.f;
+            for (int q = 0; q < S; ++q) sum += rd[k * S + q];
+            const int bq = gh / Hq, hq = gh % Hq;
+            D.o_out[(size_t)bq * D.ldo_attn + (size_t)hq * hd + dd] = __float2bfloat16_rn(sum);
+          }
+          named_sync(kBarCons, NC * 32);
         }
       }
       // ---- end of phase: this CTA's writes are done; arrive ----
@@ -773,6 +872,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
     // Lane l holds tile values (r, c) = (l/8 + 4k, l%8), k = 0..3.
     const int c = lane & 7, rb = lane >> 3;
     int tc_run = 0;
+    int rseq = 0;  // position in the tile list
     float amv = -FLT_MAX;
     int ami = 0x7fffffff;
     bool lm = false;
@@ -785,11 +885,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
       }
       const PhaseDesc& D = rdesc;
       if (D.kind == PH_GEMV && !s_abort) {
-        const GRange r = gemv_range(D.N, D.Kp, D.split, cta, grid);
-        const int UPT = r.UPT;
-        const long long U = (long long)r.ntiles * UPT;
-        const int first_tile = (int)(r.c0 / UPT);
-        const int ntl = r.c1 > r.c0 ? (int)((r.c1 - 1) / UPT) - first_tile + 1 : 0;
         if (D.epi == EPI_LMHEAD) lm = true;
         if (D.xmode == X_SCALED) {
           // RMSNorm scale and exit decision from the previous phase's per-tile
@@ -852,8 +947,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           }
           __syncwarp();
         }
-        for (int tc = 0; tc < ntl; ++tc) {
-          const int tl = first_tile + tc;
+        for (;;) {
+          // the next tile of this CTA, as the producer published it
+          long long spin = 0;
+          while (s_tcount <= rseq && !s_abort && spin < kSpinBar) {
+            __nanosleep(20);
+            ++spin;
+          }
+          if (s_tcount <= rseq) {
+            if (!s_abort && lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+            s_abort = 1;
+            break;
+          }
+          const int tl = s_tl[rseq % kTileList];
+          ++rseq;
+          __syncwarp();
+          if (lane == 0) s_rseq = rseq;
+          if (tl < 0) break;
           const int buf = tc_run & 1;
           float res[4] = {0.f, 0.f, 0.f, 0.f}, hin[4] = {0.f, 0.f, 0.f, 0.f}, gn[4] = {0.f, 0.f, 0.f, 0.f};
           if (D.epi == EPI_RESID && c < B) {
@@ -884,31 +994,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           __syncwarp();
           if (lane == 0) mbar_arrive(&rempty[buf]);
           ++tc_run;
-          // tile split between CTAs: the last to arrive completes it
-          const long long tc0 = (long long)tl * UPT, tc1 = tc0 + UPT;
-          if (tc0 < r.c0 || tc1 > r.c1) {
-            const int slot = tl == first_tile ? 0 : 1;
-            float* wsp = a.ws + ((size_t)cta * 2 + slot) * 128;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) wsp[lane + 32 * k] = tv[k];
-            __threadfence();
-            __syncwarp();
-            const int oa = split_owner(tc0, U, grid), ob = split_owner(tc1 - 1, U, grid);
-            unsigned int last = 0;
-            if (lane == 0) last = atomicAdd(&a.tile_ticket[tl], 1u) == (unsigned int)(ob - oa);
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (!last) continue;
-            __threadfence();
-#pragma unroll
-            for (int k = 0; k < 4; ++k) tv[k] = 0.f;
-            for (int o = oa; o <= ob; ++o) {
-              const int ft = (int)((U * o / grid) / UPT);
-              const float* pp = a.ws + ((size_t)o * 2 + (tl == ft ? 0 : 1)) * 128;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) tv[k] += __ldcg(pp + lane + 32 * k);
-            }
-            if (lane == 0) a.tile_ticket[tl] = 0u;
-          }
           // ---- epilogue ----
           if (D.epi == EPI_RESID) {
             float s0 = 0.f, s1 = 0.f, s2 = 0.f;
@@ -1061,7 +1146,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
     }
     if (lane == 0 && a.next_token) a.next_token[warp] = bi == 0x7fffffff ? 0 : bi;
   }
-  for (int i = tid; i < a.nph; i += kThreads) a.bars[i] = 0u;
+  for (int i = tid; i < a.nph; i += kThreads) {
+    a.bars[i] = 0u;
+    a.tctr[i] = 0u;
+  }
   if (tid == 0) {
     DevState* st = a.st;
     if (a.exit_out) a.exit_out[0] = st->exit_layer;

@@ -208,15 +208,15 @@ void launch_quantize(const bf16* w, int N, int K, int Kp, uint32_t* qw, __half2*
 // weight stream of a CTA runs ahead across phase boundaries: it depends only
 // on the weight path, never on this step's activations.
 // ---------------------------------------------------------------------------
-enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1 };
+enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1, PH_MERGE = 2 };
 
 struct PhaseDesc {
-  int kind;                   // PH_GEMV / PH_ATTN
+  int kind;                   // PH_GEMV / PH_ATTN / PH_MERGE
   int layer_no;               // 1..L; 0 = LM head (always the bf16 weights)
   // GEMV weights
   const bf16* wt;             // bf16 unit-tiled (see k_bf16_tile_layout)
   const unsigned char* qwt;   // W4 unit-tiled, nullptr if there is no exit-river copy
-  int N, Kp, split;           // split: stream-K partition of the (tile, unit) pairs
+  int N, Kp, split;           // split: tiles claimed at run time (else round-robin)
   // activations
   int xmode;                  // X_COPY / X_SCALED / X_EMBED
   const bf16* xg;
@@ -270,6 +270,7 @@ struct StepArgs {
   int* am_idx;
   unsigned* cta_ticket;
   unsigned* bars;             // [nph] phase arrival counters, zero at step start
+  unsigned* tctr;             // [nph] tiles handed out per projection phase, zero at step start
   float* ws;                  // stream-K partial tiles [grid][2][128]
   unsigned* tile_ticket;      // [max tiles]
   float* part;                // attention partials [B][Hq][part_cap][hd + 2]
