@@ -55,6 +55,15 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def shape_of(shape_name, args):
+    import dataclasses
+    import synth
+    S = synth.SHAPES[shape_name]
+    if getattr(args, "layers", 0):
+        S = dataclasses.replace(S, n_layers=args.layers, name=f"{S.name} cut to {args.layers} layers")
+    return S
+
+
 def workload_desc(name, shape, B, T, G, mean):
     return (f"{shape.name} shape, random init N(0,0.02) seed 0, batch {B}, prompt {T} uniform ids "
             f"(seed 1), {G}-step generation under a forced exit schedule (geometric, target mean "
@@ -99,6 +108,14 @@ class Clocks:
                  "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+        # nvidia-smi's start-up (driver and NVML initialisation) can hold up
+        # GPU work submission: start timing only once it is sampling
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 10.0:
+            self.f.flush()
+            if os.path.getsize(self.out) > 0:
+                break
+            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -137,7 +154,7 @@ def run_river(args, rank, world, dev):
     import early_exit_decoding_gb300 as river
 
     shape_name, B, T, G, mean, taus, kvfill = CONFIGS[args.config]
-    S = synth.SHAPES[shape_name]
+    S = shape_of(shape_name, args)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream()
     t0 = time.time()
@@ -281,11 +298,11 @@ def run_river(args, rank, world, dev):
     return res
 
 
-def gemv_traffic_note():
-    """DRAM bytes over algorithmic bytes of the fused GEMV kernel from the
-    committed ncu summary, if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "gemv_dram_traffic.txt")
-    src = os.path.join(ROOT, "early_exit_decoding_gb300", "csrc", "gemv_fused.cu")
+def traffic_note(summary, source):
+    """DRAM bytes over algorithmic bytes of a kernel from a committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", summary)
+    src = os.path.join(ROOT, "early_exit_decoding_gb300", "csrc", source)
     if not os.path.exists(p):
         return None
     kv = {}
@@ -294,7 +311,7 @@ def gemv_traffic_note():
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if kv.get("gemv_source_sha256_16") != h:
+    if kv.get("source_sha256_16") != h:
         return None
     try:
         return float(kv["read_over_algorithmic"])
@@ -375,6 +392,9 @@ def main():
     ap.add_argument("--impl", default="river", choices=("river", "reference"))
     ap.add_argument("--config", default="1b-b1", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: the config's shape cut to this many layers (a small "
+                         "case for detailed ncu captures); the bench line names it")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -383,7 +403,7 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     shape_name, B, T, G, mean, taus, kvfill = CONFIGS[args.config]
     import synth
-    S = synth.SHAPES[shape_name]
+    S = shape_of(shape_name, args)
     hbm_peak, peak_src = load_peaks()
 
     if args.impl == "reference":
@@ -429,19 +449,30 @@ def main():
     full_bytes = sum(step_bytes(S, B, S.n_layers, T + (i % G)) for i in range(K))
     full_gbs = full_bytes / (res["ms_full"] / 1e3) / 1e9
 
-    # roofline of the dominant kernel (the dual-path GEMV), from the live profile
+    # roofline of the dominant kernel, from the live profile.  B <= 8: the
+    # persistent step kernel (one launch per step, every byte of the step);
+    # its phase records (first start .. last end over CTAs) give the shares.
     prof = res["prof"]
-    gemv = [r for r in prof if r[0] in ("qkv", "o_proj", "gate_up", "down", "lm_head")]
-    g_ms = sum(r[3] for r in gemv)
-    g_bytes = sum(r[4] for r in gemv)
-    all_ms = sum(r[3] for r in prof)
-    per_launch_bytes = g_bytes / max(1, len(gemv))
-    per_launch_ms = g_ms / max(1, len(gemv))
-    achieved = per_launch_bytes / (per_launch_ms / 1e3) / 1e9 if gemv else 0.0
-    ratio = gemv_traffic_note()
+    steps = [r for r in prof if r[0] == "decode_step"]
+    if steps:
+        kname = "k_decode_step (persistent decode step: every layer's projections, attention, LM head)"
+        launches = steps
+        phases = [r for r in prof if r[0] != "decode_step"]
+        ratio = traffic_note("step_dram_traffic.txt", "decode_step.cu")
+    else:
+        kname = "k_gemv_fused (bf16 / W4 projections + LM head, B <= 8)"
+        launches = [r for r in prof if r[0] in ("qkv", "o_proj", "gate_up", "down", "lm_head")]
+        phases = prof
+        ratio = traffic_note("gemv_dram_traffic.txt", "gemv_fused.cu")
+    g_ms = sum(r[3] for r in launches)
+    g_bytes = sum(r[4] for r in launches)
+    all_ms = sum(r[3] for r in phases)
+    per_launch_bytes = g_bytes / max(1, len(launches))
+    per_launch_ms = g_ms / max(1, len(launches))
+    achieved = per_launch_bytes / (per_launch_ms / 1e3) / 1e9 if launches else 0.0
     traffic = ratio * per_launch_bytes if ratio is not None else None
     shares = {}
-    for r in prof:
+    for r in phases:
         shares[r[0]] = shares.get(r[0], 0.0) + r[3]
     shares = {k: round(v / all_ms, 4) for k, v in sorted(shares.items(), key=lambda kv: -kv[1])}
 
@@ -466,12 +497,11 @@ def main():
                    "parallelism": f"replicas x{world}"},
         "hbm": {"algorithmic_bytes_per_step": tot_bytes / K, "achieved_gbs": gbs,
                 "peak_gbs": hbm_peak, "frac": gbs / hbm_peak, "peak_source": peak_src},
-        "roofline": {"kernel": "k_gemv_fused (bf16 / W4 projections + LM head, B <= 8)",
+        "roofline": {"kernel": kname,
                      "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
-                     "launches_profiled": len(gemv), "peak_source": f"{peak_src} (copy test)",
-                     "time_share_in_step": round(g_ms / all_ms, 4) if all_ms else None},
+                     "launches_profiled": len(launches), "peak_source": f"{peak_src} (copy test)"},
         "kernel_time_shares": shares,
         "variants": {
             "no_exit": {"tokens_per_s": world * B / (full_ms_step / 1e3), "ms_per_step": full_ms_step,
