@@ -182,6 +182,11 @@ struct rl_kv {
   // decode graph
   cudaGraphExec_t exec = nullptr;
   GraphKey key;
+  // step path: the captured graph, its kernel node and the arguments captured
+  // (a new token pointer only updates the node's parameters)
+  cudaGraph_t graph = nullptr;
+  cudaGraphNode_t step_node = nullptr;
+  StepArgs step_args;
   // live profiling
   bool profiling = false;
   std::vector<cudaEvent_t> ev;
@@ -208,6 +213,7 @@ struct rl_kv {
   }
   ~rl_kv() {
     if (exec) cudaGraphExecDestroy(exec);
+    if (graph) cudaGraphDestroy(graph);
     for (cudaEvent_t e : ev) cudaEventDestroy(e);
     for (void* p : allocs) cudaFree(p);
   }
@@ -1025,6 +1031,7 @@ rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStre
     RL_CUDA(cudaMemsetAsync(kv->tl + a.nph, 0, (size_t)a.nph * 8, s));
     cudaEventRecordWithFlags(kv->ev[0], s, cudaEventRecordExternal);
   }
+  kv->step_args = a;
   RL_CUDA(launch_decode_step(a, m->sm_count, smem, s));
   if (prof) {
     cudaEventRecordWithFlags(kv->ev[1], s, cudaEventRecordExternal);
@@ -1475,13 +1482,13 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
   kv->prof_B = B;
   const bool step = kv->use_step && step_fits(m, kv, B);
   const bool fused = !step && kv->use_fused && fused_fits(m, B);
-  if (step) RL_TRY(prepare_step_phases(m, kv, io, s));
   auto enqueue = [&]() -> rl_status {
     if (step) return enqueue_decode_step(m, kv, io, s);
     if (fused) return enqueue_decode_fused(m, kv, io, decode_attention_chunks(B, m->Hkv, kv->Tmax, m->sm_count), s);
     return enqueue_pass(m, kv, io, w, s);
   };
   if (!is_capturable(s)) {
+    if (step) RL_TRY(prepare_step_phases(m, kv, io, s));
     RL_TRY(enqueue());
   } else {
     GraphKey key;
@@ -1490,7 +1497,7 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
     key.tau = policy->tau;
     key.sched = policy->d_schedule;
     key.sched_len = policy->schedule_len;
-    key.tokens = d_tokens;
+    key.tokens = step ? nullptr : d_tokens;  // step path: a new token pointer is a parameter update
     key.logits = d_logits;
     key.next = d_next_token;
     key.exit = d_exit_layer;
@@ -1500,6 +1507,7 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
     key.fused = fused;
     key.step = step;
     if (!kv->exec || !(key == kv->key)) {
+      if (step) RL_TRY(prepare_step_phases(m, kv, io, s));
       cudaGraph_t g = nullptr;
       RL_CUDA(cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal));
       rl_status st = enqueue();
@@ -1509,6 +1517,16 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
         return st;
       }
       if (e != cudaSuccess) return fail(RL_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e));
+      if (kv->exec && (step || kv->graph)) {
+        // the step path keeps its graph (for node updates): instantiate afresh
+        cudaGraphExecDestroy(kv->exec);
+        kv->exec = nullptr;
+      }
+      if (kv->graph) {
+        cudaGraphDestroy(kv->graph);
+        kv->graph = nullptr;
+        kv->step_node = nullptr;
+      }
       if (kv->exec) {
         cudaGraphExecUpdateResultInfo info;
         if (cudaGraphExecUpdate(kv->exec, g, &info) != cudaSuccess) {
@@ -1525,8 +1543,32 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
           return fail(RL_ERR_CUDA, "graph instantiate: %s", cudaGetErrorString(e));
         }
       }
-      cudaGraphDestroy(g);
+      if (step) {
+        size_t nn = 0;
+        RL_CUDA(cudaGraphGetNodes(g, nullptr, &nn));
+        std::vector<cudaGraphNode_t> nodes(nn);
+        RL_CUDA(cudaGraphGetNodes(g, nodes.data(), &nn));
+        for (cudaGraphNode_t nd : nodes) {
+          cudaGraphNodeType t;
+          RL_CUDA(cudaGraphNodeGetType(nd, &t));
+          if (t == cudaGraphNodeTypeKernel) kv->step_node = nd;
+        }
+        kv->graph = g;
+        if (!kv->step_node) return fail(RL_ERR_CUDA, "decode-step graph holds no kernel node");
+      } else {
+        cudaGraphDestroy(g);
+      }
       kv->key = key;
+    } else if (step && kv->step_node && kv->step_args.tokens != d_tokens) {
+      StepArgs a2 = kv->step_args;
+      a2.tokens = d_tokens;
+      cudaKernelNodeParams kp;
+      RL_CUDA(cudaGraphKernelNodeGetParams(kv->step_node, &kp));
+      void* args[1] = {&a2};
+      kp.kernelParams = args;
+      kp.extra = nullptr;
+      RL_CUDA(cudaGraphExecKernelNodeSetParams(kv->exec, kv->step_node, &kp));
+      kv->step_args = a2;
     }
     RL_CUDA(cudaGraphLaunch(kv->exec, s));
   }
