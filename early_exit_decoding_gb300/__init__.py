@@ -28,8 +28,10 @@ EXPORTS = (
     "rl_quantize_exit_layers", "rl_exit_layer_view", "rl_kv_cache_alloc", "rl_kv_cache_free",
     "rl_kv_view", "rl_kv_position", "rl_kv_set_position", "rl_kv_set_trace", "rl_prefill",
     "rl_decode_step", "rl_decode_step_host", "rl_sync", "rl_decode_kernel_count",
-    "rl_kv_set_profiling", "rl_kv_profile", "rl_lm_head_static",
+    "rl_kv_set_profiling", "rl_kv_profile", "rl_lm_head_static", "rl_kv_set_decode_path",
+    "rl_kv_decode_path",
 )
+RL_PATH_AUTO, RL_PATH_STEP, RL_PATH_FUSED, RL_PATH_GENERIC = range(4)
 KERNEL_KINDS = ("embed", "qkv", "attention", "group_sums", "o_proj", "norm", "gate_up", "down",
                 "layer_end", "lm_head", "argmax", "decode_step")
 
@@ -91,6 +93,8 @@ def _load():
         "rl_kv_profile": (I, [P, P, I, PI, PI, PI, ctypes.POINTER(ctypes.c_float),
                               ctypes.POINTER(ctypes.c_double), PI]),
         "rl_lm_head_static": (I, [P, P, I, P, P, P, P]),
+        "rl_kv_set_decode_path": (I, [P, I]),
+        "rl_kv_decode_path": (I, [P, I]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -215,6 +219,14 @@ def rl_lm_head_static(model, d_h, B, d_logits, d_next_token=None, d_err=None, st
     library's static scratch (allocates nothing)."""
     _check(_lib.rl_lm_head_static(model, _ptr(d_h), B, _ptr(d_logits), _ptr(d_next_token),
                                   _ptr(d_err), _stream(stream)))
+
+
+def rl_kv_set_decode_path(kv, path):
+    _check(_lib.rl_kv_set_decode_path(kv, int(path)))
+
+
+def rl_kv_decode_path(kv, B):
+    return int(_lib.rl_kv_decode_path(kv, B))
 
 
 def rl_kv_set_profiling(kv, enable):
@@ -355,6 +367,12 @@ class KVCache:
     def set_trace(self, t):
         self._trace = t
         rl_kv_set_trace(self.handle, t)
+
+    def set_decode_path(self, path):
+        rl_kv_set_decode_path(self.handle, path)
+
+    def decode_path(self, B):
+        return rl_kv_decode_path(self.handle, B)
 
     def sync(self, stream=None):
         rl_sync(self.model.handle, self.handle, stream)

@@ -160,6 +160,7 @@ struct rl_kv {
   float* st_mid = nullptr;  // per-tile |h_mid|^2 of the O projection's output [d/16][8]
   float* st_end = nullptr;  // per-tile (|h_out|^2, <h_in,h_out>, |h_in|^2) of the layer [d/16][8][3]
   bool use_fused = true;
+  int path_pref = RL_PATH_AUTO;  // rl_kv_set_decode_path
   // persistent step kernel
   bool use_step = true;
   unsigned* bars = nullptr;           // phase arrival counters [nph_cap]
@@ -837,6 +838,22 @@ bool step_fits(const rl_model* m, const rl_kv* kv, int B) {
   return decode_step_occupancy(smem) >= 1;
 }
 
+bool fused_fits(const rl_model* m, int B);
+
+// The kernels a decode step of batch B runs: the persistent step kernel, the
+// fused five-launches-per-layer path, or the generic path (any batch); -1
+// when the path the cache was told to use cannot run this batch.
+int decode_path(const rl_model* m, const rl_kv* kv, int B) {
+  const bool step = kv->use_step && step_fits(m, kv, B);
+  const bool fused = kv->use_fused && fused_fits(m, B);
+  switch (kv->path_pref) {
+    case RL_PATH_STEP: return step ? RL_PATH_STEP : -1;
+    case RL_PATH_FUSED: return fused ? RL_PATH_FUSED : -1;
+    case RL_PATH_GENERIC: return RL_PATH_GENERIC;
+    default: return step ? RL_PATH_STEP : (fused ? RL_PATH_FUSED : RL_PATH_GENERIC);
+  }
+}
+
 std::vector<PhaseDesc> build_step_phases(rl_model* m, rl_kv* kv, const StepIO& io) {
   const int L = m->L, d = m->d, grid = m->sm_count;
   const int tiles_d = d / 16;
@@ -1404,6 +1421,18 @@ rl_status rl_kv_set_position(rl_kv* kv, int32_t pos, int32_t decode_step, rl_str
   return RL_OK;
 }
 
+rl_status rl_kv_set_decode_path(rl_kv* kv, int32_t path) {
+  if (!kv) return fail(RL_ERR_INVALID_ARG, "kv is NULL");
+  if (path < RL_PATH_AUTO || path > RL_PATH_GENERIC) return fail(RL_ERR_INVALID_ARG, "unknown path %d", path);
+  kv->path_pref = path;
+  return RL_OK;
+}
+
+int32_t rl_kv_decode_path(const rl_kv* kv, int32_t B) {
+  if (!kv || B < 1 || B > kv->maxB) return -1;
+  return decode_path(kv->m, kv, B);
+}
+
 rl_status rl_kv_set_trace(rl_kv* kv, float* d_hidden) {
   if (!kv) return fail(RL_ERR_INVALID_ARG, "kv is NULL");
   kv->trace = d_hidden;
@@ -1480,8 +1509,10 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
   const Work w = decode_work(kv, B);
   kv->prof_pos = kv->host_pos;
   kv->prof_B = B;
-  const bool step = kv->use_step && step_fits(m, kv, B);
-  const bool fused = !step && kv->use_fused && fused_fits(m, B);
+  const int path = decode_path(m, kv, B);
+  if (path < 0) return fail(RL_ERR_UNSUPPORTED, "the requested decode path does not fit batch %d", B);
+  const bool step = path == RL_PATH_STEP;
+  const bool fused = path == RL_PATH_FUSED;
   auto enqueue = [&]() -> rl_status {
     if (step) return enqueue_decode_step(m, kv, io, s);
     if (fused) return enqueue_decode_fused(m, kv, io, decode_attention_chunks(B, m->Hkv, kv->Tmax, m->sm_count), s);

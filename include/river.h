@@ -166,6 +166,20 @@ RL_API rl_status rl_kv_set_position(rl_kv* kv, int32_t pos, int32_t decode_step,
  * NULL switches it off. */
 RL_API rl_status rl_kv_set_trace(rl_kv* kv, float* d_hidden);
 
+/* Which kernels run a decode step.  RL_PATH_STEP: one persistent cooperative
+ * kernel per step (batch <= 8, shapes whose activations and weight ring fit in
+ * shared memory, GQA ratio 1, 2 or 4, head_dim 64 or 128); RL_PATH_FUSED: five
+ * launches per layer plus the LM head (batch <= 8); RL_PATH_GENERIC: ten
+ * launches per layer, any batch.  RL_PATH_AUTO (default) takes the first that
+ * fits, in that order.  A forced path that does not fit a call's batch makes
+ * that rl_decode_step return RL_ERR_UNSUPPORTED.  The math is the same on
+ * every path (explainer sections 三, 四); they differ in rounding order only. */
+enum { RL_PATH_AUTO = 0, RL_PATH_STEP = 1, RL_PATH_FUSED = 2, RL_PATH_GENERIC = 3 };
+RL_API rl_status rl_kv_set_decode_path(rl_kv* kv, int32_t path);
+/* The path a decode step of batch B would take (-1: none fits the forced path,
+ * or bad arguments). */
+RL_API int32_t rl_kv_decode_path(const rl_kv* kv, int32_t B);
+
 /* prefill (explainer section 五, sequence-level exit): run d_tokens [B][T]
  * (device int32) at positions 0..T-1, resetting the cache position to 0 and the
  * decode-step counter to 0; one exit decision for all B*T tokens.

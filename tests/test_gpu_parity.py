@@ -40,13 +40,20 @@ def tiny(river, stream):
     return m, om, w
 
 
+PATHS = {"step": 1, "fused": 2, "generic": 3}
+
+
 def _run_sequence(river, m, om, stream, policies, B=1, prompt=32, steps=16, seed=1, trace=True,
-                  max_seq=128):
+                  max_seq=128, path=None):
     """Prefill + decode with teacher forcing on the oracle's greedy tokens.
-    ``policies``: (gpu Policy, oracle Policy) for prefill, then per decode step."""
+    ``policies``: (gpu Policy, oracle Policy) for prefill, then per decode step.
+    ``path``: force the decode kernels (step / fused / generic)."""
     S = m.shape
     toks = synth.gen_tokens(S.vocab, (B, prompt), seed=seed)
     kv = m.kv_cache_alloc(B, max_seq)
+    if path is not None:
+        kv.set_decode_path(PATHS[path])
+        assert kv.decode_path(B) == PATHS[path], f"path {path} does not fit batch {B}"
     st = KVState(S, B, max_seq)
     tr = None
     if trace:
@@ -99,21 +106,24 @@ def test_quantizer_is_bit_exact(river, tiny):
             assert np.array_equal(zt.cpu().numpy().view(np.uint16), z_ref.view(np.uint16)), (l, name)
 
 
-def test_full_depth_matches_oracle(river, tiny, stream):
+@pytest.mark.parametrize("path", ["step", "fused", "generic"])
+def test_full_depth_matches_oracle(river, tiny, stream, path):
     """tau = 1.01 > 1 >= cos: never exits; prompt 32, 16 greedy steps."""
     m, om, _ = tiny
     pol = [(river.Policy.tau_(1.01), OPolicy.tau_(1.01))] * 17
-    res, _ = _run_sequence(river, m, om, stream, pol)
+    res, _ = _run_sequence(river, m, om, stream, pol, path=path)
     assert all(int(o["exit_layer"].item()) == TINY.n_layers for o, _ in res)
 
 
-def test_tau_half_matches_oracle(river, tiny, stream):
+@pytest.mark.parametrize("path", ["step", "fused", "generic"])
+def test_tau_half_matches_oracle(river, tiny, stream, path):
     m, om, _ = tiny
     pol = [(river.Policy.tau_(0.5), OPolicy.tau_(0.5))] * 17
-    _run_sequence(river, m, om, stream, pol)
+    _run_sequence(river, m, om, stream, pol, path=path)
 
 
-def test_forced_schedule_exit_layers_bit_exact(river, tiny, stream):
+@pytest.mark.parametrize("path", ["step", "fused", "generic"])
+def test_forced_schedule_exit_layers_bit_exact(river, tiny, stream, path):
     m, om, _ = tiny
     L = TINY.n_layers
     sched = [L, 1, 0, 2, 3, 4, 1, 1, 2, 0, 4, 3, 2, 1, 0, 1, 2]
@@ -121,16 +131,17 @@ def test_forced_schedule_exit_layers_bit_exact(river, tiny, stream):
     d_pre = torch.tensor([sched[0]], dtype=torch.int32, device="cuda")
     pol = [(river.Policy.forced(d_pre), OPolicy.forced(sched[0]))]
     pol += [(river.Policy.forced(d_sched), OPolicy.forced(e)) for e in sched[1:]]
-    res, _ = _run_sequence(river, m, om, stream, pol)
+    res, _ = _run_sequence(river, m, om, stream, pol, path=path)
     assert [int(o["exit_layer"].item()) for o, _ in res] == sched
 
 
-def test_batch_min_rule_batch3(river, tiny, stream):
+@pytest.mark.parametrize("path", ["step", "fused", "generic"])
+def test_batch_min_rule_batch3(river, tiny, stream, path):
     """Batch of 3: the minimum over the batch decides (section 四)."""
     m, om, _ = tiny
     for tau in (0.3, 0.5, 0.7):
         pol = [(river.Policy.tau_(tau), OPolicy.tau_(tau))] * 7
-        _run_sequence(river, m, om, stream, pol, B=3, prompt=12, steps=6, seed=4)
+        _run_sequence(river, m, om, stream, pol, B=3, prompt=12, steps=6, seed=4, path=path)
 
 
 def test_batch_forced_and_ragged_shapes(river, stream):
