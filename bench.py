@@ -108,14 +108,6 @@ class Clocks:
                  "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-        # nvidia-smi's start-up (driver and NVML initialisation) can hold up
-        # GPU work submission: start timing only once it is sampling
-        t0 = time.time()
-        while self.proc is not None and time.time() - t0 < 10.0:
-            self.f.flush()
-            if os.path.getsize(self.out) > 0:
-                break
-            time.sleep(0.05)
 
     def stop(self):
         if self.proc is None:
@@ -200,14 +192,24 @@ def run_river(args, rank, world, dev):
     def timed(policy, K, W, flush_clocks=None):
         state["i"] = 0
         kv.set_position(T, 0, stream)
+        # the clock sampler starts before the warm-up, which runs at least W
+        # steps and at least half a second, so that neither the sampler's
+        # start-up nor a GPU still leaving idle clocks falls in the timed region
+        clocks = Clocks(args.smi_id) if flush_clocks else None
         with torch.cuda.stream(stream):
-            for _ in range(W):
+            t_w = time.time()
+            n_w = 0
+            while n_w < W or time.time() - t_w < 0.5:
                 one_step(policy)
+                n_w += 1
+                if n_w % 32 == 0:
+                    stream.synchronize()
+            state["i"] = 0
+            kv.set_position(T, 0, stream)
             kv.sync(stream)
             if world > 1:
                 torch.distributed.barrier()
             torch.cuda.synchronize()
-            clocks = Clocks(args.smi_id) if flush_clocks else None
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             resets = 0
