@@ -52,6 +52,7 @@ struct Linear {
   int N = 0, K = 0, Kp = 0;
   int view_base = 0;        // first rl linear index this fused matrix maps to
   const int2* rowmap = nullptr;
+  CUtensorMap tm;           // TMA map of w for the tensor-core GEMM (128 x 64 boxes)
 };
 
 struct Layer {
@@ -70,6 +71,7 @@ struct rl_model {
   bf16* embed = nullptr;
   bf16* lm_head = nullptr;  // [V][Kd]
   bf16* lm_head_t = nullptr;  // unit-tiled copy
+  CUtensorMap tm_lm;          // TMA map of lm_head for the tensor-core GEMM
   bool step_ok = false;       // the persistent step kernel can be launched cooperatively
   float* g_final = nullptr;
   float* inv_freq = nullptr;
@@ -147,6 +149,7 @@ struct rl_kv {
   bf16 *x_attn = nullptr, *x_ffn = nullptr, *o = nullptr, *u = nullptr;
   float *xs_attn = nullptr, *xs_ffn = nullptr, *xs_o = nullptr, *xs_u = nullptr;
   float* q = nullptr;
+  float2* rope_cs = nullptr;  // (cos, sin) of pos * inv_freq[i], [Tmax][hd/2]
   float* part = nullptr;
   int nchunks_cap = 1;
   float* cosbuf = nullptr;
@@ -362,6 +365,24 @@ struct Work {
   float* cosbuf;
 };
 
+// Below this many tokens the GEMV's weight stream is the whole cost and the
+// tensor-core GEMM gains nothing.
+constexpr int kTcMinTokens = 16;
+
+// One projection over a.B tokens: the bf16 weights on the tensor cores (or
+// the GEMV for a few tokens), the exit river's W4 weights in the dequantising
+// GEMV; which of the two runs is decided on the device.
+rl_status project(const rl_model* m, const CUtensorMap& tm, GemvArgs a, cudaStream_t s) {
+  if (a.B >= kTcMinTokens) {
+    RL_CUDA(launch_gemm_tc(tm, a, m->sm_count, s));
+    if (a.w4_mode == W4_OFF) return RL_OK;
+    a.w4_only = 1;
+  }
+  launch_gemv(a, m->sm_count, s);
+  RL_LAUNCHED();
+  return RL_OK;
+}
+
 rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, cudaStream_t s) {
   const int L = m->L, d = m->d;
   Prof pf{kv, s, kv->profiling && !io.prefill};
@@ -403,19 +424,18 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
   RL_LAUNCHED();
   pf.end(RL_K_EMBED, 0, 0, 0, false);
 
-  const int colstep = prefill ? kMaxBatch : M;
   int cur = 0;
   for (int l = 0; l < L; ++l) {
     const Layer& ly = m->layers[l];
     const int mid = (cur + 1) % 3, nxt = (cur + 2) % 3;
     // QKV + RoPE + KV append
-    for (int cb = 0; cb < M; cb += colstep) {
+    {
       GemvArgs a = gemv_base(m, ly.qkv, w4mode, kv->st, l + 1);
-      a.x = w.x_attn + (size_t)cb * m->Kd;
+      a.x = w.x_attn;
       a.ldx = m->Kd;
-      a.xsum = w.xs_attn + (size_t)cb * Gd;
+      a.xsum = w.xs_attn;
       a.ldxs = Gd;
-      a.B = std::min(colstep, M - cb);
+      a.B = M;
       a.epi = EPI_QKV_ROPE;
       a.q_out = w.q;
       a.kc = kv->K[l];
@@ -427,13 +447,13 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       a.hd = m->hd;
       a.pos_ptr = &kv->st->pos;
       a.T_prefill = prefill ? T : 0;
-      a.col_base = cb;
+      a.col_base = 0;
       a.inv_freq = m->inv_freq;
+      a.rope_cs = kv->rope_cs;
       a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      launch_gemv(a, m->sm_count, s);
-      RL_LAUNCHED();
+      RL_TRY(project(m, ly.qkv.tm, a, s));
       pf.end(RL_K_QKV, l + 1, bytes_bf16(ly.qkv), bytes_w4(ly.qkv), true);
     }
     // attention over the shared cache
@@ -463,22 +483,22 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
     RL_LAUNCHED();
     pf.end(RL_K_GSUM, l + 1, 0, 0, false);
     // O projection + residual
-    for (int cb = 0; cb < M; cb += colstep) {
+    {
       GemvArgs a = gemv_base(m, ly.o, w4mode, kv->st, l + 1);
-      a.x = w.o + (size_t)cb * m->Ko;
+      a.x = w.o;
       a.ldx = m->Ko;
-      a.xsum = w.xs_o + (size_t)cb * Go;
+      a.xsum = w.xs_o;
       a.ldxs = Go;
-      a.B = std::min(colstep, M - cb);
+      a.B = M;
       a.epi = EPI_RESID;
-      a.out = w.h[mid] + (size_t)cb * d;
+      a.out = w.h[mid];
       a.ldo = d;
-      a.resid = w.h[cur] + (size_t)cb * d;
+      a.resid = w.h[cur];
       a.ldr = d;
+      a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      launch_gemv(a, m->sm_count, s);
-      RL_LAUNCHED();
+      RL_TRY(project(m, ly.o.tm, a, s));
       pf.end(RL_K_O, l + 1, bytes_bf16(ly.o), bytes_w4(ly.o), true);
     }
     // pre-FFN RMSNorm
@@ -499,20 +519,20 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
     RL_LAUNCHED();
     pf.end(RL_K_NORM, l + 1, 0, 0, false);
     // gate/up + SwiGLU
-    for (int cb = 0; cb < M; cb += colstep) {
+    {
       GemvArgs a = gemv_base(m, ly.gu, w4mode, kv->st, l + 1);
-      a.x = w.x_ffn + (size_t)cb * m->Kd;
+      a.x = w.x_ffn;
       a.ldx = m->Kd;
-      a.xsum = w.xs_ffn + (size_t)cb * Gd;
+      a.xsum = w.xs_ffn;
       a.ldxs = Gd;
-      a.B = std::min(colstep, M - cb);
+      a.B = M;
       a.epi = EPI_SWIGLU;
-      a.out_h = w.u + (size_t)cb * m->Kf;
+      a.out_h = w.u;
       a.ldoh = m->Kf;
+      a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      launch_gemv(a, m->sm_count, s);
-      RL_LAUNCHED();
+      RL_TRY(project(m, ly.gu.tm, a, s));
       pf.end(RL_K_GU, l + 1, bytes_bf16(ly.gu), bytes_w4(ly.gu), true);
     }
     pf.begin();
@@ -520,22 +540,22 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
     RL_LAUNCHED();
     pf.end(RL_K_GSUM, l + 1, 0, 0, false);
     // down + residual
-    for (int cb = 0; cb < M; cb += colstep) {
+    {
       GemvArgs a = gemv_base(m, ly.dn, w4mode, kv->st, l + 1);
-      a.x = w.u + (size_t)cb * m->Kf;
+      a.x = w.u;
       a.ldx = m->Kf;
-      a.xsum = w.xs_u + (size_t)cb * Gf;
+      a.xsum = w.xs_u;
       a.ldxs = Gf;
-      a.B = std::min(colstep, M - cb);
+      a.B = M;
       a.epi = EPI_RESID;
-      a.out = w.h[nxt] + (size_t)cb * d;
+      a.out = w.h[nxt];
       a.ldo = d;
-      a.resid = w.h[mid] + (size_t)cb * d;
+      a.resid = w.h[mid];
       a.ldr = d;
+      a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      launch_gemv(a, m->sm_count, s);
-      RL_LAUNCHED();
+      RL_TRY(project(m, ly.dn.tm, a, s));
       pf.end(RL_K_DOWN, l + 1, bytes_bf16(ly.dn), bytes_w4(ly.dn), true);
     }
     // layer end: cosine, batch-min, tau compare, next RMSNorm
@@ -585,10 +605,10 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
     a.epi = EPI_STORE;
     a.out = io.logits;
     a.ldo = m->V;
+    a.err = &kv->st->err;
     pf.begin();
     a.path_out = pf.slot();
-    launch_gemv(a, m->sm_count, s);
-    RL_LAUNCHED();
+    RL_TRY(project(m, m->tm_lm, a, s));
     const double lm = (double)m->V * m->d * 2.0;
     pf.end(RL_K_LM_HEAD, 0, lm, lm, true);
   }
@@ -1153,6 +1173,17 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
   gemv_fused_setup();
   attention_setup();
   decode_step_setup();
+  if (!tc_gemm_available()) {
+    delete m;
+    return fail(RL_ERR_CUDA, "the driver does not export cuTensorMapEncodeTiled");
+  }
+  {
+    cudaError_t e = tc_gemm_init();
+    if (e != cudaSuccess) {
+      delete m;
+      return fail(RL_ERR_CUDA, "tensor-core GEMM setup: %s", cudaGetErrorString(e));
+    }
+  }
   {
     int coop = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
@@ -1194,6 +1225,8 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
     RL_TRY(m->alloc(&lin.w, (size_t)N * lin.Kp));
     launch_gather_rows(lin.w, lin.Kp, N, K, map, src, K, s);
     RL_LAUNCHED();
+    if (!make_weight_tmap(&lin.tm, lin.w, N, lin.Kp))
+      return fail(RL_ERR_CUDA, "tensor map of a %d x %d weight could not be encoded", N, lin.Kp);
     RL_TRY(m->alloc(&lin.wt, (size_t)N * lin.Kp));
     launch_bf16_tile_layout(lin.w, N, lin.Kp, lin.wt, s);
     RL_LAUNCHED();
@@ -1223,6 +1256,8 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
   M_TRY(m->alloc(&m->lm_head, (size_t)m->V * m->Kd));
   launch_gather_rows(m->lm_head, m->Kd, m->V, m->d, m->map_id,
                      GatherSrcs{{(const bf16*)wts->lm_head, nullptr, nullptr}}, m->d, s);
+  if (!make_weight_tmap(&m->tm_lm, m->lm_head, m->V, m->Kd))
+    return bail(fail(RL_ERR_CUDA, "tensor map of the LM head could not be encoded"));
   M_TRY(m->alloc(&m->lm_head_t, (size_t)m->V * m->Kd));
   launch_bf16_tile_layout(m->lm_head, m->V, m->Kd, m->lm_head_t, s);
   M_TRY(m->alloc(&m->g_final, m->d));
@@ -1384,6 +1419,12 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
   K_TRY(kv->alloc(&kv->d_exit, 1));
   K_TRY(kv->alloc(&kv->d_logits, (size_t)B * m->V));
   K_TRY(kv->alloc(&kv->d_mincos, (size_t)m->L));
+  K_TRY(kv->alloc(&kv->rope_cs, (size_t)max_seq * (m->hd / 2)));
+  launch_rope_table(m->inv_freq, m->hd / 2, max_seq, kv->rope_cs, 0);
+  {
+    cudaError_t e = cudaStreamSynchronize(0);
+    if (e != cudaSuccess) return bail(fail(RL_ERR_CUDA, "RoPE table: %s", cudaGetErrorString(e)));
+  }
 #undef K_TRY
   *out = kv;
   return RL_OK;

@@ -1,0 +1,483 @@
+// Tensor-core GEMM for the many-token passes (prefill, large decode
+// batches): out[t][n] = sum_k W[n][k] x[t][k] with the backbone's bf16
+// weights, on the 5th-generation tensor cores (tcgen05, accumulators in
+// tensor memory), operands brought in by TMA.
+//
+// The projection is computed "swap-AB": the MMA's M side is 128 weight rows
+// (output features), its N side is BN tokens, so one kernel serves a
+// 32-token decode batch (BN = 32) and a 2048-token prompt (BN = 256) alike,
+// and the epilogue reads one feature per TMEM lane, i.e. 32 consecutive
+// features per warp, which makes every output store a coalesced row segment.
+// The epilogues are the decode GEMV's (store, residual add, SwiGLU on the
+// interleaved gate/up rows, RoPE + K/V append on the permuted QKV rows; the
+// row orders put each rotate-half / gate-up pair 8 rows apart, so a pair sits
+// in one warp and is exchanged with one shuffle).
+//
+// The weights of exit layers are W4 and run in the dequantising GEMV: this
+// kernel returns at once when the device-side exit layer says the layer is on
+// the exit river (River-LLM explainer, section 四).
+//
+// Persistent CTAs (one per SM) walk the output tiles; 320 threads: warp 0
+// lane 0 issues the TMA loads into a STAGES-deep ring of (128 x 64 weight
+// tile, BN x 64 token tile), warp 1 owns the tensor-memory allocation (two
+// BN-column fp32 accumulators) and its lane 0 issues the MMAs, warps 2..9 run
+// the epilogue of one tile while the MMAs of the next fill the other
+// accumulator (warp w reads TMEM lanes 32 (w % 4) .. +31, one half of the
+// columns).  Every wait is bounded; a wait that runs out sets
+// RL_DEVERR_TIMEOUT and the CTA winds down (all MMAs retired, all copies
+// landed, tensor memory freed).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "dev_common.cuh"
+#include "internal.h"
+
+namespace river {
+
+namespace {
+
+using dev::smem_u32;
+
+constexpr int kThreadsTc = 320;
+constexpr int kBM = 128;           // weight rows per tile (MMA M)
+constexpr int kBK = 64;            // K per stage: one 128-byte swizzle row of bf16
+constexpr int kABytes = kBM * kBK * 2;
+constexpr long long kSpinTc = 1ll << 20;
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes, 8-row (1024-byte) swizzle atoms
+// stacked along M/N (stride byte offset 1024), the tile base 1024-aligned.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);        // start address
+  d |= (uint64_t)1 << 16;                          // leading byte offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset
+  d |= (uint64_t)1 << 46;                          // descriptor version
+  d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both
+// K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_tc(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+// Arrives on `bar` once every MMA this thread issued before has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 16 consecutive fp32 columns: thread i of the warp gets lane
+// (taddr lane + i), columns taddr col .. +15.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// SiLU for the gate/up epilogue (fast reciprocal: the product is rounded to
+// bf16 right after).
+__device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.f + __expf(-v)); }
+
+// Epilogue of one 16-column chunk: this thread's feature row R (< N when
+// `row_ok`) for launch columns col0 .. col0 + 15 (those < B), read from the
+// accumulator at `taddr`.  All 32 lanes of the warp call it together (the
+// gate/up and rotate-half partners, 8 rows apart, are exchanged by shuffles).
+__device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok, int lane,
+                                          int col0, uint32_t taddr) {
+  const int nc = min(16, a.B - col0);
+  float v[16];
+  if (a.epi == EPI_RESID) {
+    float r[16];  // residual loads issued before the accumulator read
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      r[j] = (row_ok && j < nc) ? __ldg(a.resid + (size_t)(col0 + j) * a.ldr + R) : 0.f;
+    tmem_ld16(taddr, v);
+    if (row_ok) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < nc) a.out[(size_t)(col0 + j) * a.ldo + R] = v[j] + r[j];
+    }
+    return;
+  }
+  tmem_ld16(taddr, v);
+  if (a.epi == EPI_STORE) {
+    if (row_ok) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < nc) a.out[(size_t)(col0 + j) * a.ldo + R] = v[j];
+    }
+    return;
+  }
+  float o[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j] = __shfl_xor_sync(0xffffffffu, v[j], 8);
+  const bool low = (lane & 8) == 0;
+  if (a.epi == EPI_SWIGLU) {
+    if (row_ok && low) {
+      bf16* dst = a.out_h + (R >> 4) * 8 + (R & 7);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < nc) dst[(size_t)(col0 + j) * a.ldoh] = __float2bfloat16_rn(silu_fast(v[j]) * o[j]);
+    }
+    return;
+  }
+  // EPI_QKV_ROPE: row R of head R / hd holds dim 8 jt + (R % 8) (+ hd/2 in
+  // the upper half of its 16-row tile), jt = (R % hd) / 16.
+  if (!row_ok) return;
+  const int hd = a.hd, half = hd / 2;
+  const int head_all = R / hd;
+  const int dim0 = 8 * ((R % hd) >> 4) + (R & 7);
+  const int dim = low ? dim0 : dim0 + half;
+  const bool rot = head_all < a.Hq + a.Hkv;
+  const bool is_q = head_all < a.Hq;
+  const bool is_k = !is_q && rot;
+  const int hk = is_q ? 0 : (is_k ? head_all - a.Hq : head_all - a.Hq - a.Hkv);
+  bf16* cache = is_k ? a.kc : a.vc;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j >= nc) break;
+    const int c = col0 + j;
+    int seq, pos, qrow;
+    if (a.T_prefill > 0) {
+      const int tok = a.col_base + c;
+      seq = tok / a.T_prefill;
+      pos = tok - seq * a.T_prefill;
+      qrow = tok;
+    } else {
+      seq = c;
+      pos = *a.pos_ptr;
+      qrow = c;
+    }
+    const bool in_cache = pos >= 0 && pos < a.Tmax;
+    float x = v[j];
+    if (rot) {
+      float sn, cs;
+      if (a.rope_cs != nullptr && in_cache) {
+        const float2 t = a.rope_cs[(size_t)pos * half + dim0];
+        cs = t.x;
+        sn = t.y;
+      } else {
+        sincosf((float)pos * a.inv_freq[dim0], &sn, &cs);
+      }
+      x = low ? x * cs - o[j] * sn : x * cs + o[j] * sn;
+    }
+    if (is_q) {
+      a.q_out[(size_t)qrow * a.Hq * hd + head_all * hd + dim] = x;
+    } else if (!in_cache) {
+      atomicOr(a.err, RL_DEVERR_CAPACITY);
+    } else {
+      cache[(((size_t)seq * a.Hkv + hk) * a.Tmax + pos) * hd + dim] = __float2bfloat16_rn(x);
+    }
+  }
+}
+
+constexpr int kEpiWarps = 8;
+
+// Persistent: CTA b takes tiles b, b + grid, ...; tile t covers weight rows
+// (t / tiles_m) * 128 .. +127 and tokens (t % tiles_m) * BN .. +BN-1, so the
+// CTAs running at one time share weight tiles in L2.  Two accumulators in
+// tensor memory: the epilogue of tile i overlaps the MMAs of tile i + 1.
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              const GemvArgs a) {
+  constexpr int kBBytes = BN * kBK * 2;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  bool w4 = a.w4_mode == W4_ON;
+  if (a.w4_mode == W4_BY_LAYER) w4 = a.layer_no > *a.exit_layer;
+  if (a.path_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && !w4) *a.path_out = 0;
+  if (w4) return;  // the exit river's W4 weights run in the dequantising GEMV
+
+  extern __shared__ unsigned char smem_dyn[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + STAGES * kABytes;
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], mma_done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_fail;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_m = (a.B + BN - 1) / BN;
+  const int ntiles = ((a.N + kBM - 1) / kBM) * tiles_m;
+  const int nk = a.Kp / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      dev::mbar_init(&full[i], 1);
+      dev::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      dev::mbar_init(&acc_full[i], 1);
+      dev::mbar_init(&acc_empty[i], kEpiWarps);
+    }
+    dev::mbar_init(&mma_done, 1);
+    s_fail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tma_prefetch_map(&tmW);
+    tma_prefetch_map(&tmX);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      int g = 0;      // k-blocks issued by this CTA
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const int n0 = (t / tiles_m) * kBM, m0 = (t % tiles_m) * BN;
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % STAGES, n = g / STAGES;
+          if (n > 0 && !dev::mbar_wait(&empty[s], (n - 1) & 1, kSpinTc)) {
+            s_fail = 1;
+            ok = false;
+            break;
+          }
+          dev::mbar_expect_tx(&full[s], kABytes + kBBytes);
+          tma_load_2d(sA + s * kABytes, &tmW, kb * kBK, n0, &full[s]);
+          tma_load_2d(sB + s * kBBytes, &tmX, kb * kBK, m0, &full[s]);
+        }
+      }
+      // the CTA may not exit with copies in flight: wait (bounded) for the
+      // last ones it issued
+      for (int g2 = g - STAGES < 0 ? 0 : g - STAGES; g2 < g; ++g2)
+        dev::mbar_wait(&full[g2 % STAGES], (g2 / STAGES) & 1, kSpinTc);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      const uint32_t idesc = idesc_bf16(kBM, BN);
+      int g = 0, i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+        const int acc = i & 1, u = i >> 1;
+        if (u > 0 && !dev::mbar_wait(&acc_empty[acc], (u - 1) & 1, kSpinTc)) {
+          s_fail = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < nk; ++kb, ++g) {
+          const int s = g % STAGES;
+          if (!dev::mbar_wait(&full[s], (g / STAGES) & 1, kSpinTc)) {
+            s_fail = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(smem_u32(sA + s * kABytes));
+          const uint64_t bd = sw128_desc(smem_u32(sB + s * kBBytes));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes = 2 in the address field
+            mma_tc(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+          mma_commit(&empty[s]);
+        }
+        mma_commit(&acc_full[acc]);
+      }
+      // every MMA has completed before tensor memory is released
+      mma_commit(&mma_done);
+      dev::mbar_wait(&mma_done, 0, kSpinTc);
+    }
+  } else {  // epilogue warps 2 .. 9: lane quarter warp % 4, column half (warp - 2) / 4
+    const int q = warp & 3, h = (warp - 2) >> 2;
+    int i = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+      const int acc = i & 1, u = i >> 1;
+      const int n0 = (t / tiles_m) * kBM, m0 = (t % tiles_m) * BN;
+      if (!dev::mbar_wait(&acc_full[acc], u & 1, kSpinTc)) {
+        s_fail = 1;
+        break;
+      }
+      tc_fence_after();
+      const int R = n0 + 32 * q + lane;
+      const bool row_ok = R < a.N;
+#pragma unroll 1
+      for (int c16 = h * (BN / 32); c16 < (h + 1) * (BN / 32); ++c16) {
+        const int col0 = m0 + c16 * 16;
+        if (col0 >= a.B) break;
+        epi_chunk(a, R, row_ok, lane, col0,
+                  tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + c16 * 16));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&acc_empty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  }
+  if (threadIdx.x == 0 && s_fail && a.err != nullptr) atomicOr(a.err, RL_DEVERR_TIMEOUT);
+}
+
+template <int BN, int STAGES>
+constexpr int tc_smem_bytes() {
+  return STAGES * (kABytes + BN * kBK * 2) + 1024;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+template <int BN, int STAGES>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(k_gemm_tc<BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              tc_smem_bytes<BN, STAGES>());
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s) {
+  constexpr int smem = tc_smem_bytes<BN, STAGES>();
+  CUtensorMap tmX;
+  if (!make_tmap_bf16(&tmX, a.x, a.Kp, a.B, a.ldx, BN)) return cudaErrorInvalidValue;
+  int grid = ((a.N + kBM - 1) / kBM) * ((a.B + BN - 1) / BN);
+  if (grid > sm_count) grid = sm_count;
+  k_gemm_tc<BN, STAGES><<<grid, kThreadsTc, smem, s>>>(tmW, tmX, a);
+  return cudaGetLastError();
+}
+
+__global__ void k_rope_table(const float* inv_freq, int half, int n, float2* out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int pos = i / half, dim = i - pos * half;
+  float sn, cs;
+  sincosf((float)pos * inv_freq[dim], &sn, &cs);
+  out[i] = make_float2(cs, sn);
+}
+
+}  // namespace
+
+void launch_rope_table(const float* inv_freq, int half, int Tmax, float2* out, cudaStream_t s) {
+  const int n = half * Tmax;
+  if (n > 0) k_rope_table<<<(n + 255) / 256, 256, 0, s>>>(inv_freq, half, n, out);
+}
+
+bool tc_gemm_available() { return encode_fn() != nullptr; }
+
+// Shared-memory opt-in of every instantiation (once per process and device,
+// before any launch or graph capture).
+cudaError_t tc_gemm_init() {
+  cudaError_t e = set_smem_attr<256, 4>();
+  if (e == cudaSuccess) e = set_smem_attr<128, 6>();
+  if (e == cudaSuccess) e = set_smem_attr<64, 8>();
+  if (e == cudaSuccess) e = set_smem_attr<32, 8>();
+  return e;
+}
+
+// 2-D bf16 tensor map over rows x inner (row stride ld elements), boxes of
+// 64 inner elements (128 bytes, 128-byte swizzle) x box_rows rows; reads
+// outside the tensor fill zeros.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int ld, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr || base == nullptr || inner <= 0 || rows <= 0 || box_rows <= 0 || box_rows > 256)
+    return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || ((size_t)ld * 2) % 16 != 0 || inner % kBK != 0)
+    return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_weight_tmap(CUtensorMap* map, const bf16* w, int N, int Kp) {
+  return make_tmap_bf16(map, w, Kp, N, Kp, kBM);
+}
+
+// Token tile: the width whose estimated makespan (tiles per CTA x the tile's
+// time, from the MMA efficiency measured per width on GB300) is smallest.
+int tc_pick_bn(int N, int M, int sm_count) {
+  static const int widths[4] = {256, 128, 64, 32};
+  static const float eff[4] = {1.0f, 0.65f, 0.35f, 0.2f};
+  const int tn = (N + kBM - 1) / kBM;
+  int best = 32;
+  float best_cost = 1e30f;
+  for (int i = 0; i < 4; ++i) {
+    const int bn = widths[i];
+    if (bn > 32 && bn / 2 >= M) continue;  // more than half the tile would be padding
+    const int tiles = tn * ((M + bn - 1) / bn);
+    const float cost = (float)((tiles + sm_count - 1) / sm_count) * bn / eff[i];
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s) {
+  if (a.B <= 0 || a.N <= 0) return cudaSuccess;
+  switch (tc_pick_bn(a.N, a.B, sm_count)) {
+    case 256: return launch_tc<256, 4>(tmW, a, sm_count, s);
+    case 128: return launch_tc<128, 6>(tmW, a, sm_count, s);
+    case 64: return launch_tc<64, 8>(tmW, a, sm_count, s);
+    default: return launch_tc<32, 8>(tmW, a, sm_count, s);
+  }
+}
+
+}  // namespace river

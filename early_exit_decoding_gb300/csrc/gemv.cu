@@ -54,7 +54,7 @@ __device__ __forceinline__ uint32_t u4get(const uint4& v, int i) {
 // Lane (g = lane/4, t = lane%4) owns rows g and g+8 and, in group gi, the
 // 32 inputs gi*128 + 32t .. +31.
 template <int NT, bool W4>
-__device__ __forceinline__ void tile_partial(const GemvArgs& a, int rt, int warp, int lane,
+__device__ __forceinline__ void tile_partial(const GemvArgs& a, int rt, int cb, int warp, int lane,
                                              float (&y)[NT][4]) {
   const int g = lane >> 2, t = lane & 3;
   const int r0 = rt * 16 + g, r1 = r0 + 8;
@@ -80,7 +80,7 @@ __device__ __forceinline__ void tile_partial(const GemvArgs& a, int rt, int warp
         uint4 X[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          const int col = j * 8 + g;
+          const int col = cb + j * 8 + g;
           X[j] = col < a.B ? ldg_x(a.x + (size_t)col * a.ldx + gi * 128 + 32 * t + 8 * m)
                            : make_uint4(0, 0, 0, 0);
         }
@@ -106,7 +106,7 @@ __device__ __forceinline__ void tile_partial(const GemvArgs& a, int rt, int warp
       const float o0 = 128.f + sz0.y, o1 = 128.f + sz1.y;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        const int c0 = j * 8 + 2 * t, c1 = c0 + 1;
+        const int c0 = cb + j * 8 + 2 * t, c1 = c0 + 1;
         const float xs0 = c0 < a.B ? a.xsum[(size_t)c0 * a.ldxs + gi] : 0.f;
         const float xs1 = c1 < a.B ? a.xsum[(size_t)c1 * a.ldxs + gi] : 0.f;
         y[j][0] += sz0.x * (acc[j][0] - o0 * xs0);
@@ -128,7 +128,7 @@ __device__ __forceinline__ void tile_partial(const GemvArgs& a, int rt, int warp
         uint4 X[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          const int col = j * 8 + g;
+          const int col = cb + j * 8 + g;
           X[j] = col < a.B ? ldg_x(a.x + (size_t)col * a.ldx + gi * 128 + 32 * t + 8 * hq)
                            : make_uint4(0, 0, 0, 0);
         }
@@ -148,18 +148,19 @@ __device__ __forceinline__ void tile_partial(const GemvArgs& a, int rt, int warp
 __device__ __forceinline__ float silu_f(float v) { return v / (1.f + __expf(-v)); }
 
 // Epilogue on a finished tile: tile[r][c] holds output row rt*16 + r for
-// column c (< B).
+// column cb + c (< B).
 template <int NT>
-__device__ void epilogue(const GemvArgs& a, int rt, const float (*tile)[NT * 8]) {
+__device__ void epilogue(const GemvArgs& a, int rt, int cb, const float (*tile)[NT * 8]) {
   const int tid = threadIdx.x;
-  const int ncol = a.B;
+  const int ncol = min(NT * 8, a.B - cb);
   if (a.epi == EPI_STORE || a.epi == EPI_RESID) {
     for (int idx = tid; idx < 16 * ncol; idx += blockDim.x) {
       const int c = idx / 16, r = idx % 16;
       const int n = rt * 16 + r;
+      const size_t gc = (size_t)(cb + c);
       float v = tile[r][c];
-      if (a.epi == EPI_RESID) v += a.resid[(size_t)c * a.ldr + n];
-      a.out[(size_t)c * a.ldo + n] = v;
+      if (a.epi == EPI_RESID) v += a.resid[gc * a.ldr + n];
+      a.out[gc * a.ldo + n] = v;
     }
     return;
   }
@@ -167,7 +168,7 @@ __device__ void epilogue(const GemvArgs& a, int rt, const float (*tile)[NT * 8])
     for (int idx = tid; idx < 8 * ncol; idx += blockDim.x) {
       const int c = idx / 8, r = idx % 8;
       const float gv = tile[r][c], uv = tile[r + 8][c];
-      a.out_h[(size_t)c * a.ldoh + rt * 8 + r] = __float2bfloat16_rn(silu_f(gv) * uv);
+      a.out_h[(size_t)(cb + c) * a.ldoh + rt * 8 + r] = __float2bfloat16_rn(silu_f(gv) * uv);
     }
     return;
   }
@@ -182,19 +183,25 @@ __device__ void epilogue(const GemvArgs& a, int rt, const float (*tile)[NT * 8])
     const int dim = 8 * jt + r;
     int seq, pos, qrow;
     if (a.T_prefill > 0) {
-      const int tok = a.col_base + c;
+      const int tok = a.col_base + cb + c;
       seq = tok / a.T_prefill;
       pos = tok % a.T_prefill;
       qrow = tok;
     } else {
-      seq = c;
+      seq = cb + c;
       pos = *a.pos_ptr;
-      qrow = c;
+      qrow = cb + c;
     }
     float lo = tile[r][c], hi = tile[r + 8][c];
     if (head_all < a.Hq + a.Hkv) {  // q or k head: rotate
       float sn, cs;
-      sincosf((float)pos * a.inv_freq[dim], &sn, &cs);
+      if (a.rope_cs != nullptr && pos >= 0 && pos < a.Tmax) {
+        const float2 cs_sn = a.rope_cs[(size_t)pos * half + dim];
+        cs = cs_sn.x;
+        sn = cs_sn.y;
+      } else {
+        sincosf((float)pos * a.inv_freq[dim], &sn, &cs);
+      }
       const float nlo = lo * cs - hi * sn;
       const float nhi = hi * cs + lo * sn;
       lo = nlo;
@@ -226,14 +233,17 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv(GemvArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bool w4 = a.w4_mode == W4_ON;
   if (a.w4_mode == W4_BY_LAYER) w4 = a.layer_no > *a.exit_layer;
+  if (a.w4_only && !w4) return;  // the tensor-core GEMM ran the bf16 weights
   if (a.path_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.path_out = w4 ? 1 : 0;
   const int ntiles = a.N / 16;
-  for (int rt = blockIdx.x; rt < ntiles; rt += gridDim.x) {
+  const int nitems = ntiles * ((a.B + NT * 8 - 1) / (NT * 8));
+  for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+    const int rt = item % ntiles, cb = (item / ntiles) * NT * 8;
     float y[NT][4];
     if (w4)
-      tile_partial<NT, true>(a, rt, warp, lane, y);
+      tile_partial<NT, true>(a, rt, cb, warp, lane, y);
     else
-      tile_partial<NT, false>(a, rt, warp, lane, y);
+      tile_partial<NT, false>(a, rt, cb, warp, lane, y);
 #pragma unroll
     for (int j = 0; j < NT; ++j) red[warp][j][lane] = make_float4(y[j][0], y[j][1], y[j][2], y[j][3]);
     __syncthreads();
@@ -251,7 +261,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv(GemvArgs a) {
       tile[r][c] = s;
     }
     __syncthreads();
-    epilogue<NT>(a, rt, tile);
+    epilogue<NT>(a, rt, cb, tile);
     __syncthreads();
   }
 }
@@ -259,7 +269,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_gemv(GemvArgs a) {
 }  // namespace
 
 void launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t s) {
-  const int ntiles = a.N / 16;
+  const int ntiles = a.N / 16 * ((a.B + kMaxBatch - 1) / kMaxBatch);
   int grid = sm_count * 4;
   if (grid > ntiles) grid = ntiles;
   if (grid < 1) grid = 1;

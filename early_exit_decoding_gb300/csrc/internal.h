@@ -2,6 +2,7 @@
 // libriver.so.  Nothing here is part of the C ABI (see include/river.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -57,7 +58,7 @@ struct GemvArgs {
   int ldx;
   const float* xsum;      // per (b, group) sum of x, [B][ldxs] (W4 path only)
   int ldxs;
-  int B;                  // columns in this launch (<= 64)
+  int B;                  // columns (tokens) in this launch; k_gemv walks them 64 at a time
   int epi;
   float* out; int ldo;            // STORE / RESID
   const float* resid; int ldr;    // RESID
@@ -70,11 +71,27 @@ struct GemvArgs {
   int T_prefill;          // >0: column c is token (col_base + c) = seq*T + t at position t
   int col_base;
   const float* inv_freq;  // [hd/2]
+  const float2* rope_cs;  // nullable: (cos, sin) of pos * inv_freq[i], [Tmax][hd/2]
   int* err;
   int* path_out;          // nullable: CTA 0 records the path taken (0 bf16, 1 W4)
+  int w4_only;            // k_gemv: return at once unless the W4 path is taken
 };
 
 void launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Tensor-core GEMM (tcgen05 + TMA) over many tokens (see gemm_tc.cu): the
+// GemvArgs' bf16 weights against B tokens of x (no 64-column limit), the same
+// epilogues; returns at once when the layer takes the W4 path.
+// ---------------------------------------------------------------------------
+bool tc_gemm_available();
+cudaError_t tc_gemm_init();
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int ld, int box_rows);
+bool make_weight_tmap(CUtensorMap* map, const bf16* w, int N, int Kp);
+int tc_pick_bn(int N, int M, int sm_count);
+cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s);
+// (cos, sin) of pos * inv_freq[i] for pos < Tmax, i < half: [Tmax][half].
+void launch_rope_table(const float* inv_freq, int half, int Tmax, float2* out, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Fused small-batch decode GEMV (B <= 8): norm / exit decision / embedding in
