@@ -28,7 +28,7 @@ EXPORTS = (
     "rl_quantize_exit_layers", "rl_exit_layer_view", "rl_kv_cache_alloc", "rl_kv_cache_free",
     "rl_kv_view", "rl_kv_position", "rl_kv_set_position", "rl_kv_set_trace", "rl_prefill",
     "rl_decode_step", "rl_decode_step_host", "rl_sync", "rl_decode_kernel_count",
-    "rl_kv_set_profiling", "rl_kv_profile", "rl_lm_head_static", "rl_kv_set_decode_path",
+    "rl_kv_set_profiling", "rl_kv_profile", "rl_kv_timeline", "rl_lm_head_static", "rl_kv_set_decode_path",
     "rl_kv_decode_path",
 )
 RL_PATH_AUTO, RL_PATH_STEP, RL_PATH_FUSED, RL_PATH_GENERIC = range(4)
@@ -92,6 +92,7 @@ def _load():
         "rl_kv_set_profiling": (I, [P, I]),
         "rl_kv_profile": (I, [P, P, I, PI, PI, PI, ctypes.POINTER(ctypes.c_float),
                               ctypes.POINTER(ctypes.c_double), PI]),
+        "rl_kv_timeline": (I, [P, P, ctypes.c_int64, P, PI, PI, PI]),
         "rl_lm_head_static": (I, [P, P, I, P, P, P, P]),
         "rl_kv_set_decode_path": (I, [P, I]),
         "rl_kv_decode_path": (I, [P, I]),
@@ -230,7 +231,21 @@ def rl_kv_decode_path(kv, B):
 
 
 def rl_kv_set_profiling(kv, enable):
-    _check(_lib.rl_kv_set_profiling(kv, int(bool(enable))))
+    """0 off; 1 (or True) event records and the per-phase timeline; 2 also the
+    per-CTA timeline of the step kernel (rl_kv_timeline)."""
+    _check(_lib.rl_kv_set_profiling(kv, int(enable)))
+
+
+def rl_kv_timeline(kv, stream=None):
+    """Per-CTA timeline of the last profiled step: numpy uint64 array
+    [phase][CTA][stamp] of globaltimer nanoseconds (0 = no such event)."""
+    import numpy as np
+    n_ph, n_cta, n_st = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    cap = 1 << 22
+    buf = np.zeros(cap, dtype=np.uint64)
+    _check(_lib.rl_kv_timeline(kv, _stream(stream), cap, buf.ctypes.data_as(ctypes.c_void_p),
+                               ctypes.byref(n_ph), ctypes.byref(n_cta), ctypes.byref(n_st)))
+    return buf[: n_ph.value * n_cta.value * n_st.value].reshape(n_ph.value, n_cta.value, n_st.value)
 
 
 def rl_kv_profile(kv, stream=None, cap=1024):

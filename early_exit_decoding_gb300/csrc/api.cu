@@ -117,7 +117,7 @@ struct GraphKey {
   int* exit = nullptr;
   float* min_cos = nullptr;
   float* trace = nullptr;
-  bool prof = false;
+  int prof = 0;  // 0 off, 1 event records, 2 + per-CTA timeline
   bool fused = false;
   bool step = false;
   bool operator==(const GraphKey& o) const {
@@ -174,6 +174,8 @@ struct rl_kv {
   float* part_s = nullptr;            // attention partials [min(maxB,8)][Hq][part_cap][hd+2]
   int part_cap = 0;
   unsigned long long* tl = nullptr;   // per-phase timeline (profiling) [2][nph_cap]
+  unsigned long long* tl2 = nullptr;  // per-CTA timeline (profiling level 2) [nph_cap][grid][kTl2]
+  bool timeline = false;
   int nph_last = 0;
   int n_tile_ticket = 0;
   // buffers of the host-pointer entry point
@@ -1066,6 +1068,10 @@ rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStre
     a.tl = kv->tl;
     RL_CUDA(cudaMemsetAsync(kv->tl, 0xff, (size_t)a.nph * 8, s));
     RL_CUDA(cudaMemsetAsync(kv->tl + a.nph, 0, (size_t)a.nph * 8, s));
+    if (kv->timeline) {
+      a.tl2 = kv->tl2;
+      RL_CUDA(cudaMemsetAsync(kv->tl2, 0, (size_t)a.nph * m->sm_count * kTl2 * 8, s));
+    }
     cudaEventRecordWithFlags(kv->ev[0], s, cudaEventRecordExternal);
   }
   kv->step_args = a;
@@ -1575,7 +1581,7 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
     key.exit = d_exit_layer;
     key.min_cos = d_min_cos;
     key.trace = kv->trace;
-    key.prof = kv->profiling;
+    key.prof = kv->profiling ? (kv->timeline ? 2 : 1) : 0;
     key.fused = fused;
     key.step = step;
     if (!kv->exec || !(key == kv->key)) {
@@ -1701,7 +1707,24 @@ rl_status rl_kv_set_profiling(rl_kv* kv, int32_t enable) {
     RL_TRY(kv->alloc(&kv->d_paths, (size_t)cap));
     RL_TRY(kv->alloc(&kv->tl, (size_t)2 * kv->nph_cap));
   }
+  if (enable >= 2 && !kv->tl2)
+    RL_TRY(kv->alloc(&kv->tl2, (size_t)kv->nph_cap * kv->m->sm_count * kTl2));
   kv->profiling = enable != 0;
+  kv->timeline = enable >= 2;
+  return RL_OK;
+}
+
+rl_status rl_kv_timeline(rl_kv* kv, rl_stream_t stream, int64_t cap, uint64_t* out, int32_t* nphase,
+                         int32_t* nctas, int32_t* nstamps) {
+  if (!kv || !out || !nphase || !nctas || !nstamps) return fail(RL_ERR_INVALID_ARG, "NULL argument");
+  if (!kv->tl2 || kv->nrec != -1) return fail(RL_ERR_STATE, "no per-CTA timeline recorded");
+  RL_CUDA(cudaStreamSynchronize(as_stream(stream)));
+  const int64_t need = (int64_t)kv->nph_last * kv->m->sm_count * kTl2;
+  if (cap < need) return fail(RL_ERR_INVALID_ARG, "timeline buffer too small");
+  RL_CUDA(cudaMemcpy(out, kv->tl2, (size_t)need * 8, cudaMemcpyDeviceToHost));
+  *nphase = kv->nph_last;
+  *nctas = kv->m->sm_count;
+  *nstamps = kTl2;
   return RL_OK;
 }
 

@@ -96,6 +96,14 @@ __device__ __forceinline__ void tl_mark(unsigned long long* tl, int nph, int p, 
     atomicMax(tl + nph + p, t);
 }
 
+// Per-CTA timeline stamp (profiling only).
+__device__ __forceinline__ void tl2_mark(unsigned long long* tl2, int grid, int p, int cta, int k) {
+  if (!tl2) return;
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  tl2[((size_t)p * grid + cta) * kTl2 + k] = t;
+}
+
 // Sum 32 values over the 32 lanes of a warp, leaving the total of value i
 // in lane i (31 shuffles: each step halves the values a lane carries).
 __device__ __forceinline__ float butterfly32(float (&v)[32], int lane) {
@@ -322,6 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
       };
       for (int p = 0; p < a.nph && !s_abort; ++p) {
         const PhaseDesc* D = a.ph + p;
+        bool first_copy = true;
+        auto stamp_copy = [&]() {
+          if (!a.tl2) return;
+          if (first_copy) tl2_mark(a.tl2, grid, p, cta, TL2_P0);
+          first_copy = false;
+          tl2_mark(a.tl2, grid, p, cta, TL2_P1);
+        };
         if (D->kind == PH_GEMV) {
           const int layer_no = D->layer_no;
           const unsigned char* qwt = D->qwt;
@@ -364,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 mbar_expect_tx(&full[slot], (uint32_t)(ns * STAGE_W));
                 bulk_g2s(ring + (size_t)slot * SLOT_B, qwt + ((size_t)tl * UPT + s0) * STAGE_W,
                          (uint32_t)(ns * STAGE_W), &full[slot]);
+                stamp_copy();
                 rp.next(NS);
                 ++issued;
               }
@@ -376,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 mbar_expect_tx(&full[slot], bytes);
                 bulk_g2s(ring + (size_t)slot * SLOT_B, wt + (size_t)tl * 16 * Kp + (size_t)16 * k0, bytes,
                          &full[slot]);
+                stamp_copy();
                 rp.next(NS);
                 ++issued;
               }
@@ -405,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             const int sk = rp.slot;
             rp.next(NS);
             ++issued;
+            stamp_copy();
             if (!two) {
               mbar_expect_tx(&full[sk], 2 * bytes);
               if (bytes) {
@@ -458,7 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         fence_proxy_async();
       }
       named_sync(kBarCons, NC * 32);
-      if (ct == 0) tl_mark(a.tl, a.nph, p, 0);
+      if (ct == 0) {
+        tl_mark(a.tl, a.nph, p, 0);
+        tl2_mark(a.tl2, grid, p, cta, TL2_BAR);
+      }
       const PhaseDesc& D = cdesc;
 
       if (D.kind == PH_GEMV) {
@@ -570,6 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           }
           xpar ^= 1u;
         }
+        if (ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
+        bool first_w = true;
         if (w4) {  // per-group sums of the bf16 activations
           for (int gw = warp; gw < B * G; gw += NC) {
             const int b = gw / G, gi = gw % G;
@@ -633,6 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
             s_abort = 1;
           }
+          if (first_w && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_W);
+          first_w = false;
           const unsigned char* sb = ring + (size_t)slot * SLOT_B;
           const int ns = min(step_u, UPT - i0);
           for (int s = 0; s < ns; ++s) {
@@ -739,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
             s_abort = 1;
           }
+          if (it == cta && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
           unsigned char* Ks = ring + (size_t)slot * SLOT_B;
           unsigned char* Vs = two ? ring + (size_t)slot_v * SLOT_B : Ks + kAttnHalf;
           const size_t head_base = ((size_t)b * Hkv + hk) * a.Tmax;
@@ -859,9 +885,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         }
       }
       // ---- end of phase: this CTA's writes are done; arrive ----
+      if (ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_CDONE);
       named_sync(kBarPhase, (NC + 1) * 32);
       if (ct == 0) {
         tl_mark(a.tl, a.nph, p, 1);
+        tl2_mark(a.tl2, grid, p, cta, TL2_ARRIVE);
         // the release orders every write of this CTA's phase (made before the
         // barrier above) before the arrival
         if (p + 1 < a.nph) red_release_add(a.bars + p, 1u);
@@ -929,6 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
           }
           if (lane < B) s_rs[lane] = 1.f / sqrtf(cs0 / (float)a.d + a.eps);
+          if (lane == 0) tl2_mark(a.tl2, grid, p, cta, TL2_RED);
           if (D.dec_layer > 0 && D.stats_k == 3) {
             float m = lane < B ? cs1 / fmaxf(sqrtf(cs2) * sqrtf(cs0), 1e-12f) : FLT_MAX;
 #pragma unroll

@@ -297,6 +297,19 @@ struct StepArgs {
   int xs_row_bytes;           // activation row stride in shared memory
   int gmax;                   // max 128-input groups over the phases
   unsigned long long* tl;     // optional timeline: [nph] first starts, then [nph] last ends
+  unsigned long long* tl2;    // optional per-CTA timeline [nph][grid][kTl2] (globaltimer ns)
+};
+// Stamps of the per-CTA timeline, per (phase, CTA).
+enum Tl2Stamp {
+  TL2_BAR = 0,     // consumers: previous phase complete (grid barrier passed)
+  TL2_X = 1,       // consumers: activation rows in shared memory (attention: first chunk)
+  TL2_W = 2,       // consumers: first weight unit in shared memory
+  TL2_CDONE = 3,   // consumers: last tile / chunk computed
+  TL2_ARRIVE = 4,  // epilogues done, arrival at the phase counter
+  TL2_P0 = 5,      // producer: first copy of the phase issued
+  TL2_P1 = 6,      // producer: last copy of the phase issued
+  TL2_RED = 7,     // reducer: RMSNorm scale / exit decision ready
+  kTl2 = 8
 };
 
 // Shared memory the step kernel needs (0 if it does not fit).

@@ -246,6 +246,21 @@ RL_API rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32
                                int32_t* layers, int32_t* paths, float* ms, double* bytes,
                                int32_t* n);
 
+/* Per-CTA timeline of the last profiled decode step of the persistent step
+ * kernel (rl_kv_set_profiling(kv, 2) records it; level 1 does not).  Waits for
+ * `stream`, then copies into the host buffer `out` (capacity `cap` entries)
+ * the globaltimer stamps, in nanoseconds, laid out [phase][CTA][stamp]: for
+ * each phase of the step and each CTA, *nstamps values (0 = the event did not
+ * happen on that CTA): 0 previous phase complete, 1 activation rows (or the
+ * first attention chunk) in shared memory, 2 first weight unit in shared
+ * memory, 3 last tile computed, 4 arrival at the phase counter, 5 / 6 first /
+ * last weight copy issued by the producer, 7 RMSNorm scale and exit decision
+ * ready.  RL_ERR_STATE if the last step did not record one; RL_ERR_INVALID_ARG
+ * if `cap` < phases x CTAs x stamps.  Measurement only: not part of the
+ * method (the pages time only whole decode steps). */
+RL_API rl_status rl_kv_timeline(rl_kv* kv, rl_stream_t stream, int64_t cap, uint64_t* out,
+                                int32_t* nphase, int32_t* nctas, int32_t* nstamps);
+
 /* Number of kernels one decode step launches for batch B (for launch
  * accounting); 0 on bad arguments. */
 RL_API int32_t rl_decode_kernel_count(const rl_model* m, int32_t B);
