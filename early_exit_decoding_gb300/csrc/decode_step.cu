@@ -1,11 +1,11 @@
 // Persistent decode step for small batches (B <= 8): ONE cooperative kernel
 // per decode step runs every phase -- for each layer QKV (+ exit decision,
-// RoPE, KV append), attention, O (+ residual), gate/up (+ SwiGLU), down (+
-// residual, next RMSNorm input, cosine partials); then the LM head (+ greedy
-// argmax).  River-LLM explainer, section 四: the batch-minimum cosine of a
-// layer's input and output residual decides, once, that the remaining layers
-// run on the W4A16 exit river; section 三: those layers write K/V into the
-// backbone's own cache slot.
+// RoPE, KV append), attention, merge, O (+ residual), gate/up (+ SwiGLU), down
+// (+ residual, next RMSNorm input, cosine partials); then the LM head (+
+// greedy argmax).  River-LLM explainer, section 四: the batch-minimum cosine of
+// a layer's input and output residual decides, once, that the remaining
+// layers run on the W4A16 exit river; section 三: those layers write K/V into
+// the backbone's own cache slot.
 //
 // One CTA per SM, warp-specialised:
 //   * producer warp: streams, through a ring of shared-memory slots, every
@@ -17,14 +17,14 @@
 //     exit -- for this CTA's exit decision of the previous layer, which picks
 //     bf16 or W4 weights for the next one;
 //   * eight consumer warps: wait for the previous phase (grid-wide arrival
-//     counter), fetch the phase's activation rows, then run mma.sync on the
-//     staged weights (or the attention math on staged K/V);
-//   * reducer warp: sums the consumer warps' partial tiles and runs the
-//     epilogues.
-// Tiles of the small projections are split across CTAs in (tile, unit) order
-// (stream-K); the last CTA to finish a split tile merges it (ticket, partials
-// summed in CTA order: deterministic).  Every wait is bounded: on timeout the
-// kernel sets RL_DEVERR_TIMEOUT and winds down without touching more memory.
+//     counter); reduce the norm / cosine statistics while the phase's
+//     activation rows arrive; run mma.sync on the staged weights, each warp on
+//     its own 128 inputs of every unit, keeping per-warp partial tiles in
+//     shared memory; every few tiles, all 256 threads sum the partials (fixed
+//     order: deterministic) and run the epilogue in parallel.
+// A CTA takes the 16-row tiles cta, cta + grid, ... of each projection.  Every
+// wait is bounded: on timeout the kernel sets RL_DEVERR_TIMEOUT and winds down
+// without touching more memory.
 #include "dev_common.cuh"
 
 namespace river {
@@ -35,8 +35,7 @@ using namespace dev;
 
 constexpr int NC = 8;                     // consumer warps
 constexpr int WP = NC;                    // producer warp
-constexpr int WR = NC + 1;                // reducer warp
-constexpr int kThreads = (NC + 2) * 32;
+constexpr int kThreads = (NC + 1) * 32;
 constexpr int KU = 1024;                  // inputs per unit
 constexpr int STAGE_W = 16 * 512 + 512;   // one W4 unit: 16 rows x 512 B nibbles + 16 x 8 (s, z)
 constexpr int W4U = 4;                    // W4 units per ring slot
@@ -47,30 +46,7 @@ constexpr int kAttnHalf = 16384;          // V offset in a one-slot chunk (head_
 constexpr long long kSpin = 1LL << 20;     // mbarrier polls
 constexpr long long kSpinBar = 1LL << 24;  // grid-barrier polls (each with a short sleep)
 constexpr int kBarCons = 1;                // named barrier: consumer warps
-constexpr int kBarPhase = 2;               // named barrier: consumers + reducer
-constexpr int kTileList = 16;              // circular list of the tiles a CTA took
 constexpr int kStaticSmem = 12 * 1024;     // upper bound of the kernel's static shared memory
-
-struct GRange {
-  long long c0, c1;
-  int UPT, ntiles;
-};
-
-// (tile, unit) range of CTA `cta`: whole tiles, or stream-K when `split`.
-__device__ __forceinline__ GRange gemv_range(int N, int Kp, int split, int cta, int grid) {
-  GRange r;
-  r.UPT = (Kp + KU - 1) / KU;
-  r.ntiles = N >> 4;
-  const long long U = (long long)r.ntiles * r.UPT;
-  if (split) {
-    r.c0 = U * cta / grid;
-    r.c1 = U * (cta + 1) / grid;
-  } else {
-    r.c0 = ((long long)r.ntiles * cta / grid) * r.UPT;
-    r.c1 = ((long long)r.ntiles * (cta + 1) / grid) * r.UPT;
-  }
-  return r;
-}
 
 // Position in the ring of shared-memory slots: slot index and how many times
 // the ring has wrapped (the mbarrier phase parity), advanced without divisions.
@@ -239,22 +215,17 @@ __device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigne
 
 __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_constant__ StepArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t full[kMaxSlots], empty[kMaxSlots], xbar, rfull[2], rempty[2];
+  __shared__ __align__(8) uint64_t full[kMaxSlots], empty[kMaxSlots], xbar;
   __shared__ __align__(16) PhaseDesc cdesc;  // consumers' copy of the current phase
-  __shared__ __align__(16) PhaseDesc rdesc;  // reducer's copy
-  __shared__ float s_col[8][3];
+  __shared__ float s_col[8][3];              // per column: the phase's reduced statistics
+  __shared__ float s_stw[NC][24];            // per warp partial statistics
   __shared__ float s_rs[8];
   __shared__ float s_freq[64];
   __shared__ volatile int s_e;    // exit layer as far as this CTA knows it
   __shared__ volatile int s_dec;  // last layer whose exit decision this CTA has taken
   __shared__ volatile int s_abort;
-  // Tiles this CTA took, in ring order (circular; the producer is at most a few
-  // tiles ahead of the consumers, the reducer at most two behind them); -1
-  // closes a phase.  s_tcount = entries written so far.
-  __shared__ volatile int s_tl[kTileList];
-  __shared__ volatile int s_tcount, s_cseq, s_rseq;  // written / read by consumers / by reducer
   __shared__ int s_pos, s_last;
-  __shared__ __align__(16) float s_mrg[1024];  // attention merge: chunk (max, sum), weights, partial sums
+  __shared__ __align__(16) float s_mrg[1024];  // attention merge scratch; LM-head argmax scratch
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -265,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
   float* xsum = reinterpret_cast<float*>(xs + (size_t)B * RSX);
   float4* red = reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(xsum) +
                                           ((((size_t)B * a.gmax * 4) + 15) & ~(size_t)15));
+  float* redf = reinterpret_cast<float*>(red);
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -272,10 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
       mbar_init(&empty[i], NC);
     }
     mbar_init(&xbar, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&rfull[i], NC);
-      mbar_init(&rempty[i], 1);
-    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_abort = 0;
     s_pos = a.st->pos;
@@ -286,9 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
     }
     s_e = e;
     s_dec = 0;
-    s_tcount = 0;
-    s_cseq = 0;
-    s_rseq = 0;
   }
   if (tid < 8) s_rs[tid] = 1.f;
   if (tid < 64) s_freq[tid] = tid < a.hd / 2 ? a.inv_freq[tid] : 0.f;
@@ -299,24 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
     if (lane == 0) {
       RingPos rp{0, 0};
       int issued = 0;
-      int tseq = 0;
-      // append to the tile list once both readers are less than a list length behind
-      auto publish = [&](int v) -> bool {
-        long long i = 0;
-        while (tseq - min(s_cseq, s_rseq) >= kTileList - 1 && !s_abort && i < kSpinBar) {
-          __nanosleep(32);
-          ++i;
-        }
-        if (tseq - min(s_cseq, s_rseq) >= kTileList - 1) {
-          if (!s_abort) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-          s_abort = 1;
-          return false;
-        }
-        s_tl[tseq % kTileList] = v;
-        __threadfence_block();
-        s_tcount = ++tseq;
-        return true;
-      };
       int e_known = s_e;
       auto take_slot = [&]() -> bool {
         if (rp.round == 0) return true;
@@ -341,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           const int layer_no = D->layer_no;
           const unsigned char* qwt = D->qwt;
           const bf16* wt = D->wt;
-          const int N = D->N, Kp = D->Kp, split = D->split;
+          const int N = D->N, Kp = D->Kp;
           bool w4 = false;
           if (qwt && layer_no > 0) {
             if (a.mode == RL_EXIT_TAU && e_known >= a.L && layer_no >= 2) {
@@ -360,17 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
             w4 = layer_no > e_known;
           }
-          // Whole 16-row tiles.  Large projections (D->split != 0): taken from
-          // the phase's shared counter, so CTAs that stream faster take more
-          // (the next claim overlaps the current tile's copies).  Small ones:
-          // tiles cta, cta + grid, ... -- a claim made early, while the ring
-          // prefetches ahead, would pile several tiles onto one CTA.
-          const bool dyn = split != 0;
+          // whole 16-row tiles cta, cta + grid, ... (the consumers walk the same list)
           const int UPT = (Kp + KU - 1) / KU, ntiles = N >> 4;
-          int tl = dyn ? (int)atomicAdd(a.tctr + p, 1u) : cta;
-          while (tl < ntiles && !s_abort) {
-            const int nxt = dyn ? (int)atomicAdd(a.tctr + p, 1u) : tl + grid;
-            if (!publish(tl)) break;
+          for (int tl = cta; tl < ntiles && !s_abort; tl += grid) {
             if (w4) {
               for (int s0 = 0; s0 < UPT; s0 += W4U) {
                 if (!take_slot()) break;
@@ -397,9 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 ++issued;
               }
             }
-            tl = nxt;
           }
-          if (!publish(-1)) break;  // end of this CTA's tiles in the phase
         } else if (D->kind == PH_ATTN) {
           // attention: K and V rows below this step's position; a chunk of up
           // to 128 positions takes one slot (head_dim 64: K, then V at 16 KB)
@@ -447,13 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         for (int u = issued - NS < 0 ? 0 : issued - NS; u < issued; ++u)
           mbar_wait(&full[u % NS], (uint32_t)((u / NS) & 1), kSpin);
     }
-  } else if (warp < NC) {
+  } else {
     // ================================ consumers ==================================
     const int ct = tid;
     RingPos rc{0, 0};
-    int tcount = 0;
-    int cseq = 0;  // position in the tile list
     uint32_t xpar = 0;
+    float amv = -FLT_MAX;  // LM head: running argmax of this thread's outputs
+    int ami = 0x7fffffff;
     for (int p = 0; p < a.nph; ++p) {
       {
         const int* src = reinterpret_cast<const int*>(a.ph + p);
@@ -484,8 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
 
       if (D.kind == PH_GEMV) {
         const int Kp = D.Kp, G = Kp >> 7;
-        const GRange r = gemv_range(D.N, Kp, D.split, cta, grid);
-        // ---- activation rows ----
+        // ---- activation rows (bulk copy), concurrently with the statistics ----
         if (D.xmode != X_EMBED && ct == 0 && !s_abort) {
           mbar_expect_tx(&xbar, (uint32_t)B * Kp * 2);
           for (int b = 0; b < B; ++b)
@@ -557,6 +493,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             s_col[ct][0] = sum;
           }
         }
+        if (D.xmode == X_SCALED) {
+          // per column: sums of the producing phase's per-tile partials
+          // (|h|^2; with three partials also <h_in, h> and |h_in|^2)
+          float acc[kFusedMaxB][3];
+#pragma unroll
+          for (int b = 0; b < kFusedMaxB; ++b)
+#pragma unroll
+            for (int j = 0; j < 3; ++j) acc[b][j] = 0.f;
+          const int sk = D.stats_k;
+          for (int tt = ct; tt < D.stats_tiles; tt += NC * 32) {
+            const float* sp = D.stats_in + (size_t)tt * 8 * sk;
+#pragma unroll
+            for (int b = 0; b < kFusedMaxB; ++b)
+#pragma unroll
+              for (int j = 0; j < 3; ++j)
+                if (b < B && j < sk) acc[b][j] += __ldcg(sp + b * sk + j);
+          }
+#pragma unroll
+          for (int b = 0; b < kFusedMaxB; ++b)
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+              if (b < B && j < sk) {
+                const float v = warp_sum(acc[b][j]);
+                if (lane == 0) s_stw[warp][b * 3 + j] = v;
+              }
+          named_sync(kBarCons, NC * 32);
+          if (ct < 3 * B && (ct % 3) < sk) {
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < NC; ++w) sum += s_stw[w][ct];
+            s_col[ct / 3][ct % 3] = sum;
+          }
+        }
         named_sync(kBarCons, NC * 32);
         if (ct == 0) {
           if (D.xmode == X_EMBED) {  // step begin
@@ -566,24 +535,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
             if (cta == 0) a.st->exit_layer = s_e;
           }
-          if (D.xmode == X_EMBED)
+          if (D.xmode == X_EMBED || D.xmode == X_SCALED)
             for (int b = 0; b < B; ++b) s_rs[b] = 1.f / sqrtf(s_col[b][0] / (float)a.d + a.eps);
-          // tau mode before the exit: this layer's weight path is the reducer's
-          // decision on the previous layer (taken concurrently with the x fetch)
-          if (a.mode == RL_EXIT_TAU && D.dec_layer > 0 && D.qwt && D.layer_no > 0 && s_e == a.L) {
-            long long i = 0;
-            while (s_dec < D.dec_layer && !s_abort && i < kSpinBar) {
-              __nanosleep(32);
-              ++i;
+          if (D.xmode == X_SCALED && D.dec_layer > 0 && D.stats_k == 3) {
+            // exit decision of layer dec_layer: batch minimum of the cosine
+            // between the residual entering and leaving it
+            float m = FLT_MAX;
+            for (int b = 0; b < B; ++b)
+              m = fminf(m, s_col[b][1] / fmaxf(sqrtf(s_col[b][2]) * sqrtf(s_col[b][0]), 1e-12f));
+            int e = s_e;
+            if (a.mode == RL_EXIT_TAU && e == a.L && D.dec_layer < a.L && m > a.tau) e = D.dec_layer;
+            s_e = e;
+            if (cta == 0) {
+              if (a.min_cos_out) a.min_cos_out[D.dec_layer - 1] = m;
+              a.st->exit_layer = e;
             }
-            if (s_dec < D.dec_layer && !s_abort) {
-              atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-              s_abort = 1;
-            }
+            __threadfence_block();
+            s_dec = D.dec_layer;
           }
+          tl2_mark(a.tl2, grid, p, cta, TL2_RED);
         }
         named_sync(kBarCons, NC * 32);
         const bool w4 = D.qwt && D.layer_no > 0 && D.layer_no > s_e;
+        const int ntiles = D.N >> 4, UPT = (Kp + KU - 1) / KU;
+        const int nt = cta < ntiles ? (ntiles - cta + grid - 1) / grid : 0;  // this CTA's tiles
+        // flush batches: TB tiles of per-warp partials in shared memory; an
+        // epilogue round covers R outputs (a multiple of 16 B, so a thread keeps
+        // its column c in every round and 16 consecutive lanes hold one tile column)
+        const int TB = max(1, 16 / B);
+        const int R = ((NC * 32) / (16 * B)) * 16 * B;
+        const int my_c = (ct >> 4) % B, my_r = ct & 15;
+        // residual epilogues: this thread's inputs of the first round, fetched now
+        float pre_res = 0.f, pre_hin = 0.f, pre_gn = 0.f;
+        if (D.epi == EPI_RESID && ct < R && ct < min(TB, nt) * 16 * B) {
+          const int n = (cta + (ct / (16 * B)) * grid) * 16 + my_r;
+          pre_res = __ldcg(D.resid + (size_t)my_c * D.ldr + n);
+          if (D.h_in) pre_hin = __ldcg(D.h_in + (size_t)my_c * a.d + n);
+          if (D.gnext) pre_gn = D.gnext[n];
+        }
         if (D.xmode != X_EMBED) {
           if (!s_abort && !mbar_wait(&xbar, xpar, kSpin)) {
             if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
@@ -592,7 +581,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           xpar ^= 1u;
         }
         if (ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
-        bool first_w = true;
         if (w4) {  // per-group sums of the bf16 activations
           for (int gw = warp; gw < B * G; gw += NC) {
             const int b = gw / G, gi = gw % G;
@@ -604,65 +592,139 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           }
           named_sync(kBarCons, NC * 32);
         }
-        float y[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) y[j][i] = 0.f;
         // MMA column g reads activation row min(g, B-1); columns >= B are dropped
         const unsigned char* xrow = xs + (size_t)(g < B ? g : B - 1) * RSX;
-        auto hand_off = [&]() {
-          const int buf = tcount & 1;
-          if (tcount >= 2 && !s_abort && !mbar_wait(&rempty[buf], (uint32_t)(((tcount >> 1) - 1) & 1), kSpin))
-            s_abort = 1;
-          float4 v;
-          v.x = (y[0][0] + y[1][0]) + (y[2][0] + y[3][0]);
-          v.y = (y[0][1] + y[1][1]) + (y[2][1] + y[3][1]);
-          v.z = (y[0][2] + y[1][2]) + (y[2][2] + y[3][2]);
-          v.w = (y[0][3] + y[1][3]) + (y[2][3] + y[3][3]);
-          red[(buf * NC + warp) * 32 + lane] = v;
+        const int step_u = w4 ? W4U : 1;
+        bool first_w = true;
+
+        // epilogue of a batch of nb tiles starting at tile t_first (all consumer threads)
+        auto flush = [&](int nb, int t_first, bool first_batch) {
+          named_sync(kBarCons, NC * 32);
+          const int nout = nb * 16 * B;
+          const int rounds = (nout + R - 1) / R;
+          for (int rd = 0; rd < rounds; ++rd) {
+            const int i = rd * R + ct;
+            const bool act = ct < R && i < nout;
+            const int tb = act ? i / (16 * B) : 0;
+            const int tl = t_first + tb * grid;
+            float v = 0.f;
+            if (act) {
+#pragma unroll
+              for (int w = 0; w < NC; ++w) v += redf[((tb * NC + w) * B + my_c) * 16 + my_r];
+            }
+            if (D.epi == EPI_RESID) {
+              float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+              if (act) {
+                const int n = tl * 16 + my_r;
+                float res = pre_res, hin = pre_hin, gn = pre_gn;
+                if (!(first_batch && rd == 0)) {
+                  res = __ldcg(D.resid + (size_t)my_c * D.ldr + n);
+                  hin = D.h_in ? __ldcg(D.h_in + (size_t)my_c * a.d + n) : 0.f;
+                  gn = D.gnext ? D.gnext[n] : 0.f;
+                }
+                const float val = v + res;
+                D.out[(size_t)my_c * D.ldo + n] = val;
+                if (D.trace) D.trace[((size_t)D.trace_layer * a.trace_maxB + my_c) * D.ldo + n] = val;
+                if (D.xnext) D.xnext[(size_t)my_c * D.ldxnext + n] = __float2bfloat16_rn(val * gn);
+                s0 = val * val;
+                s1 = val * hin;
+                s2 = hin * hin;
+              }
+              if (D.stats_out) {
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                  s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+                  s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                  s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+                }
+                if (act && my_r == 0) {
+                  float* so = D.stats_out + ((size_t)tl * 8 + my_c) * D.stats_k_out;
+                  so[0] = s0;
+                  if (D.stats_k_out == 3) {
+                    so[1] = s1;
+                    so[2] = s2;
+                  }
+                }
+              }
+            } else if (D.epi == EPI_SWIGLU) {
+              // rows r < 8 of a tile are gate rows, r + 8 the matching up rows
+              const float up = __shfl_down_sync(0xffffffffu, v, 8);
+              if (act && my_r < 8) {
+                const float rs = s_rs[my_c];
+                D.out_h[(size_t)my_c * D.ldoh + tl * 8 + my_r] = __float2bfloat16_rn(silu_f(v * rs) * (up * rs));
+              }
+            } else if (D.epi == EPI_QKV_ROPE) {
+              // rows r and r + 8 of a tile are one RoPE pair (dims dim, dim + hd/2)
+              const float hv = __shfl_down_sync(0xffffffffu, v, 8);
+              if (act && my_r < 8) {
+                const int hd = a.hd, half = hd >> 1;
+                const int row0 = tl * 16;
+                const int head_all = row0 / hd;
+                const float rs = s_rs[my_c];
+                const int pos = s_pos;
+                const int dim = 8 * ((row0 % hd) >> 4) + my_r;
+                float lo = v * rs, hi = hv * rs;
+                if (head_all < a.Hq + a.Hkv) {
+                  float sn, cs;
+                  sincosf((float)pos * s_freq[dim], &sn, &cs);
+                  const float nlo = lo * cs - hi * sn, nhi = hi * cs + lo * sn;
+                  lo = nlo;
+                  hi = nhi;
+                }
+                if (head_all < a.Hq) {
+                  float* q = D.q_out + (size_t)my_c * a.Hq * hd + head_all * hd;
+                  q[dim] = lo;
+                  q[dim + half] = hi;
+                } else if (pos >= 0 && pos < a.Tmax) {
+                  const bool is_k = head_all < a.Hq + a.Hkv;
+                  const int hk = is_k ? head_all - a.Hq : head_all - a.Hq - a.Hkv;
+                  bf16* dst = (is_k ? D.kc : D.vc) + (((size_t)my_c * a.Hkv + hk) * a.Tmax + pos) * hd;
+                  dst[dim] = __float2bfloat16_rn(lo);
+                  dst[dim + half] = __float2bfloat16_rn(hi);
+                } else if (my_r == 0 && my_c == 0) {
+                  atomicOr(&a.st->err, RL_DEVERR_CAPACITY);
+                }
+              }
+            } else if (D.epi == EPI_LMHEAD) {
+              if (act) {
+                const int n = tl * 16 + my_r;
+                const float val = v * s_rs[my_c];
+                D.out[(size_t)my_c * D.ldo + n] = val;
+                if (val > amv || (val == amv && n < ami)) {
+                  amv = val;
+                  ami = n;
+                }
+              }
+            } else {  // EPI_STORE
+              if (act) D.out[(size_t)my_c * D.ldo + tl * 16 + my_r] = v * s_rs[my_c];
+            }
+          }
+          named_sync(kBarCons, NC * 32);
+        };
+
+        int nb = 0, t_first = cta;
+        bool first_batch = true;
+        for (int tl = cta; tl < ntiles; tl += grid) {
+          float y[4][4];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) y[j][q] = 0.f;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&rfull[buf]);
-          ++tcount;
-        };
-        const int UPT = r.UPT;
-        const int step_u = w4 ? W4U : 1;
-        for (;;) {
-          // next tile this CTA took (the producer publishes it before its copies)
-          long long spin = 0;
-          while (s_tcount <= cseq && !s_abort && spin < kSpinBar) {
-            __nanosleep(20);
-            ++spin;
-          }
-          if (s_tcount <= cseq) {
-            if (!s_abort && lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-            s_abort = 1;
-            break;
-          }
-          const int tile = s_tl[cseq % kTileList];
-          ++cseq;
-          named_sync(kBarCons, NC * 32);  // every consumer warp has read the entry
-          if (ct == 0) s_cseq = cseq;
-          if (tile < 0) break;
+            for (int i = 0; i < 4; ++i) y[j][i] = 0.f;
           int uk = 0;
-        for (int i0 = 0; i0 < UPT; i0 += step_u) {
-          const int slot = rc.slot;
-          bool ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
-          if (!ok && s_abort == 0) {
-            if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-            s_abort = 1;
-          }
-          if (first_w && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_W);
-          first_w = false;
-          const unsigned char* sb = ring + (size_t)slot * SLOT_B;
-          const int ns = min(step_u, UPT - i0);
-          for (int s = 0; s < ns; ++s) {
-            const int gi = uk * 8 + warp;  // this warp's group
-            if (ok && gi < G) {
+          for (int i0 = 0; i0 < UPT; i0 += step_u) {
+            const int slot = rc.slot;
+            bool ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
+            if (!ok && s_abort == 0) {
+              if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+              s_abort = 1;
+            }
+            if (first_w && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_W);
+            first_w = false;
+            const unsigned char* sb = ring + (size_t)slot * SLOT_B;
+            const int ns = min(step_u, UPT - i0);
+            for (int s = 0; s < ns; ++s) {
+              const int gi = uk * 8 + warp;  // this warp's group
+              if (ok && gi < G) {
               if (w4) {
                 // Lane t's word m holds the eight nibbles of input chunk 4m + t of
                 // the group; odd rows have their 64-byte halves swapped.
@@ -727,13 +789,64 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 }
               }
             }
-            if (uk + 1 == UPT) hand_off();
-            ++uk;
+              ++uk;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            rc.next(NS);
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[slot]);
-          rc.next(NS);
+          // this warp's partial tile -> the batch buffer ([tile][warp][column][row])
+          {
+            const float v0 = (y[0][0] + y[1][0]) + (y[2][0] + y[3][0]);
+            const float v1 = (y[0][1] + y[1][1]) + (y[2][1] + y[3][1]);
+            const float v2 = (y[0][2] + y[1][2]) + (y[2][2] + y[3][2]);
+            const float v3 = (y[0][3] + y[1][3]) + (y[2][3] + y[3][3]);
+            float* rw = redf + (size_t)(nb * NC + warp) * B * 16;
+            if (2 * t < B) {
+              rw[(2 * t) * 16 + g] = v0;
+              rw[(2 * t) * 16 + g + 8] = v2;
+            }
+            if (2 * t + 1 < B) {
+              rw[(2 * t + 1) * 16 + g] = v1;
+              rw[(2 * t + 1) * 16 + g + 8] = v3;
+            }
+          }
+          if (++nb == TB || tl + grid >= ntiles) {
+            flush(nb, t_first, first_batch);
+            first_batch = false;
+            t_first = tl + grid;
+            nb = 0;
+          }
         }
+        if (D.epi == EPI_LMHEAD) {
+          // this CTA's argmax per column: 16-lane groups, then one thread per column
+#pragma unroll
+          for (int o = 1; o < 16; o <<= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, amv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, ami, o);
+            if (ov > amv || (ov == amv && oi < ami)) {
+              amv = ov;
+              ami = oi;
+            }
+          }
+          float* sv = s_mrg;
+          int* si = reinterpret_cast<int*>(s_mrg + 2 * NC);
+          if (my_r == 0) {
+            sv[ct >> 4] = ct < R ? amv : -FLT_MAX;
+            si[ct >> 4] = ct < R ? ami : 0x7fffffff;
+          }
+          named_sync(kBarCons, NC * 32);
+          if (ct < B) {
+            float bv = -FLT_MAX;
+            int bi = 0x7fffffff;
+            for (int h = 0; h < 2 * NC; ++h)
+              if (h % B == ct && (sv[h] > bv || (sv[h] == bv && si[h] < bi))) {
+                bv = sv[h];
+                bi = si[h];
+              }
+            a.am_val[(size_t)cta * 8 + ct] = bv;
+            a.am_idx[(size_t)cta * 8 + ct] = bi;
+          }
         }
       } else if (D.kind == PH_ATTN) {
         // ---- attention over this CTA's chunks: partial (max, sum, o) per chunk ----
@@ -886,254 +999,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
       }
       // ---- end of phase: this CTA's writes are done; arrive ----
       if (ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_CDONE);
-      named_sync(kBarPhase, (NC + 1) * 32);
+      named_sync(kBarCons, NC * 32);
       if (ct == 0) {
         tl_mark(a.tl, a.nph, p, 1);
         tl2_mark(a.tl2, grid, p, cta, TL2_ARRIVE);
         // the release orders every write of this CTA's phase (made before the
         // barrier above) before the arrival
         if (p + 1 < a.nph) red_release_add(a.bars + p, 1u);
-      }
-    }
-  } else if (warp == WR) {
-    // ================================ reducer ====================================
-    // Lane l holds tile values (r, c) = (l/8 + 4k, l%8), k = 0..3.
-    const int c = lane & 7, rb = lane >> 3;
-    int tc_run = 0;
-    int rseq = 0;  // position in the tile list
-    float amv = -FLT_MAX;
-    int ami = 0x7fffffff;
-    bool lm = false;
-    for (int p = 0; p < a.nph; ++p) {
-      {
-        const int* src = reinterpret_cast<const int*>(a.ph + p);
-        int* dst = reinterpret_cast<int*>(&rdesc);
-        for (int i = lane; i < (int)(sizeof(PhaseDesc) / 4); i += 32) dst[i] = __ldg(src + i);
-        __syncwarp();
-      }
-      const PhaseDesc& D = rdesc;
-      if (D.kind == PH_GEMV && !s_abort) {
-        if (D.epi == EPI_LMHEAD) lm = true;
-        if (D.xmode == X_SCALED) {
-          // RMSNorm scale and exit decision from the previous phase's per-tile
-          // partial sums, off the consumers' path: they only need x to start
-          if (lane == 0 && p > 0) {
-            long long i = 0;
-            while (ld_acquire(a.bars + (p - 1)) < (unsigned)grid && i < kSpinBar) {
-              __nanosleep(20);
-              ++i;
-            }
-            if (i >= kSpinBar) {
-              atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-              s_abort = 1;
-            }
-          }
-          __syncwarp();
-          float cs0 = 0.f, cs1 = 0.f, cs2 = 0.f;  // lane b keeps column b's sums
-          for (int b = 0; b < B; ++b) {
-            float acc[3] = {0.f, 0.f, 0.f};
-            for (int t0 = 0; t0 < D.stats_tiles; t0 += 32 * 16) {
-              float v[16][3];
-#pragma unroll
-              for (int q = 0; q < 16; ++q) {
-                const int tt = t0 + q * 32 + lane;
-#pragma unroll
-                for (int j = 0; j < 3; ++j)
-                  v[q][j] = (tt < D.stats_tiles && j < D.stats_k)
-                                ? __ldcg(D.stats_in + ((size_t)tt * 8 + b) * D.stats_k + j)
-                                : 0.f;
-              }
-#pragma unroll
-              for (int q = 0; q < 16; ++q)
-#pragma unroll
-                for (int j = 0; j < 3; ++j) acc[j] += v[q][j];
-            }
-#pragma unroll
-            for (int j = 0; j < 3; ++j) acc[j] = warp_sum(acc[j]);
-            if (lane == b) {
-              cs0 = acc[0];
-              cs1 = acc[1];
-              cs2 = acc[2];
-            }
-          }
-          if (lane < B) s_rs[lane] = 1.f / sqrtf(cs0 / (float)a.d + a.eps);
-          if (lane == 0) tl2_mark(a.tl2, grid, p, cta, TL2_RED);
-          if (D.dec_layer > 0 && D.stats_k == 3) {
-            float m = lane < B ? cs1 / fmaxf(sqrtf(cs2) * sqrtf(cs0), 1e-12f) : FLT_MAX;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fminf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) {
-              int e = s_e;
-              if (a.mode == RL_EXIT_TAU && e == a.L && D.dec_layer < a.L && m > a.tau) e = D.dec_layer;
-              s_e = e;
-              if (cta == 0) {
-                if (a.min_cos_out) a.min_cos_out[D.dec_layer - 1] = m;
-                a.st->exit_layer = e;
-              }
-              __threadfence_block();
-              s_dec = D.dec_layer;
-            }
-          }
-          __syncwarp();
-        }
-        for (;;) {
-          // the next tile of this CTA, as the producer published it
-          long long spin = 0;
-          while (s_tcount <= rseq && !s_abort && spin < kSpinBar) {
-            __nanosleep(20);
-            ++spin;
-          }
-          if (s_tcount <= rseq) {
-            if (!s_abort && lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-            s_abort = 1;
-            break;
-          }
-          const int tl = s_tl[rseq % kTileList];
-          ++rseq;
-          __syncwarp();
-          if (lane == 0) s_rseq = rseq;
-          if (tl < 0) break;
-          const int buf = tc_run & 1;
-          float res[4] = {0.f, 0.f, 0.f, 0.f}, hin[4] = {0.f, 0.f, 0.f, 0.f}, gn[4] = {0.f, 0.f, 0.f, 0.f};
-          if (D.epi == EPI_RESID && c < B) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int n = tl * 16 + rb + 4 * k;
-              res[k] = __ldcg(D.resid + (size_t)c * D.ldr + n);
-              if (D.h_in) hin[k] = __ldcg(D.h_in + (size_t)c * a.d + n);
-              if (D.gnext) gn[k] = D.gnext[n];
-            }
-          }
-          if (s_abort || !mbar_wait(&rfull[buf], (uint32_t)((tc_run >> 1) & 1), kSpin)) {
-            if (!s_abort && lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-            s_abort = 1;
-            break;
-          }
-          float tv[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int rr = rb + 4 * k;
-            const int ln = (rr & 7) * 4 + (c >> 1);
-            const int comp = (rr >= 8 ? 2 : 0) + (c & 1);
-            float sum = 0.f;
-#pragma unroll
-            for (int w = 0; w < NC; ++w) sum += f4get(red[(buf * NC + w) * 32 + ln], comp);
-            tv[k] = sum;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&rempty[buf]);
-          ++tc_run;
-          // ---- epilogue ----
-          if (D.epi == EPI_RESID) {
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f;
-            if (c < B) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int n = tl * 16 + rb + 4 * k;
-                const float v = tv[k] + res[k];
-                D.out[(size_t)c * D.ldo + n] = v;
-                if (D.trace) D.trace[((size_t)D.trace_layer * a.trace_maxB + c) * D.ldo + n] = v;
-                if (D.xnext) D.xnext[(size_t)c * D.ldxnext + n] = __float2bfloat16_rn(v * gn[k]);
-                s0 += v * v;
-                s1 += v * hin[k];
-                s2 += hin[k] * hin[k];
-              }
-            }
-            if (D.stats_out) {
-#pragma unroll
-              for (int o = 8; o < 32; o <<= 1) {
-                s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-                s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-                s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-              }
-              if (lane < 8 && c < B) {
-                float* so = D.stats_out + ((size_t)tl * 8 + c) * D.stats_k_out;
-                so[0] = s0;
-                if (D.stats_k_out == 3) {
-                  so[1] = s1;
-                  so[2] = s2;
-                }
-              }
-            }
-          } else if (D.epi == EPI_SWIGLU) {
-            if (c < B) {
-              const float rs = s_rs[c];
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const float gv = tv[k] * rs, uv = tv[k + 2] * rs;
-                D.out_h[(size_t)c * D.ldoh + tl * 8 + rb + 4 * k] = __float2bfloat16_rn(silu_f(gv) * uv);
-              }
-            }
-          } else if (D.epi == EPI_QKV_ROPE) {
-            if (c < B) {
-              const int hd = a.hd, half = hd >> 1;
-              const int row0 = tl * 16;
-              const int head_all = row0 / hd;
-              const float rs = s_rs[c];
-              const int pos = s_pos;
-#pragma unroll
-              for (int k = 0; k < 2; ++k) {
-                const int rr = rb + 4 * k;
-                const int dim = 8 * ((row0 % hd) >> 4) + rr;
-                float lo = tv[k] * rs, hi = tv[k + 2] * rs;
-                if (head_all < a.Hq + a.Hkv) {
-                  float sn, cs;
-                  sincosf((float)pos * s_freq[dim], &sn, &cs);
-                  const float nlo = lo * cs - hi * sn, nhi = hi * cs + lo * sn;
-                  lo = nlo;
-                  hi = nhi;
-                }
-                if (head_all < a.Hq) {
-                  float* q = D.q_out + (size_t)c * a.Hq * hd + head_all * hd;
-                  q[dim] = lo;
-                  q[dim + half] = hi;
-                } else if (pos >= 0 && pos < a.Tmax) {
-                  const bool is_k = head_all < a.Hq + a.Hkv;
-                  const int hk = is_k ? head_all - a.Hq : head_all - a.Hq - a.Hkv;
-                  bf16* dst = (is_k ? D.kc : D.vc) + (((size_t)c * a.Hkv + hk) * a.Tmax + pos) * hd;
-                  dst[dim] = __float2bfloat16_rn(lo);
-                  dst[dim + half] = __float2bfloat16_rn(hi);
-                } else if (rr == 0 && c == 0) {
-                  atomicOr(&a.st->err, RL_DEVERR_CAPACITY);
-                }
-              }
-            }
-          } else if (D.epi == EPI_LMHEAD) {
-            if (c < B) {
-              const float rs = s_rs[c];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int n = tl * 16 + rb + 4 * k;
-                const float v = tv[k] * rs;
-                D.out[(size_t)c * D.ldo + n] = v;
-                if (v > amv || (v == amv && n < ami)) {
-                  amv = v;
-                  ami = n;
-                }
-              }
-            }
-          } else {  // EPI_STORE
-            if (c < B)
-#pragma unroll
-              for (int k = 0; k < 4; ++k) D.out[(size_t)c * D.ldo + tl * 16 + rb + 4 * k] = tv[k] * s_rs[c];
-          }
-        }
-      }
-      named_sync(kBarPhase, (NC + 1) * 32);
-    }
-    if (lm) {
-#pragma unroll
-      for (int o = 8; o < 32; o <<= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, amv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, ami, o);
-        if (ov > amv || (ov == amv && oi < ami)) {
-          amv = ov;
-          ami = oi;
-        }
-      }
-      if (lane < 8) {
-        a.am_val[(size_t)cta * 8 + lane] = amv;
-        a.am_idx[(size_t)cta * 8 + lane] = ami;
       }
     }
   }
