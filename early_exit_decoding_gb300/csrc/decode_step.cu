@@ -220,6 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
   __shared__ float s_col[8][3];              // per column: the phase's reduced statistics
   __shared__ float s_stw[NC][24];            // per warp partial statistics
   __shared__ float s_rs[8];
+  __shared__ float s_xsc[8];        // W4 phases: 2^-k undoing the activation rows' scale
+  __shared__ float s_xmax[NC][8];   // per warp max |x| of each row
   __shared__ float s_freq[64];
   __shared__ volatile int s_e;    // exit layer as far as this CTA knows it
   __shared__ volatile int s_dec;  // last layer whose exit decision this CTA has taken
@@ -483,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
             for (int k = d + ct; k < Kp; k += NC * 32)
               reinterpret_cast<bf16*>(xs + (size_t)b * RSX)[k] = __float2bfloat16_rn(0.f);
+            fence_proxy_async_smem();  // later phases bulk-copy into these bytes
             ss = warp_sum(ss);
             if (lane == 0) red[warp * 32 + b] = make_float4(ss, 0.f, 0.f, 0.f);
           }
@@ -493,31 +496,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             s_col[ct][0] = sum;
           }
         }
-        if (D.xmode == X_SCALED) {
-          // per column: sums of the producing phase's per-tile partials
-          // (|h|^2; with three partials also <h_in, h> and |h_in|^2)
-          float acc[kFusedMaxB][3];
+        // ---- statistics of the producing phase (X_SCALED): per column sums of its
+        // per-tile partials (|h|^2; with three partials also <h_in, h> and
+        // |h_in|^2).  The loads are issued now; the reduction waits for the first
+        // epilogue unless the exit decision is needed first (tau mode, not yet
+        // exited: it picks this layer's weights).
+        const int sk = D.stats_k;
+        const bool scaled = D.xmode == X_SCALED;
+        const bool regs = scaled && B * sk <= 6 && D.stats_tiles <= NC * 32;
+        float pv[6];
 #pragma unroll
-          for (int b = 0; b < kFusedMaxB; ++b)
+        for (int i = 0; i < 6; ++i) pv[i] = 0.f;
+        if (regs && ct < D.stats_tiles) {
+          const float* sp = D.stats_in + (size_t)ct * 8 * sk;
 #pragma unroll
-            for (int j = 0; j < 3; ++j) acc[b][j] = 0.f;
-          const int sk = D.stats_k;
-          for (int tt = ct; tt < D.stats_tiles; tt += NC * 32) {
-            const float* sp = D.stats_in + (size_t)tt * 8 * sk;
+          for (int i = 0; i < 6; ++i)
+            if (i < B * sk) pv[i] = __ldcg(sp + i);
+        }
+        auto reduce_stats = [&]() {
+          if (regs) {
+#pragma unroll
+            for (int i = 0; i < 6; ++i)
+              if (i < B * sk) {
+                const float v = warp_sum(pv[i]);
+                if (lane == 0) s_stw[warp][(i / sk) * 3 + i % sk] = v;
+              }
+          } else {
+            float acc[kFusedMaxB][3];
+#pragma unroll
+            for (int b = 0; b < kFusedMaxB; ++b)
+#pragma unroll
+              for (int j = 0; j < 3; ++j) acc[b][j] = 0.f;
+            for (int tt = ct; tt < D.stats_tiles; tt += NC * 32) {
+              const float* sp = D.stats_in + (size_t)tt * 8 * sk;
+#pragma unroll
+              for (int b = 0; b < kFusedMaxB; ++b)
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                  if (b < B && j < sk) acc[b][j] += __ldcg(sp + b * sk + j);
+            }
 #pragma unroll
             for (int b = 0; b < kFusedMaxB; ++b)
 #pragma unroll
               for (int j = 0; j < 3; ++j)
-                if (b < B && j < sk) acc[b][j] += __ldcg(sp + b * sk + j);
+                if (b < B && j < sk) {
+                  const float v = warp_sum(acc[b][j]);
+                  if (lane == 0) s_stw[warp][b * 3 + j] = v;
+                }
           }
-#pragma unroll
-          for (int b = 0; b < kFusedMaxB; ++b)
-#pragma unroll
-            for (int j = 0; j < 3; ++j)
-              if (b < B && j < sk) {
-                const float v = warp_sum(acc[b][j]);
-                if (lane == 0) s_stw[warp][b * 3 + j] = v;
-              }
           named_sync(kBarCons, NC * 32);
           if (ct < 3 * B && (ct % 3) < sk) {
             float sum = 0.f;
@@ -525,37 +551,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             for (int w = 0; w < NC; ++w) sum += s_stw[w][ct];
             s_col[ct / 3][ct % 3] = sum;
           }
-        }
-        named_sync(kBarCons, NC * 32);
-        if (ct == 0) {
-          if (D.xmode == X_EMBED) {  // step begin
+          named_sync(kBarCons, NC * 32);
+          if (ct == 0) {
+            for (int b = 0; b < B; ++b) s_rs[b] = 1.f / sqrtf(s_col[b][0] / (float)a.d + a.eps);
+            if (D.dec_layer > 0 && sk == 3) {
+              // exit decision of layer dec_layer: batch minimum of the cosine
+              // between the residual entering and leaving it
+              float m = FLT_MAX;
+              for (int b = 0; b < B; ++b)
+                m = fminf(m, s_col[b][1] / fmaxf(sqrtf(s_col[b][2]) * sqrtf(s_col[b][0]), 1e-12f));
+              int e = s_e;
+              if (a.mode == RL_EXIT_TAU && e == a.L && D.dec_layer < a.L && m > a.tau) e = D.dec_layer;
+              s_e = e;
+              if (cta == 0) {
+                if (a.min_cos_out) a.min_cos_out[D.dec_layer - 1] = m;
+                a.st->exit_layer = e;
+              }
+              __threadfence_block();
+              s_dec = D.dec_layer;
+            }
+            tl2_mark(a.tl2, grid, p, cta, TL2_RED);
+          }
+          named_sync(kBarCons, NC * 32);
+        };
+        bool stats_pending = scaled;
+        if (D.xmode == X_EMBED) {
+          named_sync(kBarCons, NC * 32);
+          if (ct == 0) {  // step begin
             if (a.mode == RL_EXIT_FORCED && cta == 0) {
               const int raw = a.schedule[a.st->step % a.schedule_len];
               if (raw < 0 || raw > a.L) atomicOr(&a.st->err, RL_DEVERR_SCHEDULE);
             }
             if (cta == 0) a.st->exit_layer = s_e;
-          }
-          if (D.xmode == X_EMBED || D.xmode == X_SCALED)
             for (int b = 0; b < B; ++b) s_rs[b] = 1.f / sqrtf(s_col[b][0] / (float)a.d + a.eps);
-          if (D.xmode == X_SCALED && D.dec_layer > 0 && D.stats_k == 3) {
-            // exit decision of layer dec_layer: batch minimum of the cosine
-            // between the residual entering and leaving it
-            float m = FLT_MAX;
-            for (int b = 0; b < B; ++b)
-              m = fminf(m, s_col[b][1] / fmaxf(sqrtf(s_col[b][2]) * sqrtf(s_col[b][0]), 1e-12f));
-            int e = s_e;
-            if (a.mode == RL_EXIT_TAU && e == a.L && D.dec_layer < a.L && m > a.tau) e = D.dec_layer;
-            s_e = e;
-            if (cta == 0) {
-              if (a.min_cos_out) a.min_cos_out[D.dec_layer - 1] = m;
-              a.st->exit_layer = e;
-            }
-            __threadfence_block();
-            s_dec = D.dec_layer;
           }
-          tl2_mark(a.tl2, grid, p, cta, TL2_RED);
+          named_sync(kBarCons, NC * 32);
+        } else if (scaled && (!regs || (a.mode == RL_EXIT_TAU && s_e == a.L && D.dec_layer > 0 && D.dec_layer < a.L && sk == 3))) {
+          reduce_stats();
+          stats_pending = false;
         }
-        named_sync(kBarCons, NC * 32);
         const bool w4 = D.qwt && D.layer_no > 0 && D.layer_no > s_e;
         const int ntiles = D.N >> 4, UPT = (Kp + KU - 1) / KU;
         const int nt = cta < ntiles ? (ntiles - cta + grid - 1) / grid : 0;  // this CTA's tiles
@@ -581,16 +615,82 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           xpar ^= 1u;
         }
         if (ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
-        if (w4) {  // per-group sums of the bf16 activations
-          for (int gw = warp; gw < B * G; gw += NC) {
-            const int b = gw / G, gi = gw % G;
-            const uint2 v = *reinterpret_cast<const uint2*>(xs + (size_t)b * RSX + (gi * 128 + 4 * lane) * 2);
-            const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-            const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-            const float s2 = warp_sum((f0.x + f0.y) + (f1.x + f1.y));
-            if (lane == 0) xsum[b * G + gi] = s2;
+        if (w4) {
+          // The W4 MMAs run in fp16: every activation row is scaled by a power
+          // of two 2^k that brings its largest |x| just below 2^15 (exact, and
+          // bf16 values in the fp16 normal range convert exactly), converted to
+          // fp16 in place, and each 8-input chunk is reordered as (x0,x4),
+          // (x2,x6), (x1,x5), (x3,x7) to match the nibble fields the MMA reads;
+          // xsum[b][group] = sum of the group's scaled inputs (zero-point term).
+          const int nchk = Kp >> 3;
+          float mx[kFusedMaxB];
+#pragma unroll
+          for (int b = 0; b < kFusedMaxB; ++b) mx[b] = 0.f;
+          for (int ch = ct; ch < nchk; ch += NC * 32) {
+#pragma unroll
+            for (int b = 0; b < kFusedMaxB; ++b)
+              if (b < B) {
+                const uint4 v = *reinterpret_cast<const uint4*>(xs + (size_t)b * RSX + ch * 16);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+                  mx[b] = fmaxf(mx[b], fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+              }
+          }
+#pragma unroll
+          for (int b = 0; b < kFusedMaxB; ++b)
+            if (b < B) {
+              const float v = warp_max(mx[b]);
+              if (lane == 0) s_xmax[warp][b] = v;
+            }
+          named_sync(kBarCons, NC * 32);
+          if (ct < B) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < NC; ++w) v = fmaxf(v, s_xmax[w][ct]);
+            int e = 0;
+            if (v > 0.f) frexpf(v, &e);  // v < 2^e
+            const int k = min(max(15 - e, -120), 120);
+            s_xmax[0][ct] = ldexpf(1.f, k);
+            s_xsc[ct] = ldexpf(1.f, -k);
           }
           named_sync(kBarCons, NC * 32);
+          // each thread converts whole 8-input chunks; the 16 chunks of a group
+          // sit in 16 consecutive lanes, whose sum gives the group's term
+          for (int c0 = 0; c0 < nchk; c0 += NC * 32) {
+            const int ch = c0 + ct;
+            const bool on = ch < nchk;  // nchk is a multiple of 16: groups are all on or all off
+            for (int b = 0; b < B; ++b) {
+              float sum = 0.f;
+              if (on) {
+                const float sc = s_xmax[0][b];
+                uint4* cp = reinterpret_cast<uint4*>(xs + (size_t)b * RSX + ch * 16);
+                const uint4 v = *cp;
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 ff = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+                  f[2 * i] = ff.x * sc;
+                  f[2 * i + 1] = ff.y * sc;
+                }
+                sum = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+                const __half2 p0 = __floats2half2_rn(f[0], f[4]), p1 = __floats2half2_rn(f[2], f[6]);
+                const __half2 p2 = __floats2half2_rn(f[1], f[5]), p3 = __floats2half2_rn(f[3], f[7]);
+                *cp = make_uint4(*reinterpret_cast<const uint32_t*>(&p0), *reinterpret_cast<const uint32_t*>(&p1),
+                                 *reinterpret_cast<const uint32_t*>(&p2), *reinterpret_cast<const uint32_t*>(&p3));
+              }
+#pragma unroll
+              for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+              if (on && (ct & 15) == 0) xsum[b * G + (ch >> 4)] = sum;
+            }
+          }
+          fence_proxy_async_smem();  // a later phase's bulk copy rewrites these bytes
+          named_sync(kBarCons, NC * 32);
+        } else if (ct < 8) {
+          s_xsc[ct] = 1.f;
         }
         // MMA column g reads activation row min(g, B-1); columns >= B are dropped
         const unsigned char* xrow = xs + (size_t)(g < B ? g : B - 1) * RSX;
@@ -599,6 +699,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
 
         // epilogue of a batch of nb tiles starting at tile t_first (all consumer threads)
         auto flush = [&](int nb, int t_first, bool first_batch) {
+          if (stats_pending) {
+            reduce_stats();
+            stats_pending = false;
+          }
           named_sync(kBarCons, NC * 32);
           const int nout = nb * 16 * B;
           const int rounds = (nout + R - 1) / R;
@@ -611,6 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             if (act) {
 #pragma unroll
               for (int w = 0; w < NC; ++w) v += redf[((tb * NC + w) * B + my_c) * 16 + my_r];
+              v *= s_xsc[my_c];
             }
             if (D.epi == EPI_RESID) {
               float s0 = 0.f, s1 = 0.f, s2 = 0.f;
@@ -727,7 +832,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               if (ok && gi < G) {
               if (w4) {
                 // Lane t's word m holds the eight nibbles of input chunk 4m + t of
-                // the group; odd rows have their 64-byte halves swapped.
+                // the group; odd rows have their 64-byte halves swapped.  Each
+                // nibble field, masked in place, is the bit pattern of the
+                // subnormal fp16 q * 2^-24 (fields at bits 4..7 read 16 q * 2^-24):
+                // one AND per operand register, exact products in the MMA.
                 const unsigned char* st = sb + (size_t)s * STAGE_W;
                 const int cw = warp * 4 + t;
                 const uint4 wa = *reinterpret_cast<const uint4*>(st + g * 512 + ((cw ^ ((g & 1) << 2)) * 16));
@@ -736,24 +844,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 const uint32_t* szs = reinterpret_cast<const uint32_t*>(st + 16 * 512);
                 const uint32_t s0 = szs[g * 8 + (warp ^ (g >> 2))];
                 const uint32_t s1 = szs[(g + 8) * 8 + (warp ^ ((g + 8) >> 2))];
-                float acc[4][4];
+                float c1[2][4], c2[2][4];
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
+                for (int m = 0; m < 2; ++m)
 #pragma unroll
-                  for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
+                  for (int q = 0; q < 4; ++q) c1[m][q] = c2[m][q] = 0.f;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                  const uint32_t va = u4get(wa, m), vb = u4get(wb, m);
+                  const uint32_t va = u4get(wa, m), vb = u4get(wb, m), ha = va >> 8, hb = vb >> 8;
                   const uint4 X = *reinterpret_cast<const uint4*>(xrow + (gi * 128 + 32 * m + 8 * t) * 2);
-#pragma unroll
-                  for (int h = 0; h < 2; ++h) {
-                    const uint32_t A0 = ((va >> (4 * h)) & 0x000F000Fu) | 0x43004300u;
-                    const uint32_t A1 = ((vb >> (4 * h)) & 0x000F000Fu) | 0x43004300u;
-                    const uint32_t A2 = ((va >> (4 * h + 8)) & 0x000F000Fu) | 0x43004300u;
-                    const uint32_t A3 = ((vb >> (4 * h + 8)) & 0x000F000Fu) | 0x43004300u;
-                    const uint32_t sel = h ? 0x7632u : 0x5410u;
-                    mma_bf16(acc[m], A0, A1, A2, A3, __byte_perm(X.x, X.z, sel), __byte_perm(X.y, X.w, sel));
-                  }
+                  mma_f16(c1[m & 1], va & 0x000F000Fu, vb & 0x000F000Fu, ha & 0x000F000Fu, hb & 0x000F000Fu, X.x,
+                          X.y);
+                  mma_f16(c2[m & 1], va & 0x00F000F0u, vb & 0x00F000F0u, ha & 0x00F000F0u, hb & 0x00F000F0u, X.z,
+                          X.w);
                 }
                 __half2 h0, h1;
                 *reinterpret_cast<uint32_t*>(&h0) = s0;
@@ -761,15 +864,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 const float2 sz0 = __half22float2(h0), sz1 = __half22float2(h1);
                 const float xs0 = 2 * t < B ? xsum[(2 * t) * G + gi] : 0.f;
                 const float xs1 = 2 * t + 1 < B ? xsum[(2 * t + 1) * G + gi] : 0.f;
-                const float o0 = 128.f + sz0.y, o1 = 128.f + sz1.y;
-                const float a0 = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
-                const float a1 = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
-                const float a2 = (acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2]);
-                const float a3 = (acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3]);
-                y[0][0] += sz0.x * (a0 - o0 * xs0);
-                y[0][1] += sz0.x * (a1 - o0 * xs1);
-                y[0][2] += sz1.x * (a2 - o1 * xs0);
-                y[0][3] += sz1.x * (a3 - o1 * xs1);
+                // sum_k (q_k - z) s x_k = s 2^24 (c1 + c2 / 16) - s z sum_k x_k
+                const float p0 = sz0.x * 16777216.f, p1 = sz1.x * 16777216.f;
+                const float q0 = sz0.x * sz0.y, q1 = sz1.x * sz1.y;
+                float av[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) av[c] = (c1[0][c] + c1[1][c]) + 0.0625f * (c2[0][c] + c2[1][c]);
+                y[0][0] = fmaf(p0, av[0], fmaf(-q0, xs0, y[0][0]));
+                y[0][1] = fmaf(p0, av[1], fmaf(-q0, xs1, y[0][1]));
+                y[0][2] = fmaf(p1, av[2], fmaf(-q1, xs0, y[0][2]));
+                y[0][3] = fmaf(p1, av[3], fmaf(-q1, xs1, y[0][3]));
               } else {
                 // bf16 unit: 16 rows of kn inputs; 16-byte chunk c of row r at
                 // c ^ 4 (r & 1): the 8 lanes of a quarter warp (rows 2q, 2q+1,
@@ -818,6 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             nb = 0;
           }
         }
+        if (stats_pending) reduce_stats();  // a CTA without tiles still takes the decision
         if (D.epi == EPI_LMHEAD) {
           // this CTA's argmax per column: 16-lane groups, then one thread per column
 #pragma unroll
@@ -888,6 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             const uint4 vv = __ldcg(reinterpret_cast<const uint4*>(D.vc + (head_base + pos) * hd) + ct);
             *reinterpret_cast<uint4*>(Ks + rw * RK + ct * 16) = kv;
             *reinterpret_cast<uint4*>(Vs + rw * RK + ct * 16) = vv;
+            fence_proxy_async_smem();  // the slot is refilled by bulk copies later
           }
           named_sync(kBarCons, NC * 32);
           // per-warp scores, softmax and P V; the warps' partials overlay the K rows
@@ -926,6 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               pp[hd + 1] = den;
             }
           }
+          fence_proxy_async_smem();  // the warps' partials overlay the slot, refilled by bulk copies
           named_sync(kBarCons, NC * 32);
           if (lane == 0) {
             mbar_arrive(&empty[slot]);
