@@ -211,6 +211,53 @@ __device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigne
     for (int d = 0; d < DPL; ++d) w0[h * WS + 2 + DPL * lane + d] = o[h][d];
 }
 
+// One W4 unit of the step kernel's consumer warp: this warp's 128-input group
+// gi of 16 weight rows (stage `st`) against the activation rows.  Lane t's word
+// m holds the eight nibbles of input chunk 4m + t of the group; odd rows have
+// their 64-byte halves swapped.  Each nibble field, masked in place, is the bit
+// pattern of the subnormal fp16 q * 2^-24 (fields at bits 4..7 read
+// 16 q * 2^-24): one AND per operand register, exact products in the MMA.  The
+// activations are fp16, scaled and reordered per 8-input chunk as (x0,x4),
+// (x2,x6), (x1,x5), (x3,x7); xsum holds the groups' input sums.
+__device__ __forceinline__ void w4_unit(const unsigned char* st, int gi, const unsigned char* xrow,
+                                        const float* xsum, int B, int G, int warp, int g, int t,
+                                        float (&y)[4]) {
+  const int cw = warp * 4 + t;
+  const uint4 wa = *reinterpret_cast<const uint4*>(st + g * 512 + ((cw ^ ((g & 1) << 2)) * 16));
+  const uint4 wb = *reinterpret_cast<const uint4*>(st + (g + 8) * 512 + ((cw ^ (((g + 8) & 1) << 2)) * 16));
+  const uint32_t* szs = reinterpret_cast<const uint32_t*>(st + 16 * 512);
+  const uint32_t s0 = szs[g * 8 + (warp ^ (g >> 2))];
+  const uint32_t s1 = szs[(g + 8) * 8 + (warp ^ ((g + 8) >> 2))];
+  float c1[2][4], c2[2][4];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c1[m][q] = c2[m][q] = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t va = u4get(wa, m), vb = u4get(wb, m), ha = va >> 8, hb = vb >> 8;
+    const uint4 X = *reinterpret_cast<const uint4*>(xrow + (gi * 128 + 32 * m + 8 * t) * 2);
+    mma_f16(c1[m & 1], va & 0x000F000Fu, vb & 0x000F000Fu, ha & 0x000F000Fu, hb & 0x000F000Fu, X.x, X.y);
+    mma_f16(c2[m & 1], va & 0x00F000F0u, vb & 0x00F000F0u, ha & 0x00F000F0u, hb & 0x00F000F0u, X.z, X.w);
+  }
+  __half2 h0, h1;
+  *reinterpret_cast<uint32_t*>(&h0) = s0;
+  *reinterpret_cast<uint32_t*>(&h1) = s1;
+  const float2 sz0 = __half22float2(h0), sz1 = __half22float2(h1);
+  const float xs0 = 2 * t < B ? xsum[(2 * t) * G + gi] : 0.f;
+  const float xs1 = 2 * t + 1 < B ? xsum[(2 * t + 1) * G + gi] : 0.f;
+  // sum_k (q_k - z) s x_k = s 2^24 (c1 + c2 / 16) - s z sum_k x_k
+  const float p0 = sz0.x * 16777216.f, p1 = sz1.x * 16777216.f;
+  const float q0 = sz0.x * sz0.y, q1 = sz1.x * sz1.y;
+  float av[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) av[c] = (c1[0][c] + c1[1][c]) + 0.0625f * (c2[0][c] + c2[1][c]);
+  y[0] = fmaf(p0, av[0], fmaf(-q0, xs0, y[0]));
+  y[1] = fmaf(p0, av[1], fmaf(-q0, xs1, y[1]));
+  y[2] = fmaf(p1, av[2], fmaf(-q1, xs0, y[2]));
+  y[3] = fmaf(p1, av[3], fmaf(-q1, xs1, y[3]));
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_constant__ StepArgs a) {
@@ -827,57 +874,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             first_w = false;
             const unsigned char* sb = ring + (size_t)slot * SLOT_B;
             const int ns = min(step_u, UPT - i0);
-            for (int s = 0; s < ns; ++s) {
-              const int gi = uk * 8 + warp;  // this warp's group
-              if (ok && gi < G) {
-              if (w4) {
-                // Lane t's word m holds the eight nibbles of input chunk 4m + t of
-                // the group; odd rows have their 64-byte halves swapped.  Each
-                // nibble field, masked in place, is the bit pattern of the
-                // subnormal fp16 q * 2^-24 (fields at bits 4..7 read 16 q * 2^-24):
-                // one AND per operand register, exact products in the MMA.
-                const unsigned char* st = sb + (size_t)s * STAGE_W;
-                const int cw = warp * 4 + t;
-                const uint4 wa = *reinterpret_cast<const uint4*>(st + g * 512 + ((cw ^ ((g & 1) << 2)) * 16));
-                const uint4 wb = *reinterpret_cast<const uint4*>(st + (g + 8) * 512 +
-                                                                 ((cw ^ (((g + 8) & 1) << 2)) * 16));
-                const uint32_t* szs = reinterpret_cast<const uint32_t*>(st + 16 * 512);
-                const uint32_t s0 = szs[g * 8 + (warp ^ (g >> 2))];
-                const uint32_t s1 = szs[(g + 8) * 8 + (warp ^ ((g + 8) >> 2))];
-                float c1[2][4], c2[2][4];
-#pragma unroll
-                for (int m = 0; m < 2; ++m)
-#pragma unroll
-                  for (int q = 0; q < 4; ++q) c1[m][q] = c2[m][q] = 0.f;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                  const uint32_t va = u4get(wa, m), vb = u4get(wb, m), ha = va >> 8, hb = vb >> 8;
-                  const uint4 X = *reinterpret_cast<const uint4*>(xrow + (gi * 128 + 32 * m + 8 * t) * 2);
-                  mma_f16(c1[m & 1], va & 0x000F000Fu, vb & 0x000F000Fu, ha & 0x000F000Fu, hb & 0x000F000Fu, X.x,
-                          X.y);
-                  mma_f16(c2[m & 1], va & 0x00F000F0u, vb & 0x00F000F0u, ha & 0x00F000F0u, hb & 0x00F000F0u, X.z,
-                          X.w);
+            if (w4) {
+              // two units at a time: independent MMA chains interleave
+              for (int s = 0; s < ns; s += 2) {
+                const int ga = (uk + s) * 8 + warp, gb = ga + 8;
+                const bool on_a = ok && ga < G, on_b = ok && s + 1 < ns && gb < G;
+                if (on_b) {
+                  w4_unit(sb + (size_t)s * STAGE_W, ga, xrow, xsum, B, G, warp, g, t, y[0]);
+                  w4_unit(sb + (size_t)(s + 1) * STAGE_W, gb, xrow, xsum, B, G, warp, g, t, y[1]);
+                } else if (on_a) {
+                  w4_unit(sb + (size_t)s * STAGE_W, ga, xrow, xsum, B, G, warp, g, t, y[0]);
                 }
-                __half2 h0, h1;
-                *reinterpret_cast<uint32_t*>(&h0) = s0;
-                *reinterpret_cast<uint32_t*>(&h1) = s1;
-                const float2 sz0 = __half22float2(h0), sz1 = __half22float2(h1);
-                const float xs0 = 2 * t < B ? xsum[(2 * t) * G + gi] : 0.f;
-                const float xs1 = 2 * t + 1 < B ? xsum[(2 * t + 1) * G + gi] : 0.f;
-                // sum_k (q_k - z) s x_k = s 2^24 (c1 + c2 / 16) - s z sum_k x_k
-                const float p0 = sz0.x * 16777216.f, p1 = sz1.x * 16777216.f;
-                const float q0 = sz0.x * sz0.y, q1 = sz1.x * sz1.y;
-                float av[4];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) av[c] = (c1[0][c] + c1[1][c]) + 0.0625f * (c2[0][c] + c2[1][c]);
-                y[0][0] = fmaf(p0, av[0], fmaf(-q0, xs0, y[0][0]));
-                y[0][1] = fmaf(p0, av[1], fmaf(-q0, xs1, y[0][1]));
-                y[0][2] = fmaf(p1, av[2], fmaf(-q1, xs0, y[0][2]));
-                y[0][3] = fmaf(p1, av[3], fmaf(-q1, xs1, y[0][3]));
-              } else {
-                // bf16 unit: 16 rows of kn inputs; 16-byte chunk c of row r at
-                // c ^ 4 (r & 1): the 8 lanes of a quarter warp (rows 2q, 2q+1,
-                // chunks c0..c0+3) hit 8 different 16-byte bank groups
+              }
+              uk += ns;
+            } else {
+              // bf16 unit: 16 rows of kn inputs; 16-byte chunk c of row r at
+              // c ^ 4 (r & 1): the 8 lanes of a quarter warp (rows 2q, 2q+1,
+              // chunks c0..c0+3) hit 8 different 16-byte bank groups
+              const int gi = uk * 8 + warp;  // this warp's 128 inputs of the unit
+              if (ok && gi < G) {
                 const int k0 = uk * KU, kn = min(KU, Kp - k0), RS = kn * 2;
                 const int sw = (g & 1) << 2;
 #pragma unroll
@@ -892,7 +907,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                              u4get(wb, 2 * e + 1), u4get(X, 2 * e), u4get(X, 2 * e + 1));
                 }
               }
-            }
               ++uk;
             }
             __syncwarp();
