@@ -166,7 +166,8 @@ struct rl_kv {
   int path_pref = RL_PATH_AUTO;  // rl_kv_set_decode_path
   // persistent step kernel
   bool use_step = true;
-  unsigned* bars = nullptr;           // phase arrival counters [nph_cap]
+  unsigned* bars = nullptr;           // per-CTA phase flags [n_bars], 128 bytes apart
+  size_t n_bars = 0;
   unsigned* tctr = nullptr;           // per-phase tile counters [nph_cap]
   PhaseDesc* d_ph = nullptr;          // phase descriptors [nph_cap]
   std::vector<PhaseDesc> h_ph;        // host copy of what d_ph holds
@@ -819,7 +820,7 @@ rl_status enqueue_decode_fused(rl_model* m, rl_kv* kv, const StepIO& io, int nch
 // Zero the cross-CTA counters of the decode kernels (after an aborted step,
 // or when the position is rewound).
 rl_status reset_sync_words(rl_kv* kv, cudaStream_t s) {
-  RL_CUDA(cudaMemsetAsync(kv->bars, 0, (size_t)kv->nph_cap * sizeof(unsigned), s));
+  RL_CUDA(cudaMemsetAsync(kv->bars, 0, kv->n_bars * sizeof(unsigned), s));
   RL_CUDA(cudaMemsetAsync(kv->tctr, 0, (size_t)kv->nph_cap * sizeof(unsigned), s));
   RL_CUDA(cudaMemsetAsync(kv->tile_ticket, 0, (size_t)kv->n_tile_ticket * sizeof(unsigned), s));
   RL_CUDA(cudaMemsetAsync(kv->attn_ticket, 0, (size_t)kv->maxB * kv->m->Hkv * sizeof(unsigned), s));
@@ -1193,7 +1194,8 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
   {
     int coop = 0;
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-    m->step_ok = coop != 0;
+    // one consumer thread per CTA polls that CTA's phase flag: grid <= 256
+    m->step_ok = coop != 0 && m->sm_count <= 256;
   }
 
   auto bail = [&](rl_status st) {
@@ -1407,7 +1409,8 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
   {
     // persistent step kernel: phase counters, descriptors, attention partials
     kv->nph_cap = 6 * m->L + 2;
-    K_TRY(kv->alloc(&kv->bars, (size_t)kv->nph_cap));
+    kv->n_bars = (size_t)m->sm_count * 32;
+    K_TRY(kv->alloc(&kv->bars, kv->n_bars));
     K_TRY(kv->alloc(&kv->tctr, (size_t)kv->nph_cap));
     K_TRY(kv->alloc(&kv->d_ph, (size_t)kv->nph_cap));
     const int CH = 128;  // positions per attention chunk

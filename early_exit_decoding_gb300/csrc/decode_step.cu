@@ -446,20 +446,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         int* dst = reinterpret_cast<int*>(&cdesc);
         for (int i = ct; i < (int)(sizeof(PhaseDesc) / 4); i += NC * 32) dst[i] = __ldg(src + i);
       }
-      if (p > 0 && ct == 0 && !s_abort) {
-        // every CTA has finished phase p - 1
-        const unsigned* bp = a.bars + (p - 1);
+      if (p > 0 && ct < grid && !s_abort) {
+        // every CTA has finished phase p - 1: thread j waits for CTA j's flag
+        // (CTA j stores p after its phase p - 1; flags sit 128 bytes apart)
+        const unsigned* fp = a.bars + (size_t)ct * 32;
         long long i = 0;
-        while (ld_acquire(bp) < (unsigned)grid && i < kSpinBar) {
-          __nanosleep(20);
-          ++i;
-        }
+        while (ld_acquire(fp) < (unsigned)p && i < kSpinBar) ++i;
         if (i >= kSpinBar) {
           atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
           s_abort = 1;
         }
-        __threadfence();
-        fence_proxy_async();
+        if (ct == 0) fence_proxy_async();  // the phase's bulk copies read other CTAs' writes
       }
       named_sync(kBarCons, NC * 32);
       if (ct == 0) {
@@ -1126,7 +1123,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         tl2_mark(a.tl2, grid, p, cta, TL2_ARRIVE);
         // the release orders every write of this CTA's phase (made before the
         // barrier above) before the arrival
-        if (p + 1 < a.nph) red_release_add(a.bars + p, 1u);
+        if (p + 1 < a.nph) st_release(a.bars + (size_t)cta * 32, (unsigned)(p + 1));
       }
     }
   }
@@ -1168,10 +1165,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
     }
     if (lane == 0 && a.next_token) a.next_token[warp] = bi == 0x7fffffff ? 0 : bi;
   }
-  for (int i = tid; i < a.nph; i += kThreads) {
-    a.bars[i] = 0u;
-    a.tctr[i] = 0u;
-  }
+  for (int i = tid; i < grid; i += kThreads) a.bars[(size_t)i * 32] = 0u;
+  for (int i = tid; i < a.nph; i += kThreads) a.tctr[i] = 0u;
   if (tid == 0) {
     DevState* st = a.st;
     if (a.exit_out) a.exit_out[0] = st->exit_layer;

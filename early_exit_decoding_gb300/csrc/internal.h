@@ -286,7 +286,7 @@ struct StepArgs {
   float* am_val;
   int* am_idx;
   unsigned* cta_ticket;
-  unsigned* bars;             // [nph] phase arrival counters, zero at step start
+  unsigned* bars;             // [grid * 32] per-CTA phase flags (128 B apart), zero at step start
   unsigned* tctr;             // [nph] tiles handed out per projection phase, zero at step start
   float* ws;                  // stream-K partial tiles [grid][2][128]
   unsigned* tile_ticket;      // [max tiles]
