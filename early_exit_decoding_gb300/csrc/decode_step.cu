@@ -25,6 +25,8 @@
 // A CTA takes the 16-row tiles cta, cta + grid, ... of each projection.  Every
 // wait is bounded: on timeout the kernel sets RL_DEVERR_TIMEOUT and winds down
 // without touching more memory.
+#include <type_traits>
+
 #include "dev_common.cuh"
 
 namespace river {
@@ -96,35 +98,32 @@ __device__ __forceinline__ float butterfly32(float (&v)[32], int lane) {
   return v[0];
 }
 
-// One warp's share of an attention chunk: positions 16*warp .. 16*warp+15
-// (those below n) against the REP query heads of one KV head.  Lane l holds
-// dims [DPL*l, DPL*(l+1)) of q (pre-scaled by 1/sqrt(hd)) and of each K / V
-// row.  Scores come 32 at a time from the butterfly (P positions x REP heads,
+// One warp's share of an attention chunk: positions j0 .. j0 + jn - 1 (jn <= 16)
+// against the REP query heads of one KV head.  Lane l holds dims [DPL*l,
+// DPL*(l+1)) of q (pre-scaled by 1/sqrt(hd), in qr) and of each K / V row.
+// Scores come 32 at a time from the butterfly (P positions x REP heads,
 // output i in lane i); the warp keeps its own running max / sum per head and
-// its P V partial.  After a barrier of the consumer warps (every warp is
-// done reading K and V) writes, per head, (max, sum, o[hd]) to wb, which may
+// its P V partial.  After a barrier of the consumer warps (every warp is done
+// reading K and V) writes, per head, (max, sum, o[hd]) to w0, which may
 // overlay the chunk's K / V rows.
 template <int REP, int DPL>
-__device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigned char* Vs, int n,
-                                          const float* qg, float scale, int warp, int lane, float* wb) {
+__device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigned char* Vs, int j0, int jn,
+                                          const float (&qr)[REP][DPL], int lane, float* w0) {
   constexpr int HD = 32 * DPL, RK = HD * 2, P = 32 / REP, NB = (16 + P - 1) / P, WS = 2 + HD;
-  float qr[REP][DPL];
-#pragma unroll
-  for (int h = 0; h < REP; ++h)
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) qr[h][d] = __ldcg(qg + h * HD + DPL * lane + d) * scale;
   float sc[NB];
   float mloc = -FLT_MAX;
 #pragma unroll
   for (int bb = 0; bb < NB; ++bb) {
+    sc[bb] = -FLT_MAX;
+    if (bb * P >= jn) continue;  // uniform over the warp
     float vals[32];
 #pragma unroll
     for (int jj = 0; jj < P; ++jj) {
-      const int jw = bb * P + jj, j = warp * 16 + jw;
+      const int jw = bb * P + jj, j = j0 + jw;
       float kf[DPL];
 #pragma unroll
       for (int d = 0; d < DPL; ++d) kf[d] = 0.f;
-      if (jw < 16 && j < n) {
+      if (jw < jn) {
         if (DPL == 4) {
           const uint2 w = *reinterpret_cast<const uint2*>(Ks + j * RK + lane * 8);
           const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
@@ -149,8 +148,8 @@ __device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigne
       }
     }
     const float s = butterfly32(vals, lane);
-    const int jw = bb * P + lane / REP, j = warp * 16 + jw;
-    sc[bb] = (jw < 16 && j < n) ? s : -FLT_MAX;
+    const int jw = bb * P + lane / REP;
+    sc[bb] = jw < jn ? s : -FLT_MAX;
     mloc = fmaxf(mloc, sc[bb]);
   }
   // lanes with the same head (lane % REP) share max and sum
@@ -174,8 +173,8 @@ __device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigne
   for (int bb = 0; bb < NB; ++bb) {
 #pragma unroll
     for (int jj = 0; jj < P; ++jj) {
-      const int jw = bb * P + jj, j = warp * 16 + jw;
-      if (!(jw < 16 && j < n)) continue;  // uniform over the warp
+      const int jw = bb * P + jj, j = j0 + jw;
+      if (!(jw < jn)) continue;  // uniform over the warp
       float vf[DPL];
       if (DPL == 4) {
         const uint2 w = *reinterpret_cast<const uint2*>(Vs + j * RK + lane * 8);
@@ -200,7 +199,6 @@ __device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigne
     }
   }
   dev::named_sync(1, 8 * 32);
-  float* w0 = wb + (size_t)warp * REP * WS;
   if (lane < REP) {
     w0[lane * WS] = mloc;
     w0[lane * WS + 1] = lloc;
@@ -976,79 +974,102 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         const float scale = rsqrtf((float)hd);
         const int WS = 2 + hd;
         if (clen > kCHP && cta == 0 && ct == 0) atomicOr(&a.st->err, RL_DEVERR_CAPACITY);
-        for (int it = cta; it < nitems; it += grid) {
-          const int b = it / (Hkv * nch), rr = it % (Hkv * nch), hk = rr / nch, ch = rr % nch;
-          const int start = ch * clen, end = min(start + clen, ctx);
-          const int n = min(kCHP, max(0, end - start));
-          const int slot = rc.slot;
-          bool ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
-          rc.next(NS);
-          int slot_v = slot;
-          if (two) {
-            slot_v = rc.slot;
-            ok = ok && mbar_wait(&full[slot_v], (uint32_t)(rc.round & 1), kSpin);
+        auto run = [&](auto rep_c, auto dpl_c) {
+          constexpr int REP = decltype(rep_c)::value, DPL = decltype(dpl_c)::value, HDC = 32 * DPL;
+          // q of an item: loaded (scaled) before its chunk is waited for
+          float qr[REP][DPL];
+          auto load_q = [&](int it) {
+            const int b = it / (Hkv * nch), hk = (it % (Hkv * nch)) / nch;
+            const float* qg = D.q_out + (size_t)b * Hq * HDC + (size_t)hk * REP * HDC;
+#pragma unroll
+            for (int h = 0; h < REP; ++h)
+#pragma unroll
+              for (int d = 0; d < DPL; ++d) qr[h][d] = __ldcg(qg + h * HDC + DPL * lane + d) * scale;
+          };
+          for (int it = cta; it < nitems; it += grid) {
+            load_q(it);
+            const int b = it / (Hkv * nch), rr = it % (Hkv * nch), hk = rr / nch, ch = rr % nch;
+            const int start = ch * clen, end = min(start + clen, ctx);
+            const int n = min(kCHP, max(0, end - start));
+            // the row written by this step's QKV phase: loads issued before the wait
+            const size_t head_base = ((size_t)b * Hkv + hk) * a.Tmax;
+            const bool has_new = pos >= start && pos < start + n && ct < HDC / 8;
+            uint4 kv_new = make_uint4(0u, 0u, 0u, 0u), vv_new = kv_new;
+            if (has_new) {
+              kv_new = __ldcg(reinterpret_cast<const uint4*>(D.kc + (head_base + pos) * HDC) + ct);
+              vv_new = __ldcg(reinterpret_cast<const uint4*>(D.vc + (head_base + pos) * HDC) + ct);
+            }
+            const int slot = rc.slot;
+            bool ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
             rc.next(NS);
-          }
-          if (!ok && s_abort == 0) {
-            if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-            s_abort = 1;
-          }
-          if (it == cta && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
-          unsigned char* Ks = ring + (size_t)slot * SLOT_B;
-          unsigned char* Vs = two ? ring + (size_t)slot_v * SLOT_B : Ks + kAttnHalf;
-          const size_t head_base = ((size_t)b * Hkv + hk) * a.Tmax;
-          if (ok && pos >= start && pos < start + n && ct < hd / 8) {
-            // the row written by this step's QKV phase
-            const int rw = pos - start;
-            const uint4 kv = __ldcg(reinterpret_cast<const uint4*>(D.kc + (head_base + pos) * hd) + ct);
-            const uint4 vv = __ldcg(reinterpret_cast<const uint4*>(D.vc + (head_base + pos) * hd) + ct);
-            *reinterpret_cast<uint4*>(Ks + rw * RK + ct * 16) = kv;
-            *reinterpret_cast<uint4*>(Vs + rw * RK + ct * 16) = vv;
-            fence_proxy_async_smem();  // the slot is refilled by bulk copies later
-          }
-          named_sync(kBarCons, NC * 32);
-          // per-warp scores, softmax and P V; the warps' partials overlay the K rows
-          float* wb = reinterpret_cast<float*>(Ks);
-          const float* qg = D.q_out + (size_t)b * Hq * hd + (size_t)hk * rep * hd;
-          const int nn = ok ? n : 0;
-          const int key = rep * 8 + (hd >> 5);
-          switch (key) {
-            case 1 * 8 + 2: attn_warp<1, 2>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
-            case 2 * 8 + 2: attn_warp<2, 2>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
-            case 4 * 8 + 2: attn_warp<4, 2>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
-            case 1 * 8 + 4: attn_warp<1, 4>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
-            case 2 * 8 + 4: attn_warp<2, 4>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
-            default: attn_warp<4, 4>(Ks, Vs, nn, qg, scale, warp, lane, wb); break;
-          }
-          named_sync(kBarCons, NC * 32);
-          // combine the eight warps (online-softmax rescale) into this chunk's partial
-          float* part = a.part + ((size_t)b * Hq + (size_t)hk * rep) * a.part_cap * (hd + 2);
-          for (int i = ct; i < rep * hd; i += NC * 32) {
-            const int h = i / hd, dd = i % hd;
-            float M = -FLT_MAX;
-#pragma unroll
-            for (int w = 0; w < NC; ++w) M = fmaxf(M, wb[(w * rep + h) * WS]);
-            float num = 0.f, den = 0.f;
-#pragma unroll
-            for (int w = 0; w < NC; ++w) {
-              const float* ww = wb + (w * rep + h) * WS;
-              const float f = ww[1] > 0.f ? __expf(ww[0] - M) : 0.f;
-              num += f * ww[2 + dd];
-              den += f * ww[1];
+            int slot_v = slot;
+            if (two) {
+              slot_v = rc.slot;
+              ok = ok && mbar_wait(&full[slot_v], (uint32_t)(rc.round & 1), kSpin);
+              rc.next(NS);
             }
-            float* pp = part + ((size_t)h * a.part_cap + ch) * (hd + 2);
-            pp[dd] = num;
-            if (dd == 0) {
-              pp[hd] = den > 0.f ? M : -FLT_MAX;
-              pp[hd + 1] = den;
+            if (!ok && s_abort == 0) {
+              if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+              s_abort = 1;
+            }
+            if (it == cta && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
+            unsigned char* Ks = ring + (size_t)slot * SLOT_B;
+            unsigned char* Vs = two ? ring + (size_t)slot_v * SLOT_B : Ks + kAttnHalf;
+            if (ok && has_new) {
+              const int rw = pos - start;
+              *reinterpret_cast<uint4*>(Ks + rw * RK + ct * 16) = kv_new;
+              *reinterpret_cast<uint4*>(Vs + rw * RK + ct * 16) = vv_new;
+              fence_proxy_async_smem();  // the slot is refilled by bulk copies later
+            }
+            named_sync(kBarCons, NC * 32);
+            // per-warp scores, softmax and P V over an even share of the chunk's
+            // positions; the warps' partials overlay the K rows
+            float* wb = reinterpret_cast<float*>(Ks);
+            const int nn = ok ? n : 0;
+            const int pw = (nn + NC - 1) / NC;
+            const int j0 = warp * pw, jn = max(0, min(pw, nn - j0));
+            attn_warp<REP, DPL>(Ks, Vs, j0, jn, qr, lane, wb + (size_t)warp * REP * WS);
+            named_sync(kBarCons, NC * 32);
+            // combine the eight warps (online-softmax rescale) into this chunk's partial
+            float* part = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * (HDC + 2);
+            for (int i = ct; i < REP * HDC; i += NC * 32) {
+              const int h = i / HDC, dd = i % HDC;
+              float M = -FLT_MAX;
+#pragma unroll
+              for (int w = 0; w < NC; ++w) M = fmaxf(M, wb[(w * REP + h) * WS]);
+              float num = 0.f, den = 0.f;
+#pragma unroll
+              for (int w = 0; w < NC; ++w) {
+                const float* ww = wb + (w * REP + h) * WS;
+                const float f = ww[1] > 0.f ? __expf(ww[0] - M) : 0.f;
+                num += f * ww[2 + dd];
+                den += f * ww[1];
+              }
+              float* pp = part + ((size_t)h * a.part_cap + ch) * (HDC + 2);
+              pp[dd] = num;
+              if (dd == 0) {
+                pp[HDC] = den > 0.f ? M : -FLT_MAX;
+                pp[HDC + 1] = den;
+              }
+            }
+            fence_proxy_async_smem();  // the warps' partials overlay the slot, refilled by bulk copies
+            named_sync(kBarCons, NC * 32);
+            if (lane == 0) {
+              mbar_arrive(&empty[slot]);
+              if (two) mbar_arrive(&empty[slot_v]);
             }
           }
-          fence_proxy_async_smem();  // the warps' partials overlay the slot, refilled by bulk copies
-          named_sync(kBarCons, NC * 32);
-          if (lane == 0) {
-            mbar_arrive(&empty[slot]);
-            if (two) mbar_arrive(&empty[slot_v]);
-          }
+        };
+        using I1 = std::integral_constant<int, 1>;
+        using I2 = std::integral_constant<int, 2>;
+        using I4 = std::integral_constant<int, 4>;
+        switch (rep * 8 + (hd >> 5)) {
+          case 1 * 8 + 2: run(I1{}, I2{}); break;
+          case 2 * 8 + 2: run(I2{}, I2{}); break;
+          case 4 * 8 + 2: run(I4{}, I2{}); break;
+          case 1 * 8 + 4: run(I1{}, I4{}); break;
+          case 2 * 8 + 4: run(I2{}, I4{}); break;
+          default: run(I4{}, I4{}); break;
         }
       } else {
         // ---- merge of the attention chunks, spread over all CTAs ------------------------
