@@ -245,8 +245,6 @@ def rl_kv_timeline(kv, stream=None):
     buf = np.zeros(cap, dtype=np.uint64)
     _check(_lib.rl_kv_timeline(kv, _stream(stream), cap, buf.ctypes.data_as(ctypes.c_void_p),
                                ctypes.byref(n_ph), ctypes.byref(n_cta), ctypes.byref(n_st)))
-    global _dbg_raw
-    _dbg_raw = buf[: n_ph.value * n_cta.value * n_st.value + n_cta.value * 16].copy()
     return buf[: n_ph.value * n_cta.value * n_st.value].reshape(n_ph.value, n_cta.value, n_st.value)
 
 

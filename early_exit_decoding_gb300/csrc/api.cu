@@ -1071,7 +1071,7 @@ rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStre
     RL_CUDA(cudaMemsetAsync(kv->tl + a.nph, 0, (size_t)a.nph * 8, s));
     if (kv->timeline) {
       a.tl2 = kv->tl2;
-      RL_CUDA(cudaMemsetAsync(kv->tl2, 0, ((size_t)a.nph * m->sm_count * kTl2 + (size_t)m->sm_count * 16) * 8, s));
+      RL_CUDA(cudaMemsetAsync(kv->tl2, 0, (size_t)a.nph * m->sm_count * kTl2 * 8, s));
     }
     cudaEventRecordWithFlags(kv->ev[0], s, cudaEventRecordExternal);
   }
@@ -1711,7 +1711,7 @@ rl_status rl_kv_set_profiling(rl_kv* kv, int32_t enable) {
     RL_TRY(kv->alloc(&kv->tl, (size_t)2 * kv->nph_cap));
   }
   if (enable >= 2 && !kv->tl2)
-    RL_TRY(kv->alloc(&kv->tl2, (size_t)kv->nph_cap * kv->m->sm_count * kTl2 + (size_t)kv->m->sm_count * 16));
+    RL_TRY(kv->alloc(&kv->tl2, (size_t)kv->nph_cap * kv->m->sm_count * kTl2));
   kv->profiling = enable != 0;
   kv->timeline = enable >= 2;
   return RL_OK;
@@ -1722,7 +1722,7 @@ rl_status rl_kv_timeline(rl_kv* kv, rl_stream_t stream, int64_t cap, uint64_t* o
   if (!kv || !out || !nphase || !nctas || !nstamps) return fail(RL_ERR_INVALID_ARG, "NULL argument");
   if (!kv->tl2 || kv->nrec != -1) return fail(RL_ERR_STATE, "no per-CTA timeline recorded");
   RL_CUDA(cudaStreamSynchronize(as_stream(stream)));
-  const int64_t need = (int64_t)kv->nph_last * kv->m->sm_count * kTl2 + kv->m->sm_count * 16;
+  const int64_t need = (int64_t)kv->nph_last * kv->m->sm_count * kTl2;
   if (cap < need) return fail(RL_ERR_INVALID_ARG, "timeline buffer too small");
   RL_CUDA(cudaMemcpy(out, kv->tl2, (size_t)need * 8, cudaMemcpyDeviceToHost));
   *nphase = kv->nph_last;
