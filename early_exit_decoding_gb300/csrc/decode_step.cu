@@ -555,7 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           for (int i = 0; i < 6; ++i)
             if (i < B * sk) pv[i] = __ldcg(sp + i);
         }
-        auto reduce_stats = [&]() {
+        // (1) per-warp partial sums into s_stw (no barrier)
+        auto stats_partials = [&]() {
           if (regs) {
 #pragma unroll
             for (int i = 0; i < 6; ++i)
@@ -586,35 +587,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                   if (lane == 0) s_stw[warp][b * 3 + j] = v;
                 }
           }
-          named_sync(kBarCons, NC * 32);
-          if (ct < 3 * B && (ct % 3) < sk) {
-            float sum = 0.f;
+        };
+        // (2) after a barrier: column sums in a fixed order (the same in every thread)
+        auto col_sum = [&](int b, int j) {
+          float sum = 0.f;
 #pragma unroll
-            for (int w = 0; w < NC; ++w) sum += s_stw[w][ct];
-            s_col[ct / 3][ct % 3] = sum;
-          }
-          named_sync(kBarCons, NC * 32);
-          if (ct == 0) {
-            for (int b = 0; b < B; ++b) s_rs[b] = 1.f / sqrtf(s_col[b][0] / (float)a.d + a.eps);
-            if (D.dec_layer > 0 && sk == 3) {
-              // exit decision of layer dec_layer: batch minimum of the cosine
-              // between the residual entering and leaving it
-              float m = FLT_MAX;
-              for (int b = 0; b < B; ++b)
-                m = fminf(m, s_col[b][1] / fmaxf(sqrtf(s_col[b][2]) * sqrtf(s_col[b][0]), 1e-12f));
-              int e = s_e;
-              if (a.mode == RL_EXIT_TAU && e == a.L && D.dec_layer < a.L && m > a.tau) e = D.dec_layer;
-              s_e = e;
-              if (cta == 0) {
-                if (a.min_cos_out) a.min_cos_out[D.dec_layer - 1] = m;
-                a.st->exit_layer = e;
-              }
-              __threadfence_block();
-              s_dec = D.dec_layer;
+          for (int w = 0; w < NC; ++w) sum += s_stw[w][b * 3 + j];
+          return sum;
+        };
+        auto col_rs = [&](int b) { return 1.f / sqrtf(col_sum(b, 0) / (float)a.d + a.eps); };
+        // (3) thread 0: RMSNorm scales and the exit decision of layer dec_layer
+        // (batch minimum of the cosine between the residual entering and leaving it)
+        auto stats_decide = [&]() {
+          for (int b = 0; b < B; ++b) s_rs[b] = col_rs(b);
+          if (D.dec_layer > 0 && sk == 3) {
+            float m = FLT_MAX;
+            for (int b = 0; b < B; ++b)
+              m = fminf(m, col_sum(b, 1) / fmaxf(sqrtf(col_sum(b, 2)) * sqrtf(col_sum(b, 0)), 1e-12f));
+            int e = s_e;
+            if (a.mode == RL_EXIT_TAU && e == a.L && D.dec_layer < a.L && m > a.tau) e = D.dec_layer;
+            s_e = e;
+            if (cta == 0) {
+              if (a.min_cos_out) a.min_cos_out[D.dec_layer - 1] = m;
+              a.st->exit_layer = e;
             }
-            tl2_mark(a.tl2, grid, p, cta, TL2_RED);
+            __threadfence_block();
+            s_dec = D.dec_layer;
           }
-          named_sync(kBarCons, NC * 32);
+          tl2_mark(a.tl2, grid, p, cta, TL2_RED);
         };
         bool stats_pending = scaled;
         if (D.xmode == X_EMBED) {
@@ -629,7 +629,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           }
           named_sync(kBarCons, NC * 32);
         } else if (scaled && (!regs || (a.mode == RL_EXIT_TAU && s_e == a.L && D.dec_layer > 0 && D.dec_layer < a.L && sk == 3))) {
-          reduce_stats();
+          stats_partials();
+          named_sync(kBarCons, NC * 32);
+          if (ct == 0) stats_decide();
+          named_sync(kBarCons, NC * 32);
           stats_pending = false;
         }
         const bool w4 = D.qwt && D.layer_no > 0 && D.layer_no > s_e;
@@ -741,11 +744,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
 
         // epilogue of a batch of nb tiles starting at tile t_first (all consumer threads)
         auto flush = [&](int nb, int t_first, bool first_batch) {
-          if (stats_pending) {
-            reduce_stats();
-            stats_pending = false;
-          }
+          // deferred statistics: warp partials, then (after the batch barrier)
+          // every epilogue thread sums its own column's scale; thread 0 decides
+          const bool fresh = stats_pending;
+          if (fresh) stats_partials();
           named_sync(kBarCons, NC * 32);
+          if (fresh) {
+            stats_pending = false;
+            if (ct == 0) stats_decide();
+          }
+          const float rsv = scaled ? col_rs(my_c) : s_rs[my_c];
           const int nout = nb * 16 * B;
           const int rounds = (nout + R - 1) / R;
           for (int rd = 0; rd < rounds; ++rd) {
@@ -797,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               // rows r < 8 of a tile are gate rows, r + 8 the matching up rows
               const float up = __shfl_down_sync(0xffffffffu, v, 8);
               if (act && my_r < 8) {
-                const float rs = s_rs[my_c];
+                const float rs = rsv;
                 D.out_h[(size_t)my_c * D.ldoh + tl * 8 + my_r] = __float2bfloat16_rn(silu_f(v * rs) * (up * rs));
               }
             } else if (D.epi == EPI_QKV_ROPE) {
@@ -807,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 const int hd = a.hd, half = hd >> 1;
                 const int row0 = tl * 16;
                 const int head_all = row0 / hd;
-                const float rs = s_rs[my_c];
+                const float rs = rsv;
                 const int pos = s_pos;
                 const int dim = 8 * ((row0 % hd) >> 4) + my_r;
                 float lo = v * rs, hi = hv * rs;
@@ -835,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             } else if (D.epi == EPI_LMHEAD) {
               if (act) {
                 const int n = tl * 16 + my_r;
-                const float val = v * s_rs[my_c];
+                const float val = v * rsv;
                 D.out[(size_t)my_c * D.ldo + n] = val;
                 if (val > amv || (val == amv && n < ami)) {
                   amv = val;
@@ -843,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 }
               }
             } else {  // EPI_STORE
-              if (act) D.out[(size_t)my_c * D.ldo + tl * 16 + my_r] = v * s_rs[my_c];
+              if (act) D.out[(size_t)my_c * D.ldo + tl * 16 + my_r] = v * rsv;
             }
           }
           named_sync(kBarCons, NC * 32);
@@ -931,7 +939,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             nb = 0;
           }
         }
-        if (stats_pending) reduce_stats();  // a CTA without tiles still takes the decision
+        if (stats_pending) {  // a CTA without tiles still takes the decision
+          stats_partials();
+          named_sync(kBarCons, NC * 32);
+          if (ct == 0) stats_decide();
+        }
         if (D.epi == EPI_LMHEAD) {
           // this CTA's argmax per column: 16-lane groups, then one thread per column
 #pragma unroll
