@@ -928,9 +928,7 @@ std::vector<PhaseDesc> build_step_phases(rl_model* m, rl_kv* kv, const StepIO& i
       p.vc = kv->V[l];
       p.o_out = kv->o;
       p.ldo_attn = m->Ko;
-      ph.push_back(p);
-      p.kind = PH_MERGE;  // the chunks' partials merged, spread over all CTAs
-      ph.push_back(p);
+      ph.push_back(p);  // the last CTA of each (sequence, KV head) merges its chunks
     }
     {  // O + residual; x' and |h_mid|^2 partials for the FFN norm
       PhaseDesc p = gemv(ly.o, l + 1);
@@ -1755,8 +1753,6 @@ rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32_t* kin
       if (d.kind == PH_ATTN) {
         kind = RL_K_ATTN;
         b = 2.0 * kv->prof_B * m->Hkv * (double)(kv->prof_pos + 1) * m->hd * 2.0;
-      } else if (d.kind == PH_MERGE) {
-        kind = RL_K_ATTN;
       } else {
         if (d.layer_no > 0)
           kind = d.epi == EPI_QKV_ROPE ? RL_K_QKV

@@ -1,6 +1,6 @@
 // Persistent decode step for small batches (B <= 8): ONE cooperative kernel
 // per decode step runs every phase -- for each layer QKV (+ exit decision,
-// RoPE, KV append), attention, merge, O (+ residual), gate/up (+ SwiGLU), down
+// RoPE, KV append), attention (the last CTA of each KV head merges its chunks), O (+ residual), gate/up (+ SwiGLU), down
 // (+ residual, next RMSNorm input, cosine partials); then the LM head (+
 // greedy argmax).  River-LLM explainer, section 四: the batch-minimum cosine of
 // a layer's input and output residual decides, once, that the remaining
@@ -271,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
   __shared__ volatile int s_e;    // exit layer as far as this CTA knows it
   __shared__ volatile int s_dec;  // last layer whose exit decision this CTA has taken
   __shared__ volatile int s_abort;
-  __shared__ int s_pos, s_last;
-  __shared__ __align__(16) float s_mrg[1024];  // attention merge scratch; LM-head argmax scratch
+  __shared__ int s_pos, s_last, s_merge;
+  __shared__ __align__(16) float s_mrg[4 * NC];  // LM-head argmax scratch: per half warp (value, index)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -1070,6 +1070,79 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               mbar_arrive(&empty[slot]);
               if (two) mbar_arrive(&empty[slot_v]);
             }
+            // ---- the last CTA to finish a chunk of (b, hk) merges its chunks ----
+            // (release: this CTA's partial writes, ordered by the barrier above,
+            // before the ticket; acquire: every other chunk's partial after it)
+            if (ct == 0) {
+              const unsigned tk = atom_add_acq_rel(a.attn_ticket + b * Hkv + hk, 1u);
+              s_merge = tk == (unsigned)(nch - 1);
+            }
+            named_sync(kBarCons, NC * 32);
+            if (s_merge) {
+              // per head: chunk weights exp(m_c - M) / sum_c exp(m_c - M) l_c, staged
+              // as [h][c][2] in the (idle) partial-tile buffer; then o = sum_c w_c o_c
+              float* mw = redf;
+              const float* hp = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * (HDC + 2);
+              for (int i = ct; i < REP * nch; i += NC * 32) {
+                const int h = i / nch, c = i % nch;
+                const float* pc = hp + ((size_t)h * a.part_cap + c) * (HDC + 2);
+                mw[2 * i] = __ldcg(pc + HDC);
+                mw[2 * i + 1] = __ldcg(pc + HDC + 1);
+              }
+              named_sync(kBarCons, NC * 32);
+              if (warp < REP) {
+                float* mh = mw + (size_t)warp * nch * 2;
+                float M = -FLT_MAX;
+                for (int c = lane; c < nch; c += 32)
+                  if (mh[2 * c + 1] > 0.f) M = fmaxf(M, mh[2 * c]);
+                M = warp_max(M);
+                float den = 0.f;
+                for (int c = lane; c < nch; c += 32)
+                  if (mh[2 * c + 1] > 0.f) den += __expf(mh[2 * c] - M) * mh[2 * c + 1];
+                den = warp_sum(den);
+                const float inv = den > 0.f ? 1.f / den : 0.f;
+                __syncwarp();
+                for (int c = lane; c < nch; c += 32)
+                  mh[2 * c] = mh[2 * c + 1] > 0.f ? __expf(mh[2 * c] - M) * inv : 0.f;
+              }
+              named_sync(kBarCons, NC * 32);
+              // o = sum_c w_c o_c: each thread owns outputs ct and ct + 256 (REP * hd
+              // <= 512); the loads of 16 chunks are issued together
+              constexpr int NOUT = (REP * HDC + NC * 32 - 1) / (NC * 32);
+              float acc[NOUT];
+#pragma unroll
+              for (int k = 0; k < NOUT; ++k) acc[k] = 0.f;
+              for (int c0 = 0; c0 < nch; c0 += 16) {
+                float v[NOUT][16];
+#pragma unroll
+                for (int k = 0; k < NOUT; ++k) {
+                  const int i = ct + k * NC * 32;
+                  const int h = i / HDC, dd = i % HDC;
+                  const float* ph = hp + (size_t)h * a.part_cap * (HDC + 2) + dd;
+#pragma unroll
+                  for (int q = 0; q < 16; ++q)
+                    v[k][q] = (i < REP * HDC && c0 + q < nch) ? __ldcg(ph + (size_t)(c0 + q) * (HDC + 2)) : 0.f;
+                }
+#pragma unroll
+                for (int k = 0; k < NOUT; ++k) {
+                  const int i = ct + k * NC * 32;
+                  const float* wh = mw + (size_t)(i < REP * HDC ? i / HDC : 0) * nch * 2;
+#pragma unroll
+                  for (int q = 0; q < 16; ++q)
+                    if (c0 + q < nch) acc[k] += wh[2 * (c0 + q)] * v[k][q];
+                }
+              }
+#pragma unroll
+              for (int k = 0; k < NOUT; ++k) {
+                const int i = ct + k * NC * 32;
+                if (i < REP * HDC) {
+                  const int h = i / HDC, dd = i % HDC;
+                  D.o_out[(size_t)b * D.ldo_attn + (size_t)(hk * REP + h) * HDC + dd] = __float2bfloat16_rn(acc[k]);
+                }
+              }
+              if (ct == 0) a.attn_ticket[b * Hkv + hk] = 0u;  // next step starts from zero
+              named_sync(kBarCons, NC * 32);
+            }
           }
         };
         using I1 = std::integral_constant<int, 1>;
@@ -1082,70 +1155,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           case 1 * 8 + 4: run(I1{}, I4{}); break;
           case 2 * 8 + 4: run(I2{}, I4{}); break;
           default: run(I4{}, I4{}); break;
-        }
-      } else {
-        // ---- merge of the attention chunks, spread over all CTAs ------------------------
-        // item = (sequence, query head, slice of head dims); threads split the chunks
-        const int pos = s_pos, hd = a.hd, Hkv = a.Hkv, Hq = a.Hq;
-        const int ctx = min(pos + 1, a.Tmax);
-        const int nch = step_attn_chunks(ctx, B, Hkv, hd, grid, a.part_cap);
-        const int nheads = B * Hq;
-        const int spl = max(1, min(hd / 8, grid / nheads));  // slices per head
-        const int sl = (hd + spl - 1) / spl;                    // outputs per slice
-        const int S = (NC * 32) / sl;                           // threads per output
-        float* ml = s_mrg;                                       // [nch][2]
-        float* wc = ml + 2 * 256;                                // [nch]
-        float* rd = wc + 256;                                    // [NC * 32]
-        for (int item = cta; item < nheads * spl; item += grid) {
-          const int gh = item / spl, sc0 = (item % spl) * sl;
-          const float* hp = a.part + (size_t)gh * a.part_cap * (hd + 2);
-          const int k = ct / S, sidx = ct % S;
-          const int dd = sc0 + k;
-          const bool act = k < sl && dd < hd;
-          float v[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int c = sidx + q * S;
-            v[q] = (act && c < nch) ? __ldcg(hp + (size_t)c * (hd + 2) + dd) : 0.f;
-          }
-          for (int c = ct; c < nch; c += NC * 32) {
-            ml[2 * c] = __ldcg(hp + (size_t)c * (hd + 2) + hd);
-            ml[2 * c + 1] = __ldcg(hp + (size_t)c * (hd + 2) + hd + 1);
-          }
-          named_sync(kBarCons, NC * 32);
-          if (warp == 0) {
-            float M = -FLT_MAX;
-            for (int c = lane; c < nch; c += 32)
-              if (ml[2 * c + 1] > 0.f) M = fmaxf(M, ml[2 * c]);
-            M = warp_max(M);
-            float den = 0.f;
-            for (int c = lane; c < nch; c += 32) {
-              const float w = ml[2 * c + 1] > 0.f ? __expf(ml[2 * c] - M) : 0.f;
-              wc[c] = w;
-              den += w * ml[2 * c + 1];
-            }
-            den = warp_sum(den);
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-            __syncwarp();
-            for (int c = lane; c < nch; c += 32) wc[c] *= inv;
-          }
-          named_sync(kBarCons, NC * 32);
-          float acc = 0.f;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int c = sidx + q * S;
-            if (act && c < nch) acc += wc[c] * v[q];
-          }
-          for (int c = sidx + 8 * S; act && c < nch; c += S) acc += wc[c] * __ldcg(hp + (size_t)c * (hd + 2) + dd);
-          rd[ct] = acc;
-          named_sync(kBarCons, NC * 32);
-          if (act && sidx == 0) {
-            float sum = 0.f;
-            for (int q = 0; q < S; ++q) sum += rd[k * S + q];
-            const int bq = gh / Hq, hq = gh % Hq;
-            D.o_out[(size_t)bq * D.ldo_attn + (size_t)hq * hd + dd] = __float2bfloat16_rn(sum);
-          }
-          named_sync(kBarCons, NC * 32);
         }
       }
       // ---- end of phase: this CTA's writes are done; arrive ----

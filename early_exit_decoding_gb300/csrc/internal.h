@@ -225,10 +225,10 @@ void launch_quantize(const bf16* w, int N, int K, int Kp, uint32_t* qw, __half2*
 // weight stream of a CTA runs ahead across phase boundaries: it depends only
 // on the weight path, never on this step's activations.
 // ---------------------------------------------------------------------------
-enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1, PH_MERGE = 2 };
+enum PhaseKind { PH_GEMV = 0, PH_ATTN = 1 };
 
 struct PhaseDesc {
-  int kind;                   // PH_GEMV / PH_ATTN / PH_MERGE
+  int kind;                   // PH_GEMV / PH_ATTN
   int layer_no;               // 1..L; 0 = LM head (always the bf16 weights)
   // GEMV weights
   const bf16* wt;             // bf16 unit-tiled (see k_bf16_tile_layout)
