@@ -319,3 +319,69 @@ def test_host_buffer_entry_point(river, tiny, stream):
                     res.append((o["logits"].cpu(), o["next_token"].cpu(), int(o["exit_layer"].item())))
     for a, b in zip(res[:2], res[2:]):
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and a[2] == b[2]
+
+
+@pytest.mark.parametrize("emb_scale", [2.0 ** 22, 2.0 ** -20])
+def test_w4_path_activations_outside_fp16_range(river, stream, emb_scale):
+    """The exit river's MMAs read the bf16 activations as fp16 after scaling
+    each row by a power of two: residual streams far above the fp16 range
+    (embedding x 2^22) or deep in its subnormals (x 2^-20) must give the
+    oracle's logits and each layer's contribution to the residual."""
+    from oracle.model import OracleModel
+    from tests.harness import to_cuda, cos_rows
+    S = synth.scaled(TINY, n_layers=2)
+    w = synth.gen_weights(S, seed=11, device="cpu", gains="random")
+    w["embed"] = (w["embed"].float() * emb_scale).to(torch.bfloat16)  # exact: power of two
+    m = river.Model(S, to_cuda(w), stream)
+    m.quantize_exit_layers(stream)
+    om = OracleModel(S, synth.weights_to_numpy(w))
+    om.quantize_exit_layers()
+    toks = synth.gen_tokens(S.vocab, (1, 10), seed=12)
+    kv = m.kv_cache_alloc(1, 32)
+    kv.set_decode_path(PATHS["step"])
+    st = KVState(S, 1, 32)
+    tr = torch.zeros((S.n_layers + 1, 1, S.d_model), dtype=torch.float32, device="cuda")
+    kv.set_trace(tr)
+    sched = torch.tensor([0], dtype=torch.int32, device="cuda")  # every layer on the exit river
+    with torch.cuda.stream(stream):
+        river.prefill(m, kv, torch.from_numpy(toks[:, :9]).cuda(), river.Policy.forced(sched),
+                      stream=stream)
+        om.prefill(toks[:, :9], st, OPolicy.forced(0))
+        out = river.decode_step(m, kv, torch.from_numpy(toks[:, 9].copy()).cuda(),
+                                river.Policy.forced(sched), stream=stream)
+        kv.sync(stream)
+    ref = om.decode_step(toks[:, 9], st, OPolicy.forced(0))
+    kv.set_trace(None)
+    logits = out["logits"].cpu().numpy()
+    assert np.isfinite(logits).all()
+    assert np.abs(logits - ref.logits).max() <= 5e-2
+    h = tr.cpu().numpy().astype(np.float64)
+    for l in range(S.n_layers):
+        c = cos_rows(h[l + 1] - h[l], ref.hidden[l + 1] - ref.hidden[l])
+        assert c.min() >= 0.99, (l, c)
+
+
+def test_step_timeline_orders_every_phase(river, tiny, stream):
+    """Per-CTA timeline of the persistent step kernel (profiling level 2): no
+    CTA starts phase p + 1 before every CTA has arrived at the end of phase p
+    (the grid barrier), and each CTA's stamps of a phase are in order."""
+    m, om, _ = tiny
+    S = TINY
+    kv = m.kv_cache_alloc(1, 64)
+    kv.set_decode_path(PATHS["step"])
+    toks = torch.from_numpy(synth.gen_tokens(S.vocab, (1, 10), seed=13)).cuda()
+    with torch.cuda.stream(stream):
+        river.prefill(m, kv, toks[:, :8].contiguous(), river.Policy.tau_(1.01), stream=stream)
+        river.rl_kv_set_profiling(kv.handle, 2)
+        river.decode_step(m, kv, toks[:, 8].contiguous(), river.Policy.tau_(0.5), stream=stream)
+        river.rl_kv_profile(kv.handle, stream)
+        tl = river.rl_kv_timeline(kv.handle, stream).astype(np.int64)
+        river.rl_kv_set_profiling(kv.handle, 0)
+        kv.sync(stream)
+    nph, grid, nst = tl.shape
+    assert nph == 5 * S.n_layers + 1 and nst == 8
+    BAR, ARRIVE = 0, 4
+    assert (tl[:, :, BAR] > 0).all() and (tl[:, :, ARRIVE] > 0).all()
+    assert (tl[:, :, ARRIVE] >= tl[:, :, BAR]).all()
+    for p in range(nph - 1):
+        assert tl[p + 1, :, BAR].min() >= tl[p, :, ARRIVE].max(), p
