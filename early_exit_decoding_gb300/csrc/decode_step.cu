@@ -216,7 +216,8 @@ __device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigne
 // pattern of the subnormal fp16 q * 2^-24 (fields at bits 4..7 read
 // 16 q * 2^-24): one AND per operand register, exact products in the MMA.  The
 // activations are fp16, scaled and reordered per 8-input chunk as (x0,x4),
-// (x2,x6), (x1,x5), (x3,x7); xsum holds the groups' input sums.
+// (x2,x6), (x1,x5), (x3,x7), each group scaled by 2^k; xsum holds per
+// (row, group) the input sum and 2^-k.
 __device__ __forceinline__ void w4_unit(const unsigned char* st, int gi, const unsigned char* xrow,
                                         const float* xsum, int B, int G, int warp, int g, int t,
                                         float (&y)[4]) {
@@ -242,18 +243,19 @@ __device__ __forceinline__ void w4_unit(const unsigned char* st, int gi, const u
   *reinterpret_cast<uint32_t*>(&h0) = s0;
   *reinterpret_cast<uint32_t*>(&h1) = s1;
   const float2 sz0 = __half22float2(h0), sz1 = __half22float2(h1);
-  const float xs0 = 2 * t < B ? xsum[(2 * t) * G + gi] : 0.f;
-  const float xs1 = 2 * t + 1 < B ? xsum[(2 * t + 1) * G + gi] : 0.f;
-  // sum_k (q_k - z) s x_k = s 2^24 (c1 + c2 / 16) - s z sum_k x_k
+  const float2* xs2 = reinterpret_cast<const float2*>(xsum);
+  const float2 xa = 2 * t < B ? xs2[(2 * t) * G + gi] : make_float2(0.f, 0.f);
+  const float2 xb = 2 * t + 1 < B ? xs2[(2 * t + 1) * G + gi] : make_float2(0.f, 0.f);
+  // sum_k (q_k - z) s x_k = s 2^24 2^-k (c1 + c2 / 16) - s z sum_k x_k
   const float p0 = sz0.x * 16777216.f, p1 = sz1.x * 16777216.f;
   const float q0 = sz0.x * sz0.y, q1 = sz1.x * sz1.y;
   float av[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) av[c] = (c1[0][c] + c1[1][c]) + 0.0625f * (c2[0][c] + c2[1][c]);
-  y[0] = fmaf(p0, av[0], fmaf(-q0, xs0, y[0]));
-  y[1] = fmaf(p0, av[1], fmaf(-q0, xs1, y[1]));
-  y[2] = fmaf(p1, av[2], fmaf(-q1, xs0, y[2]));
-  y[3] = fmaf(p1, av[3], fmaf(-q1, xs1, y[3]));
+  y[0] = fmaf(p0 * xa.y, av[0], fmaf(-q0, xa.x, y[0]));
+  y[1] = fmaf(p0 * xb.y, av[1], fmaf(-q0, xb.x, y[1]));
+  y[2] = fmaf(p1 * xa.y, av[2], fmaf(-q1, xa.x, y[2]));
+  y[3] = fmaf(p1 * xb.y, av[3], fmaf(-q1, xb.x, y[3]));
 }
 
 }  // namespace
@@ -265,8 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
   __shared__ float s_col[8][3];              // per column: the phase's reduced statistics
   __shared__ float s_stw[NC][24];            // per warp partial statistics
   __shared__ float s_rs[8];
-  __shared__ float s_xsc[8];        // W4 phases: 2^-k undoing the activation rows' scale
-  __shared__ float s_xmax[NC][8];   // per warp max |x| of each row
   __shared__ float s_freq[64];
   __shared__ volatile int s_e;    // exit layer as far as this CTA knows it
   __shared__ volatile int s_dec;  // last layer whose exit decision this CTA has taken
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
   unsigned char* xs = smem + (size_t)NS * SLOT_B;
   float* xsum = reinterpret_cast<float*>(xs + (size_t)B * RSX);
   float4* red = reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(xsum) +
-                                          ((((size_t)B * a.gmax * 4) + 15) & ~(size_t)15));
+                                          ((((size_t)B * a.gmax * 8) + 15) & ~(size_t)15));
   float* redf = reinterpret_cast<float*>(red);
 
   if (tid == 0) {
@@ -661,66 +661,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         }
         if (ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
         if (w4) {
-          // The W4 MMAs run in fp16: every activation row is scaled by a power
-          // of two 2^k that brings its largest |x| just below 2^15 (exact, and
-          // bf16 values in the fp16 normal range convert exactly), converted to
-          // fp16 in place, and each 8-input chunk is reordered as (x0,x4),
-          // (x2,x6), (x1,x5), (x3,x7) to match the nibble fields the MMA reads;
-          // xsum[b][group] = sum of the group's scaled inputs (zero-point term).
+          // The W4 MMAs run in fp16.  Each 128-input group of every activation
+          // row is scaled by its own power of two 2^k (largest |x| of the group
+          // just below 2^15: exact, and bf16 values in the fp16 normal range
+          // convert exactly), converted to fp16 in place and reordered per
+          // 8-input chunk as (x0,x4), (x2,x6), (x1,x5), (x3,x7) to match the
+          // nibble fields the MMA reads; xsum[b][group] = (sum of the group's
+          // inputs, 2^-k).  The 16 chunks of a group sit in 16 consecutive
+          // lanes: group max and sum take four shuffles each, no block barrier.
           const int nchk = Kp >> 3;
-          float mx[kFusedMaxB];
-#pragma unroll
-          for (int b = 0; b < kFusedMaxB; ++b) mx[b] = 0.f;
-          for (int ch = ct; ch < nchk; ch += NC * 32) {
-#pragma unroll
-            for (int b = 0; b < kFusedMaxB; ++b)
-              if (b < B) {
-                const uint4 v = *reinterpret_cast<const uint4*>(xs + (size_t)b * RSX + ch * 16);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-                  mx[b] = fmaxf(mx[b], fmaxf(fabsf(f.x), fabsf(f.y)));
-                }
-              }
-          }
-#pragma unroll
-          for (int b = 0; b < kFusedMaxB; ++b)
-            if (b < B) {
-              const float v = warp_max(mx[b]);
-              if (lane == 0) s_xmax[warp][b] = v;
-            }
-          named_sync(kBarCons, NC * 32);
-          if (ct < B) {
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < NC; ++w) v = fmaxf(v, s_xmax[w][ct]);
-            int e = 0;
-            if (v > 0.f) frexpf(v, &e);  // v < 2^e
-            const int k = min(max(15 - e, -120), 120);
-            s_xmax[0][ct] = ldexpf(1.f, k);
-            s_xsc[ct] = ldexpf(1.f, -k);
-          }
-          named_sync(kBarCons, NC * 32);
-          // each thread converts whole 8-input chunks; the 16 chunks of a group
-          // sit in 16 consecutive lanes, whose sum gives the group's term
+          float2* xs2 = reinterpret_cast<float2*>(xsum);
           for (int c0 = 0; c0 < nchk; c0 += NC * 32) {
             const int ch = c0 + ct;
             const bool on = ch < nchk;  // nchk is a multiple of 16: groups are all on or all off
             for (int b = 0; b < B; ++b) {
-              float sum = 0.f;
+              uint4* cp = reinterpret_cast<uint4*>(xs + (size_t)b * RSX + (on ? ch : 0) * 16);
+              float f[8];
+              float mx = 0.f;
               if (on) {
-                const float sc = s_xmax[0][b];
-                uint4* cp = reinterpret_cast<uint4*>(xs + (size_t)b * RSX + ch * 16);
                 const uint4 v = *cp;
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                float f[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                   const float2 ff = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-                  f[2 * i] = ff.x * sc;
-                  f[2 * i + 1] = ff.y * sc;
+                  f[2 * i] = ff.x;
+                  f[2 * i + 1] = ff.y;
+                  mx = fmaxf(mx, fmaxf(fabsf(ff.x), fabsf(ff.y)));
                 }
+              }
+#pragma unroll
+              for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+              int e = 0;
+              if (mx > 0.f) frexpf(mx, &e);  // mx < 2^e
+              const int k = min(max(15 - e, -120), 120);
+              const float sc = ldexpf(1.f, k);
+              float sum = 0.f;
+              if (on) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] *= sc;
                 sum = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
                 const __half2 p0 = __floats2half2_rn(f[0], f[4]), p1 = __floats2half2_rn(f[2], f[6]);
                 const __half2 p2 = __floats2half2_rn(f[1], f[5]), p3 = __floats2half2_rn(f[3], f[7]);
@@ -729,13 +707,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               }
 #pragma unroll
               for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-              if (on && (ct & 15) == 0) xsum[b * G + (ch >> 4)] = sum;
+              const float inv = ldexpf(1.f, -k);
+              if (on && (ct & 15) == 0) xs2[b * G + (ch >> 4)] = make_float2(sum * inv, inv);
             }
           }
           fence_proxy_async_smem();  // a later phase's bulk copy rewrites these bytes
           named_sync(kBarCons, NC * 32);
-        } else if (ct < 8) {
-          s_xsc[ct] = 1.f;
         }
         // MMA column g reads activation row min(g, B-1); columns >= B are dropped
         const unsigned char* xrow = xs + (size_t)(g < B ? g : B - 1) * RSX;
@@ -765,7 +742,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             if (act) {
 #pragma unroll
               for (int w = 0; w < NC; ++w) v += redf[((tb * NC + w) * B + my_c) * 16 + my_r];
-              v *= s_xsc[my_c];
             }
             if (D.epi == EPI_RESID) {
               float s0 = 0.f, s1 = 0.f, s2 = 0.f;
@@ -1221,7 +1197,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
 
 size_t step_smem_bytes(int B, int kmax, int gmax, int* nslot) {
   const size_t xs = (size_t)B * (kmax * 2 + 64);
-  const size_t xsum = (((size_t)B * gmax * 4) + 15) & ~(size_t)15;
+  const size_t xsum = (((size_t)B * gmax * 8) + 15) & ~(size_t)15;
   const size_t red = (size_t)2 * NC * 32 * 16;
   const size_t budget = 227 * 1024 - kStaticSmem;
   const size_t fixed = xs + xsum + red;
