@@ -141,7 +141,9 @@ struct ProfRec {
 struct rl_kv {
   rl_model* m = nullptr;
   int maxB = 0, Tmax = 0;
-  std::vector<bf16*> K, V;
+  std::vector<bf16*> K, V;     // per-layer views into one allocation each
+  CUtensorMap tmk, tmv;        // all layers' K / V as one 2-D tensor [L*maxB*Hkv*Tmax][hd] (step kernel)
+  bool tm_ok = false;
   DevState* st = nullptr;
   int host_pos = 0, host_step = 0;
   // decode workspace
@@ -851,7 +853,8 @@ bool step_fits_model(const rl_model* m, int B) {
 }
 
 bool step_fits(const rl_model* m, const rl_kv* kv, int B) {
-  if (!m->step_ok || !kv->part_s || B < 1 || B > kFusedMaxB || B > kv->maxB || m->d % 16) return false;
+  if (!m->step_ok || !kv->tm_ok || !kv->part_s || B < 1 || B > kFusedMaxB || B > kv->maxB || m->d % 16)
+    return false;
   const int rep = m->Hq / m->Hkv;
   if ((rep != 1 && rep != 2 && rep != 4) || (m->hd != 64 && m->hd != 128)) return false;
   if (6 * m->L + 1 > kv->nph_cap) return false;
@@ -1058,6 +1061,9 @@ rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStre
   a.part = kv->part_s;
   a.attn_ticket = kv->attn_ticket;
   a.part_cap = kv->part_cap;
+  a.tmk = kv->tmk;
+  a.tmv = kv->tmv;
+  a.kv_rows_layer = kv->maxB * m->Hkv * kv->Tmax;
   a.xs_row_bytes = step_kmax(m) * 2 + 64;
   a.gmax = step_kmax(m) / kGroup;
   const size_t smem = step_smem_bytes(B, step_kmax(m), a.gmax, &a.nslot);
@@ -1365,9 +1371,19 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
   const size_t per_layer = (size_t)max_batch * m->Hkv * max_seq * m->hd;
   kv->K.resize(m->L);
   kv->V.resize(m->L);
-  for (int l = 0; l < m->L; ++l) {
-    K_TRY(kv->alloc(&kv->K[l], per_layer));
-    K_TRY(kv->alloc(&kv->V[l], per_layer));
+  {
+    bf16 *k_all = nullptr, *v_all = nullptr;
+    K_TRY(kv->alloc(&k_all, per_layer * m->L));
+    K_TRY(kv->alloc(&v_all, per_layer * m->L));
+    for (int l = 0; l < m->L; ++l) {
+      kv->K[l] = k_all + per_layer * l;
+      kv->V[l] = v_all + per_layer * l;
+    }
+    // the step kernel's attention reads K / V chunks by TMA: 16-row x 64-dim boxes
+    const long long rows = (long long)m->L * max_batch * m->Hkv * max_seq;
+    kv->tm_ok = rows < (1ll << 31) && (m->hd == 64 || m->hd == 128) &&
+                make_tmap_bf16(&kv->tmk, k_all, m->hd, (int)rows, m->hd, 16) &&
+                make_tmap_bf16(&kv->tmv, v_all, m->hd, (int)rows, m->hd, 16);
   }
   K_TRY(kv->alloc(&kv->st, 1));
   const int B = max_batch;

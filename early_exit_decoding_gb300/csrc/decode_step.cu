@@ -82,131 +82,121 @@ __device__ __forceinline__ void tl2_mark(unsigned long long* tl2, int grid, int 
   tl2[((size_t)p * grid + cta) * kTl2 + k] = t;
 }
 
-// Sum 32 values over the 32 lanes of a warp, leaving the total of value i
-// in lane i (31 shuffles: each step halves the values a lane carries).
-__device__ __forceinline__ float butterfly32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
-    const bool upper = (lane & s) != 0;
-#pragma unroll
-    for (int i = 0; i < s; ++i) {
-      const float send = upper ? v[i] : v[i + s];
-      const float keep = upper ? v[i + s] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-    }
-  }
-  return v[0];
+// Byte offset of 16-byte chunk c of K/V row r in an attention chunk staged by
+// TMA with the 128-byte swizzle: 64-dim halves of 128 rows x 128 bytes at
+// 16 KB apart, chunk c & 7 of a row stored at (c & 7) ^ (r & 7).
+__device__ __forceinline__ uint32_t kv_off(int r, int c) {
+  return (uint32_t)((c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// One warp's share of an attention chunk: positions j0 .. j0 + jn - 1 (jn <= 16)
-// against the REP query heads of one KV head.  Lane l holds dims [DPL*l,
-// DPL*(l+1)) of q (pre-scaled by 1/sqrt(hd), in qr) and of each K / V row.
-// Scores come 32 at a time from the butterfly (P positions x REP heads,
-// output i in lane i); the warp keeps its own running max / sum per head and
-// its P V partial.  After a barrier of the consumer warps (every warp is done
-// reading K and V) writes, per head, (max, sum, o[hd]) to w0, which may
-// overlay the chunk's K / V rows.
-template <int REP, int DPL>
-__device__ __forceinline__ void attn_warp(const unsigned char* Ks, const unsigned char* Vs, int j0, int jn,
-                                          const float (&qr)[REP][DPL], int lane, float* w0) {
-  constexpr int HD = 32 * DPL, RK = HD * 2, P = 32 / REP, NB = (16 + P - 1) / P, WS = 2 + HD;
-  float sc[NB];
-  float mloc = -FLT_MAX;
+// A operand of m16n8k16 for one 16-dim k-step of q (rows = the REP query
+// heads; rows >= REP zero) from q staged in shared memory (fp32 [REP][HDC],
+// scaled by 1/sqrt(hd)), split into bf16 hi + lo parts: a[0..1] = a0 hi / lo,
+// a[2..3] = a2 hi / lo.
+template <int REP, int HDC>
+__device__ __forceinline__ void q_frag(const float* qs, int ks, int g, int t, uint32_t (&a)[4]) {
+  float2 lo = make_float2(0.f, 0.f), hi = lo;
+  if (g < REP) {
+    lo = *reinterpret_cast<const float2*>(qs + g * HDC + ks * 16 + 2 * t);
+    hi = *reinterpret_cast<const float2*>(qs + g * HDC + ks * 16 + 8 + 2 * t);
+  }
+  split_bf16x2(lo.x, lo.y, a[0], a[1]);
+  split_bf16x2(hi.x, hi.y, a[2], a[3]);
+}
+
+// One warp's share of an attention chunk on the tensor cores: positions
+// j0 .. j0 + jn - 1 (jn <= 16; two 8-position n-tiles) against the REP query
+// heads of one KV head.  S = q K^T and O = P V run as m16n8k16 MMAs (q and P
+// split into bf16 hi + lo: fp32-level accuracy; q from shared memory); K / V
+// fragments come from the
+// swizzled chunk by ldmatrix (V transposed), conflict free.  After S, a
+// barrier of the consumer warps (every warp is done reading K) frees the K
+// rows, which then hold the warps' partials: per head (max, sum, o[hd]) at w0,
+// o written 64 dims at a time.
+template <int REP, int HDC>
+__device__ __forceinline__ void attn_warp_tc(const unsigned char* Ks, const unsigned char* Vs, int j0, int jn,
+                                             const float* qs, int lane, float* w0) {
+  constexpr int WS = 2 + HDC;
+  const int g = lane >> 2, t = lane & 3;
+  const int mi = lane >> 3, ri = lane & 7;
+  float sacc[2][4];
 #pragma unroll
-  for (int bb = 0; bb < NB; ++bb) {
-    sc[bb] = -FLT_MAX;
-    if (bb * P >= jn) continue;  // uniform over the warp
-    float vals[32];
+  for (int n = 0; n < 2; ++n)
 #pragma unroll
-    for (int jj = 0; jj < P; ++jj) {
-      const int jw = bb * P + jj, j = j0 + jw;
-      float kf[DPL];
+    for (int i = 0; i < 4; ++i) sacc[n][i] = 0.f;
+  if (jn > 0) {  // uniform over the warp
+    // S: ldmatrix x4 = K rows j0 .. j0 + 15 x 16 dims -> b0 / b1 of both n-tiles
+    const uint32_t kb = smem_u32(Ks);
+    const int row = j0 + (mi >> 1) * 8 + ri;
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) kf[d] = 0.f;
-      if (jw < jn) {
-        if (DPL == 4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(Ks + j * RK + lane * 8);
-          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
-          const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
-          kf[0] = f0.x;
-          kf[1] = f0.y;
-          kf[DPL > 2 ? 2 : 0] = f1.x;
-          kf[DPL > 3 ? 3 : 0] = f1.y;
-        } else {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(Ks + j * RK + lane * 4);
-          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-          kf[0] = f0.x;
-          kf[1] = f0.y;
+    for (int ks = 0; ks < HDC / 16; ++ks) {
+      uint32_t kf[4], qa[4];
+      ldsm_x4(kf, kb + kv_off(row, ks * 2 + (mi & 1)));
+      q_frag<REP, HDC>(qs, ks, g, t, qa);
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        mma_bf16(sacc[n], qa[0], 0u, qa[2], 0u, kf[2 * n], kf[2 * n + 1]);
+        mma_bf16(sacc[n], qa[1], 0u, qa[3], 0u, kf[2 * n], kf[2 * n + 1]);
+      }
+    }
+  }
+  // row g's scores at positions 2t, 2t + 1 (n-tile 0) and 8 + 2t, 9 + 2t (n-tile 1)
+  const float sv[4] = {sacc[0][0], sacc[0][1], sacc[1][0], sacc[1][1]};
+  const int pidx[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+  float m = -FLT_MAX;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (pidx[i] < jn) m = fmaxf(m, sv[i]);
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+  float pv[4], l = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    pv[i] = pidx[i] < jn ? __expf(sv[i] - m) : 0.f;
+    l += pv[i];
+  }
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  uint32_t pa0h, pa0l, pa2h, pa2l;
+  split_bf16x2(pv[0], pv[1], pa0h, pa0l);
+  split_bf16x2(pv[2], pv[3], pa2h, pa2l);
+  dev::named_sync(1, 8 * 32);  // K is no longer read: the partials may overlay it
+  float* wr = w0 + g * WS;
+  if (g < REP && t == 0) {
+    wr[0] = m;
+    wr[1] = l;
+  }
+  // O = P V, 64 dims at a time: ldmatrix x4 trans = V rows j0 .. j0 + 15 x 16
+  // dims -> b0 / b1 of two 8-dim n-tiles
+  const uint32_t vb = smem_u32(Vs);
+  const int vrow = j0 + (mi & 1) * 8 + ri;
+#pragma unroll
+  for (int hh = 0; hh < HDC / 64; ++hh) {
+    float o[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[n][i] = 0.f;
+    if (jn > 0) {
+#pragma unroll
+      for (int nd = 0; nd < 8; nd += 2) {
+        uint32_t vf[4];
+        ldsm_x4_t(vf, vb + kv_off(vrow, hh * 8 + nd + (mi >> 1)));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mma_bf16(o[nd + h], pa0h, 0u, pa2h, 0u, vf[2 * h], vf[2 * h + 1]);
+          mma_bf16(o[nd + h], pa0l, 0u, pa2l, 0u, vf[2 * h], vf[2 * h + 1]);
         }
       }
-#pragma unroll
-      for (int h = 0; h < REP; ++h) {
-        float acc = 0.f;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) acc += qr[h][d] * kf[d];
-        vals[jj * REP + h] = acc;
-      }
     }
-    const float s = butterfly32(vals, lane);
-    const int jw = bb * P + lane / REP;
-    sc[bb] = jw < jn ? s : -FLT_MAX;
-    mloc = fmaxf(mloc, sc[bb]);
-  }
-  // lanes with the same head (lane % REP) share max and sum
+    if (g < REP) {
 #pragma unroll
-  for (int o = 16; o >= REP; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-  float pv[NB];
-  float lloc = 0.f;
-#pragma unroll
-  for (int bb = 0; bb < NB; ++bb) {
-    pv[bb] = sc[bb] > -FLT_MAX ? __expf(sc[bb] - mloc) : 0.f;
-    lloc += pv[bb];
-  }
-#pragma unroll
-  for (int o = 16; o >= REP; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
-  float o[REP][DPL];
-#pragma unroll
-  for (int h = 0; h < REP; ++h)
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) o[h][d] = 0.f;
-#pragma unroll
-  for (int bb = 0; bb < NB; ++bb) {
-#pragma unroll
-    for (int jj = 0; jj < P; ++jj) {
-      const int jw = bb * P + jj, j = j0 + jw;
-      if (!(jw < jn)) continue;  // uniform over the warp
-      float vf[DPL];
-      if (DPL == 4) {
-        const uint2 w = *reinterpret_cast<const uint2*>(Vs + j * RK + lane * 8);
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
-        vf[0] = f0.x;
-        vf[1] = f0.y;
-        vf[DPL > 2 ? 2 : 0] = f1.x;
-        vf[DPL > 3 ? 3 : 0] = f1.y;
-      } else {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + j * RK + lane * 4);
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-        vf[0] = f0.x;
-        vf[1] = f0.y;
-      }
-#pragma unroll
-      for (int h = 0; h < REP; ++h) {
-        const float pj = __shfl_sync(0xffffffffu, pv[bb], jj * REP + h);
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) o[h][d] += pj * vf[d];
+      for (int nd = 0; nd < 8; ++nd) {
+        wr[2 + hh * 64 + nd * 8 + 2 * t] = o[nd][0];
+        wr[2 + hh * 64 + nd * 8 + 2 * t + 1] = o[nd][1];
       }
     }
   }
-  dev::named_sync(1, 8 * 32);
-  if (lane < REP) {
-    w0[lane * WS] = mloc;
-    w0[lane * WS + 1] = lloc;
-  }
-#pragma unroll
-  for (int h = 0; h < REP; ++h)
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) w0[h * WS + 2 + DPL * lane + d] = o[h][d];
 }
 
 // One W4 unit of the step kernel's consumer warp: this warp's 128-input group
@@ -278,8 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
   const int g = lane >> 2, t = lane & 3;
   const int grid = gridDim.x, cta = blockIdx.x;
   const int B = a.B, NS = a.nslot, RSX = a.xs_row_bytes;
-  unsigned char* ring = smem;
-  unsigned char* xs = smem + (size_t)NS * SLOT_B;
+  // the ring starts on a 1024-byte boundary (128-byte-swizzled TMA destinations)
+  unsigned char* ring = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+  unsigned char* xs = ring + (size_t)NS * SLOT_B;
   float* xsum = reinterpret_cast<float*>(xs + (size_t)B * RSX);
   float4* red = reinterpret_cast<float4*>(reinterpret_cast<unsigned char*>(xsum) +
                                           ((((size_t)B * a.gmax * 8) + 15) & ~(size_t)15));
@@ -385,23 +376,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
           }
         } else if (D->kind == PH_ATTN) {
-          // attention: K and V rows below this step's position; a chunk of up
-          // to 128 positions takes one slot (head_dim 64: K, then V at 16 KB)
-          // or two (head_dim 128: K in the first, V in the second)
+          // attention: the chunk's K and V rows by TMA in 16-row boxes of 64
+          // dims (128-byte swizzle), every row a warp may read (ceil16 of the
+          // chunk); the row at this step's position is rewritten by the
+          // consumers once it has landed.  head_dim 64: K and V in one slot (V
+          // at 16 KB); head_dim 128: K in one slot, V in the next, each as two
+          // 64-dim halves 16 KB apart.
           const int pos = s_pos, hd = a.hd, Hkv = a.Hkv;
           const int ctx = min(pos + 1, a.Tmax);
           const int nch = step_attn_chunks(ctx, B, Hkv, hd, grid, a.part_cap);
           const int clen = (ctx + nch - 1) / nch;
           const int nitems = B * Hkv * nch;
           const bool two = hd * 2 * kCHP > kAttnHalf;
-          const bf16* kc = D->kc;
-          const bf16* vc = D->vc;
+          const int halves = hd / 64;
+          const int lrow0 = (D->layer_no - 1) * a.kv_rows_layer;
           for (int it = cta; it < nitems && !s_abort; it += grid) {
             const int b = it / (Hkv * nch), rr = it % (Hkv * nch), hk = rr / nch, ch = rr % nch;
             const int start = ch * clen, end = min(start + clen, ctx);
-            const int npre = min(kCHP, max(0, min(end, pos) - start));
-            const uint32_t bytes = (uint32_t)(npre * hd * 2);
-            const size_t off = (((size_t)b * Hkv + hk) * a.Tmax + start) * hd;
+            const int n = min(kCHP, max(0, end - start));
+            const int nbox = (n + 15) >> 4;
+            const int row0 = lrow0 + (b * Hkv + hk) * a.Tmax + start;
+            const uint32_t bytes = (uint32_t)(nbox * 2048 * halves);  // per tensor (K or V)
+            auto load = [&](const CUtensorMap* tm, unsigned char* dst, uint64_t* bar) {
+              for (int h = 0; h < halves; ++h)
+                for (int i = 0; i < nbox; ++i) tma_load_2d(dst + h * 16384 + i * 2048, tm, h * 64, row0 + 16 * i, bar);
+            };
             if (!take_slot()) break;
             const int sk = rp.slot;
             rp.next(NS);
@@ -409,19 +408,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             stamp_copy();
             if (!two) {
               mbar_expect_tx(&full[sk], 2 * bytes);
-              if (bytes) {
-                bulk_g2s(ring + (size_t)sk * SLOT_B, kc + off, bytes, &full[sk]);
-                bulk_g2s(ring + (size_t)sk * SLOT_B + kAttnHalf, vc + off, bytes, &full[sk]);
-              }
+              load(&a.tmk, ring + (size_t)sk * SLOT_B, &full[sk]);
+              load(&a.tmv, ring + (size_t)sk * SLOT_B + kAttnHalf, &full[sk]);
             } else {
               mbar_expect_tx(&full[sk], bytes);
-              if (bytes) bulk_g2s(ring + (size_t)sk * SLOT_B, kc + off, bytes, &full[sk]);
+              load(&a.tmk, ring + (size_t)sk * SLOT_B, &full[sk]);
               if (!take_slot()) break;
               const int sv = rp.slot;
               rp.next(NS);
               ++issued;
               mbar_expect_tx(&full[sv], bytes);
-              if (bytes) bulk_g2s(ring + (size_t)sv * SLOT_B, vc + off, bytes, &full[sv]);
+              load(&a.tmv, ring + (size_t)sv * SLOT_B, &full[sv]);
             }
           }
         }
@@ -958,21 +955,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         const int clen = (ctx + nch - 1) / nch;
         const int nitems = B * Hkv * nch;
         const bool two = hd * 2 * kCHP > kAttnHalf;
-        const int RK = hd * 2;  // K/V row bytes
         const float scale = rsqrtf((float)hd);
         const int WS = 2 + hd;
         if (clen > kCHP && cta == 0 && ct == 0) atomicOr(&a.st->err, RL_DEVERR_CAPACITY);
         auto run = [&](auto rep_c, auto dpl_c) {
           constexpr int REP = decltype(rep_c)::value, DPL = decltype(dpl_c)::value, HDC = 32 * DPL;
-          // q of an item: loaded (scaled) before its chunk is waited for
-          float qr[REP][DPL];
+          // q of an item, scaled by 1/sqrt(hd), staged in the (idle) activation
+          // buffer: loaded before the chunk is waited for
+          float* qs = reinterpret_cast<float*>(xs);
           auto load_q = [&](int it) {
             const int b = it / (Hkv * nch), hk = (it % (Hkv * nch)) / nch;
-            const float* qg = D.q_out + (size_t)b * Hq * HDC + (size_t)hk * REP * HDC;
-#pragma unroll
-            for (int h = 0; h < REP; ++h)
-#pragma unroll
-              for (int d = 0; d < DPL; ++d) qr[h][d] = __ldcg(qg + h * HDC + DPL * lane + d) * scale;
+            const float4* qg = reinterpret_cast<const float4*>(D.q_out + (size_t)b * Hq * HDC + (size_t)hk * REP * HDC);
+            for (int i = ct; i < REP * HDC / 4; i += NC * 32) {
+              float4 v = __ldcg(qg + i);
+              v.x *= scale;
+              v.y *= scale;
+              v.z *= scale;
+              v.w *= scale;
+              reinterpret_cast<float4*>(qs)[i] = v;
+            }
           };
           for (int it = cta; it < nitems; it += grid) {
             load_q(it);
@@ -1003,20 +1004,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             if (it == cta && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
             unsigned char* Ks = ring + (size_t)slot * SLOT_B;
             unsigned char* Vs = two ? ring + (size_t)slot_v * SLOT_B : Ks + kAttnHalf;
-            if (ok && has_new) {
+            if (ok && has_new) {  // 16-byte chunk ct of the row, into its swizzled place
               const int rw = pos - start;
-              *reinterpret_cast<uint4*>(Ks + rw * RK + ct * 16) = kv_new;
-              *reinterpret_cast<uint4*>(Vs + rw * RK + ct * 16) = vv_new;
+              *reinterpret_cast<uint4*>(Ks + kv_off(rw, ct)) = kv_new;
+              *reinterpret_cast<uint4*>(Vs + kv_off(rw, ct)) = vv_new;
               fence_proxy_async_smem();  // the slot is refilled by bulk copies later
             }
             named_sync(kBarCons, NC * 32);
-            // per-warp scores, softmax and P V over an even share of the chunk's
-            // positions; the warps' partials overlay the K rows
+            // per-warp scores, softmax and P V on the tensor cores, 16 positions
+            // per warp; the warps' partials overlay the K rows
             float* wb = reinterpret_cast<float*>(Ks);
             const int nn = ok ? n : 0;
-            const int pw = (nn + NC - 1) / NC;
-            const int j0 = warp * pw, jn = max(0, min(pw, nn - j0));
-            attn_warp<REP, DPL>(Ks, Vs, j0, jn, qr, lane, wb + (size_t)warp * REP * WS);
+            const int j0 = warp * 16, jn = max(0, min(16, nn - j0));
+            attn_warp_tc<REP, HDC>(Ks, Vs, j0, jn, qs, lane, wb + (size_t)warp * REP * WS);
             named_sync(kBarCons, NC * 32);
             // combine the eight warps (online-softmax rescale) into this chunk's partial
             float* part = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * (HDC + 2);
@@ -1200,7 +1200,7 @@ size_t step_smem_bytes(int B, int kmax, int gmax, int* nslot) {
   const size_t xsum = (((size_t)B * gmax * 8) + 15) & ~(size_t)15;
   const size_t red = (size_t)2 * NC * 32 * 16;
   const size_t budget = 227 * 1024 - kStaticSmem;
-  const size_t fixed = xs + xsum + red;
+  const size_t fixed = xs + xsum + red + 1024;  // + alignment of the ring
   if (fixed >= budget) return 0;
   int ns = (int)((budget - fixed) / SLOT_B);
   if (ns > 6) ns = 6;

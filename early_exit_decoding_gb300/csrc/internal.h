@@ -265,6 +265,8 @@ struct PhaseDesc {
 };
 
 struct StepArgs {
+  CUtensorMap tmk, tmv;       // every layer's K / V cache as one 2-D tensor [rows][hd], 16 x 64 boxes, 128 B swizzle
+  int kv_rows_layer;          // rows of one layer's cache: maxB * Hkv * Tmax
   const PhaseDesc* ph;
   int nph;
   DevState* st;
