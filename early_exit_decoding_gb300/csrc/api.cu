@@ -174,7 +174,7 @@ struct rl_kv {
   PhaseDesc* d_ph = nullptr;          // phase descriptors [nph_cap]
   std::vector<PhaseDesc> h_ph;        // host copy of what d_ph holds
   int nph_cap = 0;
-  float* part_s = nullptr;            // attention partials [min(maxB,8)][Hq][part_cap][hd+2]
+  float* part_s = nullptr;            // attention partials [min(maxB,8)][Hq][part_cap][hd+4]
   int part_cap = 0;
   unsigned long long* tl = nullptr;   // per-phase timeline (profiling) [2][nph_cap]
   unsigned long long* tl2 = nullptr;  // per-CTA timeline (profiling level 2) [nph_cap][grid][kTl2]
@@ -1432,7 +1432,7 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
     kv->part_cap = std::min(256, need + m->sm_count + 1);
     if (need <= 256) {
       const int bs = std::min(B, kFusedMaxB);
-      K_TRY(kv->alloc(&kv->part_s, (size_t)bs * m->Hq * kv->part_cap * (m->hd + 2)));
+      K_TRY(kv->alloc(&kv->part_s, (size_t)bs * m->Hq * kv->part_cap * (m->hd + 4)));
     } else {
       kv->part_cap = 0;  // context too long for the step kernel's chunking: fused path
     }

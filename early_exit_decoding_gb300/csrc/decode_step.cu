@@ -1018,8 +1018,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             const int j0 = warp * 16, jn = max(0, min(16, nn - j0));
             attn_warp_tc<REP, HDC>(Ks, Vs, j0, jn, qs, lane, wb + (size_t)warp * REP * WS);
             named_sync(kBarCons, NC * 32);
-            // combine the eight warps (online-softmax rescale) into this chunk's partial
-            float* part = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * (HDC + 2);
+            // combine the eight warps (online-softmax rescale) into this chunk's
+            // partial; partial rows of PS floats (o[hd], max, sum, 2 pad: 16-byte rows)
+            constexpr int PS = HDC + 4;
+            float* part = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * PS;
             for (int i = ct; i < REP * HDC; i += NC * 32) {
               const int h = i / HDC, dd = i % HDC;
               float M = -FLT_MAX;
@@ -1033,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 num += f * ww[2 + dd];
                 den += f * ww[1];
               }
-              float* pp = part + ((size_t)h * a.part_cap + ch) * (HDC + 2);
+              float* pp = part + ((size_t)h * a.part_cap + ch) * PS;
               pp[dd] = num;
               if (dd == 0) {
                 pp[HDC] = den > 0.f ? M : -FLT_MAX;
@@ -1042,10 +1044,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
             fence_proxy_async_smem();  // the warps' partials overlay the slot, refilled by bulk copies
             named_sync(kBarCons, NC * 32);
-            if (lane == 0) {
-              mbar_arrive(&empty[slot]);
-              if (two) mbar_arrive(&empty[slot_v]);
-            }
             // ---- the last CTA to finish a chunk of (b, hk) merges its chunks ----
             // (release: this CTA's partial writes, ordered by the barrier above,
             // before the ticket; acquire: every other chunk's partial after it)
@@ -1054,16 +1052,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               s_merge = tk == (unsigned)(nch - 1);
             }
             named_sync(kBarCons, NC * 32);
-            if (s_merge) {
-              // per head: chunk weights exp(m_c - M) / sum_c exp(m_c - M) l_c, staged
-              // as [h][c][2] in the (idle) partial-tile buffer; then o = sum_c w_c o_c
+            const bool merge = s_merge;
+            // The merging CTA keeps this item's slot(s) and stages the head group's
+            // partials there (one bulk copy per head, heads split over the slots)
+            // when they fit; otherwise it reads them from global memory.
+            const int nslot_item = two ? 2 : 1;
+            const int hps = (REP + nslot_item - 1) / nslot_item;  // heads per slot
+            const bool staged = merge && (size_t)hps * nch * PS * 4 <= (size_t)SLOT_B;
+            if (lane == 0 && !staged) {
+              mbar_arrive(&empty[slot]);
+              if (two) mbar_arrive(&empty[slot_v]);
+            }
+            if (merge) {
+              const float* hp = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * PS;
+              auto stage_of = [&](int h) -> float* {
+                unsigned char* base = ring + (size_t)(h / hps == 0 ? slot : slot_v) * SLOT_B;
+                return reinterpret_cast<float*>(base) + (size_t)(h % hps) * nch * PS;
+              };
+              if (staged) {
+                if (ct == 0) {
+                  fence_proxy_async();  // the partials were written by generic stores
+                  mbar_expect_tx(&xbar, (uint32_t)(REP * nch * PS * 4));
+                  for (int h = 0; h < REP; ++h)
+                    bulk_g2s(stage_of(h), hp + (size_t)h * a.part_cap * PS, (uint32_t)(nch * PS * 4), &xbar);
+                }
+                if (!s_abort && !mbar_wait(&xbar, xpar, kSpin)) {
+                  if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+                  s_abort = 1;
+                }
+                xpar ^= 1u;
+              }
+              // per head: chunk weights exp(m_c - M) / sum_c exp(m_c - M) l_c into mw [h][c]
               float* mw = redf;
-              const float* hp = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * (HDC + 2);
               for (int i = ct; i < REP * nch; i += NC * 32) {
                 const int h = i / nch, c = i % nch;
-                const float* pc = hp + ((size_t)h * a.part_cap + c) * (HDC + 2);
-                mw[2 * i] = __ldcg(pc + HDC);
-                mw[2 * i + 1] = __ldcg(pc + HDC + 1);
+                const float* pc = staged ? stage_of(h) + (size_t)c * PS : hp + ((size_t)h * a.part_cap + c) * PS;
+                mw[2 * i] = staged ? pc[HDC] : __ldcg(pc + HDC);
+                mw[2 * i + 1] = staged ? pc[HDC + 1] : __ldcg(pc + HDC + 1);
               }
               named_sync(kBarCons, NC * 32);
               if (warp < REP) {
@@ -1082,42 +1107,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                   mh[2 * c] = mh[2 * c + 1] > 0.f ? __expf(mh[2 * c] - M) * inv : 0.f;
               }
               named_sync(kBarCons, NC * 32);
-              // o = sum_c w_c o_c: each thread owns outputs ct and ct + 256 (REP * hd
-              // <= 512); the loads of 16 chunks are issued together
+              // o = sum_c w_c o_c, chunks in order; each thread owns outputs ct and ct + 256
               constexpr int NOUT = (REP * HDC + NC * 32 - 1) / (NC * 32);
-              float acc[NOUT];
-#pragma unroll
-              for (int k = 0; k < NOUT; ++k) acc[k] = 0.f;
-              for (int c0 = 0; c0 < nch; c0 += 16) {
-                float v[NOUT][16];
-#pragma unroll
-                for (int k = 0; k < NOUT; ++k) {
-                  const int i = ct + k * NC * 32;
-                  const int h = i / HDC, dd = i % HDC;
-                  const float* ph = hp + (size_t)h * a.part_cap * (HDC + 2) + dd;
-#pragma unroll
-                  for (int q = 0; q < 16; ++q)
-                    v[k][q] = (i < REP * HDC && c0 + q < nch) ? __ldcg(ph + (size_t)(c0 + q) * (HDC + 2)) : 0.f;
-                }
-#pragma unroll
-                for (int k = 0; k < NOUT; ++k) {
-                  const int i = ct + k * NC * 32;
-                  const float* wh = mw + (size_t)(i < REP * HDC ? i / HDC : 0) * nch * 2;
-#pragma unroll
-                  for (int q = 0; q < 16; ++q)
-                    if (c0 + q < nch) acc[k] += wh[2 * (c0 + q)] * v[k][q];
-                }
-              }
 #pragma unroll
               for (int k = 0; k < NOUT; ++k) {
                 const int i = ct + k * NC * 32;
                 if (i < REP * HDC) {
                   const int h = i / HDC, dd = i % HDC;
-                  D.o_out[(size_t)b * D.ldo_attn + (size_t)(hk * REP + h) * HDC + dd] = __float2bfloat16_rn(acc[k]);
+                  const float* wh = mw + (size_t)h * nch * 2;
+                  float acc = 0.f;
+                  if (staged) {
+                    const float* ph = stage_of(h) + dd;
+                    for (int c = 0; c < nch; ++c) acc += wh[2 * c] * ph[(size_t)c * PS];
+                  } else {
+                    const float* ph = hp + (size_t)h * a.part_cap * PS + dd;
+                    for (int c = 0; c < nch; ++c) acc += wh[2 * c] * __ldcg(ph + (size_t)c * PS);
+                  }
+                  D.o_out[(size_t)b * D.ldo_attn + (size_t)(hk * REP + h) * HDC + dd] = __float2bfloat16_rn(acc);
                 }
               }
               if (ct == 0) a.attn_ticket[b * Hkv + hk] = 0u;  // next step starts from zero
               named_sync(kBarCons, NC * 32);
+              if (lane == 0 && staged) {
+                mbar_arrive(&empty[slot]);
+                if (two) mbar_arrive(&empty[slot_v]);
+              }
             }
           }
         };
