@@ -1061,6 +1061,7 @@ rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStre
   a.part = kv->part_s;
   a.attn_ticket = kv->attn_ticket;
   a.part_cap = kv->part_cap;
+  a.rope_cs = kv->rope_cs;
   a.tmk = kv->tmk;
   a.tmv = kv->tmv;
   a.kv_rows_layer = kv->maxB * m->Hkv * kv->Tmax;

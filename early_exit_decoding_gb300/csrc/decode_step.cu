@@ -643,6 +643,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         const int my_c = (ct >> 4) % B, my_r = ct & 15;
         // residual epilogues: this thread's inputs of the first round, fetched now
         float pre_res = 0.f, pre_hin = 0.f, pre_gn = 0.f;
+        float2 pre_cs = make_float2(1.f, 0.f);  // QKV: (cos, sin) of this thread's first-round RoPE pair
+        if (D.epi == EPI_QKV_ROPE && my_r < 8 && ct < R && ct < min(TB, nt) * 16 * B) {
+          const int row0 = (cta + (ct / (16 * B)) * grid) * 16;
+          const int pos = s_pos;
+          if (row0 / a.hd < a.Hq + a.Hkv && pos >= 0 && pos < a.Tmax)
+            pre_cs = __ldg(a.rope_cs + (size_t)pos * (a.hd >> 1) + 8 * ((row0 % a.hd) >> 4) + my_r);
+        }
         if (D.epi == EPI_RESID && ct < R && ct < min(TB, nt) * 16 * B) {
           const int n = (cta + (ct / (16 * B)) * grid) * 16 + my_r;
           pre_res = __ldcg(D.resid + (size_t)my_c * D.ldr + n);
@@ -794,7 +801,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 float lo = v * rs, hi = hv * rs;
                 if (head_all < a.Hq + a.Hkv) {
                   float sn, cs;
-                  sincosf((float)pos * s_freq[dim], &sn, &cs);
+                  if (first_batch && rd == 0 && pos >= 0 && pos < a.Tmax) {
+                    cs = pre_cs.x;
+                    sn = pre_cs.y;
+                  } else {
+                    sincosf((float)pos * s_freq[dim], &sn, &cs);
+                  }
                   const float nlo = lo * cs - hi * sn, nhi = hi * cs + lo * sn;
                   lo = nlo;
                   hi = nhi;

@@ -282,6 +282,7 @@ struct StepArgs {
   float* h_store;
   int trace_maxB;
   const float* inv_freq;
+  const float2* rope_cs;      // (cos, sin) of pos * inv_freq[i], [Tmax][hd/2], the same sincosf values
   float* min_cos_out;
   int* next_token;
   int* exit_out;
