@@ -480,7 +480,36 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
     at.o = w.o;
     at.ldo = m->Ko;
     pf.begin();
-    launch_attention(at, s);
+    if (prefill) {
+      launch_attention(at, s);
+    } else if (kv->tm_ok && attn_stream_supported(m->Hq / m->Hkv, m->hd)) {
+      // decode: persistent CTAs stream the chunks (TMA ring, tensor cores),
+      // then the chunks are merged
+      at.nchunks = decode_attention_chunks(M, m->Hkv, kv->Tmax, m->sm_count);
+      AttnStreamArgs as;
+      memset(&as, 0, sizeof(as));
+      as.tmk = kv->tmk;
+      as.tmv = kv->tmv;
+      as.layer_row0 = l * kv->maxB * m->Hkv * kv->Tmax;
+      as.q = w.q;
+      as.pos_ptr = &kv->st->pos;
+      as.Tmax = kv->Tmax;
+      as.Hq = m->Hq;
+      as.Hkv = m->Hkv;
+      as.nq = M;
+      as.nchunks = at.nchunks;
+      attn_stream_smem(&as.nslot);
+      as.part = w.part;
+      as.err = &kv->st->err;
+      RL_CUDA(launch_attn_stream(as, m->Hq / m->Hkv, m->hd, m->sm_count, s));
+      launch_attention_combine(at, s);
+    } else {
+      // decode: chunks of <= 128 positions staged in shared memory, the last
+      // CTA of each (sequence, KV head) combines them (one launch)
+      at.nchunks = decode_attention_chunks(M, m->Hkv, kv->Tmax, m->sm_count);
+      at.ticket = kv->attn_ticket;
+      RL_CUDA(launch_attention_fused(at, false, s));
+    }
     RL_LAUNCHED();
     pf.end(RL_K_ATTN, l + 1, 0, 0, false, true);
     pf.begin();
@@ -1184,6 +1213,7 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
   if (m->sm_count < 1) m->sm_count = 1;
   gemv_fused_setup();
   attention_setup();
+  attn_stream_setup();
   decode_step_setup();
   if (!tc_gemm_available()) {
     delete m;
@@ -1829,8 +1859,10 @@ int32_t rl_decode_kernel_count(const rl_model* m, int32_t B) {
   if (step_fits_model(m, B)) return 1;  // one persistent kernel per step
   if (fused_fits(m, B))  // fused path: QKV, attention, O, gate/up, down; LM head
     return m->L * 5 + 1;
-  // per layer: QKV, attention (2), group sums, O, RMSNorm, gate/up, group sums, down, layer end
-  return 1 + m->L * 10 + 1 + 1;
+  // per layer: QKV, attention (stream + combine, or one fused launch), group
+  // sums, O, RMSNorm, gate/up, group sums, down, layer end
+  const int attn = attn_stream_supported(m->Hq / m->Hkv, m->hd) ? 2 : 1;
+  return 1 + m->L * (8 + attn) + 1 + 1;
 }
 
 }  // extern "C"

@@ -519,6 +519,14 @@ cudaError_t launch_attention_fused(const AttnArgs& a, bool pdl, cudaStream_t s) 
   return cudaLaunchKernelEx(&cfg, k_attn_decode<128>, a);
 }
 
+void launch_attention_combine(const AttnArgs& a, cudaStream_t s) {
+  dim3 g2(a.Hq, a.nq);
+  if (a.hd == 64)
+    k_attn_combine<64><<<g2, 64, 0, s>>>(a);
+  else
+    k_attn_combine<128><<<g2, 128, 0, s>>>(a);
+}
+
 void launch_attention(const AttnArgs& a, cudaStream_t s) {
   dim3 g1(a.nchunks, a.Hkv, a.nq);
   dim3 g2(a.Hq, a.nq);

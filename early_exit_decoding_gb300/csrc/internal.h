@@ -194,6 +194,25 @@ void launch_attention(const AttnArgs& a, cudaStream_t s);
 // Single-kernel decode attention: partials + combine by the last CTA per (row, KV head).
 cudaError_t launch_attention_fused(const AttnArgs& a, bool pdl, cudaStream_t s);
 void attention_setup();
+
+// Streaming decode attention (any batch): persistent CTAs, K/V chunks and
+// query rows by TMA into a shared-memory ring, tensor-core chunks; writes the
+// chunk partials [nq][Hq][nchunks][hd + 2] that k_attn_combine merges.
+struct AttnStreamArgs {
+  CUtensorMap tmk, tmv;   // every layer's K / V cache as one 2-D tensor [rows][hd], 16 x 64 boxes
+  int layer_row0;         // first row of this layer: layer * maxB * Hkv * Tmax
+  const float* q;         // [nq][Hq][hd] (RoPE applied)
+  const int* pos_ptr;
+  int Tmax, Hq, Hkv, nq, nchunks, nslot;
+  float* part;            // [nq][Hq][nchunks][hd + 2]
+  int* err;
+};
+size_t attn_stream_smem(int* nslot);
+void attn_stream_setup();
+bool attn_stream_supported(int rep, int hd);
+cudaError_t launch_attn_stream(const AttnStreamArgs& a, int rep, int hd, int grid, cudaStream_t s);
+// The combine half of launch_attention: merge a.nchunks partials into a.o.
+void launch_attention_combine(const AttnArgs& a, cudaStream_t s);
 // Context chunks per (sequence, KV head) of the fused decode attention (<= 256
 // supported by its merge; <= 128 positions per chunk).
 int decode_attention_chunks(int B, int Hkv, int Tmax, int sm_count);
