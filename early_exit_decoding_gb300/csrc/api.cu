@@ -160,6 +160,10 @@ struct rl_kv {
   unsigned* tile_ticket = nullptr;
   unsigned* cta_ticket = nullptr;
   unsigned* attn_ticket = nullptr;
+  float* tc_ws = nullptr;             // split-K partial tiles of the tensor-core GEMM
+  size_t tc_ws_floats = 0;
+  unsigned* tc_ticket = nullptr;      // per output tile, zero between launches
+  int tc_ticket_n = 0;
   float* am_val = nullptr;
   int* am_idx = nullptr;
   float* st_mid = nullptr;  // per-tile |h_mid|^2 of the O projection's output [d/16][8]
@@ -377,10 +381,18 @@ constexpr int kTcMinTokens = 16;
 // One projection over a.B tokens: the bf16 weights on the tensor cores (or
 // the GEMV for a few tokens), the exit river's W4 weights in the dequantising
 // GEMV; which of the two runs is decided on the device.
-rl_status project(const rl_model* m, const CUtensorMap& tm, GemvArgs a, cudaStream_t s) {
+rl_status project(const rl_model* m, rl_kv* kv, const CUtensorMap& tm, GemvArgs a, cudaStream_t s) {
+  a.tc_ws = kv->tc_ws;
+  a.tc_ws_floats = kv->tc_ws_floats;
+  a.tc_ticket = kv->tc_ticket;
+  a.tc_ticket_n = kv->tc_ticket_n;
   if (a.B >= kTcMinTokens) {
+    // the tensor-core GEMM runs bf16 layers and, when the projection has
+    // enough output tiles, the W4 exit-river layers (dequantised in shared
+    // memory); otherwise the dequantising GEMV runs the W4 layers
+    a.tc_w4 = a.qw != nullptr && tc_gemm_runs_w4(a.N, a.B, m->sm_count);
     RL_CUDA(launch_gemm_tc(tm, a, m->sm_count, s));
-    if (a.w4_mode == W4_OFF) return RL_OK;
+    if (a.w4_mode == W4_OFF || a.tc_w4) return RL_OK;
     a.w4_only = 1;
   }
   launch_gemv(a, m->sm_count, s);
@@ -458,7 +470,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      RL_TRY(project(m, ly.qkv.tm, a, s));
+      RL_TRY(project(m, kv, ly.qkv.tm, a, s));
       pf.end(RL_K_QKV, l + 1, bytes_bf16(ly.qkv), bytes_w4(ly.qkv), true);
     }
     // attention over the shared cache
@@ -532,7 +544,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      RL_TRY(project(m, ly.o.tm, a, s));
+      RL_TRY(project(m, kv, ly.o.tm, a, s));
       pf.end(RL_K_O, l + 1, bytes_bf16(ly.o), bytes_w4(ly.o), true);
     }
     // pre-FFN RMSNorm
@@ -566,7 +578,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      RL_TRY(project(m, ly.gu.tm, a, s));
+      RL_TRY(project(m, kv, ly.gu.tm, a, s));
       pf.end(RL_K_GU, l + 1, bytes_bf16(ly.gu), bytes_w4(ly.gu), true);
     }
     pf.begin();
@@ -589,7 +601,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      RL_TRY(project(m, ly.dn.tm, a, s));
+      RL_TRY(project(m, kv, ly.dn.tm, a, s));
       pf.end(RL_K_DOWN, l + 1, bytes_bf16(ly.dn), bytes_w4(ly.dn), true);
     }
     // layer end: cosine, batch-min, tau compare, next RMSNorm
@@ -642,7 +654,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
     a.err = &kv->st->err;
     pf.begin();
     a.path_out = pf.slot();
-    RL_TRY(project(m, m->tm_lm, a, s));
+    RL_TRY(project(m, kv, m->tm_lm, a, s));
     const double lm = (double)m->V * m->d * 2.0;
     pf.end(RL_K_LM_HEAD, 0, lm, lm, true);
   }
@@ -856,6 +868,7 @@ rl_status reset_sync_words(rl_kv* kv, cudaStream_t s) {
   RL_CUDA(cudaMemsetAsync(kv->tile_ticket, 0, (size_t)kv->n_tile_ticket * sizeof(unsigned), s));
   RL_CUDA(cudaMemsetAsync(kv->attn_ticket, 0, (size_t)kv->maxB * kv->m->Hkv * sizeof(unsigned), s));
   RL_CUDA(cudaMemsetAsync(kv->cta_ticket, 0, sizeof(unsigned), s));
+  RL_CUDA(cudaMemsetAsync(kv->tc_ticket, 0, (size_t)kv->tc_ticket_n * sizeof(unsigned), s));
   return RL_OK;
 }
 
@@ -1446,6 +1459,10 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
     kv->n_tile_ticket = max_tiles;
     K_TRY(kv->alloc(&kv->cta_ticket, 1));
     K_TRY(kv->alloc(&kv->attn_ticket, (size_t)B * m->Hkv));
+    kv->tc_ws_floats = (size_t)2 * sm * 64 * 128;
+    K_TRY(kv->alloc(&kv->tc_ws, kv->tc_ws_floats));
+    kv->tc_ticket_n = 1024;
+    K_TRY(kv->alloc(&kv->tc_ticket, (size_t)kv->tc_ticket_n));
     K_TRY(kv->alloc(&kv->am_val, (size_t)sm * kFusedMaxB));
     K_TRY(kv->alloc(&kv->am_idx, (size_t)sm * kFusedMaxB));
     K_TRY(kv->alloc(&kv->st_mid, (size_t)(m->d / 16) * 8));

@@ -13,19 +13,33 @@
 // row orders put each rotate-half / gate-up pair 8 rows apart, so a pair sits
 // in one warp and is exchanged with one shuffle).
 //
-// The weights of exit layers are W4 and run in the dequantising GEMV: this
-// kernel returns at once when the device-side exit layer says the layer is on
-// the exit river (River-LLM explainer, section 四).
+// The weights of exit layers are W4 (River-LLM explainer, section 四: the
+// device-side exit layer picks the path): four more warps dequantise each
+// 128 x 64 weight block, (q - z) * s rounded to bf16, straight into the
+// 128-byte-swizzled shared-memory layout the TMA would have written, and the
+// MMAs run as for the backbone's bf16 weights.  The dequantising warps, not
+// the quarter-size weight bytes, bound this path, so a W4 projection runs
+// here only when it has at least half as many output tiles as SMs
+// (tc_gemm_runs_w4); narrower ones stay on the dequantising GEMV.
 //
-// Persistent CTAs (one per SM) walk the output tiles; 320 threads: warp 0
+// When the output tiles are fewer than the SMs (a decode batch's narrow
+// projections), K is split: unit u = (tile, split), each split accumulates
+// its contiguous range of 64-input blocks and writes the fp32 tile to a
+// workspace; the last of the tile's CTAs (ticket) sums the splits in split
+// order and runs the epilogue, so the result does not depend on timing.
+//
+// Persistent CTAs (one per SM) walk the units; 448 threads: warp 0
 // lane 0 issues the TMA loads into a STAGES-deep ring of (128 x 64 weight
 // tile, BN x 64 token tile), warp 1 owns the tensor-memory allocation (two
 // BN-column fp32 accumulators) and its lane 0 issues the MMAs, warps 2..9 run
 // the epilogue of one tile while the MMAs of the next fill the other
 // accumulator (warp w reads TMEM lanes 32 (w % 4) .. +31, one half of the
-// columns).  Every wait is bounded; a wait that runs out sets
+// columns), warps 10..13 write the W4 weight tiles of exit-river layers.
+// Every wait is bounded; a wait that runs out sets
 // RL_DEVERR_TIMEOUT and the CTA winds down (all MMAs retired, all copies
 // landed, tensor memory freed).
+#include <algorithm>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -38,7 +52,7 @@ namespace {
 
 using dev::smem_u32;
 
-constexpr int kThreadsTc = 320;
+constexpr int kThreadsTc = 448;  // TMA, MMA, 8 epilogue warps, 4 W4 dequantising warps
 constexpr int kBM = 128;           // weight rows per tile (MMA M)
 constexpr int kBK = 64;            // K per stage: one 128-byte swizzle row of bf16
 constexpr int kABytes = kBM * kBK * 2;
@@ -118,16 +132,26 @@ __device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.f +
 // `row_ok`) for launch columns col0 .. col0 + 15 (those < B), read from the
 // accumulator at `taddr`.  All 32 lanes of the warp call it together (the
 // gate/up and rotate-half partners, 8 rows apart, are exchanged by shuffles).
+// TM: the values come from the accumulator at `taddr`; otherwise from `vin`.
+template <bool TM>
 __device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok, int lane,
-                                          int col0, uint32_t taddr) {
+                                          int col0, uint32_t taddr, const float* vin = nullptr) {
   const int nc = min(16, a.B - col0);
   float v[16];
+  auto fetch = [&]() {
+    if constexpr (TM) {
+      tmem_ld16(taddr, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = vin[j];
+    }
+  };
   if (a.epi == EPI_RESID) {
     float r[16];  // residual loads issued before the accumulator read
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       r[j] = (row_ok && j < nc) ? __ldg(a.resid + (size_t)(col0 + j) * a.ldr + R) : 0.f;
-    tmem_ld16(taddr, v);
+    fetch();
     if (row_ok) {
 #pragma unroll
       for (int j = 0; j < 16; ++j)
@@ -135,7 +159,7 @@ __device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok,
     }
     return;
   }
-  tmem_ld16(taddr, v);
+  fetch();
   if (a.epi == EPI_STORE) {
     if (row_ok) {
 #pragma unroll
@@ -208,6 +232,7 @@ __device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok,
 }
 
 constexpr int kEpiWarps = 8;
+constexpr int kDqWarps = 4;  // W4 dequantising warps
 
 // Persistent: CTA b takes tiles b, b + grid, ...; tile t covers weight rows
 // (t / tiles_m) * 128 .. +127 and tokens (t % tiles_m) * BN .. +BN-1, so the
@@ -221,27 +246,35 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   constexpr uint32_t kTmemCols = 2 * BN;
   bool w4 = a.w4_mode == W4_ON;
   if (a.w4_mode == W4_BY_LAYER) w4 = a.layer_no > *a.exit_layer;
-  if (a.path_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && !w4) *a.path_out = 0;
-  if (w4) return;  // the exit river's W4 weights run in the dequantising GEMV
+  if (w4 && (a.qw == nullptr || !a.tc_w4)) return;  // the dequantising GEMV runs this W4 layer
+  if (a.path_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.path_out = w4 ? 1 : 0;
 
   extern __shared__ unsigned char smem_dyn[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
   unsigned char* sA = smem;
   unsigned char* sB = smem + STAGES * kABytes;
-  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], mma_done;
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], afull[STAGES], acc_full[2], acc_empty[2],
+      mma_done;
   __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
+  __shared__ volatile int s_fail;
+  __shared__ volatile int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_m = (a.B + BN - 1) / BN;
   const int ntiles = ((a.N + kBM - 1) / kBM) * tiles_m;
   const int nk = a.Kp / kBK;
+  // work units: (tile t, split sp) = u = t * S + sp covers k-blocks kb0(u) .. kb1(u) - 1
+  const int S = a.tc_ws != nullptr && a.ksplit > 1 ? a.ksplit : 1;
+  const int nunits = ntiles * S;
+  auto kb0_of = [&](int u) { return nk * (u % S) / S; };
+  auto kb1_of = [&](int u) { return nk * (u % S + 1) / S; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       dev::mbar_init(&full[i], 1);
       dev::mbar_init(&empty[i], 1);
+      dev::mbar_init(&afull[i], kDqWarps);
     }
     for (int i = 0; i < 2; ++i) {
       dev::mbar_init(&acc_full[i], 1);
@@ -269,17 +302,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (lane == 0) {  // TMA producer
       int g = 0;      // k-blocks issued by this CTA
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int t = u / S;
         const int n0 = (t / tiles_m) * kBM, m0 = (t % tiles_m) * BN;
-        for (int kb = 0; kb < nk; ++kb, ++g) {
+        for (int kb = kb0_of(u); kb < kb1_of(u); ++kb, ++g) {
           const int s = g % STAGES, n = g / STAGES;
           if (n > 0 && !dev::mbar_wait(&empty[s], (n - 1) & 1, kSpinTc)) {
             s_fail = 1;
             ok = false;
             break;
           }
-          dev::mbar_expect_tx(&full[s], kABytes + kBBytes);
-          tma_load_2d(sA + s * kABytes, &tmW, kb * kBK, n0, &full[s]);
+          dev::mbar_expect_tx(&full[s], (w4 ? 0 : kABytes) + kBBytes);
+          if (!w4) tma_load_2d(sA + s * kABytes, &tmW, kb * kBK, n0, &full[s]);
           tma_load_2d(sB + s * kBBytes, &tmX, kb * kBK, m0, &full[s]);
         }
       }
@@ -293,7 +327,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint32_t idesc = idesc_bf16(kBM, BN);
       int g = 0, i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+      for (int uu = blockIdx.x; uu < nunits && ok; uu += gridDim.x, ++i) {
         const int acc = i & 1, u = i >> 1;
         if (u > 0 && !dev::mbar_wait(&acc_empty[acc], (u - 1) & 1, kSpinTc)) {
           s_fail = 1;
@@ -301,9 +335,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int kbs = kb0_of(uu);
+        for (int kb = kbs; kb < kb1_of(uu); ++kb, ++g) {
           const int s = g % STAGES;
-          if (!dev::mbar_wait(&full[s], (g / STAGES) & 1, kSpinTc)) {
+          if (!dev::mbar_wait(&full[s], (g / STAGES) & 1, kSpinTc) ||
+              (w4 && !dev::mbar_wait(&afull[s], (g / STAGES) & 1, kSpinTc))) {
             s_fail = 1;
             ok = false;
             break;
@@ -313,7 +349,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const uint64_t bd = sw128_desc(smem_u32(sB + s * kBBytes));
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes = 2 in the address field
-            mma_tc(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+            mma_tc(d, ad + 2 * k, bd + 2 * k, idesc, (kb != kbs || k != 0) ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         mma_commit(&acc_full[acc]);
@@ -322,29 +358,125 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mma_commit(&mma_done);
       dev::mbar_wait(&mma_done, 0, kSpinTc);
     }
+  } else if (warp >= 2 + kEpiWarps) {
+    // W4 dequantising warps: thread r writes weight row n0 + r of every 128 x 64
+    // block, 8 chunks of 8 bf16 at chunk position c ^ (r & 7) (128-byte swizzle)
+    if (w4) {
+      const int r = threadIdx.x - (2 + kEpiWarps) * 32;
+      const int wpr = a.Kp >> 3, gpr = a.Kp >> 7;
+      int g = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+        const int t = u / S;
+        const int R = (t / tiles_m) * kBM + r;
+        const bool row_ok = R < a.N;
+        const uint32_t* qrow = a.qw + (size_t)(row_ok ? R : 0) * wpr;
+        const __half2* zrow = a.sz + (size_t)(row_ok ? R : 0) * gpr;
+        for (int kb = kb0_of(u); kb < kb1_of(u); ++kb, ++g) {
+          const int s = g % STAGES, n = g / STAGES;
+          uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+          float2 sz = make_float2(0.f, 0.f);
+          if (row_ok) {  // loads first, then the wait for the slot
+            w0 = __ldg(reinterpret_cast<const uint4*>(qrow + kb * 8));
+            w1 = __ldg(reinterpret_cast<const uint4*>(qrow + kb * 8 + 4));
+            sz = __half22float2(zrow[(kb * kBK) >> 7]);
+          }
+          if (n > 0 && !dev::mbar_wait(&empty[s], (n - 1) & 1, kSpinTc)) {
+            s_fail = 1;
+            ok = false;
+            break;
+          }
+          unsigned char* dst = sA + s * kABytes + r * 128;
+          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {  // chunk c: inputs 8c .. 8c + 7 = the nibbles of word c
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = ((float)((wv[c] >> (8 * e)) & 15u) - sz.y) * sz.x;
+              const float hi = ((float)((wv[c] >> (8 * e + 4)) & 15u) - sz.y) * sz.x;
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+              pk[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          dev::fence_proxy_async_smem();  // generic writes before the MMAs' reads
+          __syncwarp();
+          if ((threadIdx.x & 31) == 0) dev::mbar_arrive(&afull[s]);
+        }
+      }
+    }
   } else {  // epilogue warps 2 .. 9: lane quarter warp % 4, column half (warp - 2) / 4
     const int q = warp & 3, h = (warp - 2) >> 2;
     int i = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-      const int acc = i & 1, u = i >> 1;
+    for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++i) {
+      const int t = u / S;
+      const int acc = i & 1, ua = i >> 1;
       const int n0 = (t / tiles_m) * kBM, m0 = (t % tiles_m) * BN;
-      if (!dev::mbar_wait(&acc_full[acc], u & 1, kSpinTc)) {
-        s_fail = 1;
+      const bool got = dev::mbar_wait(&acc_full[acc], ua & 1, kSpinTc);
+      if (!got) s_fail = 1;
+      if (S > 1) {
+        // every epilogue warp takes the same decision after the barrier (a wait
+        // that ran out in one warp stops all of them)
+        dev::named_sync(2, kEpiWarps * 32);
+        if (s_fail) break;
+      } else if (!got) {
         break;
       }
       tc_fence_after();
       const int R = n0 + 32 * q + lane;
       const bool row_ok = R < a.N;
+      const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
+      if (S == 1) {
+#pragma unroll 1
+        for (int c16 = h * (BN / 32); c16 < (h + 1) * (BN / 32); ++c16) {
+          const int col0 = m0 + c16 * 16;
+          if (col0 >= a.B) break;
+          epi_chunk<true>(a, R, row_ok, lane, col0, tacc + (uint32_t)(c16 * 16));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive(&acc_empty[acc]);
+        continue;
+      }
+      // split K: this unit's fp32 partial tile -> ws[u][column][128 rows]
+      float* wsu = a.tc_ws + (size_t)u * BN * kBM;
 #pragma unroll 1
       for (int c16 = h * (BN / 32); c16 < (h + 1) * (BN / 32); ++c16) {
-        const int col0 = m0 + c16 * 16;
-        if (col0 >= a.B) break;
-        epi_chunk(a, R, row_ok, lane, col0,
-                  tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN + c16 * 16));
+        float v[16];
+        tmem_ld16(tacc + (uint32_t)(c16 * 16), v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) wsu[(size_t)(c16 * 16 + j) * kBM + 32 * q + lane] = v[j];
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(&acc_empty[acc]);
+      // the last unit of tile t to finish sums the partials in split order and
+      // runs the epilogue (release: the partial stores before the ticket,
+      // ordered by the barrier; acquire: the other units' partials after it)
+      dev::named_sync(2, kEpiWarps * 32);
+      if (warp == 2 && lane == 0) s_last = dev::atom_add_acq_rel(a.tc_ticket + t, 1u) == (unsigned)(S - 1);
+      dev::named_sync(2, kEpiWarps * 32);
+      if (s_last) {
+        const float* wst = a.tc_ws + (size_t)t * S * BN * kBM;
+#pragma unroll 1
+        for (int c16 = h * (BN / 32); c16 < (h + 1) * (BN / 32); ++c16) {
+          const int col0 = m0 + c16 * 16;
+          if (col0 >= a.B) break;
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0.f;
+          for (int sp = 0; sp < S; ++sp) {
+            const float* p = wst + ((size_t)sp * BN + c16 * 16) * kBM + 32 * q + lane;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] += __ldcg(p + (size_t)j * kBM);
+          }
+          epi_chunk<false>(a, R, row_ok, lane, col0, 0u, v);
+        }
+        dev::named_sync(2, kEpiWarps * 32);
+        if (warp == 2 && lane == 0) a.tc_ticket[t] = 0u;  // the next launch starts from zero
+      }
+      dev::named_sync(2, kEpiWarps * 32);
     }
   }
   tc_fence_before();
@@ -386,9 +518,20 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, c
   constexpr int smem = tc_smem_bytes<BN, STAGES>();
   CUtensorMap tmX;
   if (!make_tmap_bf16(&tmX, a.x, a.Kp, a.B, a.ldx, BN)) return cudaErrorInvalidValue;
-  int grid = ((a.N + kBM - 1) / kBM) * ((a.B + BN - 1) / BN);
+  const int tiles = ((a.N + kBM - 1) / kBM) * ((a.B + BN - 1) / BN);
+  // split K when the output tiles would leave SMs idle (decode batches): at
+  // least 4 k-blocks per split, partial tiles within the workspace
+  GemvArgs b = a;
+  int S = 1;
+  if (a.tc_ws != nullptr && BN <= 64 && tiles < sm_count && tiles <= a.tc_ticket_n) {
+    S = std::min((sm_count + tiles - 1) / tiles, (a.Kp / kBK) / 4);
+    while (S > 1 && (size_t)tiles * S * BN * kBM > a.tc_ws_floats) --S;
+    if (S < 1) S = 1;
+  }
+  b.ksplit = S;
+  int grid = tiles * S;
   if (grid > sm_count) grid = sm_count;
-  k_gemm_tc<BN, STAGES><<<grid, kThreadsTc, smem, s>>>(tmW, tmX, a);
+  k_gemm_tc<BN, STAGES><<<grid, kThreadsTc, smem, s>>>(tmW, tmX, b);
   return cudaGetLastError();
 }
 
@@ -461,6 +604,12 @@ int tc_pick_bn(int N, int M, int sm_count) {
     }
   }
   return best;
+}
+
+bool tc_gemm_runs_w4(int N, int B, int sm_count) {
+  const int bn = tc_pick_bn(N, B, sm_count);
+  const int tiles = ((N + kBM - 1) / kBM) * ((B + bn - 1) / bn);
+  return 2 * tiles >= sm_count;
 }
 
 cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s) {

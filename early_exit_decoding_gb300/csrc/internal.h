@@ -75,6 +75,10 @@ struct GemvArgs {
   int* err;
   int* path_out;          // nullable: CTA 0 records the path taken (0 bf16, 1 W4)
   int w4_only;            // k_gemv: return at once unless the W4 path is taken
+  // k_gemm_tc split-K (few output tiles): fp32 partial tiles and per-tile tickets
+  float* tc_ws; size_t tc_ws_floats; unsigned* tc_ticket; int tc_ticket_n;
+  int ksplit;             // set by launch_gemm_tc
+  int tc_w4;              // k_gemm_tc runs the W4 path too (else it returns at once for W4 layers)
 };
 
 void launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t s);
@@ -90,6 +94,9 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int
 bool make_weight_tmap(CUtensorMap* map, const bf16* w, int N, int Kp);
 int tc_pick_bn(int N, int M, int sm_count);
 cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s);
+// Whether the tensor-core GEMM should also run a W4 layer of this shape (enough
+// output tiles that its dequantising warps are not the bottleneck).
+bool tc_gemm_runs_w4(int N, int B, int sm_count);
 // (cos, sin) of pos * inv_freq[i] for pos < Tmax, i < half: [Tmax][half].
 void launch_rope_table(const float* inv_freq, int half, int Tmax, float2* out, cudaStream_t s);
 

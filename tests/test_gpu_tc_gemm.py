@@ -56,12 +56,31 @@ def _forced(river, sched):
 @pytest.mark.parametrize("B", [16, 21, 40])
 def test_decode_batches_on_tensor_cores(river, tiny, stream, B):
     """Decode batches of 16 / 21 / 40 sequences run the GEMM with 32- and
-    64-token tiles (ragged); exit layers mix in on the W4 GEMV."""
+    64-token tiles (ragged); exit layers mix in (W4 weights dequantised in
+    shared memory for the tensor cores)."""
     m, om, _ = tiny
     L = TINY.n_layers
     sched = [L, L, 0, 2, 1, L]
     res, _ = _run_sequence(river, m, om, stream, _forced(river, sched), B=B, prompt=9,
                            steps=len(sched) - 1, seed=20 + B, path="generic")
+    assert [int(o["exit_layer"].item()) for o, _ in res] == sched
+
+
+@pytest.mark.parametrize("B", [16, 40])
+def test_decode_batches_split_k_and_w4_on_tensor_cores(river, stream, B):
+    """A wider model (d_model 1024, FFN 2816: 16 to 44 k-blocks of 64 inputs)
+    whose projections at batch 16 / 40 have fewer 128-row tiles than SMs: the
+    GEMM splits K across CTAs (partial tiles summed by the tile's last CTA) on
+    the bf16 backbone; at batch 40 the W4 gate/up projection (88 tiles of 32
+    columns) runs on the tensor cores too, dequantised in shared memory and
+    split in two, while the narrower W4 projections stay on the GEMV."""
+    S = synth.scaled(TINY, d_model=1024, n_q_heads=8, n_kv_heads=2, ffn_dim=2816, n_layers=3,
+                     vocab=512)
+    with torch.cuda.stream(stream):
+        m, om, _ = build_pair(S, seed=7, gains="random", stream=stream)
+    sched = [3, 3, 0, 1, 2]
+    res, _ = _run_sequence(river, m, om, stream, _forced(river, sched), B=B, prompt=6,
+                           steps=len(sched) - 1, seed=60 + B, path="generic")
     assert [int(o["exit_layer"].item()) for o, _ in res] == sched
 
 
