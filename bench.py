@@ -300,11 +300,18 @@ def run_river(args, rank, world, dev):
     return res
 
 
-def traffic_note(summary, source):
+def source_hash(*sources):
+    """sha256 prefix of the kernel's source files (csrc/), concatenated in order."""
+    h = hashlib.sha256()
+    for src in sources:
+        h.update(open(os.path.join(ROOT, "early_exit_decoding_gb300", "csrc", src), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_note(summary, *sources):
     """DRAM bytes over algorithmic bytes of a kernel from a committed ncu
-    summary, if it was taken on the current kernel source."""
+    summary, if it was taken on the current kernel sources."""
     p = os.path.join(ROOT, "profiles", summary)
-    src = os.path.join(ROOT, "early_exit_decoding_gb300", "csrc", source)
     if not os.path.exists(p):
         return None
     kv = {}
@@ -312,7 +319,7 @@ def traffic_note(summary, source):
         if ":" in line:
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = source_hash(*sources)
     if kv.get("source_sha256_16") != h:
         return None
     try:
@@ -454,18 +461,32 @@ def main():
     # roofline of the dominant kernel, from the live profile.  B <= 8: the
     # persistent step kernel (one launch per step, every byte of the step);
     # its phase records (first start .. last end over CTAs) give the shares.
+    # B > 8: one launch per kernel kind and layer; the kind with the most time.
     prof = res["prof"]
     steps = [r for r in prof if r[0] == "decode_step"]
     if steps:
         kname = "k_decode_step (persistent decode step: every layer's projections, attention, LM head)"
         launches = steps
         phases = [r for r in prof if r[0] != "decode_step"]
-        ratio = traffic_note("step_dram_traffic.txt", "decode_step.cu")
+        ratio = traffic_note("step_dram_traffic.txt", "decode_step.cu", "attn_tc.cuh")
     else:
-        kname = "k_gemv_fused (bf16 / W4 projections + LM head, B <= 8)"
-        launches = [r for r in prof if r[0] in ("qkv", "o_proj", "gate_up", "down", "lm_head")]
         phases = prof
-        ratio = traffic_note("gemv_dram_traffic.txt", "gemv_fused.cu")
+        by_kind = {}
+        for r in prof:
+            by_kind[r[0]] = by_kind.get(r[0], 0.0) + r[3]
+        top = max(by_kind, key=by_kind.get)
+        launches = [r for r in prof if r[0] == top]
+        if top == "attention":
+            kname = ("k_attn_stream + k_attn_combine (streaming decode attention: K/V chunks by "
+                     "TMA, tensor cores; bytes = K and V rows 0..p of every sequence)")
+            ratio = traffic_note("attn_stream_dram_traffic.txt", "attn_stream.cu", "attn_tc.cuh")
+        elif B >= 16:
+            kname = (f"k_gemm_tc ({top}: tcgen05 GEMM; W4 layers dequantised in shared memory "
+                     "or on k_gemv_fused)")
+            ratio = None
+        else:
+            kname = f"k_gemv_fused ({top}: bf16 / W4 GEMV)"
+            ratio = traffic_note("gemv_dram_traffic.txt", "gemv_fused.cu")
     g_ms = sum(r[3] for r in launches)
     g_bytes = sum(r[4] for r in launches)
     all_ms = sum(r[3] for r in phases)

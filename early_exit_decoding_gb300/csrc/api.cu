@@ -142,7 +142,8 @@ struct rl_kv {
   rl_model* m = nullptr;
   int maxB = 0, Tmax = 0;
   std::vector<bf16*> K, V;     // per-layer views into one allocation each
-  CUtensorMap tmk, tmv;        // all layers' K / V as one 2-D tensor [L*maxB*Hkv*Tmax][hd] (step kernel)
+  CUtensorMap tmk, tmv;        // all layers' K / V as one 2-D tensor [L*maxB*Hkv*Tmax][hd], 16-row boxes
+  CUtensorMap tmk64, tmv64;    // the same, 64-row boxes (streaming decode attention)
   bool tm_ok = false;
   DevState* st = nullptr;
   int host_pos = 0, host_step = 0;
@@ -502,6 +503,8 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       memset(&as, 0, sizeof(as));
       as.tmk = kv->tmk;
       as.tmv = kv->tmv;
+      as.tmk64 = kv->tmk64;
+      as.tmv64 = kv->tmv64;
       as.layer_row0 = l * kv->maxB * m->Hkv * kv->Tmax;
       as.q = w.q;
       as.pos_ptr = &kv->st->pos;
@@ -1423,11 +1426,13 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
       kv->K[l] = k_all + per_layer * l;
       kv->V[l] = v_all + per_layer * l;
     }
-    // the step kernel's attention reads K / V chunks by TMA: 16-row x 64-dim boxes
+    // the decode attention reads K / V chunks by TMA: 16- and 64-row x 64-dim boxes
     const long long rows = (long long)m->L * max_batch * m->Hkv * max_seq;
     kv->tm_ok = rows < (1ll << 31) && (m->hd == 64 || m->hd == 128) &&
                 make_tmap_bf16(&kv->tmk, k_all, m->hd, (int)rows, m->hd, 16) &&
-                make_tmap_bf16(&kv->tmv, v_all, m->hd, (int)rows, m->hd, 16);
+                make_tmap_bf16(&kv->tmv, v_all, m->hd, (int)rows, m->hd, 16) &&
+                make_tmap_bf16(&kv->tmk64, k_all, m->hd, (int)rows, m->hd, 64) &&
+                make_tmap_bf16(&kv->tmv64, v_all, m->hd, (int)rows, m->hd, 64);
   }
   K_TRY(kv->alloc(&kv->st, 1));
   const int B = max_batch;

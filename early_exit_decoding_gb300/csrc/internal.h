@@ -207,6 +207,7 @@ void attention_setup();
 // chunk partials [nq][Hq][nchunks][hd + 2] that k_attn_combine merges.
 struct AttnStreamArgs {
   CUtensorMap tmk, tmv;   // every layer's K / V cache as one 2-D tensor [rows][hd], 16 x 64 boxes
+  CUtensorMap tmk64, tmv64;  // the same tensors, 64 x 64 boxes
   int layer_row0;         // first row of this layer: layer * maxB * Hkv * Tmax
   const float* q;         // [nq][Hq][hd] (RoPE applied)
   const int* pos_ptr;
