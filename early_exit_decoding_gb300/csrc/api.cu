@@ -527,10 +527,12 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
     }
     RL_LAUNCHED();
     pf.end(RL_K_ATTN, l + 1, 0, 0, false, true);
-    pf.begin();
-    launch_group_sums(w.o, m->Ko, m->Ko, M, w.xs_o, Go, s);
-    RL_LAUNCHED();
-    pf.end(RL_K_GSUM, l + 1, 0, 0, false);
+    if (M <= kTcW4AllTokens) {  // the W4 GEMV's zero-point term needs the group sums
+      pf.begin();
+      launch_group_sums(w.o, m->Ko, m->Ko, M, w.xs_o, Go, s);
+      RL_LAUNCHED();
+      pf.end(RL_K_GSUM, l + 1, 0, 0, false);
+    }
     // O projection + residual
     {
       GemvArgs a = gemv_base(m, ly.o, w4mode, kv->st, l + 1);
@@ -584,10 +586,12 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       RL_TRY(project(m, kv, ly.gu.tm, a, s));
       pf.end(RL_K_GU, l + 1, bytes_bf16(ly.gu), bytes_w4(ly.gu), true);
     }
-    pf.begin();
-    launch_group_sums(w.u, m->Kf, m->Kf, M, w.xs_u, Gf, s);
-    RL_LAUNCHED();
-    pf.end(RL_K_GSUM, l + 1, 0, 0, false);
+    if (M <= kTcW4AllTokens) {
+      pf.begin();
+      launch_group_sums(w.u, m->Kf, m->Kf, M, w.xs_u, Gf, s);
+      RL_LAUNCHED();
+      pf.end(RL_K_GSUM, l + 1, 0, 0, false);
+    }
     // down + residual
     {
       GemvArgs a = gemv_base(m, ly.dn, w4mode, kv->st, l + 1);
@@ -1464,7 +1468,7 @@ rl_status rl_kv_cache_alloc(const rl_model* mc, int32_t max_batch, int32_t max_s
     kv->n_tile_ticket = max_tiles;
     K_TRY(kv->alloc(&kv->cta_ticket, 1));
     K_TRY(kv->alloc(&kv->attn_ticket, (size_t)B * m->Hkv));
-    kv->tc_ws_floats = (size_t)2 * sm * 64 * 128;
+    kv->tc_ws_floats = (size_t)4 * sm * 64 * 128;  // split-K partial tiles (~20 MB at 152 SMs)
     K_TRY(kv->alloc(&kv->tc_ws, kv->tc_ws_floats));
     kv->tc_ticket_n = 1024;
     K_TRY(kv->alloc(&kv->tc_ticket, (size_t)kv->tc_ticket_n));
@@ -1882,9 +1886,11 @@ int32_t rl_decode_kernel_count(const rl_model* m, int32_t B) {
   if (fused_fits(m, B))  // fused path: QKV, attention, O, gate/up, down; LM head
     return m->L * 5 + 1;
   // per layer: QKV, attention (stream + combine, or one fused launch), group
-  // sums, O, RMSNorm, gate/up, group sums, down, layer end
+  // sums (up to kTcW4AllTokens tokens), O, RMSNorm, gate/up, group sums, down,
+  // layer end
   const int attn = attn_stream_supported(m->Hq / m->Hkv, m->hd) ? 2 : 1;
-  return 1 + m->L * (8 + attn) + 1 + 1;
+  const int gsum = B <= kTcW4AllTokens ? 2 : 0;
+  return 1 + m->L * (6 + gsum + attn) + 1 + 1;
 }
 
 }  // extern "C"

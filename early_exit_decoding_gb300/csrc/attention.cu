@@ -453,23 +453,47 @@ __global__ void __launch_bounds__(kThreads) k_attn_decode(AttnArgs a) {
   if (tid == 0) a.ticket[(size_t)b * a.Hkv + hk] = 0u;
 }
 
+// Merge of one (row, query head)'s chunk partials: M = the largest chunk
+// maximum (a block reduction over the chunks, read in parallel), then the
+// weights w_c = exp(m_c - M) of up to kCombBlk chunks at a time are staged in
+// shared memory and thread dd sums w_c o_c[dd] and w_c l_c in chunk order
+// (independent loads, so the chunk loop runs at L2 throughput, not latency).
+constexpr int kCombBlk = 512;
+
 template <int HD>
 __global__ void __launch_bounds__(HD) k_attn_combine(AttnArgs a) {
+  __shared__ float s_w[kCombBlk], s_l[kCombBlk];
+  __shared__ float s_red[HD / 32];
   const int hq = blockIdx.x, row = blockIdx.y, dd = threadIdx.x;
-  const float* part = a.part + ((size_t)row * a.Hq + hq) * a.nchunks * (HD + 2);
+  const int nch = a.nchunks;
+  const float* part = a.part + ((size_t)row * a.Hq + hq) * nch * (HD + 2);
   float M = -FLT_MAX;
-  for (int c = 0; c < a.nchunks; ++c) {
+  for (int c = dd; c < nch; c += HD) {
     const float* p = part + (size_t)c * (HD + 2);
     if (p[HD + 1] > 0.f) M = fmaxf(M, p[HD]);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if ((dd & 31) == 0) s_red[dd >> 5] = M;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < HD / 32; ++w) M = fmaxf(M, s_red[w]);
   float num = 0.f, den = 0.f;
-  for (int c = 0; c < a.nchunks; ++c) {
-    const float* p = part + (size_t)c * (HD + 2);
-    const float l = p[HD + 1];
-    if (l > 0.f) {
-      const float w = __expf(p[HD] - M);
-      num += w * p[dd];
-      den += w * l;
+  for (int c0 = 0; c0 < nch; c0 += kCombBlk) {
+    const int nb = min(kCombBlk, nch - c0);
+    __syncthreads();  // the previous block's weights have been used
+    for (int c = dd; c < nb; c += HD) {
+      const float* p = part + (size_t)(c0 + c) * (HD + 2);
+      const float l = p[HD + 1];
+      s_l[c] = l;
+      s_w[c] = l > 0.f ? __expf(p[HD] - M) : 0.f;
+    }
+    __syncthreads();
+    const float* pd = part + (size_t)c0 * (HD + 2) + dd;
+#pragma unroll 8
+    for (int c = 0; c < nb; ++c) {
+      num += s_w[c] * pd[(size_t)c * (HD + 2)];
+      den += s_w[c] * s_l[c];
     }
   }
   const float v = den > 0.f ? num / den : 0.f;

@@ -17,10 +17,11 @@
 // device-side exit layer picks the path): four more warps dequantise each
 // 128 x 64 weight block, (q - z) * s rounded to bf16, straight into the
 // 128-byte-swizzled shared-memory layout the TMA would have written, and the
-// MMAs run as for the backbone's bf16 weights.  The dequantising warps, not
-// the quarter-size weight bytes, bound this path, so a W4 projection runs
-// here only when it has at least half as many output tiles as SMs
-// (tc_gemm_runs_w4); narrower ones stay on the dequantising GEMV.
+// MMAs run as for the backbone's bf16 weights.  At decode batch sizes the
+// MMA issue (about 150 cycles per 128 x N x 16 instruction for N <= 64)
+// bounds this path, not the quarter-size weight bytes; up to 32 tokens a
+// narrow W4 projection (fewer output tiles than half the SMs) runs faster on
+// the dequantising GEMV, which takes it (tc_gemm_runs_w4).
 //
 // When the output tiles are fewer than the SMs (a decode batch's narrow
 // projections), K is split: unit u = (tile, split), each split accumulates
@@ -233,6 +234,26 @@ __device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok,
 
 constexpr int kEpiWarps = 8;
 constexpr int kDqWarps = 4;  // W4 dequantising warps
+constexpr int kQSlot = 4096 + 512;  // one W4 block staged: 128 rows x 32 bytes + 128 (scale, zero)
+// W4 layers: the token tiles keep all STAGES stages; the dequantised weight
+// tiles need only kNA (they are made on chip); the rest of the weight-tile
+// space stages kQD packed W4 blocks in flight
+template <int STAGES>
+constexpr int kNA = STAGES >= 8 ? 5 : (STAGES >= 6 ? 3 : 2);
+template <int STAGES>
+constexpr int kQD = (STAGES - kNA<STAGES>) * kABytes / kQSlot;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Persistent: CTA b takes tiles b, b + grid, ...; tile t covers weight rows
 // (t / tiles_m) * 128 .. +127 and tokens (t % tiles_m) * BN .. +BN-1, so the
@@ -254,8 +275,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
   unsigned char* sA = smem;
   unsigned char* sB = smem + STAGES * kABytes;
-  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], afull[STAGES], acc_full[2], acc_empty[2],
-      mma_done;
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], afull[STAGES], aempty[STAGES], acc_full[2],
+      acc_empty[2], mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ volatile int s_fail;
   __shared__ volatile int s_last;
@@ -275,6 +296,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       dev::mbar_init(&full[i], 1);
       dev::mbar_init(&empty[i], 1);
       dev::mbar_init(&afull[i], kDqWarps);
+      dev::mbar_init(&aempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       dev::mbar_init(&acc_full[i], 1);
@@ -337,20 +359,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint32_t d = tmem + (uint32_t)(acc * BN);
         const int kbs = kb0_of(uu);
         for (int kb = kbs; kb < kb1_of(uu); ++kb, ++g) {
-          const int s = g % STAGES;
+          const int s = g % STAGES, sa = w4 ? g % kNA<STAGES> : s;
           if (!dev::mbar_wait(&full[s], (g / STAGES) & 1, kSpinTc) ||
-              (w4 && !dev::mbar_wait(&afull[s], (g / STAGES) & 1, kSpinTc))) {
+              (w4 && !dev::mbar_wait(&afull[sa], (g / kNA<STAGES>) & 1, kSpinTc))) {
             s_fail = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_desc(smem_u32(sA + s * kABytes));
+          const uint64_t ad = sw128_desc(smem_u32(sA + sa * kABytes));
           const uint64_t bd = sw128_desc(smem_u32(sB + s * kBBytes));
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes = 2 in the address field
             mma_tc(d, ad + 2 * k, bd + 2 * k, idesc, (kb != kbs || k != 0) ? 1u : 0u);
           mma_commit(&empty[s]);
+          if (w4) mma_commit(&aempty[sa]);
         }
         mma_commit(&acc_full[acc]);
       }
@@ -360,51 +383,82 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   } else if (warp >= 2 + kEpiWarps) {
     // W4 dequantising warps: thread r writes weight row n0 + r of every 128 x 64
-    // block, 8 chunks of 8 bf16 at chunk position c ^ (r & 7) (128-byte swizzle)
+    // block, 8 chunks of 8 bf16 at chunk position c ^ (r & 7) (128-byte swizzle).
+    // Each thread copies its row's packed words (32 bytes) and (scale, zero)
+    // of the next kQD blocks into shared memory with cp.async, so kQD blocks
+    // (31 to 45 KB per CTA) are in flight.  A nibble q becomes the weight
+    // without an integer conversion: placed at bits 10..13 of 0x46000000 it
+    // is the float v = 8192 + q, and fma(v, s, c) with c = -(8192 + z) s
+    // rounded once gives (q - z) s within s 2^-10 (8192 + z is exact: z is an
+    // fp16 in [0, 16)).
     if (w4) {
+      unsigned char* sQ = sA + kNA<STAGES> * kABytes;
       const int r = threadIdx.x - (2 + kEpiWarps) * 32;
       const int wpr = a.Kp >> 3, gpr = a.Kp >> 7;
-      int g = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-        const int t = u / S;
-        const int R = (t / tiles_m) * kBM + r;
-        const bool row_ok = R < a.N;
-        const uint32_t* qrow = a.qw + (size_t)(row_ok ? R : 0) * wpr;
-        const __half2* zrow = a.sz + (size_t)(row_ok ? R : 0) * gpr;
-        for (int kb = kb0_of(u); kb < kb1_of(u); ++kb, ++g) {
-          const int s = g % STAGES, n = g / STAGES;
-          uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
-          float2 sz = make_float2(0.f, 0.f);
-          if (row_ok) {  // loads first, then the wait for the slot
-            w0 = __ldg(reinterpret_cast<const uint4*>(qrow + kb * 8));
-            w1 = __ldg(reinterpret_cast<const uint4*>(qrow + kb * 8 + 4));
-            sz = __half22float2(zrow[(kb * kBK) >> 7]);
+      int G = 0;  // k-blocks this CTA runs
+      for (int u = blockIdx.x; u < nunits; u += gridDim.x) G += kb1_of(u) - kb0_of(u);
+      int lu = blockIdx.x, lkb = lu < nunits ? kb0_of(lu) : 0, lj = 0;  // the next block to copy
+      // slot j: [two 16-byte halves][128 rows] of packed words, then [128 rows] of (scale, zero)
+      auto issue_next = [&]() {
+        if (lu < nunits) {
+          const int R = ((lu / S) / tiles_m) * kBM + r;
+          unsigned char* d = sQ + lj * kQSlot;
+          if (R < a.N) {
+            const uint32_t* src = a.qw + (size_t)R * wpr + lkb * 8;
+            cp_async16(smem_u32(d + r * 16), src);
+            cp_async16(smem_u32(d + 2048 + r * 16), src + 4);
+            cp_async4(smem_u32(d + 4096 + r * 4), a.sz + (size_t)R * gpr + ((lkb * kBK) >> 7));
+          } else {  // rows past N: zero weights (plain stores; the slot's last copies have landed)
+            *reinterpret_cast<uint4*>(d + r * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(d + 2048 + r * 16) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint32_t*>(d + 4096 + r * 4) = 0u;
           }
-          if (n > 0 && !dev::mbar_wait(&empty[s], (n - 1) & 1, kSpinTc)) {
-            s_fail = 1;
-            ok = false;
-            break;
+          if (++lkb == kb1_of(lu)) {
+            lu += gridDim.x;
+            if (lu < nunits) lkb = kb0_of(lu);
           }
-          unsigned char* dst = sA + s * kABytes + r * 128;
-          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {  // chunk c: inputs 8c .. 8c + 7 = the nibbles of word c
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float lo = ((float)((wv[c] >> (8 * e)) & 15u) - sz.y) * sz.x;
-              const float hi = ((float)((wv[c] >> (8 * e + 4)) & 15u) - sz.y) * sz.x;
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-              pk[e] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-            *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          }
-          dev::fence_proxy_async_smem();  // generic writes before the MMAs' reads
-          __syncwarp();
-          if ((threadIdx.x & 31) == 0) dev::mbar_arrive(&afull[s]);
         }
+        cp_async_commit();
+        if (++lj == kQD<STAGES>) lj = 0;
+      };
+      for (int j = 0; j < kQD<STAGES>; ++j) issue_next();
+      for (int g = 0; g < G; ++g) {
+        cp_async_wait<kQD<STAGES> - 1>();  // block g has landed
+        const unsigned char* qs = sQ + (g % kQD<STAGES>) * kQSlot;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(qs + r * 16);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(qs + 2048 + r * 16);
+        const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(qs + 4096 + r * 4));
+        issue_next();  // refill the slot just read
+        const int s = g % kNA<STAGES>, n = g / kNA<STAGES>;
+        const bool got = n == 0 || dev::mbar_wait(&aempty[s], (n - 1) & 1, kSpinTc);
+        if (!__all_sync(0xffffffffu, got)) {  // the same decision in every lane
+          s_fail = 1;
+          break;
+        }
+        unsigned char* dst = sA + s * kABytes + r * 128;
+        const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        const float sc = zs.x, c0 = -(8192.f + zs.y) * zs.x;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // chunk c: inputs 8c .. 8c + 7 = the nibbles of word c
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            // nibble 2e sits at bits 8e, nibble 2e + 1 at 8e + 4: move each to bit 10
+            const int sh0 = 8 * e - 10, sh1 = 8 * e - 6;
+            const uint32_t b0 = sh0 < 0 ? wv[c] << -sh0 : wv[c] >> sh0;
+            const uint32_t b1 = sh1 < 0 ? wv[c] << -sh1 : wv[c] >> sh1;
+            const float v0 = __uint_as_float((b0 & 0x3C00u) | 0x46000000u);
+            const float v1 = __uint_as_float((b1 & 0x3C00u) | 0x46000000u);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(fmaf(v0, sc, c0), fmaf(v1, sc, c0));
+            pk[e] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        dev::fence_proxy_async_smem();  // generic writes before the MMAs' reads
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) dev::mbar_arrive(&afull[s]);
       }
+      cp_async_wait<0>();  // no copy may land after the CTA has gone
     }
   } else {  // epilogue warps 2 .. 9: lane quarter warp % 4, column half (warp - 2) / 4
     const int q = warp & 3, h = (warp - 2) >> 2;
@@ -513,22 +567,43 @@ cudaError_t set_smem_attr() {
                               tc_smem_bytes<BN, STAGES>());
 }
 
+// K splits for a decode batch's projection (memory-bound: every unit streams
+// its 128 weight rows x its share of K): the split count whose makespan,
+// waves x (a unit's fixed cost + 1 / S of a whole tile's stream), is lowest.
+// The fixed cost (pipeline fill, partial tile store and reduction; about
+// 1.5 us) is taken relative to a tile's stream of 128 rows x K bf16 at about
+// 45 GB/s per SM.  At least 4 k-blocks per split; partial tiles within the
+// workspace; a split must gain 3 % over the next smaller one.
+int tc_pick_split(int tiles, int nk, int sm_count, size_t tile_floats, size_t ws_floats) {
+  const double fixed = 1.5e-6 * 45e9 / (128.0 * 64 * 2 * nk);
+  auto cost = [&](int S) {
+    const int waves = (tiles * S + sm_count - 1) / sm_count;
+    return waves * (fixed + 1.0 / S);
+  };
+  int best = 1;
+  double best_cost = cost(1);
+  for (int S = 2; S <= 32 && S <= nk / 4; ++S) {
+    if ((size_t)tiles * S * tile_floats > ws_floats) break;
+    const double c = cost(S);
+    if (c < 0.97 * best_cost) {
+      best = S;
+      best_cost = c;
+    }
+  }
+  return best;
+}
+
 template <int BN, int STAGES>
 cudaError_t launch_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s) {
   constexpr int smem = tc_smem_bytes<BN, STAGES>();
   CUtensorMap tmX;
   if (!make_tmap_bf16(&tmX, a.x, a.Kp, a.B, a.ldx, BN)) return cudaErrorInvalidValue;
   const int tiles = ((a.N + kBM - 1) / kBM) * ((a.B + BN - 1) / BN);
-  // split K when the output tiles would leave SMs idle (decode batches): at
-  // least 4 k-blocks per split, partial tiles within the workspace
   GemvArgs b = a;
-  int S = 1;
-  if (a.tc_ws != nullptr && BN <= 64 && tiles < sm_count && tiles <= a.tc_ticket_n) {
-    S = std::min((sm_count + tiles - 1) / tiles, (a.Kp / kBK) / 4);
-    while (S > 1 && (size_t)tiles * S * BN * kBM > a.tc_ws_floats) --S;
-    if (S < 1) S = 1;
-  }
-  b.ksplit = S;
+  b.ksplit = BN <= 64 && a.tc_ws != nullptr && tiles <= a.tc_ticket_n
+                 ? tc_pick_split(tiles, a.Kp / kBK, sm_count, (size_t)BN * kBM, a.tc_ws_floats)
+                 : 1;
+  const int S = b.ksplit;
   int grid = tiles * S;
   if (grid > sm_count) grid = sm_count;
   k_gemm_tc<BN, STAGES><<<grid, kThreadsTc, smem, s>>>(tmW, tmX, b);
@@ -588,6 +663,9 @@ bool make_weight_tmap(CUtensorMap* map, const bf16* w, int N, int Kp) {
 // Token tile: the width whose estimated makespan (tiles per CTA x the tile's
 // time, from the MMA efficiency measured per width on GB300) is smallest.
 int tc_pick_bn(int N, int M, int sm_count) {
+  // a decode batch: one token tile (split K fills the SMs), since an MMA of
+  // 128 x 32 x 16 costs about as long as one of 128 x 64 x 16
+  if (M <= 64) return M <= 32 ? 32 : 64;
   static const int widths[4] = {256, 128, 64, 32};
   static const float eff[4] = {1.0f, 0.65f, 0.35f, 0.2f};
   const int tn = (N + kBM - 1) / kBM;
@@ -607,6 +685,7 @@ int tc_pick_bn(int N, int M, int sm_count) {
 }
 
 bool tc_gemm_runs_w4(int N, int B, int sm_count) {
+  if (B > kTcW4AllTokens) return true;
   const int bn = tc_pick_bn(N, B, sm_count);
   const int tiles = ((N + kBM - 1) / kBM) * ((B + bn - 1) / bn);
   return 2 * tiles >= sm_count;

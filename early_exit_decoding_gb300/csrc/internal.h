@@ -94,8 +94,11 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int
 bool make_weight_tmap(CUtensorMap* map, const bf16* w, int N, int Kp);
 int tc_pick_bn(int N, int M, int sm_count);
 cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s);
-// Whether the tensor-core GEMM should also run a W4 layer of this shape (enough
-// output tiles that its dequantising warps are not the bottleneck).
+// Whether the tensor-core GEMM also runs a W4 layer of this shape: always
+// above kTcW4AllTokens tokens, else when the projection has at least half as
+// many output tiles as SMs (narrower ones run on the dequantising GEMV, which
+// needs the activations' per-group sums).
+constexpr int kTcW4AllTokens = 32;
 bool tc_gemm_runs_w4(int N, int B, int sm_count);
 // (cos, sin) of pos * inv_freq[i] for pos < Tmax, i < half: [Tmax][half].
 void launch_rope_table(const float* inv_freq, int half, int Tmax, float2* out, cudaStream_t s);

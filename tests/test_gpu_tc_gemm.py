@@ -71,9 +71,10 @@ def test_decode_batches_split_k_and_w4_on_tensor_cores(river, stream, B):
     """A wider model (d_model 1024, FFN 2816: 16 to 44 k-blocks of 64 inputs)
     whose projections at batch 16 / 40 have fewer 128-row tiles than SMs: the
     GEMM splits K across CTAs (partial tiles summed by the tile's last CTA) on
-    the bf16 backbone; at batch 40 the W4 gate/up projection (88 tiles of 32
-    columns) runs on the tensor cores too, dequantised in shared memory and
-    split in two, while the narrower W4 projections stay on the GEMV."""
+    the bf16 backbone; at batch 40 (one 64-column token tile) every W4
+    projection runs on the tensor cores too, dequantised in shared memory and
+    split, while at batch 16 the W4 projections (at most 44 tiles) stay on the
+    dequantising GEMV."""
     S = synth.scaled(TINY, d_model=1024, n_q_heads=8, n_kv_heads=2, ffn_dim=2816, n_layers=3,
                      vocab=512)
     with torch.cuda.stream(stream):
