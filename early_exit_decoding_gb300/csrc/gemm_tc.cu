@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~(uintptr_t)1023);
   unsigned char* sA = smem;
   unsigned char* sB = smem + STAGES * kABytes;
-  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], afull[STAGES], aempty[STAGES], acc_full[2],
-      acc_empty[2], mma_done;
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], afull[STAGES], acc_full[2], acc_empty[2],
+      mma_done;
   __shared__ uint32_t tmem_base;
   __shared__ volatile int s_fail;
   __shared__ volatile int s_last;
@@ -296,7 +296,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       dev::mbar_init(&full[i], 1);
       dev::mbar_init(&empty[i], 1);
       dev::mbar_init(&afull[i], kDqWarps);
-      dev::mbar_init(&aempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       dev::mbar_init(&acc_full[i], 1);
@@ -372,8 +371,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes = 2 in the address field
             mma_tc(d, ad + 2 * k, bd + 2 * k, idesc, (kb != kbs || k != 0) ? 1u : 0u);
-          mma_commit(&empty[s]);
-          if (w4) mma_commit(&aempty[sa]);
+          mma_commit(&empty[s]);  // also frees dequantised tile sa (W4)
         }
         mma_commit(&acc_full[acc]);
       }
@@ -429,8 +427,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const uint4 w1 = *reinterpret_cast<const uint4*>(qs + 2048 + r * 16);
         const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(qs + 4096 + r * 4));
         issue_next();  // refill the slot just read
-        const int s = g % kNA<STAGES>, n = g / kNA<STAGES>;
-        const bool got = n == 0 || dev::mbar_wait(&aempty[s], (n - 1) & 1, kSpinTc);
+        // tile s was last read by k-block g - kNA, whose MMAs completing
+        // completed a phase of that k-block's token-tile barrier empty[]
+        const int s = g % kNA<STAGES>, gp = g - kNA<STAGES>;
+        const bool got = gp < 0 || dev::mbar_wait(&empty[gp % STAGES], (gp / STAGES) & 1, kSpinTc);
         if (!__all_sync(0xffffffffu, got)) {  // the same decision in every lane
           s_fail = 1;
           break;
