@@ -96,31 +96,61 @@ __global__ void __launch_bounds__(kThreads) k_rownorm(RowNormArgs a) {
       }
       a.st->exit_layer = e_l;
     }
-  } else {
-    for (int k = tid; k < d; k += kThreads) hrow[k] = hout[k];
   }
-  __syncthreads();
-
   float ss_out = 0.f, dot = 0.f, ss_in = 0.f;
   const float* hin = a.h_in ? a.h_in + (size_t)r * d : nullptr;
-  for (int k = tid; k < d; k += kThreads) {
-    const float v = hrow[k];
-    ss_out += v * v;
-    if (hin) {
-      const float u = hin[k];
-      dot += u * v;
-      ss_in += u * u;
+  if (a.tokens != nullptr) {
+    __syncthreads();
+    for (int k = tid; k < d; k += kThreads) {
+      const float v = hrow[k];
+      ss_out += v * v;
+      if (hin) {
+        const float u = hin[k];
+        dot += u * v;
+        ss_in += u * u;
+      }
+    }
+  } else {
+    // one pass over the row (and the layer's input row), four values a load
+    const float4* h4 = reinterpret_cast<const float4*>(hout);
+    const float4* i4 = reinterpret_cast<const float4*>(hin);
+    float4* s4 = reinterpret_cast<float4*>(hrow);
+    for (int k = tid; k < d / 4; k += kThreads) {
+      const float4 v = h4[k];
+      s4[k] = v;
+      ss_out += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      if (hin) {
+        const float4 u = i4[k];
+        dot += u.x * v.x + u.y * v.y + u.z * v.z + u.w * v.w;
+        ss_in += u.x * u.x + u.y * u.y + u.z * u.z + u.w * u.w;
+      }
     }
   }
-  block_sum3(ss_out, dot, ss_in);
+  block_sum3(ss_out, dot, ss_in);  // its barriers also publish hrow
 
   if (a.g != nullptr) {
     const float den = sqrtf(ss_out / (float)d + a.eps);
     bf16* x = a.x + (size_t)r * a.ldx;
-    for (int k = tid; k < d; k += kThreads) {
-      const bf16 xb = __float2bfloat16_rn(hrow[k] / den * a.g[k]);
-      x[k] = xb;
-      hrow[k] = __bfloat162float(xb);  // keep the rounded value for the group sums
+    for (int k8 = tid; k8 < d / 8; k8 += kThreads) {
+      const float4 h0 = reinterpret_cast<const float4*>(hrow)[2 * k8];
+      const float4 h1 = reinterpret_cast<const float4*>(hrow)[2 * k8 + 1];
+      const float4 g0 = reinterpret_cast<const float4*>(a.g)[2 * k8];
+      const float4 g1 = reinterpret_cast<const float4*>(a.g)[2 * k8 + 1];
+      const __nv_bfloat162 b0 = __floats2bfloat162_rn(h0.x / den * g0.x, h0.y / den * g0.y);
+      const __nv_bfloat162 b1 = __floats2bfloat162_rn(h0.z / den * g0.z, h0.w / den * g0.w);
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(h1.x / den * g1.x, h1.y / den * g1.y);
+      const __nv_bfloat162 b3 = __floats2bfloat162_rn(h1.z / den * g1.z, h1.w / den * g1.w);
+      uint4 pk;
+      pk.x = *reinterpret_cast<const uint32_t*>(&b0);
+      pk.y = *reinterpret_cast<const uint32_t*>(&b1);
+      pk.z = *reinterpret_cast<const uint32_t*>(&b2);
+      pk.w = *reinterpret_cast<const uint32_t*>(&b3);
+      *reinterpret_cast<uint4*>(x + (size_t)k8 * 8) = pk;
+      // keep the rounded values for the group sums
+      const float2 f0 = __bfloat1622float2(b0), f1 = __bfloat1622float2(b1);
+      const float2 f2 = __bfloat1622float2(b2), f3 = __bfloat1622float2(b3);
+      reinterpret_cast<float4*>(hrow)[2 * k8] = make_float4(f0.x, f0.y, f1.x, f1.y);
+      reinterpret_cast<float4*>(hrow)[2 * k8 + 1] = make_float4(f2.x, f2.y, f3.x, f3.y);
     }
     __syncthreads();
     const int w = tid >> 5, l = tid & 31;
