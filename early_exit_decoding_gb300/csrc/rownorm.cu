@@ -242,12 +242,36 @@ __global__ void __launch_bounds__(1024) k_argmax(const float* __restrict__ logit
   const float* p = logits + (size_t)b * ld;
   float best = -FLT_MAX;
   int bi = 0x7fffffff;
-  for (int i = threadIdx.x; i < V; i += blockDim.x) {
-    const float v = p[i];
+  // four values a load, four loads in flight; each thread scans its indices
+  // in increasing order, so a tie keeps the smaller index (V % 4 == 0)
+  const float4* p4 = reinterpret_cast<const float4*>(p);
+  const int n4 = V >> 2, step = blockDim.x;
+  auto take = [&](float v, int i) {
     if (v > best || (v == best && i < bi)) {
       best = v;
       bi = i;
     }
+  };
+  int c = threadIdx.x;
+  for (; c + 3 * step < n4; c += 4 * step) {
+    float4 q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = p4[c + j * step];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = 4 * (c + j * step);
+      take(q[j].x, i);
+      take(q[j].y, i + 1);
+      take(q[j].z, i + 2);
+      take(q[j].w, i + 3);
+    }
+  }
+  for (; c < n4; c += step) {
+    const float4 q = p4[c];
+    take(q.x, 4 * c);
+    take(q.y, 4 * c + 1);
+    take(q.z, 4 * c + 2);
+    take(q.w, 4 * c + 3);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {

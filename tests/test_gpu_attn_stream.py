@@ -5,6 +5,7 @@ empty trailing chunks, and every query-heads-per-KV-head ratio it serves (1,
 2 and 4) at head dims 64 and 128 (River-LLM explainer, section 三: every
 layer reads the backbone's own K/V slots, which the exit layers also write).
 """
+import numpy as np
 import pytest
 
 import synth
@@ -54,3 +55,7 @@ def test_streaming_attention_long_contexts(river, stream, d_model, hq, hkv, B, T
     res, _ = _run_sequence(river, m, om, stream, _forced(river, sched), B=B, prompt=T,
                            steps=len(sched) - 1, seed=70 + B, path="generic", max_seq=T + 20)
     assert [int(o["exit_layer"].item()) for o, _ in res] == sched
+    # the greedy token is the first maximum of the GPU's own logits, every row
+    for o, _ in res[1:]:
+        lg = o["logits"].float().cpu().numpy()
+        assert np.array_equal(o["next_token"].cpu().numpy(), lg.argmax(-1))
