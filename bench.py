@@ -138,6 +138,20 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def max_over_ranks(x, device):
+    """The slowest rank's time: replicas are timed together and the job's
+    throughput divides every rank's units by it (NCCL on GPUs, gloo on CPU)."""
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, seconds):
+    """Whole-job units per second: every rank processed units_per_rank."""
+    return world * units_per_rank / seconds
+
+
 # ---------------------------------------------------------------------- the library arm
 
 def run_river(args, rank, world, dev):
@@ -227,9 +241,7 @@ def run_river(args, rank, world, dev):
             kv.sync(stream)
         ms = e0.elapsed_time(e1)
         if world > 1:
-            t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
+            ms = max_over_ranks(ms, "cuda")
         return ms, ck, resets
 
     forced = river.Policy.forced(sched)
@@ -288,9 +300,7 @@ def run_river(args, rank, world, dev):
                                       None, stream)
         e2e_s = time.perf_counter() - t1
     if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+        e2e_s = max_over_ranks(e2e_s, "cuda")
     res["e2e"] = (Ke, e2e_s)
     res["prof"] = prof_rows
     res["kernels_per_step"] = model.kernel_count(B)
@@ -446,7 +456,7 @@ def main():
     res = run_river(args, rank, world, dev)
     K = args.steps
     ms_step = res["ms_forced"] / K
-    tok_s = world * B * K / (res["ms_forced"] / 1e3)
+    tok_s = job_throughput(B * K, world, res["ms_forced"] / 1e3)
     full_ms_step = res["ms_full"] / K
 
     # algorithmic bytes of the timed steps: the schedule's exit layers, positions T..T+G-1
