@@ -394,13 +394,31 @@ def threads_used():
     return os.cpu_count()
 
 
-def cpu_baseline(args):
+def oracle_sample(args):
+    """Oracle decode tokens/s over a bounded sample (15 s) of the workload."""
     om, st, sched, dec, OPolicy, dims = oracle_setup(args)
     S, B, T, G = dims
     n, t = run_oracle_steps(om, st, sched, dec, OPolicy, dims, 64, 15.0)
-    return {"value": n * B / t, "unit": "tokens/s", "cores": threads_used(), "kind": "oracle",
-            "sample": f"{n} decode steps of the same workload (after the full {T}-token prefill, "
-                      f"untimed), NumPy fp32 oracle on the host CPU"}
+    return n, B, T, t
+
+
+def cpu_baseline(args):
+    n, B, T, t = oracle_sample(args)
+    out = {"value": n * B / t, "unit": "tokens/s", "cores": threads_used(), "kind": "oracle",
+           "sample": f"{n} decode steps of the same workload (after the full {T}-token prefill, "
+                     f"untimed), NumPy fp32 oracle on the host CPU"}
+    # the same sample on one core, in a fresh process whose BLAS uses one thread
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--config", args.config,
+                            "--oracle-sample-only"], env=env, capture_output=True, text=True,
+                           timeout=600)
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        out["one_core"] = {"value": one["value"], "unit": "tokens/s", "cores": 1,
+                           "sample": f"{one['steps']} decode steps, the same sample on one core"}
+    except Exception as ex:  # reported, never required
+        out["one_core"] = {"value": None, "unit": "tokens/s", "cores": 1, "sample": f"failed: {ex!r}"}
+    return out
 
 
 def main():
@@ -411,6 +429,7 @@ def main():
     ap.add_argument("--impl", default="river", choices=("river", "reference"))
     ap.add_argument("--config", default="1b-b1", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: the config's shape cut to this many layers (a small "
                          "case for detailed ncu captures); the bench line names it")
@@ -424,6 +443,11 @@ def main():
     import synth
     S = shape_of(shape_name, args)
     hbm_peak, peak_src = load_peaks()
+
+    if args.oracle_sample_only:  # cpu_baseline's one-core leg (a child process, no GPU)
+        n, B, T, t = oracle_sample(args)
+        print(json.dumps({"value": n * B / t, "steps": n, "seconds": t, "cores": threads_used()}))
+        return
 
     if args.impl == "reference":
         # The reference arm is the oracle, timed as it stands on the host cores.
