@@ -169,8 +169,9 @@ RL_API rl_status rl_kv_set_trace(rl_kv* kv, float* d_hidden);
 /* Which kernels run a decode step.  RL_PATH_STEP: one persistent cooperative
  * kernel per step (batch <= 8, shapes whose activations and weight ring fit in
  * shared memory, GQA ratio 1, 2 or 4, head_dim 64 or 128); RL_PATH_FUSED: five
- * launches per layer plus the LM head (batch <= 8); RL_PATH_GENERIC: ten
- * launches per layer, any batch.  RL_PATH_AUTO (default) takes the first that
+ * launches per layer plus the LM head (batch <= 8); RL_PATH_GENERIC: eight
+ * to eleven launches per layer (tensor-core GEMMs from 16 tokens, streaming
+ * attention), any batch.  RL_PATH_AUTO (default) takes the first that
  * fits, in that order.  A forced path that does not fit a call's batch makes
  * that rl_decode_step return RL_ERR_UNSUPPORTED.  The math is the same on
  * every path (explainer sections 三, 四); they differ in rounding order only. */
