@@ -144,7 +144,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_fused(FusedArgs a) {
   const int G = a.Kp >> 7;
   const int UPT = (a.Kp + KU - 1) / KU;  // units per 16-row tile
   const int ntiles = a.N >> 4;
-  const long long U = (long long)ntiles * UPT;
   const int grid = gridDim.x, cta = blockIdx.x;
   // Whole 16-row tiles per CTA, spread evenly: no tile is shared between CTAs,
   // so no tile ever needs a cross-CTA merge (the stream-K merge below then
