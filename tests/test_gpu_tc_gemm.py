@@ -85,6 +85,18 @@ def test_decode_batches_split_k_and_w4_on_tensor_cores(river, stream, B):
     assert [int(o["exit_layer"].item()) for o, _ in res] == sched
 
 
+@pytest.mark.parametrize("tau", [0.3, 0.7])
+def test_decode_batch40_tau_decided_on_device(river, tiny, stream, tau):
+    """Batch 40 under tau (section 四, batch minimum): the GEMM reads the exit
+    layer the previous layer end decided on the device and runs the bf16 or
+    the W4 weights accordingly (above 32 tokens every W4 projection is on the
+    tensor cores and no group sums are launched)."""
+    m, om, _ = tiny
+    pol = [(river.Policy.tau_(tau), OPolicy.tau_(tau))] * 4
+    _run_sequence(river, m, om, stream, pol, B=40, prompt=9, steps=3, seed=80 + int(10 * tau),
+                  path="generic")
+
+
 @pytest.mark.parametrize("e_pre", [0, 1, 3])
 def test_prefill_exit_runs_later_layers_on_w4(river, tiny, stream, e_pre):
     """A forced prefill exit at e: layers <= e on the tensor cores, layers > e
