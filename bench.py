@@ -249,6 +249,10 @@ def run_river(args, rank, world, dev):
     ms_forced, clocks, resets = timed(forced, K, W, flush_clocks=True)
     res = {"ms_forced": ms_forced, "clocks": clocks, "resets": resets}
     res["ms_full"], _, _ = timed(river.Policy.tau_(1.01), K, W)
+    # every layer on its W4 exit copy (exit layer 0): the pages' full-quantisation comparison point
+    sched0 = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    res["ms_w4"], _, _ = timed(river.Policy.forced(sched0), min(K, 4 * G), W)
+    res["ms_w4"] /= min(K, 4 * G)
     res["tau"] = {}
     for tau in taus:
         ms_t, _, _ = timed(river.Policy.tau_(tau), min(K, 4 * G), W)
@@ -564,6 +568,8 @@ def main():
             "no_exit": {"tokens_per_s": world * B / (full_ms_step / 1e3), "ms_per_step": full_ms_step,
                         "hbm_frac": full_gbs / hbm_peak},
             "forced_over_no_exit": full_ms_step / ms_step,
+            "all_w4": {"tokens_per_s": world * B / (res["ms_w4"] / 1e3), "ms_per_step": res["ms_w4"],
+                       "over_no_exit": full_ms_step / res["ms_w4"]},
             **{f"tau_{t}": {"tokens_per_s": world * B / (v[0] / 1e3), "ms_per_step": v[0],
                             "mean_exit_layer": v[1]} for t, v in res["tau"].items()},
         },

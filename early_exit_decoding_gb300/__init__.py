@@ -29,7 +29,7 @@ EXPORTS = (
     "rl_kv_view", "rl_kv_position", "rl_kv_set_position", "rl_kv_set_trace", "rl_prefill",
     "rl_decode_step", "rl_decode_step_host", "rl_sync", "rl_decode_kernel_count",
     "rl_kv_set_profiling", "rl_kv_profile", "rl_kv_timeline", "rl_lm_head_static", "rl_kv_set_decode_path",
-    "rl_kv_decode_path",
+    "rl_kv_decode_path", "rl_save_exit_layers", "rl_load_exit_layers",
 )
 RL_PATH_AUTO, RL_PATH_STEP, RL_PATH_FUSED, RL_PATH_GENERIC = range(4)
 KERNEL_KINDS = ("embed", "qkv", "attention", "group_sums", "o_proj", "norm", "gate_up", "down",
@@ -96,6 +96,8 @@ def _load():
         "rl_lm_head_static": (I, [P, P, I, P, P, P, P]),
         "rl_kv_set_decode_path": (I, [P, I]),
         "rl_kv_decode_path": (I, [P, I]),
+        "rl_save_exit_layers": (I, [P, ctypes.c_char_p]),
+        "rl_load_exit_layers": (I, [P, ctypes.c_char_p, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -146,6 +148,14 @@ def rl_model_destroy(model):
 
 def rl_quantize_exit_layers(model, stream=None):
     _check(_lib.rl_quantize_exit_layers(model, _stream(stream)))
+
+
+def rl_save_exit_layers(model, path):
+    _check(_lib.rl_save_exit_layers(model, os.fsencode(path)))
+
+
+def rl_load_exit_layers(model, path, stream=None):
+    _check(_lib.rl_load_exit_layers(model, os.fsencode(path), _stream(stream)))
 
 
 def rl_exit_layer_view(model, layer, which):
@@ -331,6 +341,14 @@ class Model:
 
     def quantize_exit_layers(self, stream=None):
         rl_quantize_exit_layers(self.handle, stream)
+
+    def save_exit_layers(self, path):
+        """Write the exit river (published packing) to ``path``."""
+        rl_save_exit_layers(self.handle, path)
+
+    def load_exit_layers(self, path, stream=None):
+        """Build the exit river from a file written by save_exit_layers."""
+        rl_load_exit_layers(self.handle, path, stream)
 
     def exit_layer_view(self, layer, which):
         """(qweight int32 [N][K/8], scales fp16 [N][G], zeros fp16 [N][G]) torch views."""

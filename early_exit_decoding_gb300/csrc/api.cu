@@ -1343,12 +1343,16 @@ rl_status rl_model_create(const rl_config* cfg, const rl_weights* wts, rl_stream
 
 void rl_model_destroy(rl_model* m) { delete m; }
 
-rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream) {
-  if (!m) return fail(RL_ERR_INVALID_ARG, "model is NULL");
-  if (m->quantized) return RL_OK;
-  cudaStream_t s = as_stream(stream);
+}  // extern "C"
+
+namespace {
+
+// Device storage of the exit river: the interchange views (original row
+// order) and, per fused matrix, the W4 layout; `fill` writes them (the
+// quantizer, or the views uploaded from a file), then the unit-tiled copies.
+template <typename Fill>
+rl_status build_exit_river(rl_model* m, cudaStream_t s, Fill fill) {
   const int L = m->L;
-  // interchange views, original row order
   m->views.assign((size_t)L * 7, NSView{});
   const int outs[7] = {m->Hq * m->hd, m->Hkv * m->hd, m->Hkv * m->hd, m->d, m->F, m->F, m->d};
   const int ins[7] = {m->d, m->d, m->d, m->Hq * m->hd, m->d, m->d, m->F};
@@ -1371,9 +1375,13 @@ rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream) {
     for (Linear* lin : lins) {
       RL_TRY(m->alloc(&lin->qw, (size_t)lin->N * (lin->Kp / 8)));
       RL_TRY(m->alloc(&lin->sz, (size_t)lin->N * (lin->Kp / kGroup)));
-      launch_quantize(lin->w, lin->N, lin->K, lin->Kp, lin->qw, lin->sz, lin->rowmap,
-                      m->d_views + (size_t)l * 7 + lin->view_base, s);
-      RL_LAUNCHED();
+    }
+  }
+  RL_TRY(fill());
+  for (int l = 0; l < L; ++l) {
+    Layer& ly = m->layers[l];
+    Linear* lins[4] = {&ly.qkv, &ly.o, &ly.gu, &ly.dn};
+    for (Linear* lin : lins) {
       RL_TRY(m->alloc(&lin->qwt, w4_tiled_bytes(lin->N, lin->Kp)));
       launch_w4_tile_layout(lin->qw, lin->sz, lin->N, lin->Kp, lin->qwt, s);
       RL_LAUNCHED();
@@ -1382,6 +1390,126 @@ rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream) {
   RL_CUDA(cudaStreamSynchronize(s));
   m->quantized = true;
   return RL_OK;
+}
+
+constexpr char kExitMagic[8] = {'R', 'L', 'W', '4', 'E', 'X', 'I', 'T'};
+constexpr uint32_t kExitVersion = 1;
+
+void exit_header(const rl_model* m, uint32_t (&h)[8]) {
+  const uint32_t v[8] = {kExitVersion, (uint32_t)m->L, (uint32_t)m->d, (uint32_t)m->Hq,
+                         (uint32_t)m->Hkv, (uint32_t)m->hd, (uint32_t)m->F, (uint32_t)kGroup};
+  for (int i = 0; i < 8; ++i) h[i] = v[i];
+}
+
+}  // namespace
+
+extern "C" {
+
+rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream) {
+  if (!m) return fail(RL_ERR_INVALID_ARG, "model is NULL");
+  if (m->quantized) return RL_OK;
+  cudaStream_t s = as_stream(stream);
+  return build_exit_river(m, s, [&]() -> rl_status {
+    for (int l = 0; l < m->L; ++l) {
+      Layer& ly = m->layers[l];
+      Linear* lins[4] = {&ly.qkv, &ly.o, &ly.gu, &ly.dn};
+      for (Linear* lin : lins) {
+        launch_quantize(lin->w, lin->N, lin->K, lin->Kp, lin->qw, lin->sz, lin->rowmap,
+                        m->d_views + (size_t)l * 7 + lin->view_base, s);
+        RL_LAUNCHED();
+      }
+    }
+    return RL_OK;
+  });
+}
+
+rl_status rl_save_exit_layers(const rl_model* m, const char* path) {
+  if (!m || !path) return fail(RL_ERR_INVALID_ARG, "NULL argument");
+  if (!m->quantized) return fail(RL_ERR_STATE, "exit river not built");
+  FILE* f = fopen(path, "wb");
+  if (!f) return fail(RL_ERR_INVALID_ARG, "cannot open %s for writing", path);
+  uint32_t h[8];
+  exit_header(m, h);
+  bool ok = fwrite(kExitMagic, 1, 8, f) == 8 && fwrite(h, 4, 8, f) == 8;
+  std::vector<uint32_t> q;
+  std::vector<uint16_t> sc, zr;
+  for (size_t i = 0; ok && i < m->views.size(); ++i) {
+    const NSView& v = m->views[i];
+    const size_t nq = (size_t)v.N * (v.K / 8), ng = (size_t)v.N * ((v.K + kGroup - 1) / kGroup);
+    q.resize(nq);
+    sc.resize(ng);
+    zr.resize(ng);
+    if (cudaMemcpy(q.data(), v.q, nq * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(sc.data(), v.s, ng * 2, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(zr.data(), v.z, ng * 2, cudaMemcpyDeviceToHost) != cudaSuccess) {
+      fclose(f);
+      return fail(RL_ERR_CUDA, "copying the exit river to the host failed");
+    }
+    const uint32_t nk[2] = {(uint32_t)v.N, (uint32_t)v.K};
+    ok = fwrite(nk, 4, 2, f) == 2 && fwrite(q.data(), 4, nq, f) == nq && fwrite(sc.data(), 2, ng, f) == ng &&
+         fwrite(zr.data(), 2, ng, f) == ng;
+  }
+  ok = (fclose(f) == 0) && ok;
+  if (!ok) return fail(RL_ERR_INVALID_ARG, "writing %s failed", path);
+  return RL_OK;
+}
+
+rl_status rl_load_exit_layers(rl_model* m, const char* path, rl_stream_t stream) {
+  if (!m || !path) return fail(RL_ERR_INVALID_ARG, "NULL argument");
+  if (m->quantized) return fail(RL_ERR_STATE, "exit river already built");
+  // read and check the whole file on the host first: a bad file leaves the model unchanged
+  FILE* f = fopen(path, "rb");
+  if (!f) return fail(RL_ERR_INVALID_ARG, "cannot open %s", path);
+  char magic[8];
+  uint32_t h[8], want[8];
+  exit_header(m, want);
+  bool ok = fread(magic, 1, 8, f) == 8 && memcmp(magic, kExitMagic, 8) == 0 && fread(h, 4, 8, f) == 8 &&
+            memcmp(h, want, sizeof(h)) == 0;
+  if (!ok) {
+    fclose(f);
+    return fail(RL_ERR_INVALID_ARG, "%s is not an exit river of this model's shape", path);
+  }
+  const int L = m->L;
+  const int outs[7] = {m->Hq * m->hd, m->Hkv * m->hd, m->Hkv * m->hd, m->d, m->F, m->F, m->d};
+  const int ins[7] = {m->d, m->d, m->d, m->Hq * m->hd, m->d, m->d, m->F};
+  std::vector<std::vector<uint32_t>> q((size_t)L * 7);
+  std::vector<std::vector<uint16_t>> sc((size_t)L * 7), zr((size_t)L * 7);
+  for (int i = 0; ok && i < L * 7; ++i) {
+    uint32_t nk[2];
+    const int N = outs[i % 7], K = ins[i % 7];
+    ok = fread(nk, 4, 2, f) == 2 && nk[0] == (uint32_t)N && nk[1] == (uint32_t)K;
+    if (!ok) break;
+    const size_t nq = (size_t)N * (K / 8), ng = (size_t)N * ((K + kGroup - 1) / kGroup);
+    q[i].resize(nq);
+    sc[i].resize(ng);
+    zr[i].resize(ng);
+    ok = fread(q[i].data(), 4, nq, f) == nq && fread(sc[i].data(), 2, ng, f) == ng &&
+         fread(zr[i].data(), 2, ng, f) == ng;
+  }
+  char extra;
+  ok = ok && fread(&extra, 1, 1, f) == 0;  // nothing may follow
+  fclose(f);
+  if (!ok) return fail(RL_ERR_INVALID_ARG, "%s is truncated or does not match the model", path);
+  cudaStream_t s = as_stream(stream);
+  return build_exit_river(m, s, [&]() -> rl_status {
+    for (int i = 0; i < L * 7; ++i) {
+      const NSView& v = m->views[i];
+      RL_CUDA(cudaMemcpyAsync(v.q, q[i].data(), q[i].size() * 4, cudaMemcpyHostToDevice, s));
+      RL_CUDA(cudaMemcpyAsync(v.s, sc[i].data(), sc[i].size() * 2, cudaMemcpyHostToDevice, s));
+      RL_CUDA(cudaMemcpyAsync(v.z, zr[i].data(), zr[i].size() * 2, cudaMemcpyHostToDevice, s));
+    }
+    for (int l = 0; l < L; ++l) {
+      Layer& ly = m->layers[l];
+      Linear* lins[4] = {&ly.qkv, &ly.o, &ly.gu, &ly.dn};
+      for (Linear* lin : lins) {
+        launch_w4_from_views(lin->N, lin->K, lin->Kp, lin->qw, lin->sz, lin->rowmap,
+                             m->d_views + (size_t)l * 7 + lin->view_base, s);
+        RL_LAUNCHED();
+      }
+    }
+    RL_CUDA(cudaStreamSynchronize(s));  // the host arrays are freed on return
+    return RL_OK;
+  });
 }
 
 rl_status rl_exit_layer_view(const rl_model* m, int32_t layer, int32_t which,

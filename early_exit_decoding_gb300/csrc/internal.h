@@ -246,6 +246,10 @@ struct NSView { uint32_t* q; uint16_t* s; uint16_t* z; int N; int K; };
 // views[rowmap[r].x] at row rowmap[r].y.
 void launch_quantize(const bf16* w, int N, int K, int Kp, uint32_t* qw, __half2* sz,
                      const int2* rowmap, const NSView* views, cudaStream_t s);
+// The internal W4 layout (qw, sz) of a fused matrix from interchange views
+// that already hold the exit layer (rl_load_exit_layers).
+void launch_w4_from_views(int N, int K, int Kp, uint32_t* qw, __half2* sz, const int2* rowmap,
+                          const NSView* views, cudaStream_t s);
 
 
 // ---------------------------------------------------------------------------

@@ -78,6 +78,23 @@ __global__ void k_quantize(const bf16* __restrict__ w, int N, int K, int Kp,
   }
 }
 
+// The internal W4 layout of one fused matrix from the interchange views (the
+// inverse of the view writes in k_quantize): row r from views[rowmap[r].x]
+// row rowmap[r].y, words past K/8 zero, (scale, zero) per group.
+__global__ void k_w4_from_views(int N, int K, int Kp, uint32_t* __restrict__ qw, __half2* __restrict__ sz,
+                                const int2* __restrict__ rowmap, const NSView* __restrict__ views) {
+  const int r = blockIdx.x;
+  if (r >= N) return;
+  const int2 m = rowmap[r];
+  const NSView v = views[m.x];
+  const int W = Kp / 8, Wv = K / 8, G = Kp / kGroup;
+  for (int wi = threadIdx.x; wi < W; wi += blockDim.x)
+    qw[(size_t)r * W + wi] = wi < Wv ? v.q[(size_t)m.y * Wv + wi] : 0u;
+  for (int gi = threadIdx.x; gi < G; gi += blockDim.x)
+    sz[(size_t)r * G + gi] = __halves2half2(__ushort_as_half(v.s[(size_t)m.y * G + gi]),
+                                            __ushort_as_half(v.z[(size_t)m.y * G + gi]));
+}
+
 }  // namespace
 
 void launch_quantize(const bf16* w, int N, int K, int Kp, uint32_t* qw, __half2* sz,
@@ -85,6 +102,11 @@ void launch_quantize(const bf16* w, int N, int K, int Kp, uint32_t* qw, __half2*
   const long long warps = (long long)N * (Kp / kGroup);
   const long long blocks = (warps * 32 + 255) / 256;
   k_quantize<<<(unsigned)blocks, 256, 0, s>>>(w, N, K, Kp, qw, sz, rowmap, views);
+}
+
+void launch_w4_from_views(int N, int K, int Kp, uint32_t* qw, __half2* sz, const int2* rowmap,
+                          const NSView* views, cudaStream_t s) {
+  if (N > 0) k_w4_from_views<<<N, 128, 0, s>>>(N, K, Kp, qw, sz, rowmap, views);
 }
 
 }  // namespace river

@@ -142,6 +142,22 @@ RL_API rl_status rl_exit_layer_view(const rl_model* m, int32_t layer, int32_t wh
                              const uint32_t** qweight, const uint16_t** scales,
                              const uint16_t** zeros, int32_t* n_rows, int32_t* n_cols);
 
+/* Save / load the exit river in the published packing (per layer and linear,
+ * in RL_WQ .. RL_WD order: qweight [N][K/8] u32, scales and zeros [N][G] fp16
+ * bits).  File: the 8 bytes "RLW4EXIT", u32 version (1), u32 n_layers,
+ * d_model, n_q_heads, n_kv_heads, head_dim, ffn_dim, group_size, then per
+ * (layer, linear) u32 N, u32 K and the three arrays; host byte order.
+ * rl_save_exit_layers needs a built exit river (RL_ERR_STATE otherwise) and
+ * returns when the file is written.  rl_load_exit_layers builds the exit
+ * river from such a file instead of rl_quantize_exit_layers (a model's exit
+ * river is built once: RL_ERR_STATE if it exists); a file that cannot be read
+ * or does not match the model's shape returns RL_ERR_INVALID_ARG and leaves
+ * the model unchanged.  It returns when the exit river is ready.  Not on the
+ * pages (section 三 builds exit layers in under a minute); it skips the
+ * quantizer for a model whose exit layers were already built. */
+RL_API rl_status rl_save_exit_layers(const rl_model* m, const char* path);
+RL_API rl_status rl_load_exit_layers(rl_model* m, const char* path, rl_stream_t stream);
+
 /* kv_cache_alloc: one shared cache per layer (explainer sections 三, 六: exit
  * and backbone layers use the same slots; no duplicate cache), bf16
  * K and V each [max_batch][n_kv_heads][max_seq][head_dim], plus the decode
