@@ -234,18 +234,16 @@ __device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok,
 
 constexpr int kEpiWarps = 8;
 constexpr int kDqWarps = 4;  // W4 dequantising warps
-constexpr int kQSlot = 4096 + 512;  // one W4 block staged: 128 rows x 32 bytes + 128 (scale, zero)
+constexpr int kQWBytes = 128 * 32;  // one W4 block's packed words: 128 rows x 8 words
 // W4 layers: the token tiles keep all STAGES stages; the dequantised weight
 // tiles need only kNA (they are made on chip); the rest of the weight-tile
-// space stages kQD packed W4 blocks in flight
+// space holds each stage's packed words and (scale, zero) pairs
 template <int STAGES>
 constexpr int kNA = STAGES >= 8 ? 5 : (STAGES >= 6 ? 3 : 2);
-template <int STAGES>
-constexpr int kQD = (STAGES - kNA<STAGES>) * kABytes / kQSlot;
+static_assert((8 - kNA<8>) * kABytes >= 8 * (kQWBytes + 512), "W4 staging must fit");
+static_assert((6 - kNA<6>) * kABytes >= 6 * (kQWBytes + 512), "W4 staging must fit");
+static_assert((4 - kNA<4>) * kABytes >= 4 * (kQWBytes + 512), "W4 staging must fit");
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -262,7 +260,7 @@ __device__ __forceinline__ void cp_async_wait() {
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-              const GemvArgs a) {
+              const __grid_constant__ CUtensorMap tmQ, const GemvArgs a) {
   constexpr int kBBytes = BN * kBK * 2;
   constexpr uint32_t kTmemCols = 2 * BN;
   bool w4 = a.w4_mode == W4_ON;
@@ -306,6 +304,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_map(&tmW);
     tma_prefetch_map(&tmX);
+    if (w4) tma_prefetch_map(&tmQ);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -333,8 +332,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             ok = false;
             break;
           }
-          dev::mbar_expect_tx(&full[s], (w4 ? 0 : kABytes) + kBBytes);
-          if (!w4) tma_load_2d(sA + s * kABytes, &tmW, kb * kBK, n0, &full[s]);
+          dev::mbar_expect_tx(&full[s], (w4 ? kQWBytes : kABytes) + kBBytes);
+          if (w4)  // the packed W4 words of the block (rows past N read as zeros)
+            tma_load_2d(sA + kNA<STAGES> * kABytes + s * kQWBytes, &tmQ, kb * 8, n0, &full[s]);
+          else
+            tma_load_2d(sA + s * kABytes, &tmW, kb * kBK, n0, &full[s]);
           tma_load_2d(sB + s * kBBytes, &tmX, kb * kBK, m0, &full[s]);
         }
       }
@@ -382,55 +384,50 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else if (warp >= 2 + kEpiWarps) {
     // W4 dequantising warps: thread r writes weight row n0 + r of every 128 x 64
     // block, 8 chunks of 8 bf16 at chunk position c ^ (r & 7) (128-byte swizzle).
-    // Each thread copies its row's packed words (32 bytes) and (scale, zero)
-    // of the next kQD blocks into shared memory with cp.async, so kQD blocks
-    // (31 to 45 KB per CTA) are in flight.  A nibble q becomes the weight
-    // without an integer conversion: placed at bits 10..13 of 0x46000000 it
-    // is the float v = 8192 + q, and fma(v, s, c) with c = -(8192 + z) s
-    // rounded once gives (q - z) s within s 2^-10 (8192 + z is exact: z is an
-    // fp16 in [0, 16)).
+    // The producer TMA-loads each block's packed words (128 rows x 32 bytes)
+    // into its stage with the token tile; each thread copies its row's
+    // (scale, zero) STAGES - 1 blocks ahead with cp.async.  A nibble q becomes
+    // the weight without an integer conversion: placed at bits 10..13 of
+    // 0x46000000 it is the float v = 8192 + q, and fma(v, s, c) with
+    // c = -(8192 + z) s rounded once gives (q - z) s within s 2^-10 (8192 + z
+    // is exact: z is an fp16 in [0, 16)).
     if (w4) {
-      unsigned char* sQ = sA + kNA<STAGES> * kABytes;
+      const unsigned char* sQw = sA + kNA<STAGES> * kABytes;     // [STAGES][128 rows][32 bytes]
+      unsigned char* sQz = sA + kNA<STAGES> * kABytes + STAGES * kQWBytes;  // [STAGES][128] (s, z)
       const int r = threadIdx.x - (2 + kEpiWarps) * 32;
-      const int wpr = a.Kp >> 3, gpr = a.Kp >> 7;
+      const int gpr = a.Kp >> 7;
       int G = 0;  // k-blocks this CTA runs
       for (int u = blockIdx.x; u < nunits; u += gridDim.x) G += kb1_of(u) - kb0_of(u);
-      int lu = blockIdx.x, lkb = lu < nunits ? kb0_of(lu) : 0, lj = 0;  // the next block to copy
-      // slot j: [two 16-byte halves][128 rows] of packed words, then [128 rows] of (scale, zero)
-      auto issue_next = [&]() {
+      int lu = blockIdx.x, lkb = lu < nunits ? kb0_of(lu) : 0, lb = 0;  // the next (scale, zero) to copy
+      auto issue_sz = [&]() {
         if (lu < nunits) {
           const int R = ((lu / S) / tiles_m) * kBM + r;
-          unsigned char* d = sQ + lj * kQSlot;
-          if (R < a.N) {
-            const uint32_t* src = a.qw + (size_t)R * wpr + lkb * 8;
-            cp_async16(smem_u32(d + r * 16), src);
-            cp_async16(smem_u32(d + 2048 + r * 16), src + 4);
-            cp_async4(smem_u32(d + 4096 + r * 4), a.sz + (size_t)R * gpr + ((lkb * kBK) >> 7));
-          } else {  // rows past N: zero weights (plain stores; the slot's last copies have landed)
-            *reinterpret_cast<uint4*>(d + r * 16) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(d + 2048 + r * 16) = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint32_t*>(d + 4096 + r * 4) = 0u;
-          }
+          unsigned char* d = sQz + (lb % STAGES) * 512 + r * 4;
+          if (R < a.N)
+            cp_async4(smem_u32(d), a.sz + (size_t)R * gpr + ((lkb * kBK) >> 7));
+          else
+            *reinterpret_cast<uint32_t*>(d) = 0u;
+          ++lb;
           if (++lkb == kb1_of(lu)) {
             lu += gridDim.x;
             if (lu < nunits) lkb = kb0_of(lu);
           }
         }
         cp_async_commit();
-        if (++lj == kQD<STAGES>) lj = 0;
       };
-      for (int j = 0; j < kQD<STAGES>; ++j) issue_next();
+      for (int j = 0; j + 1 < STAGES; ++j) issue_sz();
       for (int g = 0; g < G; ++g) {
-        cp_async_wait<kQD<STAGES> - 1>();  // block g has landed
-        const unsigned char* qs = sQ + (g % kQD<STAGES>) * kQSlot;
-        const uint4 w0 = *reinterpret_cast<const uint4*>(qs + r * 16);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(qs + 2048 + r * 16);
-        const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(qs + 4096 + r * 4));
-        issue_next();  // refill the slot just read
-        // tile s was last read by k-block g - kNA, whose MMAs completing
-        // completed a phase of that k-block's token-tile barrier empty[]
+        const int st = g % STAGES;
+        cp_async_wait<STAGES - 2>();  // block g's (scale, zero) has landed
+        const bool landed = dev::mbar_wait(&full[st], (g / STAGES) & 1, kSpinTc);  // its words too
+        const uint4 w0 = *reinterpret_cast<const uint4*>(sQw + st * kQWBytes + r * 32);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(sQw + st * kQWBytes + r * 32 + 16);
+        const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(sQz + st * 512 + r * 4));
+        issue_sz();  // block g + STAGES - 1, into the slot block g - 1 used
+        // tile s was last read by k-block gp, whose MMAs completing completed a
+        // phase of that k-block's token-tile barrier empty[]
         const int s = g % kNA<STAGES>, gp = g - kNA<STAGES>;
-        const bool got = gp < 0 || dev::mbar_wait(&empty[gp % STAGES], (gp / STAGES) & 1, kSpinTc);
+        const bool got = landed && (gp < 0 || dev::mbar_wait(&empty[gp % STAGES], (gp / STAGES) & 1, kSpinTc));
         if (!__all_sync(0xffffffffu, got)) {  // the same decision in every lane
           s_fail = 1;
           break;
@@ -594,7 +591,8 @@ int tc_pick_split(int tiles, int nk, int sm_count, size_t tile_floats, size_t ws
 }
 
 template <int BN, int STAGES>
-cudaError_t launch_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s) {
+cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap* tmQ, const GemvArgs& a, int sm_count,
+                      cudaStream_t s) {
   constexpr int smem = tc_smem_bytes<BN, STAGES>();
   CUtensorMap tmX;
   if (!make_tmap_bf16(&tmX, a.x, a.Kp, a.B, a.ldx, BN)) return cudaErrorInvalidValue;
@@ -606,7 +604,7 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, c
   const int S = b.ksplit;
   int grid = tiles * S;
   if (grid > sm_count) grid = sm_count;
-  k_gemm_tc<BN, STAGES><<<grid, kThreadsTc, smem, s>>>(tmW, tmX, b);
+  k_gemm_tc<BN, STAGES><<<grid, kThreadsTc, smem, s>>>(tmW, tmX, tmQ != nullptr ? *tmQ : tmW, b);
   return cudaGetLastError();
 }
 
@@ -656,6 +654,21 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Packed W4 words [N][Kp/8] uint32: boxes of 8 words (one 64-input k-block of
+// a row) x 128 rows, no swizzle.
+bool make_w4_tmap(CUtensorMap* map, const uint32_t* qw, int N, int Kp) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr || qw == nullptr || N <= 0 || Kp % kBK != 0 || (reinterpret_cast<uintptr_t>(qw) & 15) != 0)
+    return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)(Kp / 8), (cuuint64_t)N};
+  const cuuint64_t strides[1] = {(cuuint64_t)Kp / 2};
+  const cuuint32_t box[2] = {8, (cuuint32_t)kBM};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(qw), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_weight_tmap(CUtensorMap* map, const bf16* w, int N, int Kp) {
   return make_tmap_bf16(map, w, Kp, N, Kp, kBM);
 }
@@ -691,13 +704,14 @@ bool tc_gemm_runs_w4(int N, int B, int sm_count) {
   return 2 * tiles >= sm_count;
 }
 
-cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap* tmQ, const GemvArgs& a, int sm_count,
+                           cudaStream_t s) {
   if (a.B <= 0 || a.N <= 0) return cudaSuccess;
   switch (tc_pick_bn(a.N, a.B, sm_count)) {
-    case 256: return launch_tc<256, 4>(tmW, a, sm_count, s);
-    case 128: return launch_tc<128, 6>(tmW, a, sm_count, s);
-    case 64: return launch_tc<64, 8>(tmW, a, sm_count, s);
-    default: return launch_tc<32, 8>(tmW, a, sm_count, s);
+    case 256: return launch_tc<256, 4>(tmW, tmQ, a, sm_count, s);
+    case 128: return launch_tc<128, 6>(tmW, tmQ, a, sm_count, s);
+    case 64: return launch_tc<64, 8>(tmW, tmQ, a, sm_count, s);
+    default: return launch_tc<32, 8>(tmW, tmQ, a, sm_count, s);
   }
 }
 

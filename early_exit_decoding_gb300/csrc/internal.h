@@ -92,8 +92,11 @@ bool tc_gemm_available();
 cudaError_t tc_gemm_init();
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int ld, int box_rows);
 bool make_weight_tmap(CUtensorMap* map, const bf16* w, int N, int Kp);
+bool make_w4_tmap(CUtensorMap* map, const uint32_t* qw, int N, int Kp);
 int tc_pick_bn(int N, int M, int sm_count);
-cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s);
+// tmQ: the packed W4 words of the layer's exit copy (make_w4_tmap), or null.
+cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap* tmQ, const GemvArgs& a, int sm_count,
+                           cudaStream_t s);
 // Whether the tensor-core GEMM also runs a W4 layer of this shape: always
 // above kTcW4AllTokens tokens, else when the projection has at least half as
 // many output tiles as SMs (narrower ones run on the dequantising GEMV, which
