@@ -194,6 +194,36 @@ __device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok,
   const bool is_k = !is_q && rot;
   const int hk = is_q ? 0 : (is_k ? head_all - a.Hq : head_all - a.Hq - a.Hkv);
   bf16* cache = is_k ? a.kc : a.vc;
+  if (a.T_prefill <= 0) {
+    // decode: every column is at the same position, so its (cos, sin) is
+    // loaded once (not once per column behind the column's stores)
+    const int pos = __ldg(a.pos_ptr);
+    const bool in_cache = pos >= 0 && pos < a.Tmax;
+    float sn = 0.f, cs = 1.f;
+    if (rot) {
+      if (a.rope_cs != nullptr && in_cache) {
+        const float2 t = __ldg(a.rope_cs + (size_t)pos * half + dim0);
+        cs = t.x;
+        sn = t.y;
+      } else {
+        sincosf((float)pos * a.inv_freq[dim0], &sn, &cs);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j >= nc) break;
+      const int c = col0 + j;
+      float x = v[j];
+      if (rot) x = low ? x * cs - o[j] * sn : x * cs + o[j] * sn;
+      if (is_q)
+        a.q_out[(size_t)c * a.Hq * hd + head_all * hd + dim] = x;
+      else if (!in_cache)
+        atomicOr(a.err, RL_DEVERR_CAPACITY);
+      else
+        cache[(((size_t)c * a.Hkv + hk) * a.Tmax + pos) * hd + dim] = __float2bfloat16_rn(x);
+    }
+    return;
+  }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (j >= nc) break;
@@ -214,7 +244,7 @@ __device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok,
     if (rot) {
       float sn, cs;
       if (a.rope_cs != nullptr && in_cache) {
-        const float2 t = a.rope_cs[(size_t)pos * half + dim0];
+        const float2 t = __ldg(a.rope_cs + (size_t)pos * half + dim0);  // read-only: may run ahead of the stores
         cs = t.x;
         sn = t.y;
       } else {
