@@ -17,11 +17,13 @@
 // device-side exit layer picks the path): four more warps dequantise each
 // 128 x 64 weight block, (q - z) * s rounded to bf16, straight into the
 // 128-byte-swizzled shared-memory layout the TMA would have written, and the
-// MMAs run as for the backbone's bf16 weights.  At decode batch sizes the
-// MMA issue (about 150 cycles per 128 x N x 16 instruction for N <= 64)
-// bounds this path, not the quarter-size weight bytes; up to 32 tokens a
-// narrow W4 projection (fewer output tiles than half the SMs) runs faster on
-// the dequantising GEMV, which takes it (tc_gemm_runs_w4).
+// MMAs run as for the backbone's bf16 weights; the producer TMA-loads each
+// block's packed words (128 rows x 32 bytes) into the stage in place of the
+// bf16 tile.  At decode batch sizes a W4 k-block takes about twice a bf16 one
+// (the dequantised tile's hand-off to the MMAs, not the quarter-size weight
+// bytes, bounds it); up to 32 tokens a narrow W4 projection (fewer output
+// tiles than half the SMs) runs faster on the dequantising GEMV, which takes
+// it (tc_gemm_runs_w4).
 //
 // When the output tiles are fewer than the SMs (a decode batch's narrow
 // projections), K is split: unit u = (tile, split), each split accumulates
@@ -31,7 +33,7 @@
 //
 // Persistent CTAs (one per SM) walk the units; 448 threads: warp 0
 // lane 0 issues the TMA loads into a STAGES-deep ring of (128 x 64 weight
-// tile, BN x 64 token tile), warp 1 owns the tensor-memory allocation (two
+// tile or its packed W4 words, BN x 64 token tile), warp 1 owns the tensor-memory allocation (two
 // BN-column fp32 accumulators) and its lane 0 issues the MMAs, warps 2..9 run
 // the epilogue of one tile while the MMAs of the next fill the other
 // accumulator (warp w reads TMEM lanes 32 (w % 4) .. +31, one half of the
