@@ -462,6 +462,7 @@ constexpr int kCombBlk = 512;
 
 template <int HD>
 __global__ void __launch_bounds__(HD) k_attn_combine(AttnArgs a) {
+  pdl_wait();
   __shared__ float s_w[kCombBlk], s_l[kCombBlk];
   __shared__ float s_red[HD / 32];
   const int hq = blockIdx.x, row = blockIdx.y, dd = threadIdx.x;
@@ -546,9 +547,9 @@ cudaError_t launch_attention_fused(const AttnArgs& a, bool pdl, cudaStream_t s) 
 void launch_attention_combine(const AttnArgs& a, cudaStream_t s) {
   dim3 g2(a.Hq, a.nq);
   if (a.hd == 64)
-    k_attn_combine<64><<<g2, 64, 0, s>>>(a);
+    launch_pdl(k_attn_combine<64>, g2, dim3(64), 0, s, a);
   else
-    k_attn_combine<128><<<g2, 128, 0, s>>>(a);
+    launch_pdl(k_attn_combine<128>, g2, dim3(128), 0, s, a);
 }
 
 void launch_attention(const AttnArgs& a, cudaStream_t s) {

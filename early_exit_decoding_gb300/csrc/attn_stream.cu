@@ -38,6 +38,7 @@ constexpr long long kSpinS = 1LL << 22;
 
 template <int REP, int HDC>
 __global__ void __launch_bounds__(kThreadsS, 1) k_attn_stream(const __grid_constant__ AttnStreamArgs a) {
+  pdl_wait();
   constexpr bool TWO = HDC == 128;  // K and V rows in separate slots
   constexpr int WS = 2 + HDC;
   constexpr int SPI = TWO ? 2 : 1;  // slots per item
@@ -194,8 +195,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) k_attn_stream(const __grid_const
 
 template <int REP, int HDC>
 cudaError_t launch_one(const AttnStreamArgs& a, int grid, size_t smem, cudaStream_t s) {
-  k_attn_stream<REP, HDC><<<grid, kThreadsS, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_attn_stream<REP, HDC>, dim3(grid), dim3(kThreadsS), smem, s, a);
 }
 
 template <int REP, int HDC>

@@ -293,6 +293,7 @@ template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const __grid_constant__ CUtensorMap tmQ, const GemvArgs a) {
+  pdl_wait();
   constexpr int kBBytes = BN * kBK * 2;
   constexpr uint32_t kTmemCols = 2 * BN;
   bool w4 = a.w4_mode == W4_ON;
@@ -636,8 +637,8 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap* tmQ, const Gemv
   const int S = b.ksplit;
   int grid = tiles * S;
   if (grid > sm_count) grid = sm_count;
-  k_gemm_tc<BN, STAGES><<<grid, kThreadsTc, smem, s>>>(tmW, tmX, tmQ != nullptr ? *tmQ : tmW, b);
-  return cudaGetLastError();
+  return launch_pdl(k_gemm_tc<BN, STAGES>, dim3(grid), dim3(kThreadsTc), (size_t)smem, s, tmW, tmX,
+                    tmQ != nullptr ? *tmQ : tmW, b);
 }
 
 __global__ void k_rope_table(const float* inv_freq, int half, int n, float2* out) {

@@ -228,6 +228,7 @@ __device__ void epilogue(const GemvArgs& a, int rt, int cb, const float (*tile)[
 
 template <int NT>
 __global__ void __launch_bounds__(kWarps * 32) k_gemv(GemvArgs a) {
+  pdl_wait();
   __shared__ float4 red[kWarps][NT][32];
   __shared__ float tile[16][NT * 8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -275,13 +276,13 @@ void launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t s) {
   if (grid < 1) grid = 1;
   const int nt = (a.B + 7) / 8;
   if (nt <= 1)
-    k_gemv<1><<<grid, kWarps * 32, 0, s>>>(a);
+    launch_pdl(k_gemv<1>, dim3(grid), dim3(kWarps * 32), 0, s, a);
   else if (nt <= 2)
-    k_gemv<2><<<grid, kWarps * 32, 0, s>>>(a);
+    launch_pdl(k_gemv<2>, dim3(grid), dim3(kWarps * 32), 0, s, a);
   else if (nt <= 4)
-    k_gemv<4><<<grid, kWarps * 32, 0, s>>>(a);
+    launch_pdl(k_gemv<4>, dim3(grid), dim3(kWarps * 32), 0, s, a);
   else
-    k_gemv<8><<<grid, kWarps * 32, 0, s>>>(a);
+    launch_pdl(k_gemv<8>, dim3(grid), dim3(kWarps * 32), 0, s, a);
 }
 
 }  // namespace river

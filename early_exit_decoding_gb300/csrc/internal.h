@@ -12,6 +12,30 @@
 
 namespace river {
 
+// Programmatic dependent launch for the many-launch decode path: a kernel
+// launched with launch_pdl is set up while its predecessor in the stream
+// finishes and calls pdl_wait() (the predecessor has completed and its
+// writes are visible) before it reads anything; launched without the
+// attribute the wait is a no-op.  No kernel triggers its successor early:
+// an early trigger let the next kernel's CTAs hold SMs that the current
+// kernel's later waves needed, and the batch-32 step got slower.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 typedef __nv_bfloat16 bf16;
 
 constexpr int kGroup = 128;     // quantization group along K

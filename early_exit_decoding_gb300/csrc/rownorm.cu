@@ -64,6 +64,7 @@ __device__ __forceinline__ void block_sum3(float& a, float& b, float& c) {
 }
 
 __global__ void __launch_bounds__(kThreads) k_rownorm(RowNormArgs a) {
+  pdl_wait();
   extern __shared__ float hrow[];  // d fp32 values of this row
   __shared__ int s_last;
   const int r = blockIdx.x;
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kThreads) k_rownorm(RowNormArgs a) {
 
 __global__ void k_group_sums(const bf16* __restrict__ x, int ldx, int Kp, int B,
                              float* __restrict__ xsum, int ldxs) {
+  pdl_wait();
   const int G = Kp / kGroup;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int l = threadIdx.x & 31;
@@ -238,6 +240,7 @@ __global__ void k_group_sums(const bf16* __restrict__ x, int ldx, int Kp, int B,
 
 __global__ void __launch_bounds__(1024) k_argmax(const float* __restrict__ logits, int ld, int V,
                                                  int* __restrict__ out) {
+  pdl_wait();
   const int b = blockIdx.x;
   const float* p = logits + (size_t)b * ld;
   float best = -FLT_MAX;
@@ -324,18 +327,18 @@ __global__ void k_bf16_to_f32(const bf16* __restrict__ s, float* __restrict__ d,
 }  // namespace
 
 void launch_rownorm(const RowNormArgs& a, cudaStream_t s) {
-  k_rownorm<<<a.rows, kThreads, a.d * sizeof(float), s>>>(a);
+  launch_pdl(k_rownorm, dim3(a.rows), dim3(kThreads), a.d * sizeof(float), s, a);
 }
 
 void launch_group_sums(const bf16* x, int ldx, int Kp, int B, float* xsum, int ldxs,
                        cudaStream_t s) {
   const int warps = B * (Kp / kGroup);
   const int blocks = (warps * 32 + 255) / 256;
-  k_group_sums<<<blocks, 256, 0, s>>>(x, ldx, Kp, B, xsum, ldxs);
+  launch_pdl(k_group_sums, dim3(blocks), dim3(256), 0, s, x, ldx, Kp, B, xsum, ldxs);
 }
 
 void launch_argmax(const float* logits, int ld, int V, int B, int* out, cudaStream_t s) {
-  k_argmax<<<B, 1024, 0, s>>>(logits, ld, V, out);
+  launch_pdl(k_argmax, dim3(B), dim3(1024), 0, s, logits, ld, V, out);
 }
 
 void launch_gather_rows(bf16* dst, int ldd, int N, int K, const int2* rowmap, GatherSrcs srcs,
