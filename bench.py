@@ -26,6 +26,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -99,10 +100,9 @@ class Clocks:
 
     def __init__(self, dev_id):
         self.proc = None
-        self.out = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
         try:
-            os.makedirs(os.path.dirname(self.out), exist_ok=True)
-            self.f = open(self.out, "w")
+            fd, self.out = tempfile.mkstemp(prefix="river_clocks_", suffix=".csv")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", dev_id, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
                  "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
@@ -119,7 +119,10 @@ class Clocks:
             self.proc.kill()
         self.f.close()
         rows = []
-        for line in open(self.out):
+        with open(self.out) as f:
+            lines = f.read().splitlines()
+        os.unlink(self.out)
+        for line in lines:
             p = [x.strip() for x in line.split(",")]
             if len(p) >= 8:
                 try:
@@ -154,164 +157,303 @@ def job_throughput(units_per_rank, world, seconds):
 
 # ---------------------------------------------------------------------- the library arm
 
-def run_river(args, rank, world, dev):
-    import torch
-    import synth
-    import early_exit_decoding_gb300 as river
+def gen_index(i, K, G):
+    """Generation index of timed step i: an even subsample of the G-step
+    generation when K < G (so any K sees the schedule's mix), else a cycle
+    through it."""
+    return (i * G) // K if K < G else i % G
 
-    shape_name, B, T, G, mean, taus, kvfill = CONFIGS[args.config]
-    S = shape_of(shape_name, args)
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.Stream()
-    t0 = time.time()
-    w = synth.gen_weights(S, seed=0, device="cuda", gains="ones")
-    with torch.cuda.stream(stream):
-        model = river.Model(S, w, stream)
-        model.quantize_exit_layers(stream)
-    stream.synchronize()
-    del w
-    torch.cuda.empty_cache()
-    max_seq = T + G + 1
-    kv = model.kv_cache_alloc(B, max_seq)
-    sched_np = synth.gen_schedule(S.n_layers, G, mean, seed=2)
-    sched = torch.from_numpy(sched_np).cuda()
-    prompt = torch.from_numpy(synth.gen_tokens(S.vocab, (B, T), seed=1)).cuda()
-    dec_tokens = torch.from_numpy(synth.gen_tokens(S.vocab, (G, B), seed=4)).cuda()
-    out = {"logits": torch.empty((B, S.vocab), dtype=torch.float32, device="cuda"),
-           "next_token": torch.empty((B,), dtype=torch.int32, device="cuda"),
-           "exit_layer": torch.empty((1,), dtype=torch.int32, device="cuda"),
-           "min_cos": torch.empty((S.n_layers,), dtype=torch.float32, device="cuda")}
-    with torch.cuda.stream(stream):
-        if kvfill == "prefill":
-            river.prefill(model, kv, prompt, river.Policy.tau_(1.01), out=out, stream=stream)
-        else:  # timing-only fill of the cache at the target context
-            for l in range(S.n_layers):
-                k, v = kv.view(l)
-                k[:B, :, :T].normal_()
-                v[:B, :, :T].normal_()
-            kv.set_position(T, 0, stream)
-        kv.sync(stream)
-    log(f"[rank {rank}] setup {time.time() - t0:.1f}s ({S.name}, B={B}, prompt {T})")
 
-    tok_slices = [dec_tokens[i].contiguous() for i in range(G)]
-    state = {"i": 0}
+def schedule_stats(sched, idx, L):
+    """Mean exit layer and full-depth share of the schedule entries ``idx``."""
+    e = [int(sched[j]) for j in idx]
+    return {"mean_exit_layer": sum(e) / len(e), "full_depth_share": sum(x == L for x in e) / len(e),
+            "steps": len(e)}
 
-    def one_step(policy):
-        i = state["i"]
-        if i % G == 0 and i > 0:
-            kv.set_position(T, 0, stream)
-        river.decode_step(model, kv, tok_slices[i % G], policy, out=out, stream=stream)
-        state["i"] = i + 1
 
-    def timed(policy, K, W, flush_clocks=None):
-        state["i"] = 0
-        kv.set_position(T, 0, stream)
-        # the clock sampler starts before the warm-up, which runs at least W
-        # steps and at least half a second, so that neither the sampler's
-        # start-up nor a GPU still leaving idle clocks falls in the timed region
-        clocks = Clocks(args.smi_id) if flush_clocks else None
+class Arm:
+    """One model + KV cache of a configuration, with the step driver the
+    timed passes share."""
+
+    def __init__(self, args, cfg, rank, world):
+        import torch
+        import synth
+        import early_exit_decoding_gb300 as river
+        self.torch, self.river = torch, river
+        shape_name, B, T, G, mean, taus, kvfill = CONFIGS[cfg]
+        S = shape_of(shape_name, args)
+        self.S, self.B, self.T, self.G, self.mean, self.taus = S, B, T, G, mean, taus
+        self.world = world
+        self.stream = stream = torch.cuda.Stream()
+        t0 = time.time()
+        w = synth.gen_weights(S, seed=0, device="cuda", gains="ones")
         with torch.cuda.stream(stream):
-            t_w = time.time()
-            n_w = 0
+            self.model = river.Model(S, w, stream)
+            self.model.quantize_exit_layers(stream)
+        stream.synchronize()
+        del w
+        torch.cuda.empty_cache()
+        self.kv = kv = self.model.kv_cache_alloc(B, T + G + 1)
+        self.sched_np = synth.gen_schedule(S.n_layers, G, mean, seed=2)
+        self.sched = torch.from_numpy(self.sched_np).cuda()
+        prompt = torch.from_numpy(synth.gen_tokens(S.vocab, (B, T), seed=1)).cuda()
+        self.dec_np = synth.gen_tokens(S.vocab, (G, B), seed=4)
+        dec = torch.from_numpy(self.dec_np).cuda()
+        self.out = {"logits": torch.empty((B, S.vocab), dtype=torch.float32, device="cuda"),
+                    "next_token": torch.empty((B,), dtype=torch.int32, device="cuda"),
+                    "exit_layer": torch.empty((1,), dtype=torch.int32, device="cuda"),
+                    "min_cos": torch.empty((S.n_layers,), dtype=torch.float32, device="cuda")}
+        with torch.cuda.stream(stream):
+            if kvfill == "prefill":
+                river.prefill(self.model, kv, prompt, river.Policy.tau_(1.01), out=self.out,
+                              stream=stream)
+            else:  # timing-only fill of the cache at the target context
+                for l in range(S.n_layers):
+                    k, v = kv.view(l)
+                    k[:B, :, :T].normal_()
+                    v[:B, :, :T].normal_()
+                kv.set_position(T, 0, stream)
+            kv.sync(stream)
+        self.tok = [dec[i].contiguous() for i in range(G)]
+        self.cur = None  # generation index the cache position stands at
+        self.repositions = 0
+        self.forced = river.Policy.forced(self.sched)
+        log(f"[rank {rank}] setup {time.time() - t0:.1f}s ({S.name}, B={B}, prompt {T})")
+
+    def close(self):
+        self.kv.close()
+        self.model.close()
+        self.torch.cuda.synchronize()
+        self.torch.cuda.empty_cache()
+
+    def goto(self, j):
+        """Put the cache at generation index j (position T + j, decode step j),
+        unless the previous step left it there."""
+        if self.cur != j:
+            self.kv.set_position(self.T + j, j, self.stream)
+            self.repositions += 1
+        self.cur = j
+
+    def step(self, j, policy):
+        self.goto(j)
+        self.river.decode_step(self.model, self.kv, self.tok[j], policy, out=self.out,
+                               stream=self.stream)
+        self.cur = j + 1
+
+    def timed(self, policy, K, W, clocks_dev=None):
+        """W untimed warm-up steps, then K steps; generation index
+        gen_index(i, K, G) at position T + index.  Every step is bracketed by
+        its own pair of CUDA events on the launching stream; a reposition of
+        the cache between two steps falls outside them.  Returns (ms summed
+        over the K steps, clocks sampled during them, repositions)."""
+        torch, G = self.torch, self.G
+        clocks = Clocks(clocks_dev) if clocks_dev else None
+        with torch.cuda.stream(self.stream):
+            t_w, n_w = time.time(), 0
+            # the clock sampler starts before the warm-up, which runs at least
+            # W steps and half a second, so that neither the sampler's start-up
+            # nor a GPU leaving idle clocks falls in the timed region
             while n_w < W or time.time() - t_w < 0.5:
-                one_step(policy)
+                self.step(gen_index(n_w % K, K, G), policy)
                 n_w += 1
                 if n_w % 32 == 0:
-                    stream.synchronize()
-            state["i"] = 0
-            kv.set_position(T, 0, stream)
-            kv.sync(stream)
-            if world > 1:
+                    self.stream.synchronize()
+            self.kv.sync(self.stream)
+            if self.world > 1:
                 torch.distributed.barrier()
             torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            resets = 0
-            e0.record(stream)
-            for _ in range(K):
-                if state["i"] % G == 0 and state["i"] > 0:
-                    resets += 1
-                one_step(policy)
-            e1.record(stream)
-            e1.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)]
+            self.repositions = 0
+            for i in range(K):
+                j = gen_index(i, K, G)
+                self.goto(j)
+                ev[i][0].record(self.stream)
+                self.river.decode_step(self.model, self.kv, self.tok[j], policy, out=self.out,
+                                       stream=self.stream)
+                ev[i][1].record(self.stream)
+                self.cur = j + 1
+            ev[-1][1].synchronize()
             torch.cuda.synchronize()
-            if world > 1:
+            if self.world > 1:
                 torch.distributed.barrier()
             ck = clocks.stop() if clocks else None
-            kv.sync(stream)
-        ms = e0.elapsed_time(e1)
-        if world > 1:
+            self.kv.sync(self.stream)
+        ms = sum(a.elapsed_time(b) for a, b in ev)
+        if self.world > 1:
             ms = max_over_ranks(ms, "cuda")
-        return ms, ck, resets
+        return ms, ck, self.repositions
 
-    forced = river.Policy.forced(sched)
+    def timed_bytes(self, K, forced):
+        """Algorithmic bytes of the K timed steps (schedule exit layers or full depth)."""
+        S, G = self.S, self.G
+        tot = 0.0
+        for i in range(K):
+            j = gen_index(i, K, G)
+            e = int(self.sched_np[j]) if forced else S.n_layers
+            tot += step_bytes(S, self.B, e, self.T + j)
+        return tot
+
+    def profile(self, policy, n):
+        """Live per-kernel records of n decode steps (a separate pass)."""
+        river = self.river
+        rows = []
+        river.rl_kv_set_profiling(self.kv.handle, True)
+        with self.torch.cuda.stream(self.stream):
+            for i in range(n + 2):
+                self.step(i % self.G, policy)
+                r = river.rl_kv_profile(self.kv.handle, self.stream)
+                if i >= 2:
+                    rows.extend(r)
+        river.rl_kv_set_profiling(self.kv.handle, False)
+        return rows
+
+
+def run_river(args, rank, world, dev):
+    import torch
+    torch.cuda.set_device(dev)
+    arm = Arm(args, args.config, rank, world)
+    S, B, G = arm.S, arm.B, arm.G
+    river = arm.river
     K, W = args.steps, args.warmup
-    ms_forced, clocks, resets = timed(forced, K, W, flush_clocks=True)
-    res = {"ms_forced": ms_forced, "clocks": clocks, "resets": resets}
-    res["ms_full"], _, _ = timed(river.Policy.tau_(1.01), K, W)
+    res = {"arm": arm}
+    res["ms_forced"], res["clocks"], res["repos"] = arm.timed(arm.forced, K, W, args.smi_id)
+    res["ms_full"], _, _ = arm.timed(river.Policy.tau_(1.01), K, W)
     # every layer on its W4 exit copy (exit layer 0): the pages' full-quantisation comparison point
     sched0 = torch.zeros((1,), dtype=torch.int32, device="cuda")
-    res["ms_w4"], _, _ = timed(river.Policy.forced(sched0), min(K, 4 * G), W)
-    res["ms_w4"] /= min(K, 4 * G)
+    Kw = min(K, 4 * G)
+    res["ms_w4"] = arm.timed(river.Policy.forced(sched0), Kw, W)[0] / Kw
     res["tau"] = {}
-    for tau in taus:
-        ms_t, _, _ = timed(river.Policy.tau_(tau), min(K, 4 * G), W)
-        # exit layers of one pass through the generation
-        state["i"] = 0
-        kv.set_position(T, 0, stream)
+    for tau in arm.taus:
+        ms_t, _, _ = arm.timed(river.Policy.tau_(tau), Kw, W)
         exits = []
-        with torch.cuda.stream(stream):
-            for _ in range(min(G, 64)):
-                one_step(river.Policy.tau_(tau))
-                exits.append(int(out["exit_layer"].item()))
-        res["tau"][tau] = (ms_t / min(K, 4 * G), sum(exits) / len(exits))
+        with torch.cuda.stream(arm.stream):
+            for j in range(min(G, 64)):
+                arm.step(j, river.Policy.tau_(tau))
+                exits.append(int(arm.out["exit_layer"].item()))
+        res["tau"][tau] = (ms_t / Kw, sum(exits) / len(exits))
+    res["prof"] = arm.profile(arm.forced, min(G, 64))
 
-    # live per-kernel timing inside the graph (separate pass)
-    prof_rows = []
-    river.rl_kv_set_profiling(kv.handle, True)
-    state["i"] = 0
-    kv.set_position(T, 0, stream)
-    with torch.cuda.stream(stream):
-        for i in range(min(G, 64) + 2):
-            one_step(forced)
-            rows = river.rl_kv_profile(kv.handle, stream)
-            if i >= 2:
-                prof_rows.extend(rows)
-    river.rl_kv_set_profiling(kv.handle, False)
-
-    # end to end: host buffers through rl_decode_step_host, copies inside the timed region
-    import numpy as np
+    # end to end: host buffers through rl_decode_step_host (pinned host tokens
+    # in; next tokens, exit layer and logits out), copies inside each call
     ht = torch.zeros((B,), dtype=torch.int32).pin_memory()
     hn = torch.zeros((B,), dtype=torch.int32).pin_memory()
     he = torch.zeros((1,), dtype=torch.int32).pin_memory()
-    host_tokens = dec_tokens.cpu().numpy()
+    hl = torch.zeros((B, S.vocab), dtype=torch.float32).pin_memory()
     Ke = min(K, G)
-    state["i"] = 0
-    kv.set_position(T, 0, stream)
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(arm.stream):
         for i in range(W):
-            ht.copy_(torch.from_numpy(host_tokens[i % G]))
-            river.rl_decode_step_host(model.handle, kv.handle, ht, B, forced.c(), None, hn, he, None,
-                                      stream)
-        kv.set_position(T, 0, stream)
-        stream.synchronize()
+            j = gen_index(i % Ke, Ke, G)
+            arm.goto(j)
+            ht.numpy()[:] = arm.dec_np[j]
+            river.rl_decode_step_host(arm.model.handle, arm.kv.handle, ht, B, arm.forced.c(), hl,
+                                      hn, he, None, arm.stream)
+            arm.cur = j + 1
+        arm.stream.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        t1 = time.perf_counter()
+        e2e_s = 0.0
         for i in range(Ke):
-            ht.numpy()[:] = host_tokens[i % G]
-            river.rl_decode_step_host(model.handle, kv.handle, ht, B, forced.c(), None, hn, he,
-                                      None, stream)
-        e2e_s = time.perf_counter() - t1
+            j = gen_index(i, Ke, G)
+            arm.goto(j)
+            arm.stream.synchronize()
+            t1 = time.perf_counter()
+            ht.numpy()[:] = arm.dec_np[j]
+            river.rl_decode_step_host(arm.model.handle, arm.kv.handle, ht, B, arm.forced.c(), hl,
+                                      hn, he, None, arm.stream)
+            e2e_s += time.perf_counter() - t1
+            arm.cur = j + 1
     if world > 1:
         e2e_s = max_over_ranks(e2e_s, "cuda")
     res["e2e"] = (Ke, e2e_s)
-    res["prof"] = prof_rows
-    res["kernels_per_step"] = model.kernel_count(B)
-    res["shape"], res["B"], res["T"], res["G"], res["mean"] = S, B, T, G, mean
-    res["sched_mean"] = float(sched_np.mean())
-    res["sched"] = sched_np
+    res["kernels_per_step"] = arm.model.kernel_count(B)
+    res["timed_sched"] = schedule_stats(arm.sched_np, [gen_index(i, K, G) for i in range(K)],
+                                        S.n_layers)
+    res["gen_sched"] = schedule_stats(arm.sched_np, range(G), S.n_layers)
     return res
+
+
+def dominant_kernel(prof, B):
+    """(name, launches, phase records, traffic ratio) of the kernel with the
+    most time in a live profile.  B <= 8: the persistent step kernel (one
+    launch per step, every byte of the step; its phase records give the
+    shares).  B > 8: one launch per kernel kind and layer; the kind with the
+    most time."""
+    steps = [r for r in prof if r[0] == "decode_step"]
+    if steps:
+        return ("k_decode_step (persistent decode step: every layer's projections, attention, "
+                "LM head)", steps, [r for r in prof if r[0] != "decode_step"],
+                traffic_note("step_dram_traffic.txt", "decode_step.cu", "attn_tc.cuh"))
+    by_kind = {}
+    for r in prof:
+        by_kind[r[0]] = by_kind.get(r[0], 0.0) + r[3]
+    top = max(by_kind, key=by_kind.get)
+    launches = [r for r in prof if r[0] == top]
+    if top == "attention":
+        return ("k_attn_stream + k_attn_combine (streaming decode attention: K/V chunks by TMA, "
+                "tensor cores; bytes = K and V rows 0..p of every sequence)", launches, prof,
+                traffic_note("attn_stream_dram_traffic.txt", "attn_stream.cu", "attn_tc.cuh"))
+    if B >= 16:
+        return (f"k_gemm_tc ({top}: tcgen05 GEMM; W4 layers dequantised in shared memory or on "
+                "k_gemv_fused)", launches, prof, None)
+    return (f"k_gemv_fused ({top}: bf16 / W4 GEMV)", launches, prof,
+            traffic_note("gemv_dram_traffic.txt", "gemv_fused.cu"))
+
+
+def roofline_of(prof, B, peak, peak_src):
+    kname, launches, phases, ratio = dominant_kernel(prof, B)
+    g_ms = sum(r[3] for r in launches)
+    g_bytes = sum(r[4] for r in launches)
+    per_launch_bytes = g_bytes / max(1, len(launches))
+    per_launch_ms = g_ms / max(1, len(launches))
+    achieved = per_launch_bytes / (per_launch_ms / 1e3) / 1e9 if launches else 0.0
+    all_ms = sum(r[3] for r in phases)
+    shares = {}
+    for r in phases:
+        shares[r[0]] = shares.get(r[0], 0.0) + r[3]
+    shares = {k: round(v / all_ms, 4) for k, v in sorted(shares.items(), key=lambda kv: -kv[1])}
+    roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": ratio * per_launch_bytes if ratio is not None else None,
+            "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
+            "launches_profiled": len(launches), "peak_source": f"{peak_src} (copy test)"}
+    return roof, shares
+
+
+def run_8b_b1(args, world, hbm_peak, peak_src):
+    """The Llama-3.1-8B batch-1 workload next to the default one: forced
+    schedule (mean exit 8 of 32) and full depth (the >= 70 % roofline target),
+    plus the step kernel's live roofline at full depth."""
+    import torch
+    arm = Arm(args, "8b-b1", 0, world)
+    try:
+        S, B, G = arm.S, arm.B, arm.G
+        K, W = args.steps, args.warmup
+        ms_f, ck, _ = arm.timed(arm.forced, K, W, args.smi_id)
+        ms_n, _, _ = arm.timed(arm.river.Policy.tau_(1.01), K, W)
+        roof, shares = roofline_of(arm.profile(arm.river.Policy.tau_(1.01), min(G, 32)), B,
+                                   hbm_peak, peak_src)
+        bf, bn = arm.timed_bytes(K, True), arm.timed_bytes(K, False)
+        out = {
+            "workload": workload_desc("8b-b1", S, B, arm.T, G, arm.mean),
+            "steps": K,
+            "forced": {"tokens_per_s": world * B * K / (ms_f / 1e3), "ms_per_step": ms_f / K,
+                       "hbm_frac": bf / (ms_f / 1e3) / 1e9 / hbm_peak,
+                       "timed_schedule": schedule_stats(arm.sched_np,
+                                                        [gen_index(i, K, G) for i in range(K)],
+                                                        S.n_layers),
+                       "generation_schedule": schedule_stats(arm.sched_np, range(G), S.n_layers),
+                       "target_mean_exit_layer": arm.mean},
+            "no_exit": {"tokens_per_s": world * B * K / (ms_n / 1e3), "ms_per_step": ms_n / K,
+                        "hbm_frac": bn / (ms_n / 1e3) / 1e9 / hbm_peak,
+                        "target_hbm_frac": 0.70},
+            "forced_over_no_exit": ms_n / ms_f,
+            "roofline_no_exit": roof,
+            "kernel_time_shares_no_exit": shares,
+            "clocks": ck,
+        }
+    finally:
+        arm.close()
+    return out
 
 
 def source_hash(*sources):
@@ -376,14 +518,18 @@ def oracle_setup(args, need_exit=True):
     return om, st, sched, dec, OPolicy, (S, B, T, G)
 
 
-def run_oracle_steps(om, st, sched, dec, OPolicy, dims, n, budget_s):
+def run_oracle_steps(om, st, sched, dec, OPolicy, dims, n, budget_s, K=None):
+    """Up to n oracle decode steps (stopping once budget_s seconds of them
+    have run); step i takes generation index gen_index(i, K, G) at position
+    T + index, as the library arm's timed steps do."""
     S, B, T, G = dims
+    K = n if K is None else K
     done, t = 0, 0.0
     for i in range(n):
-        if st.pos >= T + G:
-            st.pos = T
+        j = gen_index(i, K, G)
+        st.pos = T + j
         t1 = time.perf_counter()
-        om.decode_step(dec[i % G], st, OPolicy.forced(int(sched[i % G])))
+        om.decode_step(dec[j], st, OPolicy.forced(int(sched[j])))
         t += time.perf_counter() - t1
         done += 1
         if t > budget_s:
@@ -433,6 +579,8 @@ def main():
     ap.add_argument("--impl", default="river", choices=("river", "reference"))
     ap.add_argument("--config", default="1b-b1", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-8b", action="store_true",
+                    help="skip the Llama-3.1-8B batch-1 block that the default workload adds")
     ap.add_argument("--oracle-sample-only", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: the config's shape cut to this many layers (a small "
@@ -482,60 +630,35 @@ def main():
     props = torch.cuda.get_device_properties(dev)
     args.smi_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else str(dev)
     res = run_river(args, rank, world, dev)
+    arm = res["arm"]
+    S, B, T, G = arm.S, arm.B, arm.T, arm.G
     K = args.steps
     ms_step = res["ms_forced"] / K
     tok_s = job_throughput(B * K, world, res["ms_forced"] / 1e3)
     full_ms_step = res["ms_full"] / K
 
-    # algorithmic bytes of the timed steps: the schedule's exit layers, positions T..T+G-1
-    sched = res["sched"]
-    tot_bytes = 0.0
-    for i in range(K):
-        tot_bytes += step_bytes(S, B, int(sched[i % G]), T + (i % G))
+    # algorithmic bytes of the timed steps: the schedule's exit layers at their positions
+    tot_bytes = arm.timed_bytes(K, True)
     gbs = tot_bytes / (res["ms_forced"] / 1e3) / 1e9
-    full_bytes = sum(step_bytes(S, B, S.n_layers, T + (i % G)) for i in range(K))
-    full_gbs = full_bytes / (res["ms_full"] / 1e3) / 1e9
-
-    # roofline of the dominant kernel, from the live profile.  B <= 8: the
-    # persistent step kernel (one launch per step, every byte of the step);
-    # its phase records (first start .. last end over CTAs) give the shares.
-    # B > 8: one launch per kernel kind and layer; the kind with the most time.
-    prof = res["prof"]
-    steps = [r for r in prof if r[0] == "decode_step"]
-    if steps:
-        kname = "k_decode_step (persistent decode step: every layer's projections, attention, LM head)"
-        launches = steps
-        phases = [r for r in prof if r[0] != "decode_step"]
-        ratio = traffic_note("step_dram_traffic.txt", "decode_step.cu", "attn_tc.cuh")
-    else:
-        phases = prof
-        by_kind = {}
-        for r in prof:
-            by_kind[r[0]] = by_kind.get(r[0], 0.0) + r[3]
-        top = max(by_kind, key=by_kind.get)
-        launches = [r for r in prof if r[0] == top]
-        if top == "attention":
-            kname = ("k_attn_stream + k_attn_combine (streaming decode attention: K/V chunks by "
-                     "TMA, tensor cores; bytes = K and V rows 0..p of every sequence)")
-            ratio = traffic_note("attn_stream_dram_traffic.txt", "attn_stream.cu", "attn_tc.cuh")
-        elif B >= 16:
-            kname = (f"k_gemm_tc ({top}: tcgen05 GEMM; W4 layers dequantised in shared memory "
-                     "or on k_gemv_fused)")
-            ratio = None
-        else:
-            kname = f"k_gemv_fused ({top}: bf16 / W4 GEMV)"
-            ratio = traffic_note("gemv_dram_traffic.txt", "gemv_fused.cu")
-    g_ms = sum(r[3] for r in launches)
-    g_bytes = sum(r[4] for r in launches)
-    all_ms = sum(r[3] for r in phases)
-    per_launch_bytes = g_bytes / max(1, len(launches))
-    per_launch_ms = g_ms / max(1, len(launches))
-    achieved = per_launch_bytes / (per_launch_ms / 1e3) / 1e9 if launches else 0.0
-    traffic = ratio * per_launch_bytes if ratio is not None else None
-    shares = {}
-    for r in phases:
-        shares[r[0]] = shares.get(r[0], 0.0) + r[3]
-    shares = {k: round(v / all_ms, 4) for k, v in sorted(shares.items(), key=lambda kv: -kv[1])}
+    full_gbs = arm.timed_bytes(K, False) / (res["ms_full"] / 1e3) / 1e9
+    roof, shares = roofline_of(res["prof"], B, hbm_peak, peak_src)
+    Ke, e2e_s = res["e2e"]
+    line_variants = {
+        "no_exit": {"tokens_per_s": world * B / (full_ms_step / 1e3), "ms_per_step": full_ms_step,
+                    "hbm_frac": full_gbs / hbm_peak},
+        "forced_over_no_exit": full_ms_step / ms_step,
+        "all_w4": {"tokens_per_s": world * B / (res["ms_w4"] / 1e3), "ms_per_step": res["ms_w4"],
+                   "over_no_exit": full_ms_step / res["ms_w4"]},
+        **{f"tau_{t}": {"tokens_per_s": world * B / (v[0] / 1e3), "ms_per_step": v[0],
+                        "mean_exit_layer": v[1]} for t, v in res["tau"].items()},
+    }
+    arm.close()
+    del arm, res["arm"]
+    if args.config == "1b-b1" and not args.no_8b and not args.layers:
+        try:
+            line_variants["llama8b_b1"] = run_8b_b1(args, world, hbm_peak, peak_src)
+        except Exception as ex:  # reported, never required
+            line_variants["llama8b_b1"] = {"failed": repr(ex)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -545,38 +668,34 @@ def main():
             cpu = {"value": None, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                    "sample": f"failed: {ex!r}"}
 
-    Ke, e2e_s = res["e2e"]
+    ts, gs = res["timed_sched"], res["gen_sched"]
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (random-init weights, uniform token ids)",
-        "config": {"workload": workload_desc(args.config, S, B, T, G, mean), "batch": B,
-                   "prompt": T, "decode_steps": G, "policy": "forced exit schedule",
-                   "schedule_mean_exit_layer": res["sched_mean"],
+        "config": {"workload": workload_desc(args.config, S, B, T, G, CONFIGS[args.config][4]),
+                   "batch": B, "prompt": T, "decode_steps": G, "policy": "forced exit schedule",
+                   "timed_steps": (f"step i of K runs generation index floor(i*G/K) (K < G) or "
+                                   f"i mod G at position prompt + index; the sum of per-step "
+                                   f"CUDA-event intervals on the launching stream"),
+                   "schedule_mean_exit_layer": ts["mean_exit_layer"],
+                   "schedule_full_depth_share": ts["full_depth_share"],
+                   "generation_mean_exit_layer": gs["mean_exit_layer"],
+                   "generation_full_depth_share": gs["full_depth_share"],
+                   "target_mean_exit_layer": CONFIGS[args.config][4],
                    "l2": "inputs larger than L2: every step streams >= 1.4 GB of weights (L2 129 MB)",
                    "parallelism": f"replicas x{world}"},
         "hbm": {"algorithmic_bytes_per_step": tot_bytes / K, "achieved_gbs": gbs,
                 "peak_gbs": hbm_peak, "frac": gbs / hbm_peak, "peak_source": peak_src},
-        "roofline": {"kernel": kname,
-                     "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": traffic,
-                     "bytes_per_launch": per_launch_bytes, "ms_per_launch": per_launch_ms,
-                     "launches_profiled": len(launches), "peak_source": f"{peak_src} (copy test)"},
+        "roofline": roof,
         "kernel_time_shares": shares,
-        "variants": {
-            "no_exit": {"tokens_per_s": world * B / (full_ms_step / 1e3), "ms_per_step": full_ms_step,
-                        "hbm_frac": full_gbs / hbm_peak},
-            "forced_over_no_exit": full_ms_step / ms_step,
-            "all_w4": {"tokens_per_s": world * B / (res["ms_w4"] / 1e3), "ms_per_step": res["ms_w4"],
-                       "over_no_exit": full_ms_step / res["ms_w4"]},
-            **{f"tau_{t}": {"tokens_per_s": world * B / (v[0] / 1e3), "ms_per_step": v[0],
-                            "mean_exit_layer": v[1]} for t, v in res["tau"].items()},
-        },
+        "variants": line_variants,
         "e2e": {"value": world * B * Ke / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * B,
-                "d2h_bytes_per_step": 4 * B + 4,
-                "note": "rl_decode_step_host: pinned host tokens in, next tokens + exit layer out"},
-        "gpu_launches": K * res["kernels_per_step"] + res["resets"],
+                "d2h_bytes_per_step": 4 * B + 4 + 4 * B * S.vocab,
+                "note": ("rl_decode_step_host: pinned host tokens in; next tokens, exit layer and "
+                         "fp32 logits out; each call timed from the token write to its return")},
+        "gpu_launches": K * res["kernels_per_step"] + res["repos"],
         "clocks": res["clocks"],
     }
     if cpu is not None:

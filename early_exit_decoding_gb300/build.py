@@ -50,7 +50,7 @@ def _stale(objs_srcs) -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = [*sources(), *(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")),
+    deps = [*sources(), *(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))),
             os.path.join(INCLUDE, "river.h"), __file__]
     return any(os.path.getmtime(d) > t for d in deps)
 

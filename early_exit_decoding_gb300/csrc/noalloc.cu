@@ -10,8 +10,11 @@
 // whose size is fixed when the library is loaded.
 //
 // Limits: batch <= 8 rows, d_model <= 8192, at most 1024 CTAs in the LM-head
-// launch (one per streaming multiprocessor at most).  Larger requests are
-// rejected with RL_ERR_UNSUPPORTED before anything is enqueued.
+// launch (one per streaming multiprocessor at most), and the rows must fit in
+// shared memory beside the GEMV kernel's weight ring: B * (2*Kp + 64 + Kp/32)
+// <= 115,712 bytes (Kp = d_model rounded up to 128), so batch 8 up to
+// d_model 7040 and batch 6 at d_model 8192.  Larger requests are rejected
+// with RL_ERR_UNSUPPORTED before anything is enqueued.
 //
 // Every call shares the one array: two calls that overlap on the GPU (on
 // different streams, or on different host threads) race on it and may

@@ -295,8 +295,11 @@ RL_API int32_t rl_decode_kernel_count(const rl_model* m, int32_t B);
  *   d_logits     [B][vocab] fp32 out (device, caller-owned)
  *   d_next_token [B] int32 out, ties to the lowest id (device; may be NULL)
  *   d_err        [1] int32 out: RL_DEVERR_* bits of this call (device; may be NULL)
- * Limits: 1 <= B <= 8, d_model <= 8192, vocab and d_model multiples of 16;
- * beyond them the call returns RL_ERR_UNSUPPORTED and enqueues nothing.
+ * Limits: 1 <= B <= 8, d_model <= 8192, vocab and d_model multiples of 16,
+ * and the B rows must fit in the kernel's shared memory next to its weight
+ * ring: B * (2*Kp + 64 + Kp/32) <= 115,712 bytes with Kp = d_model rounded up
+ * to 128, i.e. every B <= 8 up to d_model 7040, and B <= 6 at d_model 8192.
+ * Beyond them the call returns RL_ERR_UNSUPPORTED and enqueues nothing.
  * The first call on each device resolves the array's device address with that
  * device current; make that first call before any stream capture on the
  * device.  Every call shares the one array: calls that overlap on the GPU
