@@ -157,11 +157,18 @@ def job_throughput(units_per_rank, world, seconds):
 
 # ---------------------------------------------------------------------- the library arm
 
-def gen_index(i, K, G):
-    """Generation index of timed step i: an even subsample of the G-step
-    generation when K < G (so any K sees the schedule's mix), else a cycle
-    through it."""
-    return (i * G) // K if K < G else i % G
+def timed_indices(sched, K):
+    """Generation indices of K timed steps.  K >= G: a cycle through the
+    G-step generation.  K < G: a stratified sample of it, the K quantiles
+    of its steps ordered by exit layer (index order among equal layers), so
+    that any K sees the schedule's mix of exit layers and full-depth steps,
+    run in generation order.  Each step runs at its own position (prompt +
+    index)."""
+    G = len(sched)
+    if K >= G:
+        return [i % G for i in range(K)]
+    order = sorted(range(G), key=lambda j: (int(sched[j]), j))
+    return sorted(order[int((i + 0.5) * G / K)] for i in range(K))  # in generation order
 
 
 def schedule_stats(sched, idx, L):
@@ -241,12 +248,13 @@ class Arm:
         self.cur = j + 1
 
     def timed(self, policy, K, W, clocks_dev=None):
-        """W untimed warm-up steps, then K steps; generation index
-        gen_index(i, K, G) at position T + index.  Every step is bracketed by
+        """W untimed warm-up steps, then K steps at the generation indices
+        timed_indices(schedule, K), each at position T + index.  Every step is bracketed by
         its own pair of CUDA events on the launching stream; a reposition of
         the cache between two steps falls outside them.  Returns (ms summed
         over the K steps, clocks sampled during them, repositions)."""
-        torch, G = self.torch, self.G
+        torch = self.torch
+        idx = timed_indices(self.sched_np, K)
         clocks = Clocks(clocks_dev) if clocks_dev else None
         with torch.cuda.stream(self.stream):
             t_w, n_w = time.time(), 0
@@ -254,7 +262,7 @@ class Arm:
             # W steps and half a second, so that neither the sampler's start-up
             # nor a GPU leaving idle clocks falls in the timed region
             while n_w < W or time.time() - t_w < 0.5:
-                self.step(gen_index(n_w % K, K, G), policy)
+                self.step(idx[n_w % K], policy)
                 n_w += 1
                 if n_w % 32 == 0:
                     self.stream.synchronize()
@@ -266,7 +274,7 @@ class Arm:
                   for _ in range(K)]
             self.repositions = 0
             for i in range(K):
-                j = gen_index(i, K, G)
+                j = idx[i]
                 self.goto(j)
                 ev[i][0].record(self.stream)
                 self.river.decode_step(self.model, self.kv, self.tok[j], policy, out=self.out,
@@ -286,10 +294,9 @@ class Arm:
 
     def timed_bytes(self, K, forced):
         """Algorithmic bytes of the K timed steps (schedule exit layers or full depth)."""
-        S, G = self.S, self.G
+        S = self.S
         tot = 0.0
-        for i in range(K):
-            j = gen_index(i, K, G)
+        for j in timed_indices(self.sched_np, K):
             e = int(self.sched_np[j]) if forced else S.n_layers
             tot += step_bytes(S, self.B, e, self.T + j)
         return tot
@@ -341,9 +348,10 @@ def run_river(args, rank, world, dev):
     he = torch.zeros((1,), dtype=torch.int32).pin_memory()
     hl = torch.zeros((B, S.vocab), dtype=torch.float32).pin_memory()
     Ke = min(K, G)
+    idx_e = timed_indices(arm.sched_np, Ke)
     with torch.cuda.stream(arm.stream):
         for i in range(W):
-            j = gen_index(i % Ke, Ke, G)
+            j = idx_e[i % Ke]
             arm.goto(j)
             ht.numpy()[:] = arm.dec_np[j]
             river.rl_decode_step_host(arm.model.handle, arm.kv.handle, ht, B, arm.forced.c(), hl,
@@ -354,7 +362,7 @@ def run_river(args, rank, world, dev):
             torch.distributed.barrier()
         e2e_s = 0.0
         for i in range(Ke):
-            j = gen_index(i, Ke, G)
+            j = idx_e[i]
             arm.goto(j)
             arm.stream.synchronize()
             t1 = time.perf_counter()
@@ -367,8 +375,7 @@ def run_river(args, rank, world, dev):
         e2e_s = max_over_ranks(e2e_s, "cuda")
     res["e2e"] = (Ke, e2e_s)
     res["kernels_per_step"] = arm.model.kernel_count(B)
-    res["timed_sched"] = schedule_stats(arm.sched_np, [gen_index(i, K, G) for i in range(K)],
-                                        S.n_layers)
+    res["timed_sched"] = schedule_stats(arm.sched_np, timed_indices(arm.sched_np, K), S.n_layers)
     res["gen_sched"] = schedule_stats(arm.sched_np, range(G), S.n_layers)
     return res
 
@@ -438,8 +445,7 @@ def run_8b_b1(args, world, hbm_peak, peak_src):
             "steps": K,
             "forced": {"tokens_per_s": world * B * K / (ms_f / 1e3), "ms_per_step": ms_f / K,
                        "hbm_frac": bf / (ms_f / 1e3) / 1e9 / hbm_peak,
-                       "timed_schedule": schedule_stats(arm.sched_np,
-                                                        [gen_index(i, K, G) for i in range(K)],
+                       "timed_schedule": schedule_stats(arm.sched_np, timed_indices(arm.sched_np, K),
                                                         S.n_layers),
                        "generation_schedule": schedule_stats(arm.sched_np, range(G), S.n_layers),
                        "target_mean_exit_layer": arm.mean},
@@ -518,15 +524,13 @@ def oracle_setup(args, need_exit=True):
     return om, st, sched, dec, OPolicy, (S, B, T, G)
 
 
-def run_oracle_steps(om, st, sched, dec, OPolicy, dims, n, budget_s, K=None):
+def run_oracle_steps(om, st, sched, dec, OPolicy, dims, n, budget_s):
     """Up to n oracle decode steps (stopping once budget_s seconds of them
-    have run); step i takes generation index gen_index(i, K, G) at position
-    T + index, as the library arm's timed steps do."""
+    have run) at the generation indices timed_indices(schedule, n), each at
+    position T + index, as the library arm's timed steps run."""
     S, B, T, G = dims
-    K = n if K is None else K
     done, t = 0, 0.0
-    for i in range(n):
-        j = gen_index(i, K, G)
+    for j in timed_indices(sched, n):
         st.pos = T + j
         t1 = time.perf_counter()
         om.decode_step(dec[j], st, OPolicy.forced(int(sched[j])))
@@ -676,9 +680,10 @@ def main():
         "data": "synthetic (random-init weights, uniform token ids)",
         "config": {"workload": workload_desc(args.config, S, B, T, G, CONFIGS[args.config][4]),
                    "batch": B, "prompt": T, "decode_steps": G, "policy": "forced exit schedule",
-                   "timed_steps": (f"step i of K runs generation index floor(i*G/K) (K < G) or "
-                                   f"i mod G at position prompt + index; the sum of per-step "
-                                   f"CUDA-event intervals on the launching stream"),
+                   "timed_steps": ("K < G: the K quantiles of the generation's steps ordered by "
+                                   "exit layer, K >= G: a cycle through it; each step at its own "
+                                   "position (prompt + generation index); time = the sum of "
+                                   "per-step CUDA-event intervals on the launching stream"),
                    "schedule_mean_exit_layer": ts["mean_exit_layer"],
                    "schedule_full_depth_share": ts["full_depth_share"],
                    "generation_mean_exit_layer": gs["mean_exit_layer"],

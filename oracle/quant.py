@@ -90,3 +90,116 @@ def dequantize_linear(qweight, scales, zeros, K: int, group: int = 128) -> np.nd
     qg = qg.reshape(N, G, group)
     w = ((qg - z[:, :, None]).astype(F32) * s[:, :, None]).astype(F32)
     return w.reshape(N, G * group)[:, :K].copy()
+
+
+# ---------------------------------------------------------------------------
+# HQQ refinement of the zero point (River-LLM explainer, section 六: HQQ is
+# the exit layers' default quantizer; it needs no calibration data).
+#
+# Half-quadratic quantization (Badri and Shaji, 2023) keeps the min-max scale
+# and moves the zero point z of each group to lower an lp norm (p < 1) of the
+# reconstruction error w - s (q - z), by splitting that error into an
+# auxiliary variable e and alternating two closed-form steps while the
+# penalty weight beta grows by kappa per iteration:
+#   e <- shrink_p(w - s (q(z) - z), beta)         (proximal step of |.|^p)
+#   z <- mean over the group of  q(z) - (w - e) / s   (least-squares step)
+# with q(z) = clamp(rint(w / s + z), 0, 15).
+#
+# Readings taken where the page (and the method) leave a choice open:
+#   * the iteration runs per group, in float64, for a fixed number of
+#     iterations (20, p = 0.7, beta = 10, kappa = 1.01: the method's usual
+#     settings); the zero point kept is the fp16 value, among the min-max one
+#     and those of the iterations, whose stored codes give the lowest
+#     sum |w - s (q - z)|^p in that group (ties keep the earlier), so the
+#     stored result is never worse than min-max rounding by that measure;
+#   * the scale and the code rule are min-max's (fp16 s, codes from the fp32
+#     divide and add with the stored fp16 zero), so the packed format is
+#     unchanged.
+# ---------------------------------------------------------------------------
+
+HQQ_ITERS, HQQ_P, HQQ_BETA, HQQ_KAPPA = 20, 0.7, 10.0, 1.01
+F64 = np.float64
+
+
+def hqq_shrink(x: np.ndarray, beta: float, p: float) -> np.ndarray:
+    """Generalised soft threshold of |.|^p at weight beta:
+    sign(x) max(|x| - |x|^(p-1) / beta, 0), and 0 where x == 0."""
+    x = np.asarray(x, F64)
+    ax = np.abs(x)
+    with np.errstate(divide="ignore"):
+        t = np.where(ax > 0, np.power(np.where(ax > 0, ax, 1.0), p - 1.0) / beta, 0.0)
+    return np.where(ax > 0, np.sign(x) * np.maximum(ax - t, 0.0), 0.0)
+
+
+def hqq_zero_step(w, q, e, s, mask) -> np.ndarray:
+    """Least-squares zero point: mean over each group's valid entries of
+    q - (w - e) / s.  Arrays [..][n]; s [..]; mask marks valid entries."""
+    v = np.where(mask, q - (w - e) / s[..., None], 0.0)
+    return v.sum(axis=-1) / mask.sum(axis=-1)
+
+
+def _codes(w32, s32, z16):
+    """Stored codes of min-max rounding for a given fp16 zero (fp32 steps)."""
+    v = (w32 / s32[..., None]).astype(F32)
+    v = (v + z16.astype(F32)[..., None]).astype(F32)
+    return np.clip(np.rint(v), F32(0.0), F32(15.0))
+
+
+def _lp_error(w32, s32, z16, mask, p):
+    """sum |w - s (q - z)|^p over each group's valid entries, float64."""
+    q = _codes(w32, s32, z16).astype(F64)
+    r = w32.astype(F64) - s32.astype(F64)[..., None] * (q - z16.astype(F64)[..., None])
+    return np.where(mask, np.power(np.abs(r), p), 0.0).sum(axis=-1)
+
+
+def _groups(w, group, G):
+    """``w [N][K]`` as [N][G][group] (zero padded) and the mask of valid entries."""
+    N, K = w.shape
+    wg = np.zeros((N, G * group), F32)
+    wg[:, :K] = w
+    mask = np.zeros(G * group, bool)
+    mask[:K] = True
+    return wg.reshape(N, G, group), np.broadcast_to(mask.reshape(G, group), (N, G, group))
+
+
+def hqq_iterates(wg, s16, z16, mask, iters: int = HQQ_ITERS, p: float = HQQ_P,
+                 beta: float = HQQ_BETA, kappa: float = HQQ_KAPPA):
+    """The fp16 zero points of the refinement's iterations, in order, starting
+    from min-max's scale ``s16`` and zero ``z16`` ([N][G]) on groups ``wg``."""
+    s64 = s16.astype(F32).astype(F64)
+    w64 = wg.astype(F64)
+    z = z16.astype(F64)
+    b = float(beta)
+    out = []
+    for _ in range(iters):
+        q = np.clip(np.rint(w64 / s64[..., None] + z[..., None]), 0.0, 15.0)
+        r = w64 - s64[..., None] * (q - z[..., None])
+        e = hqq_shrink(r, b, p)
+        z = hqq_zero_step(w64, q, e, s64, mask)
+        b *= kappa
+        out.append(z.astype(np.float16))
+    return out
+
+
+def quantize_linear_hqq(w: np.ndarray, group: int = 128, iters: int = HQQ_ITERS, p: float = HQQ_P,
+                        beta: float = HQQ_BETA, kappa: float = HQQ_KAPPA):
+    """Min-max quantization of ``w [N][K]`` followed by the HQQ zero-point
+    refinement of every group.  Same return format as ``quantize_linear``."""
+    w = np.asarray(w, dtype=F32)
+    N, K = w.shape
+    _, s16, z16 = quantize_linear(w, group)
+    wg, mask = _groups(w, group, s16.shape[1])
+    s32 = s16.astype(F32)
+    best_z = z16.copy()
+    best_err = _lp_error(wg, s32, z16, mask, p)
+    for zc in hqq_iterates(wg, s16, z16, mask, iters, p, beta, kappa):
+        err = _lp_error(wg, s32, zc, mask, p)
+        better = err < best_err
+        best_z = np.where(better, zc, best_z)
+        best_err = np.where(better, err, best_err)
+    # repack with the refined zeros
+    q = _codes(wg, s32, best_z).astype(np.uint32).reshape(N, -1)[:, :K]
+    qw = np.zeros((N, K // 8), dtype=np.uint32)
+    for i in range(8):
+        qw |= q[:, i::8] << np.uint32(4 * i)
+    return qw, s16, best_z
