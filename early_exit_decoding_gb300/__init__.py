@@ -25,11 +25,11 @@ LINEAR_NAMES = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
 
 EXPORTS = (
     "rl_version", "rl_last_error", "rl_model_create", "rl_model_destroy",
-    "rl_quantize_exit_layers", "rl_exit_layer_view", "rl_kv_cache_alloc", "rl_kv_cache_free",
+    "rl_quantize_exit_layers", "rl_quantize_exit_layers_hqq", "rl_exit_layer_view", "rl_kv_cache_alloc", "rl_kv_cache_free",
     "rl_kv_view", "rl_kv_position", "rl_kv_set_position", "rl_kv_set_trace", "rl_prefill",
     "rl_decode_step", "rl_decode_step_host", "rl_sync", "rl_decode_kernel_count",
     "rl_kv_set_profiling", "rl_kv_profile", "rl_kv_timeline", "rl_lm_head_static", "rl_kv_set_decode_path",
-    "rl_kv_decode_path", "rl_save_exit_layers", "rl_load_exit_layers",
+    "rl_kv_decode_path", "rl_save_exit_layers", "rl_load_exit_layers", "rl_exit_kv_cosine",
 )
 RL_PATH_AUTO, RL_PATH_STEP, RL_PATH_FUSED, RL_PATH_GENERIC = range(4)
 KERNEL_KINDS = ("embed", "qkv", "attention", "group_sums", "o_proj", "norm", "gate_up", "down",
@@ -77,6 +77,7 @@ def _load():
         "rl_model_create": (I, [ctypes.POINTER(rl_config), ctypes.POINTER(rl_weights), P, PP]),
         "rl_model_destroy": (V, [P]),
         "rl_quantize_exit_layers": (I, [P, P]),
+        "rl_quantize_exit_layers_hqq": (I, [P, I, ctypes.c_double, ctypes.c_double, ctypes.c_double, P]),
         "rl_exit_layer_view": (I, [P, I, I, PP, PP, PP, PI, PI]),
         "rl_kv_cache_alloc": (I, [P, I, I, PP]),
         "rl_kv_cache_free": (I, [P]),
@@ -97,6 +98,7 @@ def _load():
         "rl_kv_set_decode_path": (I, [P, I]),
         "rl_kv_decode_path": (I, [P, I]),
         "rl_save_exit_layers": (I, [P, ctypes.c_char_p]),
+        "rl_exit_kv_cosine": (I, [P, I, P, I, P, P]),
         "rl_load_exit_layers": (I, [P, ctypes.c_char_p, P]),
     }
     for name, (res, args) in sig.items():
@@ -148,6 +150,15 @@ def rl_model_destroy(model):
 
 def rl_quantize_exit_layers(model, stream=None):
     _check(_lib.rl_quantize_exit_layers(model, _stream(stream)))
+
+
+def rl_quantize_exit_layers_hqq(model, iters=20, lp_norm=0.7, beta=10.0, kappa=1.01, stream=None):
+    _check(_lib.rl_quantize_exit_layers_hqq(model, int(iters), float(lp_norm), float(beta),
+                                            float(kappa), _stream(stream)))
+
+
+def rl_exit_kv_cosine(model, layer, d_h, B, d_cos, stream=None):
+    _check(_lib.rl_exit_kv_cosine(model, int(layer), _ptr(d_h), int(B), _ptr(d_cos), _stream(stream)))
 
 
 def rl_save_exit_layers(model, path):
@@ -339,8 +350,16 @@ class Model:
 
     __del__ = close
 
-    def quantize_exit_layers(self, stream=None):
-        rl_quantize_exit_layers(self.handle, stream)
+    def quantize_exit_layers(self, stream=None, method="rtn", **hqq):
+        """Build the exit river: min-max rounding (``method="rtn"``) or with
+        HQQ's zero-point refinement (``method="hqq"``; keyword settings
+        iters, lp_norm, beta, kappa)."""
+        if method == "hqq":
+            rl_quantize_exit_layers_hqq(self.handle, stream=stream, **hqq)
+        elif method == "rtn":
+            rl_quantize_exit_layers(self.handle, stream)
+        else:
+            raise ValueError(f"unknown quantizer {method!r}")
 
     def save_exit_layers(self, path):
         """Write the exit river (published packing) to ``path``."""
@@ -349,6 +368,16 @@ class Model:
     def load_exit_layers(self, path, stream=None):
         """Build the exit river from a file written by save_exit_layers."""
         rl_load_exit_layers(self.handle, path, stream)
+
+    def exit_kv_cosine(self, layer, h, stream=None):
+        """Cosine between the exit layer's and the backbone layer's K and V of
+        residual rows ``h [B][d]`` (fp32 CUDA) entering ``layer`` (0-based):
+        a tensor [B][2][n_kv_heads] (K, then V)."""
+        import torch
+        B = h.shape[0]
+        out = torch.empty((B, 2, self.shape.n_kv_heads), dtype=torch.float32, device="cuda")
+        rl_exit_kv_cosine(self.handle, layer, h.contiguous(), B, out, stream)
+        return out
 
     def exit_layer_view(self, layer, which):
         """(qweight int32 [N][K/8], scales fp16 [N][G], zeros fp16 [N][G]) torch views."""

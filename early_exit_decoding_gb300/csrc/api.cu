@@ -1411,22 +1411,61 @@ void exit_header(const rl_model* m, uint32_t (&h)[8]) {
 
 extern "C" {
 
-rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream) {
-  if (!m) return fail(RL_ERR_INVALID_ARG, "model is NULL");
-  if (m->quantized) return RL_OK;
-  cudaStream_t s = as_stream(stream);
+}  // extern "C"
+
+namespace {
+
+rl_status quantize_exit_river(rl_model* m, const HqqParams* hqq, cudaStream_t s) {
   return build_exit_river(m, s, [&]() -> rl_status {
     for (int l = 0; l < m->L; ++l) {
       Layer& ly = m->layers[l];
       Linear* lins[4] = {&ly.qkv, &ly.o, &ly.gu, &ly.dn};
       for (Linear* lin : lins) {
         launch_quantize(lin->w, lin->N, lin->K, lin->Kp, lin->qw, lin->sz, lin->rowmap,
-                        m->d_views + (size_t)l * 7 + lin->view_base, s);
+                        m->d_views + (size_t)l * 7 + lin->view_base, hqq, s);
         RL_LAUNCHED();
       }
     }
     return RL_OK;
   });
+}
+
+}  // namespace
+
+extern "C" {
+
+rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream) {
+  if (!m) return fail(RL_ERR_INVALID_ARG, "model is NULL");
+  if (m->quantized) return RL_OK;
+  return quantize_exit_river(m, nullptr, as_stream(stream));
+}
+
+rl_status rl_quantize_exit_layers_hqq(rl_model* m, int32_t iters, double lp_norm, double beta,
+                                      double kappa, rl_stream_t stream) {
+  if (!m) return fail(RL_ERR_INVALID_ARG, "model is NULL");
+  if (iters < 0 || iters > 1000 || !(lp_norm > 0.0 && lp_norm <= 2.0) || !(beta > 0.0) ||
+      !(kappa >= 1.0) || !(kappa < 1e3))
+    return fail(RL_ERR_INVALID_ARG,
+                "HQQ settings: iters in [0, 1000], lp_norm in (0, 2], beta > 0, kappa in [1, 1000)");
+  if (m->quantized) return fail(RL_ERR_STATE, "the exit river is already built");
+  HqqParams hp;
+  hp.iters = iters;
+  hp.p = lp_norm;
+  hp.beta = beta;
+  hp.kappa = kappa;
+  return quantize_exit_river(m, &hp, as_stream(stream));
+}
+
+rl_status rl_exit_kv_cosine(const rl_model* m, int32_t layer, const float* d_h, int32_t B,
+                            float* d_cos, rl_stream_t stream) {
+  if (!m || !d_h || !d_cos) return fail(RL_ERR_INVALID_ARG, "NULL argument");
+  if (layer < 0 || layer >= m->L) return fail(RL_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, m->L);
+  if (B < 1 || B > 65535 / (2 * m->Hkv)) return fail(RL_ERR_INVALID_ARG, "B=%d out of range", B);
+  if (!m->quantized) return fail(RL_ERR_STATE, "exit river not built");
+  const Linear& q = m->layers[layer].qkv;
+  RL_CUDA(launch_exit_kv_cosine(d_h, B, m->d, m->layers[layer].g_attn, q.w, q.qw, q.sz, q.Kp, m->Hq,
+                                m->Hkv, m->hd, d_cos, as_stream(stream)));
+  return RL_OK;
 }
 
 rl_status rl_save_exit_layers(const rl_model* m, const char* path) {

@@ -268,11 +268,25 @@ void launch_bf16_to_f32(const bf16* src, float* dst, int n, cudaStream_t s);
 
 struct NSView { uint32_t* q; uint16_t* s; uint16_t* z; int N; int K; };
 
+// HQQ zero-point refinement settings (float64, as the iteration computes).
+struct HqqParams {
+  int iters = 0;
+  double p = 0.7, beta = 10.0, kappa = 1.01;
+};
+
 // Quantize the library's bf16 copy w [N][Kp] (K real inputs) into the
 // internal W4 layout (qw, sz) and the interchange views: row r goes to
-// views[rowmap[r].x] at row rowmap[r].y.
+// views[rowmap[r].x] at row rowmap[r].y.  hqq == nullptr: min-max rounding;
+// otherwise min-max followed by the HQQ refinement of every group's zero.
 void launch_quantize(const bf16* w, int N, int K, int Kp, uint32_t* qw, __half2* sz,
-                     const int2* rowmap, const NSView* views, cudaStream_t s);
+                     const int2* rowmap, const NSView* views, const HqqParams* hqq, cudaStream_t s);
+// Exit-vs-backbone K/V cosine per (sequence, K/V, KV head) of residual rows
+// h [B][d] entering a layer: w [N][Kp] bf16 and (qw, sz) W4 of its fused QKV
+// matrix, g its attention RMSNorm gain; out [B][2][Hkv].
+cudaError_t launch_exit_kv_cosine(const float* h, int B, int d, const float* g, const bf16* w,
+                                  const uint32_t* qw, const __half2* sz, int Kp, int Hq, int Hkv,
+                                  int hd, float* out, cudaStream_t s);
+
 // The internal W4 layout (qw, sz) of a fused matrix from interchange views
 // that already hold the exit layer (rl_load_exit_layers).
 void launch_w4_from_views(int N, int K, int Kp, uint32_t* qw, __half2* sz, const int2* rowmap,

@@ -134,6 +134,26 @@ RL_API void rl_model_destroy(rl_model* m);
  * Norm gains are shared with the backbone.  Enqueued on `stream`. */
 RL_API rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream);
 
+/* quantize_exit_layers with HQQ's zero-point refinement (explainer section
+ * 六 names HQQ, which needs no calibration data, as the exit layers'
+ * quantizer; half-quadratic quantization, Badri and Shaji 2023).  The
+ * min-max scale above stays; each group's zero point z is refined by `iters`
+ * alternations, in float64 with every operation rounded once:
+ *   q = clamp(rint(w/s + z), 0, 15),  r = w - s(q - z),
+ *   e = sign(r) max(|r| - |r|^(lp_norm-1)/beta, 0)   (0 where r == 0),
+ *   z = mean over the group of q - (w - e)/s,  beta *= kappa.
+ * The stored zero is the fp16 value (min-max's or an iteration's, rounded
+ * once from float64) whose stored codes give the lowest sum |w - s(q - z)|^p
+ * over the group (ties keep the earlier); codes follow the min-max rule with
+ * it, so the packed format and every other entry point are unchanged.  The
+ * method's usual settings: iters 20, lp_norm 0.7, beta 10, kappa 1.01.
+ * RL_ERR_INVALID_ARG for iters outside [0, 1000], lp_norm outside (0, 2],
+ * beta <= 0 (infinity allowed: no shrinkage) or kappa outside [1, 1000);
+ * RL_ERR_STATE if the exit river is already built.  Enqueued on `stream`;
+ * returns once the exit river is ready. */
+RL_API rl_status rl_quantize_exit_layers_hqq(rl_model* m, int32_t iters, double lp_norm, double beta,
+                                             double kappa, rl_stream_t stream);
+
 /* Read-only device views of one exit linear in the interchange format:
  * qweight [N][K/8] uint32, scales [N][ceil(K/128)] fp16 bits,
  * zeros [N][ceil(K/128)] fp16 bits, rows in the caller's original order.
@@ -141,6 +161,20 @@ RL_API rl_status rl_quantize_exit_layers(rl_model* m, rl_stream_t stream);
 RL_API rl_status rl_exit_layer_view(const rl_model* m, int32_t layer, int32_t which_linear,
                              const uint32_t** qweight, const uint16_t** scales,
                              const uint16_t** zeros, int32_t* n_rows, int32_t* n_cols);
+
+/* Exit-vs-backbone K/V similarity, a diagnostic (explainer section 三: the
+ * K/V an exit layer writes into the backbone's slot stays close to what the
+ * backbone layer would have written).  For B residual rows d_h [B][d_model]
+ * (fp32, device, caller-owned) entering layer `layer` (0-based), both weight
+ * sets of that layer project the same RMSNorm'd row to K and V; d_cos
+ * [B][2][n_kv_heads] (fp32, device, caller-owned) receives, per sequence, the
+ * cosine between the exit layer's and the backbone layer's K (index 0) and V
+ * (index 1) of every KV head.  RoPE rotates both keys of a head alike at any
+ * position, so the result does not depend on the position.  RL_ERR_STATE
+ * before the exit river is built; RL_ERR_INVALID_ARG for a bad layer, batch
+ * or pointer.  Enqueued on `stream`. */
+RL_API rl_status rl_exit_kv_cosine(const rl_model* m, int32_t layer, const float* d_h, int32_t B,
+                                   float* d_cos, rl_stream_t stream);
 
 /* Save / load the exit river in the published packing (per layer and linear,
  * in RL_WQ .. RL_WD order: qweight [N][K/8] u32, scales and zeros [N][G] fp16

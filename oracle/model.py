@@ -33,7 +33,7 @@ import dataclasses
 
 import numpy as np
 
-from .quant import quantize_linear, dequantize_linear
+from .quant import dequantize_linear, quantize_linear, quantize_linear_hqq
 
 F32 = np.float32
 LINEARS = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
@@ -169,14 +169,17 @@ class OracleModel:
         self.quant = None
 
     # -- exit river ---------------------------------------------------------
-    def quantize_exit_layers(self):
-        """Build the exit river: a W4 copy of every linear of every layer."""
+    def quantize_exit_layers(self, method: str = "rtn"):
+        """Build the exit river: a W4 copy of every linear of every layer, by
+        min-max rounding (``"rtn"``) or with HQQ's zero-point refinement
+        (``"hqq"``, section 六)."""
+        quant = {"rtn": quantize_linear, "hqq": quantize_linear_hqq}[method]
         self.quant = []
         self.exit = []
         for lw in self.backbone:
             qd, ed = {}, {}
             for name in LINEARS:
-                qw, s, z = quantize_linear(lw[name], self.shape.group_size)
+                qw, s, z = quant(lw[name], self.shape.group_size)
                 qd[name] = (qw, s, z)
                 ed[name] = dequantize_linear(qw, s, z, lw[name].shape[1], self.shape.group_size)
             self.quant.append(qd)
@@ -186,6 +189,30 @@ class OracleModel:
     def copy_exit_layers_unquantized(self):
         """Exit river built from the unquantized weights (invariant tests)."""
         self.exit = [{k: v.copy() for k, v in lw.items()} for lw in self.backbone]
+
+    # -- exit-vs-backbone K/V similarity (diagnostic) -------------------------
+    def exit_kv_cosine(self, l: int, h: np.ndarray, pos: int = 0) -> np.ndarray:
+        """Section 三: the K/V an exit layer writes into the backbone's slot
+        stays close to what the backbone layer would have written.  For
+        residual rows ``h [B][d]`` entering layer ``l`` (0-based) at position
+        ``pos``, the cosine per sequence and KV head between the exit layer's
+        and the backbone layer's cache entries: ``[B][2][Hkv]`` (K, then V),
+        each side RMSNorm'd, projected and (K) rotated as the layer does."""
+        S = self.shape
+        Hkv, hd = S.n_kv_heads, S.head_dim
+        h = np.asarray(h, F32)
+        B = h.shape[0]
+        x = rmsnorm(h, self.w["layers"][l]["g_attn"], S.rms_eps)
+        posa = np.array([pos])
+        out = np.empty((B, 2, Hkv), F32)
+        for j, name in enumerate(("wk", "wv")):
+            yb = (x @ self.backbone[l][name].T).astype(F32).reshape(B, 1, Hkv, hd)
+            ye = (x @ self.exit[l][name].T).astype(F32).reshape(B, 1, Hkv, hd)
+            if name == "wk":
+                yb = rope(yb, posa, S.rope_theta)
+                ye = rope(ye, posa, S.rope_theta)
+            out[:, j, :] = cosine(yb[:, 0], ye[:, 0])
+        return out
 
     # -- one decoder layer -------------------------------------------------
     def layer(self, l: int, W: dict, h: np.ndarray, st: KVState, pos0: int) -> np.ndarray:
