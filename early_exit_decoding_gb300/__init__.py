@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libriver.so")
 
 RL_OK, RL_ERR_INVALID_ARG, RL_ERR_OOM, RL_ERR_CUDA, RL_ERR_CAPACITY, RL_ERR_STATE, \
     RL_ERR_DEVICE, RL_ERR_UNSUPPORTED = range(8)
-RL_DEVERR_TOKEN, RL_DEVERR_CAPACITY, RL_DEVERR_SCHEDULE = 1, 2, 4
+RL_DEVERR_TOKEN, RL_DEVERR_CAPACITY, RL_DEVERR_SCHEDULE, RL_DEVERR_TIMEOUT = 1, 2, 4, 8
 RL_EXIT_TAU, RL_EXIT_FORCED = 0, 1
 RL_WQ, RL_WK, RL_WV, RL_WO, RL_WG, RL_WU, RL_WD = range(7)
 LINEAR_NAMES = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
@@ -30,6 +30,7 @@ EXPORTS = (
     "rl_decode_step", "rl_decode_step_host", "rl_sync", "rl_decode_kernel_count",
     "rl_kv_set_profiling", "rl_kv_profile", "rl_kv_timeline", "rl_lm_head_static", "rl_kv_set_decode_path",
     "rl_kv_decode_path", "rl_save_exit_layers", "rl_load_exit_layers", "rl_exit_kv_cosine",
+    "rl_kv_set_wait_limit", "rl_debug_fail_allocations",
 )
 RL_PATH_AUTO, RL_PATH_STEP, RL_PATH_FUSED, RL_PATH_GENERIC = range(4)
 KERNEL_KINDS = ("embed", "qkv", "attention", "group_sums", "o_proj", "norm", "gate_up", "down",
@@ -99,6 +100,8 @@ def _load():
         "rl_kv_decode_path": (I, [P, I]),
         "rl_save_exit_layers": (I, [P, ctypes.c_char_p]),
         "rl_exit_kv_cosine": (I, [P, I, P, I, P, P]),
+        "rl_kv_set_wait_limit": (I, [P, ctypes.c_int64]),
+        "rl_debug_fail_allocations": (I, [ctypes.c_int64]),
         "rl_load_exit_layers": (I, [P, ctypes.c_char_p, P]),
     }
     for name, (res, args) in sig.items():
@@ -241,6 +244,18 @@ def rl_lm_head_static(model, d_h, B, d_logits, d_next_token=None, d_err=None, st
     library's static scratch (allocates nothing)."""
     _check(_lib.rl_lm_head_static(model, _ptr(d_h), B, _ptr(d_logits), _ptr(d_next_token),
                                   _ptr(d_err), _stream(stream)))
+
+
+def rl_kv_set_wait_limit(kv, polls):
+    """Test hook: grid-barrier / first GEMM-epilogue waits give up after
+    ``polls`` polls (0 = the kernels' own limits)."""
+    _check(_lib.rl_kv_set_wait_limit(kv, int(polls)))
+
+
+def rl_debug_fail_allocations(after):
+    """Test hook: the next ``after`` library allocations succeed, later ones
+    fail (RL_ERR_OOM); negative switches it off."""
+    _check(_lib.rl_debug_fail_allocations(int(after)))
 
 
 def rl_kv_set_decode_path(kv, path):

@@ -6,6 +6,7 @@
 // in the kernels of this library; the host only validates arguments and
 // enqueues launches.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -29,6 +30,20 @@ rl_status fail(rl_status s, const char* fmt, ...) {
   va_end(ap);
   g_err = buf;
   return s;
+}
+
+// Allocation-failure injection (rl_debug_fail_allocations): the number of
+// library allocations that may still succeed; negative = no injection.
+std::atomic<long long> g_alloc_budget{-1};
+
+// True when the next allocation must fail (and counts the one that may not).
+bool alloc_injected_failure() {
+  long long b = g_alloc_budget.load();
+  while (b >= 0) {
+    if (b == 0) return true;
+    if (g_alloc_budget.compare_exchange_weak(b, b - 1)) return false;
+  }
+  return false;
 }
 
 #define RL_CUDA(call)                                                                    \
@@ -92,6 +107,7 @@ struct rl_model {
   rl_status alloc(T** p, size_t n) {
     void* q = nullptr;
     if (n == 0) n = 1;
+    if (alloc_injected_failure()) return fail(RL_ERR_OOM, "cudaMalloc(%zu bytes): injected failure", n * sizeof(T));
     cudaError_t e = cudaMalloc(&q, n * sizeof(T));
     if (e != cudaSuccess) {
       cudaGetLastError();
@@ -123,11 +139,12 @@ struct GraphKey {
   int prof = 0;  // 0 off, 1 event records, 2 + per-CTA timeline
   bool fused = false;
   bool step = false;
+  long long wait = 0;  // rl_kv_set_wait_limit
   bool operator==(const GraphKey& o) const {
     return B == o.B && mode == o.mode && tau == o.tau && sched == o.sched &&
            sched_len == o.sched_len && tokens == o.tokens && logits == o.logits &&
            next == o.next && exit == o.exit && min_cos == o.min_cos && trace == o.trace &&
-           prof == o.prof && fused == o.fused && step == o.step;
+           prof == o.prof && fused == o.fused && step == o.step && wait == o.wait;
   }
 };
 
@@ -174,6 +191,7 @@ struct rl_kv {
   float* st_end = nullptr;  // per-tile (|h_out|^2, <h_in,h_out>, |h_in|^2) of the layer [d/16][8][3]
   bool use_fused = true;
   int path_pref = RL_PATH_AUTO;  // rl_kv_set_decode_path
+  long long wait_limit = 0;      // rl_kv_set_wait_limit (0: the kernels' own limits)
   // persistent step kernel
   bool use_step = true;
   unsigned* bars = nullptr;           // per-CTA phase flags [n_bars], 128 bytes apart
@@ -217,6 +235,7 @@ struct rl_kv {
   rl_status alloc(T** p, size_t n) {
     void* q = nullptr;
     if (n == 0) n = 1;
+    if (alloc_injected_failure()) return fail(RL_ERR_OOM, "cudaMalloc(%zu bytes): injected failure", n * sizeof(T));
     cudaError_t e = cudaMalloc(&q, n * sizeof(T));
     if (e != cudaSuccess) {
       cudaGetLastError();
@@ -391,6 +410,7 @@ rl_status project(const rl_model* m, rl_kv* kv, const CUtensorMap& tm, const CUt
   a.tc_ws_floats = kv->tc_ws_floats;
   a.tc_ticket = kv->tc_ticket;
   a.tc_ticket_n = kv->tc_ticket_n;
+  a.first_wait = kv->wait_limit;
   if (a.B >= kTcMinTokens) {
     // the tensor-core GEMM runs bf16 layers and, when the projection has
     // enough output tiles, the W4 exit-river layers (dequantised in shared
@@ -1120,6 +1140,7 @@ rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStre
   a.kv_rows_layer = kv->maxB * m->Hkv * kv->Tmax;
   a.xs_row_bytes = step_kmax(m) * 2 + 64;
   a.gmax = step_kmax(m) / kGroup;
+  a.bar_wait = kv->wait_limit;
   const size_t smem = step_smem_bytes(B, step_kmax(m), a.gmax, &a.nslot);
   if (!smem) return fail(RL_ERR_UNSUPPORTED, "step kernel does not fit");
   const bool prof = kv->profiling;
@@ -1355,7 +1376,36 @@ namespace {
 // order) and, per fused matrix, the W4 layout; `fill` writes them (the
 // quantizer, or the views uploaded from a file), then the unit-tiled copies.
 template <typename Fill>
+rl_status build_exit_river_allocs(rl_model* m, cudaStream_t s, Fill fill);
+
+// Builds the exit river; on any failure every allocation it made is released
+// and the model is left as it was (no exit river).
+template <typename Fill>
 rl_status build_exit_river(rl_model* m, cudaStream_t s, Fill fill) {
+  const size_t mark = m->allocs.size();
+  const size_t bytes0 = m->bytes;
+  const rl_status st = build_exit_river_allocs(m, s, fill);
+  if (st == RL_OK) return RL_OK;
+  cudaStreamSynchronize(s);  // nothing enqueued may still use what is freed
+  cudaGetLastError();
+  for (size_t i = mark; i < m->allocs.size(); ++i) cudaFree(m->allocs[i]);
+  m->allocs.resize(mark);
+  m->bytes = bytes0;
+  m->views.clear();
+  m->d_views = nullptr;
+  for (Layer& ly : m->layers)
+    for (Linear* lin : {&ly.qkv, &ly.o, &ly.gu, &ly.dn}) {
+      lin->qw = nullptr;
+      lin->sz = nullptr;
+      lin->qwt = nullptr;
+      lin->has_tmq = false;
+    }
+  m->quantized = false;
+  return st;
+}
+
+template <typename Fill>
+rl_status build_exit_river_allocs(rl_model* m, cudaStream_t s, Fill fill) {
   const int L = m->L;
   m->views.assign((size_t)L * 7, NSView{});
   const int outs[7] = {m->Hq * m->hd, m->Hkv * m->hd, m->Hkv * m->hd, m->d, m->F, m->F, m->d};
@@ -1715,6 +1765,18 @@ rl_status rl_kv_set_position(rl_kv* kv, int32_t pos, int32_t decode_step, rl_str
   return RL_OK;
 }
 
+rl_status rl_kv_set_wait_limit(rl_kv* kv, int64_t polls) {
+  if (!kv) return fail(RL_ERR_INVALID_ARG, "kv is NULL");
+  if (polls < 0) return fail(RL_ERR_INVALID_ARG, "polls must be >= 0");
+  kv->wait_limit = polls;
+  return RL_OK;
+}
+
+rl_status rl_debug_fail_allocations(int64_t after) {
+  g_alloc_budget.store(after < 0 ? -1 : after);
+  return RL_OK;
+}
+
 rl_status rl_kv_set_decode_path(rl_kv* kv, int32_t path) {
   if (!kv) return fail(RL_ERR_INVALID_ARG, "kv is NULL");
   if (path < RL_PATH_AUTO || path > RL_PATH_GENERIC) return fail(RL_ERR_INVALID_ARG, "unknown path %d", path);
@@ -1753,6 +1815,7 @@ rl_status rl_prefill(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_t B,
                        M * (2 * Gd + Go + Gf) * 4 + M * m->Hq * m->hd * 4 +
                        M * m->Hq * (m->hd + 2) * 4 + M * 4 + 32 * 256;  // + alignment slack of the carve-up
   char* base = nullptr;
+  if (alloc_injected_failure()) return fail(RL_ERR_OOM, "prefill workspace: injected allocation failure");
   RL_CUDA(cudaMallocAsync((void**)&base, bytes, s));
   RL_CUDA(cudaMemsetAsync(base, 0, bytes, s));
   char* p = base;
@@ -1831,6 +1894,7 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
     key.prof = kv->profiling ? (kv->timeline ? 2 : 1) : 0;
     key.fused = fused;
     key.step = step;
+    key.wait = kv->wait_limit;
     if (!kv->exec || !(key == kv->key)) {
       if (step) RL_TRY(prepare_step_phases(m, kv, io, s));
       cudaGraph_t g = nullptr;

@@ -196,7 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           s_abort = 1;
           return false;
         }
-        return true;
+        // consumers that aborted free slots without waiting for their copies:
+        // never issue into such a slot (the arrival orders their abort flag
+        // before it)
+        return !s_abort;
       };
       for (int p = 0; p < a.nph && !s_abort; ++p) {
         const PhaseDesc* D = a.ph + p;
@@ -330,9 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         // every CTA has finished phase p - 1: thread j waits for CTA j's flag
         // (CTA j stores p after its phase p - 1; flags sit 128 bytes apart)
         const unsigned* fp = a.bars + (size_t)ct * 32;
-        long long i = 0;
-        while (ld_acquire(fp) < (unsigned)p && i < kSpinBar) ++i;
-        if (i >= kSpinBar) {
+        const long long lim = a.bar_wait > 0 ? a.bar_wait : kSpinBar;
+        bool arrived = false;
+        for (long long i = 0; i < lim && !arrived; ++i) arrived = ld_acquire(fp) >= (unsigned)p;
+        if (!arrived) {
           atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
           s_abort = 1;
         }
@@ -348,7 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
       if (D.kind == PH_GEMV) {
         const int Kp = D.Kp, G = Kp >> 7;
         // ---- activation rows (bulk copy), concurrently with the statistics ----
-        if (D.xmode != X_EMBED && ct == 0 && !s_abort) {
+        // (issued and waited for even after an abort: the CTA never leaves
+        // with a copy in flight)
+        if (D.xmode != X_EMBED && ct == 0) {
           mbar_expect_tx(&xbar, (uint32_t)B * Kp * 2);
           for (int b = 0; b < B; ++b)
             bulk_g2s(xs + (size_t)b * RSX, D.xg + (size_t)b * D.ldxg, (uint32_t)Kp * 2, &xbar);
@@ -542,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           if (D.gnext) pre_gn = D.gnext[n];
         }
         if (D.xmode != X_EMBED) {
-          if (!s_abort && !mbar_wait(&xbar, xpar, kSpin)) {
+          if (!mbar_wait(&xbar, xpar, kSpin)) {
             if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
             s_abort = 1;
           }
@@ -973,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                   for (int h = 0; h < REP; ++h)
                     bulk_g2s(stage_of(h), hp + (size_t)h * a.part_cap * PS, (uint32_t)(nch * PS * 4), &xbar);
                 }
-                if (!s_abort && !mbar_wait(&xbar, xpar, kSpin)) {
+                if (!mbar_wait(&xbar, xpar, kSpin)) {  // waited for even after an abort
                   if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
                   s_abort = 1;
                 }

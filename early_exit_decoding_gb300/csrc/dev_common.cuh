@@ -41,6 +41,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, long lon
     if (mbar_try(b, parity)) return true;
   return false;
 }
+// Non-blocking poll of an mbarrier phase (test_wait never suspends), at most
+// `limit` times: for waits given a short, exact limit.
+__device__ __forceinline__ bool mbar_poll(uint64_t* b, uint32_t parity, long long limit) {
+  for (long long i = 0; i < limit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
 // Bulk global -> shared copy completing `bytes` on mbarrier `bar` (16-byte
 // aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

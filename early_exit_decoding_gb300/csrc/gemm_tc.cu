@@ -497,7 +497,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int t = u / S;
       const int acc = i & 1, ua = i >> 1;
       const int n0 = (t / tiles_m) * kBM, m0 = (t % tiles_m) * BN;
-      const bool got = dev::mbar_wait(&acc_full[acc], ua & 1, kSpinTc);
+      // (a wait limit below the default only shortens this wait: every wait
+      // that keeps MMAs or copies from outliving the CTA keeps its own)
+      const bool got = a.first_wait > 0 ? dev::mbar_poll(&acc_full[acc], ua & 1, a.first_wait)
+                                        : dev::mbar_wait(&acc_full[acc], ua & 1, kSpinTc);
       if (!got) s_fail = 1;
       if (S > 1) {
         // every epilogue warp takes the same decision after the barrier (a wait

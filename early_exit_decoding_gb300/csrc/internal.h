@@ -103,6 +103,7 @@ struct GemvArgs {
   float* tc_ws; size_t tc_ws_floats; unsigned* tc_ticket; int tc_ticket_n;
   int ksplit;             // set by launch_gemm_tc
   int tc_w4;              // k_gemm_tc runs the W4 path too (else it returns at once for W4 layers)
+  long long first_wait;   // k_gemm_tc: polls of the epilogue's accumulator wait (0: the default)
 };
 
 void launch_gemv(const GemvArgs& a, int sm_count, cudaStream_t s);
@@ -376,6 +377,7 @@ struct StepArgs {
   int gmax;                   // max 128-input groups over the phases
   unsigned long long* tl;     // optional timeline: [nph] first starts, then [nph] last ends
   unsigned long long* tl2;    // optional per-CTA timeline [nph][grid][kTl2] (globaltimer ns)
+  long long bar_wait;         // polls of a grid-barrier wait before it gives up (0: the default)
 };
 // Stamps of the per-CTA timeline, per (phase, CTA).
 enum Tl2Stamp {

@@ -312,6 +312,28 @@ RL_API rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32
 RL_API rl_status rl_kv_timeline(rl_kv* kv, rl_stream_t stream, int64_t cap, uint64_t* out,
                                 int32_t* nphase, int32_t* nctas, int32_t* nstamps);
 
+/* Failure injection for tests (the pages describe no failure handling; these
+ * make the library's own failure paths run without faulting a GPU).
+ *
+ * rl_kv_set_wait_limit: from the next decode step or prefill on `kv` (a
+ * decode graph is captured again), the persistent step kernel's grid-wide
+ * phase barrier and the tensor-core GEMM's first accumulator wait give up
+ * after `polls` polls (0 restores the kernels' own limits, about a second
+ * or more).  A wait that gives up sets RL_DEVERR_TIMEOUT; the kernel then
+ * finishes its phases without computing, waits (with its own limits) for
+ * every copy and tensor-core operation it issued, frees its tensor memory
+ * and exits, so rl_sync reports RL_ERR_DEVICE and the context stays usable.
+ * The step's outputs and its K/V slot are then invalid: rewind the position
+ * (rl_kv_set_position) and run the step again.
+ *
+ * rl_debug_fail_allocations: the next `after` device allocations made by
+ * the library succeed and every later one fails as if cudaMalloc had
+ * (RL_ERR_OOM), until it is called with a negative value (the default: no
+ * injection).  Process-wide; not thread-safe with respect to concurrent
+ * allocating calls. */
+RL_API rl_status rl_kv_set_wait_limit(rl_kv* kv, int64_t polls);
+RL_API rl_status rl_debug_fail_allocations(int64_t after);
+
 /* Number of kernels one decode step launches for batch B (for launch
  * accounting); 0 on bad arguments. */
 RL_API int32_t rl_decode_kernel_count(const rl_model* m, int32_t B);

@@ -37,3 +37,15 @@ def test_host_side_argument_errors_need_no_gpu():
     assert e.value.status == river.RL_ERR_INVALID_ARG
     assert river.rl_decode_kernel_count(None, 1) == 0
     assert "NULL" in river.rl_last_error() or river.rl_last_error()
+
+
+def test_failure_injection_hooks_are_host_side():
+    """The allocation-failure hook is a host-side switch: it can be set and
+    cleared without a GPU, and rl_kv_set_wait_limit rejects a NULL cache."""
+    import early_exit_decoding_gb300 as river
+    import pytest
+    river.rl_debug_fail_allocations(3)
+    river.rl_debug_fail_allocations(-1)
+    with pytest.raises(river.RiverError) as e:
+        river.rl_kv_set_wait_limit(None, 1)
+    assert e.value.status == river.RL_ERR_INVALID_ARG
