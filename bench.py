@@ -457,6 +457,25 @@ def run_8b_b1(args, world, hbm_peak, peak_src):
             "kernel_time_shares_no_exit": shares,
             "clocks": ck,
         }
+        # backbone offloading: layers L/2+1..L in pinned host memory, read over
+        # NVLink-C2C only by steps that run them on the backbone
+        first = S.n_layers // 2
+        dev0, _ = arm.model.memory()
+        arm.model.offload_backbone(first, arm.stream)
+        dev1, host1 = arm.model.memory()
+        ms_fo, _, _ = arm.timed(arm.forced, K, W)
+        Kn = min(K, 8)
+        ms_no, _, _ = arm.timed(arm.river.Policy.tau_(1.01), Kn, W)
+        idx = timed_indices(arm.sched_np, K)
+        touch = sum(int(arm.sched_np[j]) > first for j in idx)
+        out["offload"] = {
+            "offloaded_layers": f"{first + 1}..{S.n_layers} (backbone bf16 weights in pinned host memory)",
+            "device_bytes_resident": dev0, "device_bytes_offloaded": dev1, "host_bytes": host1,
+            "forced": {"tokens_per_s": world * B * K / (ms_fo / 1e3), "ms_per_step": ms_fo / K,
+                       "timed_steps_running_offloaded_layers_on_the_backbone": touch},
+            "full_depth_ms_per_step": ms_no / Kn,
+            "full_depth_stall_ms_per_step": ms_no / Kn - ms_n / K,
+        }
     finally:
         arm.close()
     return out

@@ -30,7 +30,8 @@ EXPORTS = (
     "rl_decode_step", "rl_decode_step_host", "rl_sync", "rl_decode_kernel_count",
     "rl_kv_set_profiling", "rl_kv_profile", "rl_kv_timeline", "rl_lm_head_static", "rl_kv_set_decode_path",
     "rl_kv_decode_path", "rl_save_exit_layers", "rl_load_exit_layers", "rl_exit_kv_cosine",
-    "rl_kv_set_wait_limit", "rl_debug_fail_allocations",
+    "rl_kv_set_wait_limit", "rl_debug_fail_allocations", "rl_model_offload_backbone",
+    "rl_model_memory",
 )
 RL_PATH_AUTO, RL_PATH_STEP, RL_PATH_FUSED, RL_PATH_GENERIC = range(4)
 KERNEL_KINDS = ("embed", "qkv", "attention", "group_sums", "o_proj", "norm", "gate_up", "down",
@@ -101,6 +102,8 @@ def _load():
         "rl_save_exit_layers": (I, [P, ctypes.c_char_p]),
         "rl_exit_kv_cosine": (I, [P, I, P, I, P, P]),
         "rl_kv_set_wait_limit": (I, [P, ctypes.c_int64]),
+        "rl_model_offload_backbone": (I, [P, I, P]),
+        "rl_model_memory": (I, [P, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
         "rl_debug_fail_allocations": (I, [ctypes.c_int64]),
         "rl_load_exit_layers": (I, [P, ctypes.c_char_p, P]),
     }
@@ -246,6 +249,17 @@ def rl_lm_head_static(model, d_h, B, d_logits, d_next_token=None, d_err=None, st
                                   _ptr(d_err), _stream(stream)))
 
 
+def rl_model_offload_backbone(model, first_layer, stream=None):
+    _check(_lib.rl_model_offload_backbone(model, int(first_layer), _stream(stream)))
+
+
+def rl_model_memory(model):
+    """(device bytes, pinned host bytes) the model holds."""
+    d, h = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(_lib.rl_model_memory(model, ctypes.byref(d), ctypes.byref(h)))
+    return d.value, h.value
+
+
 def rl_kv_set_wait_limit(kv, polls):
     """Test hook: grid-barrier / first GEMM-epilogue waits give up after
     ``polls`` polls (0 = the kernels' own limits)."""
@@ -383,6 +397,14 @@ class Model:
     def load_exit_layers(self, path, stream=None):
         """Build the exit river from a file written by save_exit_layers."""
         rl_load_exit_layers(self.handle, path, stream)
+
+    def offload_backbone(self, first_layer, stream=None):
+        """Backbone weights of layers first_layer.. (0-based) to pinned host memory."""
+        rl_model_offload_backbone(self.handle, first_layer, stream)
+
+    def memory(self):
+        """(device bytes, pinned host bytes) the model holds."""
+        return rl_model_memory(self.handle)
 
     def exit_kv_cosine(self, layer, h, stream=None):
         """Cosine between the exit layer's and the backbone layer's K and V of

@@ -71,6 +71,10 @@ struct Linear {
   CUtensorMap tmq;          // TMA map of qw for the tensor-core GEMM (8 words x 128 rows)
   bool has_tmq = false;
   const CUtensorMap* tmq_ptr() const { return has_tmq ? &tmq : nullptr; }
+  // backbone offloading: w and wt live in host memory (w_host / wt points
+  // there); w points into the model's device staging buffer
+  bool offloaded = false;
+  const bf16* w_host = nullptr;
 };
 
 struct Layer {
@@ -118,8 +122,25 @@ struct rl_model {
     *p = static_cast<T*>(q);
     return RL_OK;
   }
+  // backbone offloading (rl_model_offload_backbone)
+  int offload_from = -1;          // first offloaded layer (0-based), -1: none
+  bf16* stage = nullptr;          // device buffer one offloaded layer's [N][Kp] weights are staged in
+  std::vector<void*> host_allocs; // pinned host memory of the offloaded layers
+  size_t host_bytes = 0;
+  int epoch = 0;                  // bumped when weight pointers move (decode graphs are captured again)
   ~rl_model() {
     for (void* p : allocs) cudaFree(p);
+    for (void* p : host_allocs) cudaFreeHost(p);
+  }
+  // Releases one device allocation made by alloc().
+  void release(void* p, size_t nbytes) {
+    for (size_t i = 0; i < allocs.size(); ++i)
+      if (allocs[i] == p) {
+        cudaFree(p);
+        allocs.erase(allocs.begin() + (long)i);
+        bytes -= nbytes;
+        return;
+      }
   }
 };
 
@@ -140,11 +161,13 @@ struct GraphKey {
   bool fused = false;
   bool step = false;
   long long wait = 0;  // rl_kv_set_wait_limit
+  int epoch = 0;       // the model's weight-placement epoch
   bool operator==(const GraphKey& o) const {
     return B == o.B && mode == o.mode && tau == o.tau && sched == o.sched &&
            sched_len == o.sched_len && tokens == o.tokens && logits == o.logits &&
            next == o.next && exit == o.exit && min_cos == o.min_cos && trace == o.trace &&
-           prof == o.prof && fused == o.fused && step == o.step && wait == o.wait;
+           prof == o.prof && fused == o.fused && step == o.step && wait == o.wait &&
+           epoch == o.epoch;
   }
 };
 
@@ -425,6 +448,20 @@ rl_status project(const rl_model* m, rl_kv* kv, const CUtensorMap& tm, const CUt
   return RL_OK;
 }
 
+// An offloaded layer's [N][Kp] weights into the device staging buffer, unless
+// the device-side exit state says the layer runs on the exit river.
+rl_status stage_layer(const rl_model* m, rl_kv* kv, int l, int w4mode, cudaStream_t s) {
+  const Layer& ly = m->layers[l];
+  if (!ly.qkv.offloaded) return RL_OK;
+  const int* ex = w4mode == W4_BY_LAYER ? &kv->st->exit_layer : nullptr;
+  for (const Linear* lin : {&ly.qkv, &ly.o, &ly.gu, &ly.dn}) {
+    launch_stage_weights(lin->w_host, const_cast<bf16*>(lin->w), (size_t)lin->N * lin->Kp * 2, ex, l + 1,
+                         m->sm_count, s);
+    RL_LAUNCHED();
+  }
+  return RL_OK;
+}
+
 rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, cudaStream_t s) {
   const int L = m->L, d = m->d;
   Prof pf{kv, s, kv->profiling && !io.prefill};
@@ -470,6 +507,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
   for (int l = 0; l < L; ++l) {
     const Layer& ly = m->layers[l];
     const int mid = (cur + 1) % 3, nxt = (cur + 2) % 3;
+    RL_TRY(stage_layer(m, kv, l, w4mode, s));
     // QKV + RoPE + KV append
     {
       GemvArgs a = gemv_base(m, ly.qkv, w4mode, kv->st, l + 1);
@@ -736,6 +774,7 @@ rl_status enqueue_decode_fused(rl_model* m, rl_kv* kv, const StepIO& io, int nch
   for (int l = 0; l < L; ++l) {
     const Layer& ly = m->layers[l];
     const int mid = (cur + 1) % 3, nxt = (cur + 2) % 3;
+    RL_TRY(stage_layer(m, kv, l, w4mode, s));
     // QKV: exit decision of layer l (l >= 1), RMSNorm scale, projection, RoPE, KV append
     {
       FusedArgs a = base(ly.qkv, l + 1);
@@ -963,6 +1002,7 @@ std::vector<PhaseDesc> build_step_phases(rl_model* m, rl_kv* kv, const StepIO& i
     p.kind = PH_GEMV;
     p.layer_no = layer_no;
     p.wt = lin.wt;
+    p.wt_sys = lin.offloaded ? 1 : 0;
     p.qwt = m->quantized ? lin.qwt : nullptr;
     p.N = lin.N;
     p.Kp = lin.Kp;
@@ -1513,8 +1553,9 @@ rl_status rl_exit_kv_cosine(const rl_model* m, int32_t layer, const float* d_h, 
   if (B < 1 || B > 65535 / (2 * m->Hkv)) return fail(RL_ERR_INVALID_ARG, "B=%d out of range", B);
   if (!m->quantized) return fail(RL_ERR_STATE, "exit river not built");
   const Linear& q = m->layers[layer].qkv;
-  RL_CUDA(launch_exit_kv_cosine(d_h, B, m->d, m->layers[layer].g_attn, q.w, q.qw, q.sz, q.Kp, m->Hq,
-                                m->Hkv, m->hd, d_cos, as_stream(stream)));
+  // an offloaded layer's weights are read from host memory (plain loads)
+  RL_CUDA(launch_exit_kv_cosine(d_h, B, m->d, m->layers[layer].g_attn, q.offloaded ? q.w_host : q.w, q.qw,
+                                q.sz, q.Kp, m->Hq, m->Hkv, m->hd, d_cos, as_stream(stream)));
   return RL_OK;
 }
 
@@ -1895,6 +1936,7 @@ rl_status rl_decode_step(rl_model* m, rl_kv* kv, const int32_t* d_tokens, int32_
     key.fused = fused;
     key.step = step;
     key.wait = kv->wait_limit;
+    key.epoch = m->epoch;
     if (!kv->exec || !(key == kv->key)) {
       if (step) RL_TRY(prepare_step_phases(m, kv, io, s));
       cudaGraph_t g = nullptr;
@@ -2120,14 +2162,104 @@ rl_status rl_kv_profile(rl_kv* kv, rl_stream_t stream, int32_t cap, int32_t* kin
 int32_t rl_decode_kernel_count(const rl_model* m, int32_t B) {
   if (!m || B < 1) return 0;
   if (step_fits_model(m, B)) return 1;  // one persistent kernel per step
+  // offloaded layers: four staging launches each on the other paths
+  const int stage = m->offload_from >= 0 ? 4 * (m->L - m->offload_from) : 0;
   if (fused_fits(m, B))  // fused path: QKV, attention, O, gate/up, down; LM head
-    return m->L * 5 + 1;
+    return m->L * 5 + 1 + stage;
   // per layer: QKV, attention (stream + combine, or one fused launch), group
   // sums (up to kTcW4AllTokens tokens), O, RMSNorm, gate/up, group sums, down,
   // layer end
   const int attn = attn_stream_supported(m->Hq / m->Hkv, m->hd) ? 2 : 1;
   const int gsum = B <= kTcW4AllTokens ? 2 : 0;
-  return 1 + m->L * (6 + gsum + attn) + 1 + 1;
+  return 1 + m->L * (6 + gsum + attn) + 1 + 1 + stage;
+}
+
+rl_status rl_model_offload_backbone(rl_model* m, int32_t first_layer, rl_stream_t stream) {
+  if (!m) return fail(RL_ERR_INVALID_ARG, "model is NULL");
+  if (first_layer < 0 || first_layer > m->L)
+    return fail(RL_ERR_INVALID_ARG, "first_layer %d outside [0, %d]", first_layer, m->L);
+  if (!m->quantized) return fail(RL_ERR_STATE, "build the exit river before offloading the backbone");
+  if (m->offload_from >= 0) return fail(RL_ERR_STATE, "the backbone is already offloaded");
+  if (first_layer == m->L) return RL_OK;
+  cudaStream_t s = as_stream(stream);
+  RL_CUDA(cudaStreamSynchronize(s));
+  // the staging buffer: one layer's four [N][Kp] matrices
+  const Layer& l0 = m->layers[first_layer];
+  size_t stage_elems = 0;
+  for (const Linear* lin : {&l0.qkv, &l0.o, &l0.gu, &l0.dn}) stage_elems += (size_t)lin->N * lin->Kp;
+  bf16* stage = nullptr;
+  RL_TRY(m->alloc(&stage, stage_elems));
+  // host copies first: nothing is released until every layer has its copy
+  struct Move { Linear* lin; bf16* hw; bf16* hwt; size_t off; };
+  std::vector<Move> moves;
+  auto undo = [&](rl_status st) {
+    for (Move& mv : moves) {
+      cudaFreeHost(mv.hw);
+      cudaFreeHost(mv.hwt);
+    }
+    m->release(stage, stage_elems * sizeof(bf16));
+    return st;
+  };
+  for (int l = first_layer; l < m->L; ++l) {
+    Layer& ly = m->layers[l];
+    size_t off = 0;
+    for (Linear* lin : {&ly.qkv, &ly.o, &ly.gu, &ly.dn}) {
+      const size_t nb = (size_t)lin->N * lin->Kp * sizeof(bf16);
+      Move mv{lin, nullptr, nullptr, off};
+      off += (size_t)lin->N * lin->Kp;
+      if (alloc_injected_failure() || cudaHostAlloc((void**)&mv.hw, nb, cudaHostAllocMapped) != cudaSuccess) {
+        cudaGetLastError();
+        return undo(fail(RL_ERR_OOM, "pinned host memory for layer %d", l + 1));
+      }
+      if (alloc_injected_failure() || cudaHostAlloc((void**)&mv.hwt, nb, cudaHostAllocMapped) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeHost(mv.hw);
+        return undo(fail(RL_ERR_OOM, "pinned host memory for layer %d", l + 1));
+      }
+      moves.push_back(mv);
+      if (cudaMemcpy(mv.hw, lin->w, nb, cudaMemcpyDeviceToHost) != cudaSuccess ||
+          cudaMemcpy(mv.hwt, lin->wt, nb, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return undo(fail(RL_ERR_CUDA, "copying layer %d to host memory", l + 1));
+      }
+    }
+  }
+  // device addresses of the host copies (the same as the host ones with
+  // unified addressing), the staging buffer's tensor maps
+  for (Move& mv : moves) {
+    void *dw = nullptr, *dwt = nullptr;
+    if (cudaHostGetDevicePointer(&dw, mv.hw, 0) != cudaSuccess ||
+        cudaHostGetDevicePointer(&dwt, mv.hwt, 0) != cudaSuccess) {
+      cudaGetLastError();
+      return undo(fail(RL_ERR_CUDA, "device address of pinned host memory"));
+    }
+    CUtensorMap tm;
+    if (!make_weight_tmap(&tm, stage + mv.off, mv.lin->N, mv.lin->Kp))
+      return undo(fail(RL_ERR_CUDA, "tensor map of the staging buffer"));
+    Linear& lin = *mv.lin;
+    const size_t nb = (size_t)lin.N * lin.Kp * sizeof(bf16);
+    m->release(lin.w, nb);
+    m->release(lin.wt, nb);
+    lin.w_host = static_cast<const bf16*>(dw);
+    lin.wt = static_cast<bf16*>(dwt);
+    lin.w = stage + mv.off;
+    lin.tm = tm;
+    lin.offloaded = true;
+    m->host_allocs.push_back(mv.hw);
+    m->host_allocs.push_back(mv.hwt);
+    m->host_bytes += 2 * nb;
+  }
+  m->stage = stage;
+  m->offload_from = first_layer;
+  ++m->epoch;
+  return RL_OK;
+}
+
+rl_status rl_model_memory(const rl_model* m, uint64_t* device_bytes, uint64_t* host_bytes) {
+  if (!m) return fail(RL_ERR_INVALID_ARG, "model is NULL");
+  if (device_bytes) *device_bytes = m->bytes;
+  if (host_bytes) *host_bytes = m->host_bytes;
+  return RL_OK;
 }
 
 }  // extern "C"

@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           const int layer_no = D->layer_no;
           const unsigned char* qwt = D->qwt;
           const bf16* wt = D->wt;
+          const bool wt_sys = D->wt_sys != 0;
           const int N = D->N, Kp = D->Kp;
           bool w4 = false;
           if (qwt && layer_no > 0) {
@@ -254,9 +255,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 const int k0 = uk * KU, kn = min(KU, Kp - k0);
                 const int slot = rp.slot;
                 const uint32_t bytes = (uint32_t)(16 * kn * 2);
-                mbar_expect_tx(&full[slot], bytes);
-                bulk_g2s(ring + (size_t)slot * SLOT_B, wt + (size_t)tl * 16 * Kp + (size_t)16 * k0, bytes,
-                         &full[slot]);
+                const unsigned char* src =
+                    reinterpret_cast<const unsigned char*>(wt + (size_t)tl * 16 * Kp + (size_t)16 * k0);
+                unsigned char* dst = ring + (size_t)slot * SLOT_B;
+                if (wt_sys) {
+                  // an offloaded layer's unit from host memory: 16-byte copies on
+                  // the load path, whose landing is the slot's one expected arrival
+                  for (uint32_t o = 0; o < bytes; o += 16) cp_async16(dst + o, src + o);
+                  cp_async_mbar_arrive(&full[slot]);
+                } else {
+                  mbar_expect_tx(&full[slot], bytes);
+                  bulk_g2s(dst, src, bytes, &full[slot]);
+                }
                 stamp_copy();
                 rp.next(NS);
                 ++issued;

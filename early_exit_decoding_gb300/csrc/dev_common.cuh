@@ -41,6 +41,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, long lon
     if (mbar_try(b, parity)) return true;
   return false;
 }
+// 16-byte asynchronous copy global -> shared (the load path of ordinary
+// loads: it also reads mapped host memory).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Arrive on mbarrier `b` once every cp.async this thread issued before has
+// landed; the arrival counts as one of the phase's expected arrivals.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* b) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(b)) : "memory");
+}
 // Non-blocking poll of an mbarrier phase (test_wait never suspends), at most
 // `limit` times: for waits given a short, exact limit.
 __device__ __forceinline__ bool mbar_poll(uint64_t* b, uint32_t parity, long long limit) {

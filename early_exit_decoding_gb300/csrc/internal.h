@@ -288,6 +288,12 @@ cudaError_t launch_exit_kv_cosine(const float* h, int B, int d, const float* g, 
                                   const uint32_t* qw, const __half2* sz, int Kp, int Hq, int Hkv,
                                   int hd, float* out, cudaStream_t s);
 
+// Offloaded backbone layers: copy `bytes` (a multiple of 16) from host memory
+// into the device staging buffer, unless *exit_layer says layer layer_no runs
+// on the exit river (exit_layer == nullptr: always copy).
+void launch_stage_weights(const void* src, void* dst, size_t bytes, const int* exit_layer, int layer_no,
+                          int sm_count, cudaStream_t s);
+
 // The internal W4 layout (qw, sz) of a fused matrix from interchange views
 // that already hold the exit layer (rl_load_exit_layers).
 void launch_w4_from_views(int N, int K, int Kp, uint32_t* qw, __half2* sz, const int2* rowmap,
@@ -308,6 +314,7 @@ struct PhaseDesc {
   int layer_no;               // 1..L; 0 = LM head (always the bf16 weights)
   // GEMV weights
   const bf16* wt;             // bf16 unit-tiled (see k_bf16_tile_layout)
+  int wt_sys;                 // 1: wt is in host memory (an offloaded backbone layer)
   const unsigned char* qwt;   // W4 unit-tiled, nullptr if there is no exit-river copy
   int N, Kp, split;           // split: tiles claimed at run time (else round-robin)
   // activations

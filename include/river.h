@@ -162,6 +162,29 @@ RL_API rl_status rl_exit_layer_view(const rl_model* m, int32_t layer, int32_t wh
                              const uint32_t** qweight, const uint16_t** scales,
                              const uint16_t** zeros, int32_t* n_rows, int32_t* n_cols);
 
+/* Backbone offloading (explainer section 五: once the exit river is built,
+ * deep backbone layers run only on the steps that do not exit before them,
+ * so their weights can live in host memory).  Moves the bf16 backbone
+ * weights of layers first_layer..L-1 (0-based) to pinned host memory (the
+ * Grace CPU's, reached over NVLink-C2C on GB300) and frees their device
+ * copies; the exit river, embedding, norms and LM head stay on the device,
+ * plus one device buffer the size of one layer's backbone weights.  A step
+ * reads an offloaded layer's weights from host memory only when it runs that
+ * layer on the backbone: the persistent step kernel copies them straight
+ * into its ring; the other paths (prefill, batches) first copy the layer
+ * into the device buffer, a copy skipped on the device when the layer runs
+ * on the exit river.  Results are unchanged; such steps are slower by the
+ * host-memory transfer.  Needs the exit river (RL_ERR_STATE otherwise; it is
+ * built from the device copies), once per model (RL_ERR_STATE after);
+ * first_layer == L offloads nothing.  RL_ERR_OOM if pinned host memory runs
+ * out (nothing is moved then).  Waits for `stream`; decode graphs captured
+ * before are captured again at their next step. */
+RL_API rl_status rl_model_offload_backbone(rl_model* m, int32_t first_layer, rl_stream_t stream);
+
+/* Device and pinned host bytes the model holds (weights, exit river,
+ * staging), excluding every rl_kv. */
+RL_API rl_status rl_model_memory(const rl_model* m, uint64_t* device_bytes, uint64_t* host_bytes);
+
 /* Exit-vs-backbone K/V similarity, a diagnostic (explainer section 三: the
  * K/V an exit layer writes into the backbone's slot stays close to what the
  * backbone layer would have written).  For B residual rows d_h [B][d_model]
