@@ -203,7 +203,7 @@ class Arm:
         self.kv = kv = self.model.kv_cache_alloc(B, T + G + 1)
         self.sched_np = synth.gen_schedule(S.n_layers, G, mean, seed=2)
         self.sched = torch.from_numpy(self.sched_np).cuda()
-        prompt = torch.from_numpy(synth.gen_tokens(S.vocab, (B, T), seed=1)).cuda()
+        self.prompt = prompt = torch.from_numpy(synth.gen_tokens(S.vocab, (B, T), seed=1)).cuda()
         self.dec_np = synth.gen_tokens(S.vocab, (G, B), seed=4)
         dec = torch.from_numpy(self.dec_np).cuda()
         self.out = {"logits": torch.empty((B, S.vocab), dtype=torch.float32, device="cuda"),
@@ -301,6 +301,25 @@ class Arm:
             tot += step_bytes(S, self.B, e, self.T + j)
         return tot
 
+    def time_prefill(self, n):
+        """Mean device time (ms) of n prefills of the prompt, after one warm-up."""
+        torch, river = self.torch, self.river
+        ms = []
+        with torch.cuda.stream(self.stream):
+            for i in range(n + 1):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(self.stream)
+                river.prefill(self.model, self.kv, self.prompt, river.Policy.tau_(1.01), out=self.out,
+                              stream=self.stream)
+                e1.record(self.stream)
+                e1.synchronize()
+                if i:
+                    ms.append(e0.elapsed_time(e1))
+            self.kv.sync(self.stream)
+        self.cur = None
+        return sum(ms) / len(ms)
+
     def profile(self, policy, n):
         """Live per-kernel records of n decode steps (a separate pass)."""
         river = self.river
@@ -340,6 +359,7 @@ def run_river(args, rank, world, dev):
                 exits.append(int(arm.out["exit_layer"].item()))
         res["tau"][tau] = (ms_t / Kw, sum(exits) / len(exits))
     res["prof"] = arm.profile(arm.forced, min(G, 64))
+    res["prefill_ms"] = arm.time_prefill(3)
 
     # end to end: host buffers through rl_decode_step_host (pinned host tokens
     # in; next tokens, exit layer and logits out), copies inside each call
@@ -674,6 +694,8 @@ def main():
                    "over_no_exit": full_ms_step / res["ms_w4"]},
         **{f"tau_{t}": {"tokens_per_s": world * B / (v[0] / 1e3), "ms_per_step": v[0],
                         "mean_exit_layer": v[1]} for t, v in res["tau"].items()},
+        "prefill": {"ms": res["prefill_ms"], "tokens_per_s": B * T / (res["prefill_ms"] / 1e3),
+                    "note": f"{B} x {T}-token prompt, full depth (tau 1.01), CUDA events"},
     }
     arm.close()
     del arm, res["arm"]

@@ -555,7 +555,24 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
     at.o = w.o;
     at.ldo = m->Ko;
     pf.begin();
-    if (prefill) {
+    if (prefill && kv->tm_ok && attn_prefill_supported(m->Hq / m->Hkv, m->hd)) {
+      // the prompt: causal flash-style attention on the tensor cores
+      AttnPrefillArgs ap;
+      memset(&ap, 0, sizeof(ap));
+      ap.tmk64 = kv->tmk64;
+      ap.tmv64 = kv->tmv64;
+      ap.layer_row0 = l * kv->maxB * m->Hkv * kv->Tmax;
+      ap.q = w.q;
+      ap.T = T;
+      ap.Hq = m->Hq;
+      ap.Hkv = m->Hkv;
+      ap.Tmax = kv->Tmax;
+      ap.nseq = io.B;
+      ap.o = w.o;
+      ap.ldo = m->Ko;
+      ap.err = &kv->st->err;
+      RL_CUDA(launch_attn_prefill(ap, m->Hq / m->Hkv, m->hd, s));
+    } else if (prefill) {
       launch_attention(at, s);
     } else if (kv->tm_ok && attn_stream_supported(m->Hq / m->Hkv, m->hd)) {
       // decode: persistent CTAs stream the chunks (TMA ring, tensor cores),

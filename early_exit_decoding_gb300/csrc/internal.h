@@ -250,6 +250,21 @@ size_t attn_stream_smem(int* nslot);
 void attn_stream_setup();
 bool attn_stream_supported(int rep, int hd);
 cudaError_t launch_attn_stream(const AttnStreamArgs& a, int rep, int hd, int grid, cudaStream_t s);
+// Causal prompt attention on the tensor cores (attn_prefill.cu): query row
+// (seq, t) of q [nseq*T][Hq*hd] attends to cache rows 0..t of its sequence;
+// o [nseq*T][ldo] bf16.
+struct AttnPrefillArgs {
+  CUtensorMap tmk64, tmv64;  // every layer's K / V cache as one 2-D tensor [rows][hd], 64 x 64 boxes
+  int layer_row0;            // first row of this layer: layer * maxB * Hkv * Tmax
+  const float* q;
+  int T, Hq, Hkv, Tmax, nseq;
+  bf16* o;
+  int ldo;
+  int* err;
+};
+bool attn_prefill_supported(int rep, int hd);
+cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, int rep, int hd, cudaStream_t s);
+
 // The combine half of launch_attention: merge a.nchunks partials into a.o.
 void launch_attention_combine(const AttnArgs& a, cudaStream_t s);
 // Context chunks per (sequence, KV head) of the fused decode attention (<= 256
