@@ -197,6 +197,8 @@ CASES_FORCED = [
     ("llama8b", 1, 2048, "prefill", PATH_STEP),
     ("llama1b", 32, 1030, "random", PATH_GENERIC),
     ("llama8b", 64, 4100, "random", PATH_GENERIC),
+    # 8 KV heads x 21 chunks of 128 exceed the 152 CTAs: two chunks per CTA
+    ("llama8b", 1, 2600, "prefill", PATH_STEP),
 ]
 
 

@@ -95,6 +95,15 @@ def _run_sequence(river, m, om, stream, policies, B=1, prompt=32, steps=16, seed
     return results, kv
 
 
+def _forced(river, sched):
+    """(gpu, oracle) policies for prefill + decode steps: prefill at sched[0],
+    decode step i at sched[1 + i]."""
+    d = torch.tensor(sched[1:], dtype=torch.int32, device="cuda")
+    return [(river.Policy.forced(torch.tensor(sched[:1], dtype=torch.int32, device="cuda")),
+             OPolicy.forced(sched[0]))] + \
+        [(river.Policy.forced(d), OPolicy.forced(e)) for e in sched[1:]]
+
+
 def test_quantizer_is_bit_exact(river, tiny):
     m, om, w = tiny
     for l in range(TINY.n_layers):
@@ -156,6 +165,18 @@ def test_batch_forced_and_ragged_shapes(river, stream):
         pol = [(river.Policy.forced(d_pre), OPolicy.forced(sched[0]))]
         pol += [(river.Policy.forced(d_sched), OPolicy.forced(e)) for e in sched[1:]]
         _run_sequence(river, m, om, stream, pol, B=B, prompt=7, steps=4, seed=5 + B)
+
+
+def test_step_attention_two_chunks_per_cta(river, tiny, stream):
+    """Batch 8 at a context of ~1300: 8 x 2 KV heads x 11 chunks of 128
+    positions exceed the 152 CTAs, so the step kernel's CTAs take two
+    attention chunks each (each chunk's partial merged with the others by the
+    last CTA of its head group)."""
+    m, om, _ = tiny
+    L = TINY.n_layers
+    sched = [L, 2, 0, L]
+    _run_sequence(river, m, om, stream, _forced(river, sched), B=8, prompt=1300, steps=3,
+                  seed=61, max_seq=1310, path="step")
 
 
 def test_exit_writes_slot_p_of_every_layer(river, tiny, stream):
