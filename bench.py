@@ -320,6 +320,29 @@ class Arm:
         self.cur = None
         return sum(ms) / len(ms)
 
+    def exit_kv_cosine(self):
+        """Per layer, the cosine between the K (and V) the exit layer would
+        write and the backbone layer's, for the residual entering the layer in
+        one full-depth decode step: minimum and mean over sequences and KV heads."""
+        torch, river, S = self.torch, self.river, self.S
+        tr = torch.zeros((S.n_layers + 1, self.B, S.d_model), dtype=torch.float32, device="cuda")
+        self.kv.set_trace(tr)
+        with torch.cuda.stream(self.stream):
+            self.step(0, river.Policy.tau_(1.01))
+            self.kv.sync(self.stream)
+        self.kv.set_trace(None)
+        out = {"k_min": [], "k_mean": [], "v_min": [], "v_mean": []}
+        with torch.cuda.stream(self.stream):
+            for l in range(S.n_layers):
+                c = self.model.exit_kv_cosine(l, tr[l], self.stream)
+                self.stream.synchronize()
+                k, v = c[:, 0].float().cpu(), c[:, 1].float().cpu()
+                out["k_min"].append(round(float(k.min()), 5))
+                out["k_mean"].append(round(float(k.mean()), 5))
+                out["v_min"].append(round(float(v.min()), 5))
+                out["v_mean"].append(round(float(v.mean()), 5))
+        return out
+
     def profile(self, policy, n):
         """Live per-kernel records of n decode steps (a separate pass)."""
         river = self.river
@@ -360,6 +383,7 @@ def run_river(args, rank, world, dev):
         res["tau"][tau] = (ms_t / Kw, sum(exits) / len(exits))
     res["prof"] = arm.profile(arm.forced, min(G, 64))
     res["prefill_ms"] = arm.time_prefill(3)
+    res["kv_cos"] = arm.exit_kv_cosine()
 
     # end to end: host buffers through rl_decode_step_host (pinned host tokens
     # in; next tokens, exit layer and logits out), copies inside each call
@@ -696,6 +720,10 @@ def main():
                         "mean_exit_layer": v[1]} for t, v in res["tau"].items()},
         "prefill": {"ms": res["prefill_ms"], "tokens_per_s": B * T / (res["prefill_ms"] / 1e3),
                     "note": f"{B} x {T}-token prompt, full depth (tau 1.01), CUDA events"},
+        "exit_kv_cosine_per_layer": {**res["kv_cos"],
+                                     "note": "cosine of the exit layer's K / V against the backbone "
+                                             "layer's for one decode step's residual entering each layer "
+                                             "(rl_exit_kv_cosine); min and mean over KV heads"},
     }
     arm.close()
     del arm, res["arm"]

@@ -1212,7 +1212,10 @@ rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStre
     cudaEventRecordWithFlags(kv->ev[0], s, cudaEventRecordExternal);
   }
   kv->step_args = a;
-  RL_CUDA(launch_decode_step(a, m->sm_count, smem, s));
+  // a CTA may take more than one attention chunk once B x KV heads x
+  // 128-position chunks of the cache's longest context exceed the grid
+  const bool multi = (long long)B * m->Hkv * ((kv->Tmax + 127) / 128) > m->sm_count;
+  RL_CUDA(launch_decode_step(a, m->sm_count, smem, multi, s));
   if (prof) {
     cudaEventRecordWithFlags(kv->ev[1], s, cudaEventRecordExternal);
     kv->nph_last = a.nph;

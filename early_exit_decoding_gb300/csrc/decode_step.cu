@@ -135,6 +135,12 @@ __device__ __forceinline__ void w4_unit(const unsigned char* st, int gi, const u
 
 }  // namespace
 
+// kMulti: the attention may give a CTA more than one chunk (contexts where
+// B x KV heads x 128-position chunks exceed the grid); each CTA then takes
+// consecutive chunks, and two chunks of one head group are folded into one
+// partial before the merge.  Otherwise chunks are dealt round-robin (one per
+// CTA at the contexts that instantiation is launched for).
+template <bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_constant__ StepArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[kMaxSlots], empty[kMaxSlots], xbar;
@@ -288,7 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           const bool two = hd * 2 * kCHP > kAttnHalf;
           const int halves = hd / 64;
           const int lrow0 = (D->layer_no - 1) * a.kv_rows_layer;
-          for (int it = cta; it < nitems && !s_abort; it += grid) {
+          // kMulti: CTA c takes the consecutive chunks c*per .. c*per + per - 1
+          // (mostly of one head group), so every group's last chunk ends in the
+          // last round; else chunks c, c + grid, ...
+          const int per = kMulti ? (nitems + grid - 1) / grid : 1;
+          const int it0 = kMulti ? cta * per : cta, it_end = kMulti ? min(nitems, cta * per + per) : nitems;
+          for (int it = it0; it < it_end && !s_abort; it += kMulti ? 1 : grid) {
             const int b = it / (Hkv * nch), rr = it % (Hkv * nch), hk = rr / nch, ch = rr % nch;
             const int start = ch * clen, end = min(start + clen, ctx);
             const int n = min(kCHP, max(0, end - start));
@@ -888,7 +899,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               reinterpret_cast<float4*>(qs)[i] = v;
             }
           };
-          for (int it = cta; it < nitems; it += grid) {
+          const int per = kMulti ? (nitems + grid - 1) / grid : 1;  // the producer's order
+          const int it0 = kMulti ? cta * per : cta, it_end = kMulti ? min(nitems, cta * per + per) : nitems;
+          // two chunks per CTA, of one head group (an even chunk count): the
+          // first one's partial is kept in shared memory and folded into the
+          // second, so a head group has nch / 2 partials to merge
+          const bool pair = kMulti && per == 2 && (nch & 1) == 0;
+          const int npart = pair ? nch / 2 : nch;
+          for (int it = it0; it < it_end; it += kMulti ? 1 : grid) {
+            const bool first = pair && it == it0;
             load_q(it);
             const int b = it / (Hkv * nch), rr = it % (Hkv * nch), hk = rr / nch, ch = rr % nch;
             const int start = ch * clen, end = min(start + clen, ctx);
@@ -914,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
               s_abort = 1;
             }
-            if (it == cta && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
+            if (it == it0 && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_X);
             unsigned char* Ks = ring + (size_t)slot * SLOT_B;
             unsigned char* Vs = two ? ring + (size_t)slot_v * SLOT_B : Ks + kAttnHalf;
             if (ok && has_new) {  // 16-byte chunk ct of the row, into its swizzled place
@@ -935,6 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             // partial; partial rows of PS floats (o[hd], max, sum, 2 pad: 16-byte rows)
             constexpr int PS = HDC + 4;
             float* part = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * PS;
+            float* keep = redf;  // a pair's first partial: [3][REP * HDC] numerator, max, sum
             for (int i = ct; i < REP * HDC; i += NC * 32) {
               const int h = i / HDC, dd = i % HDC;
               float M = -FLT_MAX;
@@ -948,7 +968,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 num += f * ww[2 + dd];
                 den += f * ww[1];
               }
-              float* pp = part + ((size_t)h * a.part_cap + ch) * PS;
+              if (first) {
+                keep[i] = num;
+                keep[REP * HDC + i] = M;
+                keep[2 * REP * HDC + i] = den;
+                continue;
+              }
+              if (pair) {  // fold in the pair's first chunk (it precedes this one)
+                const float n1 = keep[i], M1 = keep[REP * HDC + i], d1 = keep[2 * REP * HDC + i];
+                if (d1 > 0.f) {
+                  if (den > 0.f) {
+                    const float Mn = fmaxf(M1, M);
+                    const float a1 = __expf(M1 - Mn), a2 = __expf(M - Mn);
+                    num = n1 * a1 + num * a2;
+                    den = d1 * a1 + den * a2;
+                    M = Mn;
+                  } else {
+                    num = n1;
+                    den = d1;
+                    M = M1;
+                  }
+                }
+              }
+              float* pp = part + ((size_t)h * a.part_cap + (pair ? ch >> 1 : ch)) * PS;
               pp[dd] = num;
               if (dd == 0) {
                 pp[HDC] = den > 0.f ? M : -FLT_MAX;
@@ -957,12 +999,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
             fence_proxy_async_smem();  // the warps' partials overlay the slot, refilled by bulk copies
             named_sync(kBarCons, NC * 32);
+            if (first) {  // no partial of its own: free the slots, go on to the second chunk
+              if (lane == 0) {
+                mbar_arrive(&empty[slot]);
+                if (two) mbar_arrive(&empty[slot_v]);
+              }
+              continue;
+            }
             // ---- the last CTA to finish a chunk of (b, hk) merges its chunks ----
             // (release: this CTA's partial writes, ordered by the barrier above,
             // before the ticket; acquire: every other chunk's partial after it)
             if (ct == 0) {
               const unsigned tk = atom_add_acq_rel(a.attn_ticket + b * Hkv + hk, 1u);
-              s_merge = tk == (unsigned)(nch - 1);
+              s_merge = tk == (unsigned)(npart - 1);
             }
             named_sync(kBarCons, NC * 32);
             const bool merge = s_merge;
@@ -971,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             // when they fit; otherwise it reads them from global memory.
             const int nslot_item = two ? 2 : 1;
             const int hps = (REP + nslot_item - 1) / nslot_item;  // heads per slot
-            const bool staged = merge && (size_t)hps * nch * PS * 4 <= (size_t)SLOT_B;
+            const bool staged = merge && (size_t)hps * npart * PS * 4 <= (size_t)SLOT_B;
             if (lane == 0 && !staged) {
               mbar_arrive(&empty[slot]);
               if (two) mbar_arrive(&empty[slot_v]);
@@ -980,14 +1029,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               const float* hp = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * PS;
               auto stage_of = [&](int h) -> float* {
                 unsigned char* base = ring + (size_t)(h / hps == 0 ? slot : slot_v) * SLOT_B;
-                return reinterpret_cast<float*>(base) + (size_t)(h % hps) * nch * PS;
+                return reinterpret_cast<float*>(base) + (size_t)(h % hps) * npart * PS;
               };
               if (staged) {
                 if (ct == 0) {
                   fence_proxy_async();  // the partials were written by generic stores
-                  mbar_expect_tx(&xbar, (uint32_t)(REP * nch * PS * 4));
+                  mbar_expect_tx(&xbar, (uint32_t)(REP * npart * PS * 4));
                   for (int h = 0; h < REP; ++h)
-                    bulk_g2s(stage_of(h), hp + (size_t)h * a.part_cap * PS, (uint32_t)(nch * PS * 4), &xbar);
+                    bulk_g2s(stage_of(h), hp + (size_t)h * a.part_cap * PS, (uint32_t)(npart * PS * 4), &xbar);
                 }
                 if (!mbar_wait(&xbar, xpar, kSpin)) {  // waited for even after an abort
                   if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
@@ -997,26 +1046,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
               }
               // per head: chunk weights exp(m_c - M) / sum_c exp(m_c - M) l_c into mw [h][c]
               float* mw = redf;
-              for (int i = ct; i < REP * nch; i += NC * 32) {
-                const int h = i / nch, c = i % nch;
+              for (int i = ct; i < REP * npart; i += NC * 32) {
+                const int h = i / npart, c = i % npart;
                 const float* pc = staged ? stage_of(h) + (size_t)c * PS : hp + ((size_t)h * a.part_cap + c) * PS;
                 mw[2 * i] = staged ? pc[HDC] : __ldcg(pc + HDC);
                 mw[2 * i + 1] = staged ? pc[HDC + 1] : __ldcg(pc + HDC + 1);
               }
               named_sync(kBarCons, NC * 32);
               if (warp < REP) {
-                float* mh = mw + (size_t)warp * nch * 2;
+                float* mh = mw + (size_t)warp * npart * 2;
                 float M = -FLT_MAX;
-                for (int c = lane; c < nch; c += 32)
+                for (int c = lane; c < npart; c += 32)
                   if (mh[2 * c + 1] > 0.f) M = fmaxf(M, mh[2 * c]);
                 M = warp_max(M);
                 float den = 0.f;
-                for (int c = lane; c < nch; c += 32)
+                for (int c = lane; c < npart; c += 32)
                   if (mh[2 * c + 1] > 0.f) den += __expf(mh[2 * c] - M) * mh[2 * c + 1];
                 den = warp_sum(den);
                 const float inv = den > 0.f ? 1.f / den : 0.f;
                 __syncwarp();
-                for (int c = lane; c < nch; c += 32)
+                for (int c = lane; c < npart; c += 32)
                   mh[2 * c] = mh[2 * c + 1] > 0.f ? __expf(mh[2 * c] - M) * inv : 0.f;
               }
               named_sync(kBarCons, NC * 32);
@@ -1027,14 +1076,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 const int i = ct + k * NC * 32;
                 if (i < REP * HDC) {
                   const int h = i / HDC, dd = i % HDC;
-                  const float* wh = mw + (size_t)h * nch * 2;
+                  const float* wh = mw + (size_t)h * npart * 2;
                   float acc = 0.f;
                   if (staged) {
                     const float* ph = stage_of(h) + dd;
-                    for (int c = 0; c < nch; ++c) acc += wh[2 * c] * ph[(size_t)c * PS];
+                    for (int c = 0; c < npart; ++c) acc += wh[2 * c] * ph[(size_t)c * PS];
+                  } else if (kMulti) {
+                    // eight loads in flight at a time (the sum keeps chunk order)
+                    const float* ph = hp + (size_t)h * a.part_cap * PS + dd;
+                    int c = 0;
+                    for (; c + 8 <= npart; c += 8) {
+                      float v[8];
+#pragma unroll
+                      for (int j = 0; j < 8; ++j) v[j] = __ldcg(ph + (size_t)(c + j) * PS);
+#pragma unroll
+                      for (int j = 0; j < 8; ++j) acc += wh[2 * (c + j)] * v[j];
+                    }
+                    for (; c < npart; ++c) acc += wh[2 * c] * __ldcg(ph + (size_t)c * PS);
                   } else {
                     const float* ph = hp + (size_t)h * a.part_cap * PS + dd;
-                    for (int c = 0; c < nch; ++c) acc += wh[2 * c] * __ldcg(ph + (size_t)c * PS);
+                    for (int c = 0; c < npart; ++c) acc += wh[2 * c] * __ldcg(ph + (size_t)c * PS);
                   }
                   D.o_out[(size_t)b * D.ldo_attn + (size_t)(hk * REP + h) * HDC + dd] = __float2bfloat16_rn(acc);
                 }
@@ -1138,7 +1199,7 @@ size_t step_smem_bytes(int B, int kmax, int gmax, int* nslot) {
 
 int decode_step_occupancy(size_t smem) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode_step, kThreads, smem) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode_step<false>, kThreads, smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1146,13 +1207,13 @@ int decode_step_occupancy(size_t smem) {
 }
 
 void decode_step_setup() {
-  cudaFuncSetAttribute(k_decode_step, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       227 * 1024 - kStaticSmem);
-  cudaFuncSetAttribute(k_decode_step, cudaFuncAttributePreferredSharedMemoryCarveout,
-                       cudaSharedmemCarveoutMaxShared);
+  for (auto k : {k_decode_step<false>, k_decode_step<true>}) {
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024 - kStaticSmem);
+    cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  }
 }
 
-cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, bool multi, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -1163,7 +1224,7 @@ cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, cudaStr
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode_step, a);
+  return multi ? cudaLaunchKernelEx(&cfg, k_decode_step<true>, a) : cudaLaunchKernelEx(&cfg, k_decode_step<false>, a);
 }
 
 // ---------------------------------------------------------------------------

@@ -416,7 +416,9 @@ enum Tl2Stamp {
 
 // Shared memory the step kernel needs (0 if it does not fit).
 size_t step_smem_bytes(int B, int kmax, int gmax, int* nslot);
-cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, cudaStream_t s);
+// multi: the instantiation for contexts where a CTA may take several
+// attention chunks (see k_decode_step)
+cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, bool multi, cudaStream_t s);
 void decode_step_setup();
 int decode_step_occupancy(size_t smem);  // resident CTAs per SM at this shared-memory size
 // Attention chunks per (sequence, KV head) for context `ctx` (identical on host and device).

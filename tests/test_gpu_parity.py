@@ -167,16 +167,19 @@ def test_batch_forced_and_ragged_shapes(river, stream):
         _run_sequence(river, m, om, stream, pol, B=B, prompt=7, steps=4, seed=5 + B)
 
 
-def test_step_attention_two_chunks_per_cta(river, tiny, stream):
-    """Batch 8 at a context of ~1300: 8 x 2 KV heads x 11 chunks of 128
-    positions exceed the 152 CTAs, so the step kernel's CTAs take two
-    attention chunks each (each chunk's partial merged with the others by the
-    last CTA of its head group)."""
+@pytest.mark.parametrize("B,prompt", [(8, 1300), (4, 2500)])
+def test_step_attention_two_chunks_per_cta(river, tiny, stream, B, prompt):
+    """More chunks of 128 positions than CTAs (8 x 2 KV heads x 11 at context
+    ~1300; 4 x 2 x 20 at ~2500), so the step kernel's CTAs take two
+    consecutive attention chunks each: at batch 8 an odd chunk count per head
+    group (every chunk's partial merged by the last CTA of its group), at
+    batch 4 an even one (a CTA's two chunks of one group folded into one
+    partial in shared memory first)."""
     m, om, _ = tiny
     L = TINY.n_layers
     sched = [L, 2, 0, L]
-    _run_sequence(river, m, om, stream, _forced(river, sched), B=8, prompt=1300, steps=3,
-                  seed=61, max_seq=1310, path="step")
+    _run_sequence(river, m, om, stream, _forced(river, sched), B=B, prompt=prompt, steps=3,
+                  seed=61, max_seq=prompt + 10, path="step")
 
 
 def test_exit_writes_slot_p_of_every_layer(river, tiny, stream):
