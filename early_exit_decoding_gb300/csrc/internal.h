@@ -422,12 +422,17 @@ cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, bool mu
 void decode_step_setup();
 int decode_step_occupancy(size_t smem);  // resident CTAs per SM at this shared-memory size
 // Attention chunks per (sequence, KV head) for context `ctx` (identical on host and device).
+// Chunks of the context per (sequence, KV head) in the step kernel: as few
+// as its 128-position slots allow while every CTA takes at most one chunk (a
+// chunk's warps run 16 positions each, so longer chunks cost no latency and
+// the merge combines fewer partials); beyond one chunk per CTA, the rounds of
+// chunks are spread over the whole grid.
 __host__ __device__ inline int step_attn_chunks(int ctx, int B, int Hkv, int hd, int grid, int cap) {
   const int CH = 128;  // positions per chunk
   const int n_min = (ctx + CH - 1) / CH;
   const int items = B * Hkv * n_min;
   const int per = (items + grid - 1) / grid;
-  int n = (per * grid) / (B * Hkv);
+  int n = per == 1 ? n_min : (per * grid) / (B * Hkv);
   if (n < n_min) n = n_min;
   if (n > ctx) n = ctx;
   if (n > cap) n = cap;
