@@ -226,36 +226,35 @@ __device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok,
     }
     return;
   }
+  // prefill: every column is a token at its own position; the (cos, sin) of
+  // the 16 columns are loaded first (independent loads, in flight together),
+  // then the rotations and stores
+  float2 csn[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int tok = a.col_base + col0 + j;
+    const int pos = tok - (tok / a.T_prefill) * a.T_prefill;
+    csn[j] = make_float2(1.f, 0.f);
+    if (rot && j < nc && pos < a.Tmax) {
+      if (a.rope_cs != nullptr) {
+        csn[j] = __ldg(a.rope_cs + (size_t)pos * half + dim0);
+      } else {
+        float sn, cs;
+        sincosf((float)pos * a.inv_freq[dim0], &sn, &cs);
+        csn[j] = make_float2(cs, sn);
+      }
+    }
+  }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     if (j >= nc) break;
-    const int c = col0 + j;
-    int seq, pos, qrow;
-    if (a.T_prefill > 0) {
-      const int tok = a.col_base + c;
-      seq = tok / a.T_prefill;
-      pos = tok - seq * a.T_prefill;
-      qrow = tok;
-    } else {
-      seq = c;
-      pos = *a.pos_ptr;
-      qrow = c;
-    }
-    const bool in_cache = pos >= 0 && pos < a.Tmax;
+    const int tok = a.col_base + col0 + j;
+    const int seq = tok / a.T_prefill, pos = tok - seq * a.T_prefill;
+    const bool in_cache = pos < a.Tmax;
     float x = v[j];
-    if (rot) {
-      float sn, cs;
-      if (a.rope_cs != nullptr && in_cache) {
-        const float2 t = __ldg(a.rope_cs + (size_t)pos * half + dim0);  // read-only: may run ahead of the stores
-        cs = t.x;
-        sn = t.y;
-      } else {
-        sincosf((float)pos * a.inv_freq[dim0], &sn, &cs);
-      }
-      x = low ? x * cs - o[j] * sn : x * cs + o[j] * sn;
-    }
+    if (rot) x = low ? x * csn[j].x - o[j] * csn[j].y : x * csn[j].x + o[j] * csn[j].y;
     if (is_q) {
-      a.q_out[(size_t)qrow * a.Hq * hd + head_all * hd + dim] = x;
+      a.q_out[(size_t)tok * a.Hq * hd + head_all * hd + dim] = x;
     } else if (!in_cache) {
       atomicOr(a.err, RL_DEVERR_CAPACITY);
     } else {
