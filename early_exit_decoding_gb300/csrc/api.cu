@@ -68,9 +68,7 @@ struct Linear {
   int view_base = 0;        // first rl linear index this fused matrix maps to
   const int2* rowmap = nullptr;
   CUtensorMap tm;           // TMA map of w for the tensor-core GEMM (128 x 64 boxes)
-  CUtensorMap tmq;          // TMA map of qw for the tensor-core GEMM (8 words x 128 rows)
-  bool has_tmq = false;
-  const CUtensorMap* tmq_ptr() const { return has_tmq ? &tmq : nullptr; }
+  unsigned char* qtc = nullptr;  // W4 + (s, z) in the tensor-core GEMM's k-block layout
   // backbone offloading: w and wt live in host memory (w_host / wt points
   // there); w points into the model's device staging buffer
   bool offloaded = false;
@@ -357,6 +355,7 @@ GemvArgs gemv_base(const rl_model* m, const Linear& lin, int w4_mode, const DevS
   memset(&a, 0, sizeof(a));
   a.w = lin.w;
   a.qw = lin.qw;
+  a.qtc = lin.qtc;
   a.sz = lin.sz;
   a.N = lin.N;
   a.Kp = lin.Kp;
@@ -427,8 +426,7 @@ constexpr int kTcMinTokens = 16;
 // One projection over a.B tokens: the bf16 weights on the tensor cores (or
 // the GEMV for a few tokens), the exit river's W4 weights in the dequantising
 // GEMV; which of the two runs is decided on the device.
-rl_status project(const rl_model* m, rl_kv* kv, const CUtensorMap& tm, const CUtensorMap* tmq, GemvArgs a,
-                  cudaStream_t s) {
+rl_status project(const rl_model* m, rl_kv* kv, const CUtensorMap& tm, GemvArgs a, cudaStream_t s) {
   a.tc_ws = kv->tc_ws;
   a.tc_ws_floats = kv->tc_ws_floats;
   a.tc_ticket = kv->tc_ticket;
@@ -438,8 +436,8 @@ rl_status project(const rl_model* m, rl_kv* kv, const CUtensorMap& tm, const CUt
     // the tensor-core GEMM runs bf16 layers and, when the projection has
     // enough output tiles, the W4 exit-river layers (dequantised in shared
     // memory); otherwise the dequantising GEMV runs the W4 layers
-    a.tc_w4 = a.qw != nullptr && tmq != nullptr && tc_gemm_runs_w4(a.N, a.B, m->sm_count);
-    RL_CUDA(launch_gemm_tc(tm, tmq, a, m->sm_count, s));
+    a.tc_w4 = a.qtc != nullptr && tc_gemm_runs_w4(a.N, a.B, m->sm_count);
+    RL_CUDA(launch_gemm_tc(tm, a, m->sm_count, s));
     if (a.w4_mode == W4_OFF || a.tc_w4) return RL_OK;
     a.w4_only = 1;
   }
@@ -533,7 +531,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      RL_TRY(project(m, kv, ly.qkv.tm, ly.qkv.tmq_ptr(), a, s));
+      RL_TRY(project(m, kv, ly.qkv.tm, a, s));
       pf.end(RL_K_QKV, l + 1, bytes_bf16(ly.qkv), bytes_w4(ly.qkv), true);
     }
     // attention over the shared cache
@@ -628,7 +626,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      RL_TRY(project(m, kv, ly.o.tm, ly.o.tmq_ptr(), a, s));
+      RL_TRY(project(m, kv, ly.o.tm, a, s));
       pf.end(RL_K_O, l + 1, bytes_bf16(ly.o), bytes_w4(ly.o), true);
     }
     // pre-FFN RMSNorm
@@ -662,7 +660,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      RL_TRY(project(m, kv, ly.gu.tm, ly.gu.tmq_ptr(), a, s));
+      RL_TRY(project(m, kv, ly.gu.tm, a, s));
       pf.end(RL_K_GU, l + 1, bytes_bf16(ly.gu), bytes_w4(ly.gu), true);
     }
     if (M <= kTcW4AllTokens) {
@@ -687,7 +685,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
       a.err = &kv->st->err;
       pf.begin();
       a.path_out = pf.slot();
-      RL_TRY(project(m, kv, ly.dn.tm, ly.dn.tmq_ptr(), a, s));
+      RL_TRY(project(m, kv, ly.dn.tm, a, s));
       pf.end(RL_K_DOWN, l + 1, bytes_bf16(ly.dn), bytes_w4(ly.dn), true);
     }
     // layer end: cosine, batch-min, tau compare, next RMSNorm
@@ -740,7 +738,7 @@ rl_status enqueue_pass(rl_model* m, rl_kv* kv, const StepIO& io, const Work& w, 
     a.err = &kv->st->err;
     pf.begin();
     a.path_out = pf.slot();
-    RL_TRY(project(m, kv, m->tm_lm, nullptr, a, s));
+    RL_TRY(project(m, kv, m->tm_lm, a, s));
     const double lm = (double)m->V * m->d * 2.0;
     pf.end(RL_K_LM_HEAD, 0, lm, lm, true);
   }
@@ -1458,7 +1456,7 @@ rl_status build_exit_river(rl_model* m, cudaStream_t s, Fill fill) {
       lin->qw = nullptr;
       lin->sz = nullptr;
       lin->qwt = nullptr;
-      lin->has_tmq = false;
+      lin->qtc = nullptr;
     }
   m->quantized = false;
   return st;
@@ -1489,8 +1487,6 @@ rl_status build_exit_river_allocs(rl_model* m, cudaStream_t s, Fill fill) {
     for (Linear* lin : lins) {
       RL_TRY(m->alloc(&lin->qw, (size_t)lin->N * (lin->Kp / 8)));
       RL_TRY(m->alloc(&lin->sz, (size_t)lin->N * (lin->Kp / kGroup)));
-      lin->has_tmq = make_w4_tmap(&lin->tmq, lin->qw, lin->N, lin->Kp);
-      if (!lin->has_tmq) return fail(RL_ERR_CUDA, "TMA map of the W4 words failed");
     }
   }
   RL_TRY(fill());
@@ -1500,6 +1496,9 @@ rl_status build_exit_river_allocs(rl_model* m, cudaStream_t s, Fill fill) {
     for (Linear* lin : lins) {
       RL_TRY(m->alloc(&lin->qwt, w4_tiled_bytes(lin->N, lin->Kp)));
       launch_w4_tile_layout(lin->qw, lin->sz, lin->N, lin->Kp, lin->qwt, s);
+      RL_LAUNCHED();
+      RL_TRY(m->alloc(&lin->qtc, w4_tc_bytes(lin->N, lin->Kp)));
+      launch_w4_tc_layout(lin->qw, lin->sz, lin->N, lin->Kp, lin->qtc, s);
       RL_LAUNCHED();
     }
   }

@@ -55,7 +55,7 @@ namespace {
 
 using dev::smem_u32;
 
-constexpr int kThreadsTc = 448;  // TMA, MMA, 8 epilogue warps, 4 W4 dequantising warps
+constexpr int kThreadsTc = 512;  // 16 warps: TMA, MMA, epilogue / W4 dequantising warps, TMA
 constexpr int kBM = 128;           // weight rows per tile (MMA M)
 constexpr int kBK = 64;            // K per stage: one 128-byte swizzle row of bf16
 constexpr int kABytes = kBM * kBK * 2;
@@ -263,26 +263,48 @@ __device__ __forceinline__ void epi_chunk(const GemvArgs& a, int R, bool row_ok,
   }
 }
 
-constexpr int kEpiWarps = 8;
-constexpr int kDqWarps = 4;  // W4 dequantising warps
+// Warp roles: 0 and 15 TMA producers, 1 MMA issuer; bf16 layers: warps
+// 2 .. 9 run the epilogue; W4 layers: warps 2 .. 5 run the epilogue and warps
+// 6 .. 13 dequantise, as two sets of four that take alternate k-blocks (a set
+// covers the 128 rows of its k-block, one row per thread), so one set's waits
+// and bookkeeping overlap the other's arithmetic.
+constexpr int kEpiWarps = 8;   // bf16 layers
+constexpr int kEpiWarpsW4 = 4;
+constexpr int kDqWarps = 8;    // W4 layers: two sets of kDqSet
+constexpr int kDqSet = 4;
+constexpr int kDqWarp0 = 2 + kEpiWarpsW4;
 constexpr int kQWBytes = 128 * 32;  // one W4 block's packed words: 128 rows x 8 words
-// W4 layers: the token tiles keep all STAGES stages; the dequantised weight
-// tiles need only kNA (they are made on chip); the rest of the weight-tile
-// space holds each stage's packed words and (scale, zero) pairs
-template <int STAGES>
-constexpr int kNA = STAGES >= 8 ? 5 : (STAGES >= 6 ? 3 : 2);
-static_assert((8 - kNA<8>) * kABytes >= 8 * (kQWBytes + 512), "W4 staging must fit");
-static_assert((6 - kNA<6>) * kABytes >= 6 * (kQWBytes + 512), "W4 staging must fit");
-static_assert((4 - kNA<4>) * kABytes >= 4 * (kQWBytes + 512), "W4 staging must fit");
+constexpr int kW4Blk = kQWBytes + 512;  // + the rows' (scale, zero) pairs: one k-block of w4_tc
+// W4 layers carve the same shared memory into three rings: NA dequantised
+// weight tiles (made on chip), TS token tiles, and WS stages of packed words
+// with their (scale, zero) pairs, one contiguous block of the w4_tc layout per
+// k-block (one bulk copy; read from the row-major words, the same bytes came
+// as 32-byte pieces of 128 rows and DRAM delivered them at a fraction of its
+// bandwidth).  The packed words run WS k-blocks ahead of the token tiles.
+// The MMAs of k-block g free its token tile and its dequantised tile at once:
+// one commit per k-block to kdone[g % KD], KD = max(TS, NA) (a waiter never
+// lags the MMAs by KD k-blocks, so the parity it waits for is unambiguous).
+template <int BN>
+constexpr int kW4NA = BN >= 256 ? 2 : (BN >= 128 ? 3 : 6);
+template <int BN>
+constexpr int kW4TS = BN >= 256 ? 3 : (BN >= 128 ? 4 : 8);
+template <int BN>
+constexpr int kW4WS = 12;
+template <int BN>
+constexpr int kW4KD = kW4TS<BN> > kW4NA<BN> ? kW4TS<BN> : kW4NA<BN>;
+constexpr int kW4MaxNA = 6, kW4MaxWS = 12, kW4MaxKD = 8;
+template <int BN>
+constexpr int w4_smem_bytes() {
+  return kW4NA<BN> * kABytes + kW4TS<BN> * BN * kBK * 2 + kW4WS<BN> * kW4Blk;
+}
+template <int BN>
+constexpr bool w4_rings_ok() {
+  return kW4NA<BN> <= kW4MaxNA && kW4WS<BN> <= kW4MaxWS && kW4KD<BN> <= kW4MaxKD && kW4TS<BN> <= 8 &&
+         w4_smem_bytes<BN>() + 1024 <= 215 * 1024;
+}
+static_assert(w4_rings_ok<32>() && w4_rings_ok<64>() && w4_rings_ok<128>() && w4_rings_ok<256>(),
+              "W4 rings must fit the shared memory");
 
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 // Persistent: CTA b takes tiles b, b + grid, ...; tile t covers weight rows
 // (t / tiles_m) * 128 .. +127 and tokens (t % tiles_m) * BN .. +BN-1, so the
@@ -291,13 +313,13 @@ __device__ __forceinline__ void cp_async_wait() {
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-              const __grid_constant__ CUtensorMap tmQ, const GemvArgs a) {
+              const GemvArgs a) {
   pdl_wait();
   constexpr int kBBytes = BN * kBK * 2;
   constexpr uint32_t kTmemCols = 2 * BN;
   bool w4 = a.w4_mode == W4_ON;
   if (a.w4_mode == W4_BY_LAYER) w4 = a.layer_no > *a.exit_layer;
-  if (w4 && (a.qw == nullptr || !a.tc_w4)) return;  // the dequantising GEMV runs this W4 layer
+  if (w4 && (a.qtc == nullptr || !a.tc_w4)) return;  // the dequantising GEMV runs this W4 layer
   if (a.path_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *a.path_out = w4 ? 1 : 0;
 
   extern __shared__ unsigned char smem_dyn[];
@@ -306,7 +328,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   unsigned char* sA = smem;
   unsigned char* sB = smem + STAGES * kABytes;
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], afull[STAGES], acc_full[2], acc_empty[2],
-      mma_done;
+      mma_done, kdone[kW4MaxKD], wfull[kW4MaxWS], wempty[kW4MaxWS];
   __shared__ uint32_t tmem_base;
   __shared__ volatile int s_fail;
   __shared__ volatile int s_last;
@@ -320,23 +342,59 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int nunits = ntiles * S;
   auto kb0_of = [&](int u) { return nk * (u % S) / S; };
   auto kb1_of = [&](int u) { return nk * (u % S + 1) / S; };
+  // W4 rings (see kW4NA): dequantised tiles sA, token tiles sT, blocks of
+  // packed words and (scale, zero) pairs sQW
+  constexpr int NA = kW4NA<BN>, TS = kW4TS<BN>, WS = kW4WS<BN>, KD = kW4KD<BN>;
+  unsigned char* sT = smem + NA * kABytes;
+  unsigned char* sQW = sT + TS * kBBytes;
+  // A CTA's k-blocks in order: unit u = blockIdx.x, blockIdx.x + grid, ...,
+  // k-blocks kb0(u) .. kb1(u) - 1 of each.  The walk keeps the unit's weight
+  // row n0, token m0 and k-block range, so a step costs no division (the
+  // issuing threads' per-k-block work bounds a decode batch's GEMM).
+  struct Walk {
+    int u, kb, kbe, n0, m0;
+  };
+  auto walk_unit = [&](Walk& w) {
+    const int t = w.u / S;
+    w.n0 = (t / tiles_m) * kBM;
+    w.m0 = (t % tiles_m) * BN;
+    w.kb = kb0_of(w.u);
+    w.kbe = kb1_of(w.u);
+  };
+  auto walk_first = [&]() {
+    Walk w{(int)blockIdx.x, 0, 0, 0, 0};
+    if (w.u < nunits) walk_unit(w);
+    return w;
+  };
+  auto walk_next = [&](Walk& w) {
+    if (++w.kb == w.kbe) {
+      w.u += gridDim.x;
+      if (w.u < nunits) walk_unit(w);
+    }
+  };
+  int nkb = 0;  // k-blocks this CTA runs
+  for (int u = blockIdx.x; u < nunits; u += gridDim.x) nkb += kb1_of(u) - kb0_of(u);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      dev::mbar_init(&full[i], 1);
+      dev::mbar_init(&full[i], w4 ? 1 : 2);  // bf16: the weight tile's and the token tile's producers
       dev::mbar_init(&empty[i], 1);
-      dev::mbar_init(&afull[i], kDqWarps);
+      dev::mbar_init(&afull[i], kDqSet);
+    }
+    for (int i = 0; i < kW4MaxKD; ++i) dev::mbar_init(&kdone[i], 1);
+    for (int i = 0; i < kW4MaxWS; ++i) {
+      dev::mbar_init(&wfull[i], 1);
+      dev::mbar_init(&wempty[i], kDqSet);
     }
     for (int i = 0; i < 2; ++i) {
       dev::mbar_init(&acc_full[i], 1);
-      dev::mbar_init(&acc_empty[i], kEpiWarps);
+      dev::mbar_init(&acc_empty[i], w4 ? kEpiWarpsW4 : kEpiWarps);
     }
     dev::mbar_init(&mma_done, 1);
     s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     tma_prefetch_map(&tmW);
     tma_prefetch_map(&tmX);
-    if (w4) tma_prefetch_map(&tmQ);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -350,37 +408,62 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base;
 
-  if (warp == 0) {
-    if (lane == 0) {  // TMA producer
-      int g = 0;      // k-blocks issued by this CTA
-      bool ok = true;
-      for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-        const int t = u / S;
-        const int n0 = (t / tiles_m) * kBM, m0 = (t % tiles_m) * BN;
-        for (int kb = kb0_of(u); kb < kb1_of(u); ++kb, ++g) {
-          const int s = g % STAGES, n = g / STAGES;
-          if (n > 0 && !dev::mbar_wait(&empty[s], (n - 1) & 1, kSpinTc)) {
-            s_fail = 1;
-            ok = false;
-            break;
-          }
-          dev::mbar_expect_tx(&full[s], (w4 ? kQWBytes : kABytes) + kBBytes);
-          if (w4)  // the packed W4 words of the block (rows past N read as zeros)
-            tma_load_2d(sA + kNA<STAGES> * kABytes + s * kQWBytes, &tmQ, kb * 8, n0, &full[s]);
-          else
-            tma_load_2d(sA + s * kABytes, &tmW, kb * kBK, n0, &full[s]);
-          tma_load_2d(sB + s * kBBytes, &tmX, kb * kBK, m0, &full[s]);
+  if (warp == 0 || warp == kThreadsTc / 32 - 1) {
+    // Two TMA producer warps.  bf16: warp 0 the weight tiles, the last warp
+    // the token tiles, both into stage s of the STAGES ring (full[s] expects
+    // both) once the MMAs of its previous round completed.  W4: warp 0 the
+    // token tiles into the TS ring (freed by the MMAs), the last warp the
+    // packed-word blocks into the WS ring (freed by the dequantising warps as
+    // soon as they have read them), WS k-blocks ahead.  Each waits only for
+    // consumers of inputs issued before, so they cannot stall each other.
+    // Copies from one issuing thread complete about one per L2 round trip,
+    // so NI lanes of each warp issue in turn: lane j the k-blocks g = j mod NI,
+    // into its own slots j, j + NI, ... of the ring.
+    const bool words = w4 && warp != 0;
+    const int NSL = words ? WS : (w4 ? TS : STAGES);
+    const int NI = NSL % 4 == 0 ? 4 : (NSL % 2 == 0 ? 2 : 1);
+    if (lane < NI) {
+      uint64_t* fb = words ? wfull : full;
+      uint64_t* eb = words ? wempty : empty;
+      Walk w = walk_first();
+      for (int j = 0; j < lane && j < nkb; ++j) walk_next(w);
+      int g = lane;
+      for (; g < nkb; g += NI) {
+        const int s = g % NSL, r = g / NSL;
+        // the slot's previous k-block g - NSL must be done (W4 tokens: its MMAs, kdone)
+        const bool free = r == 0 || (w4 && !words ? dev::mbar_wait(&kdone[(g - NSL) % KD], ((g - NSL) / KD) & 1, kSpinTc)
+                                                  : dev::mbar_wait(&eb[s], (r - 1) & 1, kSpinTc));
+        if (!free) {
+          s_fail = 1;
+          break;
         }
+        if (words) {  // the block's packed W4 words and (scale, zero) pairs
+          dev::mbar_expect_tx(&fb[s], kW4Blk);
+          dev::bulk_g2s(sQW + s * kW4Blk, a.qtc + ((size_t)(w.n0 / kBM) * nk + w.kb) * kW4Blk, kW4Blk, &fb[s]);
+        } else if (w4) {
+          dev::mbar_expect_tx(&fb[s], kBBytes);
+          tma_load_2d(sT + s * kBBytes, &tmX, w.kb * kBK, w.m0, &fb[s]);
+        } else if (warp == 0) {
+          dev::mbar_expect_tx(&fb[s], kABytes);
+          tma_load_2d(sA + s * kABytes, &tmW, w.kb * kBK, w.n0, &fb[s]);
+        } else {
+          dev::mbar_expect_tx(&fb[s], kBBytes);
+          tma_load_2d(sB + s * kBBytes, &tmX, w.kb * kBK, w.m0, &fb[s]);
+        }
+        for (int j = 0; j < NI; ++j) walk_next(w);
       }
       // the CTA may not exit with copies in flight: wait (bounded) for the
-      // last ones it issued
-      for (int g2 = g - STAGES < 0 ? 0 : g - STAGES; g2 < g; ++g2)
-        dev::mbar_wait(&full[g2 % STAGES], (g2 / STAGES) & 1, kSpinTc);
+      // last ones this lane issued
+      for (int g2 = g - NI; g2 >= 0 && g2 > g - NI - NSL; g2 -= NI)
+        dev::mbar_wait(&fb[g2 % NSL], (g2 / NSL) & 1, kSpinTc);
     }
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       const uint32_t idesc = idesc_bf16(kBM, BN);
-      int g = 0, i = 0;
+      const int NSL = w4 ? TS : STAGES;
+      int i = 0;
+      int s = 0, sa = 0, kd = 0;  // token (bf16: whole) stage, W4 dequantised tile and kdone
+      uint32_t par = 0, pa = 0;   // their phase parities
       bool ok = true;
       for (int uu = blockIdx.x; uu < nunits && ok; uu += gridDim.x, ++i) {
         const int acc = i & 1, u = i >> 1;
@@ -390,22 +473,34 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * BN);
-        const int kbs = kb0_of(uu);
-        for (int kb = kbs; kb < kb1_of(uu); ++kb, ++g) {
-          const int s = g % STAGES, sa = w4 ? g % kNA<STAGES> : s;
-          if (!dev::mbar_wait(&full[s], (g / STAGES) & 1, kSpinTc) ||
-              (w4 && !dev::mbar_wait(&afull[sa], (g / kNA<STAGES>) & 1, kSpinTc))) {
+        const int kbs = kb0_of(uu), kbe = kb1_of(uu);
+        for (int kb = kbs; kb < kbe; ++kb) {
+          // bf16: stage s of the one ring; W4: token tile s of TS, dequantised tile sa of NA
+          if (!dev::mbar_wait(&full[s], par, kSpinTc) || (w4 && !dev::mbar_wait(&afull[sa], pa, kSpinTc))) {
             s_fail = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sw128_desc(smem_u32(sA + sa * kABytes));
-          const uint64_t bd = sw128_desc(smem_u32(sB + s * kBBytes));
+          const uint64_t ad = sw128_desc(smem_u32(sA + (w4 ? sa : s) * kABytes));
+          const uint64_t bd = sw128_desc(smem_u32((w4 ? sT : sB) + s * kBBytes));
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes = 2 in the address field
             mma_tc(d, ad + 2 * k, bd + 2 * k, idesc, (kb != kbs || k != 0) ? 1u : 0u);
-          mma_commit(&empty[s]);  // also frees dequantised tile sa (W4)
+          if (w4) {
+            mma_commit(&kdone[kd]);  // frees its token tile and its dequantised tile
+            if (++kd == KD) kd = 0;
+            if (++sa == NA) {
+              sa = 0;
+              pa ^= 1u;
+            }
+          } else {
+            mma_commit(&empty[s]);
+          }
+          if (++s == NSL) {
+            s = 0;
+            par ^= 1u;
+          }
         }
         mma_commit(&acc_full[acc]);
       }
@@ -413,58 +508,38 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mma_commit(&mma_done);
       dev::mbar_wait(&mma_done, 0, kSpinTc);
     }
-  } else if (warp >= 2 + kEpiWarps) {
+  } else if (w4 && warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
     // W4 dequantising warps: thread r writes weight row n0 + r of every 128 x 64
     // block, 8 chunks of 8 bf16 at chunk position c ^ (r & 7) (128-byte swizzle).
     // The producer TMA-loads each block's packed words (128 rows x 32 bytes)
-    // into its stage with the token tile; each thread copies its row's
-    // (scale, zero) STAGES - 1 blocks ahead with cp.async.  A nibble q becomes
-    // the weight without an integer conversion: placed at bits 10..13 of
-    // 0x46000000 it is the float v = 8192 + q, and fma(v, s, c) with
-    // c = -(8192 + z) s rounded once gives (q - z) s within s 2^-10 (8192 + z
-    // is exact: z is an fp16 in [0, 16)).
-    if (w4) {
-      const unsigned char* sQw = sA + kNA<STAGES> * kABytes;     // [STAGES][128 rows][32 bytes]
-      unsigned char* sQz = sA + kNA<STAGES> * kABytes + STAGES * kQWBytes;  // [STAGES][128] (s, z)
-      const int r = threadIdx.x - (2 + kEpiWarps) * 32;
-      const int gpr = a.Kp >> 7;
-      int G = 0;  // k-blocks this CTA runs
-      for (int u = blockIdx.x; u < nunits; u += gridDim.x) G += kb1_of(u) - kb0_of(u);
-      int lu = blockIdx.x, lkb = lu < nunits ? kb0_of(lu) : 0, lb = 0;  // the next (scale, zero) to copy
-      auto issue_sz = [&]() {
-        if (lu < nunits) {
-          const int R = ((lu / S) / tiles_m) * kBM + r;
-          unsigned char* d = sQz + (lb % STAGES) * 512 + r * 4;
-          if (R < a.N)
-            cp_async4(smem_u32(d), a.sz + (size_t)R * gpr + ((lkb * kBK) >> 7));
-          else
-            *reinterpret_cast<uint32_t*>(d) = 0u;
-          ++lb;
-          if (++lkb == kb1_of(lu)) {
-            lu += gridDim.x;
-            if (lu < nunits) lkb = kb0_of(lu);
-          }
-        }
-        cp_async_commit();
-      };
-      for (int j = 0; j + 1 < STAGES; ++j) issue_sz();
-      for (int g = 0; g < G; ++g) {
-        const int st = g % STAGES;
-        cp_async_wait<STAGES - 2>();  // block g's (scale, zero) has landed
-        const bool landed = dev::mbar_wait(&full[st], (g / STAGES) & 1, kSpinTc);  // its words too
-        const uint4 w0 = *reinterpret_cast<const uint4*>(sQw + st * kQWBytes + r * 32);
-        const uint4 w1 = *reinterpret_cast<const uint4*>(sQw + st * kQWBytes + r * 32 + 16);
-        const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(sQz + st * 512 + r * 4));
-        issue_sz();  // block g + STAGES - 1, into the slot block g - 1 used
-        // tile s was last read by k-block gp, whose MMAs completing completed a
-        // phase of that k-block's token-tile barrier empty[]
-        const int s = g % kNA<STAGES>, gp = g - kNA<STAGES>;
-        const bool got = landed && (gp < 0 || dev::mbar_wait(&empty[gp % STAGES], (gp / STAGES) & 1, kSpinTc));
+    // WS blocks ahead; each thread copies its row's (scale, zero) WS - 1 blocks
+    // ahead with cp.async.  A nibble q becomes the weight without an integer
+    // conversion: placed at bits 10..13 of 0x46000000 it is the float
+    // v = 8192 + q, and fma(v, s, c) with c = -(8192 + z) s rounded once gives
+    // (q - z) s within s 2^-10 (8192 + z is exact: z is an fp16 in [0, 16)).
+    {
+      const int set = (warp - kDqWarp0) / kDqSet;
+      const int r = threadIdx.x - (kDqWarp0 + set * kDqSet) * 32;
+      // this set's k-blocks are g = set, set + 2, ...
+      for (int g = set; g < nkb; g += 2) {
+        const int sw = g % WS;
+        const bool landed = dev::mbar_wait(&wfull[sw], (g / WS) & 1, kSpinTc);  // its words too
+        const unsigned char* blk = sQW + sw * kW4Blk;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(blk + r * 32);
+        const uint4 w1 = *reinterpret_cast<const uint4*>(blk + r * 32 + 16);
+        const float2 zs = __half22float2(*reinterpret_cast<const __half2*>(blk + kQWBytes + r * 4));
+        // every lane has read the stage: its words may be overwritten (a stage
+        // whose copy did not land is never handed back)
+        const bool all_landed = __all_sync(0xffffffffu, landed);
+        if (all_landed && (threadIdx.x & 31) == 0) dev::mbar_arrive(&wempty[sw]);
+        // dequantised tile sa was last read by the MMAs of k-block g - NA
+        const int sa = g % NA;
+        const bool got = all_landed && (g < NA || dev::mbar_wait(&kdone[(g - NA) % KD], ((g - NA) / KD) & 1, kSpinTc));
         if (!__all_sync(0xffffffffu, got)) {  // the same decision in every lane
           s_fail = 1;
           break;
         }
-        unsigned char* dst = sA + s * kABytes + r * 128;
+        unsigned char* dst = sA + sa * kABytes + r * 128;
         const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         const float sc = zs.x, c0 = -(8192.f + zs.y) * zs.x;
 #pragma unroll
@@ -485,12 +560,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         dev::fence_proxy_async_smem();  // generic writes before the MMAs' reads
         __syncwarp();
-        if ((threadIdx.x & 31) == 0) dev::mbar_arrive(&afull[s]);
+        if ((threadIdx.x & 31) == 0) dev::mbar_arrive(&afull[sa]);
       }
-      cp_async_wait<0>();  // no copy may land after the CTA has gone
     }
-  } else {  // epilogue warps 2 .. 9: lane quarter warp % 4, column half (warp - 2) / 4
+  } else if (warp >= 2 && warp < 2 + (w4 ? kEpiWarpsW4 : kEpiWarps)) {
+    // epilogue warps: lane quarter warp % 4; bf16: column half (warp - 2) / 4,
+    // W4 (four warps): every column
     const int q = warp & 3, h = (warp - 2) >> 2;
+    const int nthr = (w4 ? kEpiWarpsW4 : kEpiWarps) * 32;
+    const int c_lo = w4 ? 0 : h * (BN / 32), c_hi = w4 ? BN / 16 : (h + 1) * (BN / 32);
     int i = 0;
     for (int u = blockIdx.x; u < nunits; u += gridDim.x, ++i) {
       const int t = u / S;
@@ -504,7 +582,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (S > 1) {
         // every epilogue warp takes the same decision after the barrier (a wait
         // that ran out in one warp stops all of them)
-        dev::named_sync(2, kEpiWarps * 32);
+        dev::named_sync(2, nthr);
         if (s_fail) break;
       } else if (!got) {
         break;
@@ -515,7 +593,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint32_t tacc = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * BN);
       if (S == 1) {
 #pragma unroll 1
-        for (int c16 = h * (BN / 32); c16 < (h + 1) * (BN / 32); ++c16) {
+        for (int c16 = c_lo; c16 < c_hi; ++c16) {
           const int col0 = m0 + c16 * 16;
           if (col0 >= a.B) break;
           epi_chunk<true>(a, R, row_ok, lane, col0, tacc + (uint32_t)(c16 * 16));
@@ -528,7 +606,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // split K: this unit's fp32 partial tile -> ws[u][column][128 rows]
       float* wsu = a.tc_ws + (size_t)u * BN * kBM;
 #pragma unroll 1
-      for (int c16 = h * (BN / 32); c16 < (h + 1) * (BN / 32); ++c16) {
+      for (int c16 = c_lo; c16 < c_hi; ++c16) {
         float v[16];
         tmem_ld16(tacc + (uint32_t)(c16 * 16), v);
 #pragma unroll
@@ -540,29 +618,41 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // the last unit of tile t to finish sums the partials in split order and
       // runs the epilogue (release: the partial stores before the ticket,
       // ordered by the barrier; acquire: the other units' partials after it)
-      dev::named_sync(2, kEpiWarps * 32);
+      dev::named_sync(2, nthr);
       if (warp == 2 && lane == 0) s_last = dev::atom_add_acq_rel(a.tc_ticket + t, 1u) == (unsigned)(S - 1);
-      dev::named_sync(2, kEpiWarps * 32);
+      dev::named_sync(2, nthr);
       if (s_last) {
         const float* wst = a.tc_ws + (size_t)t * S * BN * kBM;
 #pragma unroll 1
-        for (int c16 = h * (BN / 32); c16 < (h + 1) * (BN / 32); ++c16) {
+        for (int c16 = c_lo; c16 < c_hi; ++c16) {
           const int col0 = m0 + c16 * 16;
           if (col0 >= a.B) break;
+          // the splits' partials summed in split order; the loads of four
+          // splits are in flight at a time (one L2 round trip per four)
           float v[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = 0.f;
-          for (int sp = 0; sp < S; ++sp) {
-            const float* p = wst + ((size_t)sp * BN + c16 * 16) * kBM + 32 * q + lane;
+          for (int sp0 = 0; sp0 < S; sp0 += 4) {
+            float t[4][16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] += __ldcg(p + (size_t)j * kBM);
+            for (int i = 0; i < 4; ++i) {
+              const float* p = wst + ((size_t)(sp0 + i) * BN + c16 * 16) * kBM + 32 * q + lane;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) t[i][j] = sp0 + i < S ? __ldcg(p + (size_t)j * kBM) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (sp0 + i < S) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += t[i][j];
+              }
           }
           epi_chunk<false>(a, R, row_ok, lane, col0, 0u, v);
         }
-        dev::named_sync(2, kEpiWarps * 32);
+        dev::named_sync(2, nthr);
         if (warp == 2 && lane == 0) a.tc_ticket[t] = 0u;  // the next launch starts from zero
       }
-      dev::named_sync(2, kEpiWarps * 32);
+      dev::named_sync(2, nthr);
     }
   }
   tc_fence_before();
@@ -577,7 +667,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
 template <int BN, int STAGES>
 constexpr int tc_smem_bytes() {
-  return STAGES * (kABytes + BN * kBK * 2) + 1024;
+  return (STAGES * (kABytes + BN * kBK * 2) > w4_smem_bytes<BN>() ? STAGES * (kABytes + BN * kBK * 2)
+                                                                   : w4_smem_bytes<BN>()) +
+         1024;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -626,7 +718,7 @@ int tc_pick_split(int tiles, int nk, int sm_count, size_t tile_floats, size_t ws
 }
 
 template <int BN, int STAGES>
-cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap* tmQ, const GemvArgs& a, int sm_count,
+cudaError_t launch_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count,
                       cudaStream_t s) {
   constexpr int smem = tc_smem_bytes<BN, STAGES>();
   CUtensorMap tmX;
@@ -640,7 +732,7 @@ cudaError_t launch_tc(const CUtensorMap& tmW, const CUtensorMap* tmQ, const Gemv
   int grid = tiles * S;
   if (grid > sm_count) grid = sm_count;
   return launch_pdl(k_gemm_tc<BN, STAGES>, dim3(grid), dim3(kThreadsTc), (size_t)smem, s, tmW, tmX,
-                    tmQ != nullptr ? *tmQ : tmW, b);
+                    b);
 }
 
 __global__ void k_rope_table(const float* inv_freq, int half, int n, float2* out) {
@@ -689,19 +781,32 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Packed W4 words [N][Kp/8] uint32: boxes of 8 words (one 64-input k-block of
-// a row) x 128 rows, no swizzle.
-bool make_w4_tmap(CUtensorMap* map, const uint32_t* qw, int N, int Kp) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (fn == nullptr || qw == nullptr || N <= 0 || Kp % kBK != 0 || (reinterpret_cast<uintptr_t>(qw) & 15) != 0)
-    return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)(Kp / 8), (cuuint64_t)N};
-  const cuuint64_t strides[1] = {(cuuint64_t)Kp / 2};
-  const cuuint32_t box[2] = {8, (cuuint32_t)kBM};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(qw), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// W4 copy in the tensor-core GEMM's k-block layout: for 128-row tile T and
+// 64-input k-block kb, one contiguous kW4Blk-byte block at (T * Kp/64 + kb):
+// the 128 rows' 8 packed words (row r at 32 r), then each row's (scale, zero)
+// pair of the block's group (kb / 2) at kQWBytes + 4 r.  Rows past N are zero.
+size_t w4_tc_bytes(int N, int Kp) { return (size_t)((N + kBM - 1) / kBM) * (Kp / kBK) * kW4Blk; }
+
+__global__ void k_w4_tc_layout(const uint32_t* __restrict__ qw, const __half2* __restrict__ sz, int N,
+                               int Kp, unsigned char* __restrict__ out) {
+  const int nk = Kp / kBK, G = Kp / 128;
+  const long long blk = blockIdx.x;  // one CTA per (tile, k-block)
+  const int T = (int)(blk / nk), kb = (int)(blk % nk);
+  unsigned char* dst = out + blk * kW4Blk;
+  for (int i = threadIdx.x; i < kBM * 8; i += blockDim.x) {
+    const int r = i >> 3, wd = i & 7, R = T * kBM + r;
+    reinterpret_cast<uint32_t*>(dst)[i] = R < N ? qw[(size_t)R * (Kp / 8) + kb * 8 + wd] : 0u;
+  }
+  for (int r = threadIdx.x; r < kBM; r += blockDim.x) {
+    const int R = T * kBM + r;
+    reinterpret_cast<__half2*>(dst + kQWBytes)[r] = R < N ? sz[(size_t)R * G + kb / 2] : __floats2half2_rn(0.f, 0.f);
+  }
+}
+
+void launch_w4_tc_layout(const uint32_t* qw, const __half2* sz, int N, int Kp, void* out, cudaStream_t s) {
+  const long long blocks = (long long)((N + kBM - 1) / kBM) * (Kp / kBK);
+  if (blocks > 0)
+    k_w4_tc_layout<<<(unsigned)blocks, 256, 0, s>>>(qw, sz, N, Kp, static_cast<unsigned char*>(out));
 }
 
 bool make_weight_tmap(CUtensorMap* map, const bf16* w, int N, int Kp) {
@@ -739,14 +844,14 @@ bool tc_gemm_runs_w4(int N, int B, int sm_count) {
   return 2 * tiles >= sm_count;
 }
 
-cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap* tmQ, const GemvArgs& a, int sm_count,
+cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count,
                            cudaStream_t s) {
   if (a.B <= 0 || a.N <= 0) return cudaSuccess;
   switch (tc_pick_bn(a.N, a.B, sm_count)) {
-    case 256: return launch_tc<256, 4>(tmW, tmQ, a, sm_count, s);
-    case 128: return launch_tc<128, 6>(tmW, tmQ, a, sm_count, s);
-    case 64: return launch_tc<64, 8>(tmW, tmQ, a, sm_count, s);
-    default: return launch_tc<32, 8>(tmW, tmQ, a, sm_count, s);
+    case 256: return launch_tc<256, 4>(tmW, a, sm_count, s);
+    case 128: return launch_tc<128, 6>(tmW, a, sm_count, s);
+    case 64: return launch_tc<64, 8>(tmW, a, sm_count, s);
+    default: return launch_tc<32, 8>(tmW, a, sm_count, s);
   }
 }
 

@@ -103,6 +103,7 @@ struct GemvArgs {
   float* tc_ws; size_t tc_ws_floats; unsigned* tc_ticket; int tc_ticket_n;
   int ksplit;             // set by launch_gemm_tc
   int tc_w4;              // k_gemm_tc runs the W4 path too (else it returns at once for W4 layers)
+  const unsigned char* qtc;  // W4 in the tensor-core GEMM's k-block layout (w4_tc_bytes), or null
   long long first_wait;   // k_gemm_tc: polls of the epilogue's accumulator wait (0: the default)
 };
 
@@ -117,11 +118,12 @@ bool tc_gemm_available();
 cudaError_t tc_gemm_init();
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int inner, int rows, int ld, int box_rows);
 bool make_weight_tmap(CUtensorMap* map, const bf16* w, int N, int Kp);
-bool make_w4_tmap(CUtensorMap* map, const uint32_t* qw, int N, int Kp);
+// W4 words and (scale, zero) pairs in the tensor-core GEMM's k-block layout.
+size_t w4_tc_bytes(int N, int Kp);
+void launch_w4_tc_layout(const uint32_t* qw, const __half2* sz, int N, int Kp, void* out, cudaStream_t s);
 int tc_pick_bn(int N, int M, int sm_count);
-// tmQ: the packed W4 words of the layer's exit copy (make_w4_tmap), or null.
-cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const CUtensorMap* tmQ, const GemvArgs& a, int sm_count,
-                           cudaStream_t s);
+// a.qtc: the layer's exit copy in the k-block layout (launch_w4_tc_layout), or null.
+cudaError_t launch_gemm_tc(const CUtensorMap& tmW, const GemvArgs& a, int sm_count, cudaStream_t s);
 // Whether the tensor-core GEMM also runs a W4 layer of this shape: always
 // above kTcW4AllTokens tokens, else when the projection has at least half as
 // many output tiles as SMs (narrower ones run on the dequantising GEMV, which
