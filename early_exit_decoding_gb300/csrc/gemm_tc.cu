@@ -14,16 +14,16 @@
 // in one warp and is exchanged with one shuffle).
 //
 // The weights of exit layers are W4 (River-LLM explainer, section 四: the
-// device-side exit layer picks the path): four more warps dequantise each
+// device-side exit layer picks the path): eight more warps dequantise each
 // 128 x 64 weight block, (q - z) * s rounded to bf16, straight into the
 // 128-byte-swizzled shared-memory layout the TMA would have written, and the
-// MMAs run as for the backbone's bf16 weights; the producer TMA-loads each
-// block's packed words (128 rows x 32 bytes) into the stage in place of the
-// bf16 tile.  At decode batch sizes a W4 k-block takes about twice a bf16 one
-// (the dequantised tile's hand-off to the MMAs, not the quarter-size weight
-// bytes, bounds it); up to 32 tokens a narrow W4 projection (fewer output
-// tiles than half the SMs) runs faster on the dequantising GEMV, which takes
-// it (tc_gemm_runs_w4).
+// MMAs run as for the backbone's bf16 weights.  The packed words and the
+// rows' (scale, zero) pairs of a block come from the W4 copy in this
+// kernel's k-block layout (w4_tc_bytes), one bulk copy per block.  At decode
+// batch sizes a W4 launch is bound by its chain of ring hand-offs and its
+// per-unit epilogue rather than by its quarter-size weight bytes; up to 32
+// tokens a narrow W4 projection (fewer output tiles than half the SMs) runs
+// faster on the dequantising GEMV, which takes it (tc_gemm_runs_w4).
 //
 // When the output tiles are fewer than the SMs (a decode batch's narrow
 // projections), K is split: unit u = (tile, split), each split accumulates
@@ -31,16 +31,16 @@
 // workspace; the last of the tile's CTAs (ticket) sums the splits in split
 // order and runs the epilogue, so the result does not depend on timing.
 //
-// Persistent CTAs (one per SM) walk the units; 448 threads: warp 0
-// lane 0 issues the TMA loads into a STAGES-deep ring of (128 x 64 weight
-// tile or its packed W4 words, BN x 64 token tile), warp 1 owns the tensor-memory allocation (two
-// BN-column fp32 accumulators) and its lane 0 issues the MMAs, warps 2..9 run
-// the epilogue of one tile while the MMAs of the next fill the other
-// accumulator (warp w reads TMEM lanes 32 (w % 4) .. +31, one half of the
-// columns), warps 10..13 write the W4 weight tiles of exit-river layers.
-// Every wait is bounded; a wait that runs out sets
-// RL_DEVERR_TIMEOUT and the CTA winds down (all MMAs retired, all copies
-// landed, tensor memory freed).
+// Persistent CTAs (one per SM) walk the units; 512 threads in 16 warps:
+// warps 0 and 15 issue the TMA loads (bf16: the 128 x 64 weight tiles and
+// the BN x 64 token tiles of a STAGES-deep ring; W4: the token tiles and the
+// W4 blocks, see kW4NA), warp 1 owns the tensor-memory allocation (two
+// BN-column fp32 accumulators) and its lane 0 issues the MMAs; the epilogue
+// warps (2..9 for bf16 layers, 2..5 for W4) run the epilogue of one tile
+// while the MMAs of the next fill the other accumulator (warp w reads TMEM
+// lanes 32 (w % 4) .. +31); for W4 layers warps 6..13 dequantise.  Every
+// wait is bounded; a wait that runs out sets RL_DEVERR_TIMEOUT and the CTA
+// winds down (all MMAs retired, all copies landed, tensor memory freed).
 #include <algorithm>
 
 #include <cuda.h>
