@@ -1213,7 +1213,7 @@ rl_status enqueue_decode_step(rl_model* m, rl_kv* kv, const StepIO& io, cudaStre
   // a CTA may take more than one attention chunk once B x KV heads x
   // 128-position chunks of the cache's longest context exceed the grid
   const bool multi = (long long)B * m->Hkv * ((kv->Tmax + 127) / 128) > m->sm_count;
-  RL_CUDA(launch_decode_step(a, m->sm_count, smem, multi, s));
+  RL_CUDA(launch_decode_step(a, m->sm_count, smem, multi, m->offload_from >= 0, s));
   if (prof) {
     cudaEventRecordWithFlags(kv->ev[1], s, cudaEventRecordExternal);
     kv->nph_last = a.nph;

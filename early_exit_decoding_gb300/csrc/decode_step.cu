@@ -49,6 +49,10 @@ constexpr int kCHP = 128;                 // positions per attention chunk
 constexpr int kAttnHalf = 16384;          // V offset in a one-slot chunk (head_dim 64)
 constexpr long long kSpin = 1LL << 20;     // mbarrier polls
 constexpr long long kSpinBar = 1LL << 24;  // grid-barrier polls (each with a short sleep)
+// kWide producer's slot wait, in ns of %globaltimer: a whole warp polling
+// spends a poll budget far faster than one lane, and with layers read from
+// host memory a slot can stay taken for milliseconds at a phase boundary
+constexpr unsigned long long kWaitNsWide = 4000000000ull;
 constexpr int kBarCons = 1;                // named barrier: consumer warps
 constexpr int kStaticSmem = 12 * 1024;     // upper bound of the kernel's static shared memory
 
@@ -140,7 +144,12 @@ __device__ __forceinline__ void w4_unit(const unsigned char* st, int gi, const u
 // consecutive chunks, and two chunks of one head group are folded into one
 // partial before the merge.  Otherwise chunks are dealt round-robin (one per
 // CTA at the contexts that instantiation is launched for).
-template <bool kMulti>
+// kWide: the model has offloaded layers, whose units the producer warp reads
+// from host memory with 16-byte copies of all 32 lanes (one lane issuing
+// them reaches ~91 GB/s over the whole GPU).  The whole warp then walks the
+// copy schedule; otherwise lane 0 alone does (the warp-wide walk measured
+// 1-2 % slower on resident models, which keep the single-lane one).
+template <bool kMulti, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_constant__ StepArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full[kMaxSlots], empty[kMaxSlots], xbar;
@@ -190,28 +199,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
 
   if (warp == WP) {
     // ================================ producer ===================================
-    if (lane == 0) {
+    // (kWide: every lane walks the same schedule; lane 0 waits for slots and
+    // issues the bulk and tensor copies; decisions that read shared state are
+    // lane 0's, broadcast.)
+    if (kWide || lane == 0) {
+      const bool l0 = !kWide || lane == 0;
+      auto uni = [&](bool v) -> bool {
+        if constexpr (kWide) return __shfl_sync(0xffffffffu, (int)v, 0) != 0;
+        return v;
+      };
       RingPos rp{0, 0};
       int issued = 0;
       int e_known = s_e;
       auto take_slot = [&]() -> bool {
         if (rp.round == 0) return true;
-        if (s_abort) return false;
-        if (!mbar_wait(&empty[rp.slot], (uint32_t)((rp.round - 1) & 1), kSpin)) {
-          atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-          s_abort = 1;
-          return false;
+        bool ok = true;
+        if (l0) {
+          if (s_abort) {
+            ok = false;
+          } else if (!(kWide ? mbar_wait_for(&empty[rp.slot], (uint32_t)((rp.round - 1) & 1), kWaitNsWide)
+                             : mbar_wait(&empty[rp.slot], (uint32_t)((rp.round - 1) & 1), kSpin))) {
+            atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+            s_abort = 1;
+            ok = false;
+          } else {
+            // consumers that aborted free slots without waiting for their
+            // copies: never issue into such a slot (the arrival orders their
+            // abort flag before it)
+            ok = !s_abort;
+          }
         }
-        // consumers that aborted free slots without waiting for their copies:
-        // never issue into such a slot (the arrival orders their abort flag
-        // before it)
-        return !s_abort;
+        return uni(ok);
       };
-      for (int p = 0; p < a.nph && !s_abort; ++p) {
+      for (int p = 0; p < a.nph && !uni(s_abort); ++p) {
         const PhaseDesc* D = a.ph + p;
         bool first_copy = true;
         auto stamp_copy = [&]() {
-          if (!a.tl2) return;
+          if (!a.tl2 || !l0) return;
           if (first_copy) tl2_mark(a.tl2, grid, p, cta, TL2_P0);
           first_copy = false;
           tl2_mark(a.tl2, grid, p, cta, TL2_P1);
@@ -226,31 +250,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           if (qwt && layer_no > 0) {
             if (a.mode == RL_EXIT_TAU && e_known >= a.L && layer_no >= 2) {
               // the weight path of this layer waits for the exit decision of the previous one
-              long long i = 0;
-              while (s_dec < layer_no - 1 && !s_abort && i < kSpinBar) {
-                __nanosleep(64);
-                ++i;
+              bool decided = true;
+              int e_now = 0;
+              if (l0) {
+                long long i = 0;
+                while (s_dec < layer_no - 1 && !s_abort && i < kSpinBar) {
+                  __nanosleep(64);
+                  ++i;
+                }
+                decided = s_dec >= layer_no - 1;
+                if (!decided) {
+                  if (!s_abort) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
+                  s_abort = 1;
+                }
+                e_now = s_e;
               }
-              if (s_dec < layer_no - 1) {
-                if (!s_abort) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-                s_abort = 1;
-                break;
-              }
-              e_known = s_e;
+              if (!uni(decided)) break;
+              if constexpr (kWide)
+                e_known = __shfl_sync(0xffffffffu, e_now, 0);
+              else
+                e_known = e_now;
             }
             w4 = layer_no > e_known;
           }
           // whole 16-row tiles cta, cta + grid, ... (the consumers walk the same list)
           const int UPT = (Kp + KU - 1) / KU, ntiles = N >> 4;
-          for (int tl = cta; tl < ntiles && !s_abort; tl += grid) {
+          for (int tl = cta; tl < ntiles && !uni(s_abort); tl += grid) {
             if (w4) {
               for (int s0 = 0; s0 < UPT; s0 += W4U) {
                 if (!take_slot()) break;
                 const int ns = min(W4U, UPT - s0);
                 const int slot = rp.slot;
-                mbar_expect_tx(&full[slot], (uint32_t)(ns * STAGE_W));
-                bulk_g2s(ring + (size_t)slot * SLOT_B, qwt + ((size_t)tl * UPT + s0) * STAGE_W,
-                         (uint32_t)(ns * STAGE_W), &full[slot]);
+                if (l0) {
+                  mbar_expect_tx(&full[slot], (uint32_t)(ns * STAGE_W));
+                  bulk_g2s(ring + (size_t)slot * SLOT_B, qwt + ((size_t)tl * UPT + s0) * STAGE_W,
+                           (uint32_t)(ns * STAGE_W), &full[slot]);
+                }
                 stamp_copy();
                 rp.next(NS);
                 ++issued;
@@ -266,10 +301,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                 unsigned char* dst = ring + (size_t)slot * SLOT_B;
                 if (wt_sys) {
                   // an offloaded layer's unit from host memory: 16-byte copies on
-                  // the load path, whose landing is the slot's one expected arrival
-                  for (uint32_t o = 0; o < bytes; o += 16) cp_async16(dst + o, src + o);
-                  cp_async_mbar_arrive(&full[slot]);
-                } else {
+                  // the load path
+                  if constexpr (kWide) {
+                    // by every lane, waited for here (the host link, not the
+                    // wait, bounds these units); lane 0's arrival after every
+                    // lane's copies have landed is the slot's one expected one
+                    for (uint32_t o = (uint32_t)lane * 16; o < bytes; o += 32 * 16) cp_async16(dst + o, src + o);
+                    asm volatile("cp.async.wait_all;" ::: "memory");
+                    __syncwarp();
+                    if (l0) mbar_arrive(&full[slot]);
+                  } else {
+                    // lane 0 alone: their landing is the slot's one expected arrival
+                    for (uint32_t o = 0; o < bytes; o += 16) cp_async16(dst + o, src + o);
+                    cp_async_mbar_arrive(&full[slot]);
+                  }
+                } else if (l0) {
                   mbar_expect_tx(&full[slot], bytes);
                   bulk_g2s(dst, src, bytes, &full[slot]);
                 }
@@ -299,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
           // last round; else chunks c, c + grid, ...
           const int per = kMulti ? (nitems + grid - 1) / grid : 1;
           const int it0 = kMulti ? cta * per : cta, it_end = kMulti ? min(nitems, cta * per + per) : nitems;
-          for (int it = it0; it < it_end && !s_abort; it += kMulti ? 1 : grid) {
+          for (int it = it0; it < it_end && !uni(s_abort); it += kMulti ? 1 : grid) {
             const int b = it / (Hkv * nch), rr = it % (Hkv * nch), hk = rr / nch, ch = rr % nch;
             const int start = ch * clen, end = min(start + clen, ctx);
             const int n = min(kCHP, max(0, end - start));
@@ -316,24 +362,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             ++issued;
             stamp_copy();
             if (!two) {
-              mbar_expect_tx(&full[sk], 2 * bytes);
-              load(&a.tmk, ring + (size_t)sk * SLOT_B, &full[sk]);
-              load(&a.tmv, ring + (size_t)sk * SLOT_B + kAttnHalf, &full[sk]);
+              if (l0) {
+                mbar_expect_tx(&full[sk], 2 * bytes);
+                load(&a.tmk, ring + (size_t)sk * SLOT_B, &full[sk]);
+                load(&a.tmv, ring + (size_t)sk * SLOT_B + kAttnHalf, &full[sk]);
+              }
             } else {
-              mbar_expect_tx(&full[sk], bytes);
-              load(&a.tmk, ring + (size_t)sk * SLOT_B, &full[sk]);
+              if (l0) {
+                mbar_expect_tx(&full[sk], bytes);
+                load(&a.tmk, ring + (size_t)sk * SLOT_B, &full[sk]);
+              }
               if (!take_slot()) break;
               const int sv = rp.slot;
               rp.next(NS);
               ++issued;
-              mbar_expect_tx(&full[sv], bytes);
-              load(&a.tmv, ring + (size_t)sv * SLOT_B, &full[sv]);
+              if (l0) {
+                mbar_expect_tx(&full[sv], bytes);
+                load(&a.tmv, ring + (size_t)sv * SLOT_B, &full[sv]);
+              }
             }
           }
         }
       }
-      // never leave with copies in flight: wait for the last NS issued units
-      if (s_abort)
+      // never leave with copies in flight: this lane's host-memory copies,
+      // and (lane 0) the last NS issued units
+      if constexpr (kWide) asm volatile("cp.async.wait_all;" ::: "memory");
+      if (l0 && s_abort)
         for (int u = issued - NS < 0 ? 0 : issued - NS; u < issued; ++u)
           mbar_wait(&full[u % NS], (uint32_t)((u / NS) & 1), kSpin);
     }
@@ -1199,7 +1253,8 @@ size_t step_smem_bytes(int B, int kmax, int gmax, int* nslot) {
 
 int decode_step_occupancy(size_t smem) {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode_step<false>, kThreads, smem) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode_step<false, false>, kThreads, smem) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -1207,13 +1262,14 @@ int decode_step_occupancy(size_t smem) {
 }
 
 void decode_step_setup() {
-  for (auto k : {k_decode_step<false>, k_decode_step<true>}) {
+  for (auto k : {k_decode_step<false, false>, k_decode_step<true, false>, k_decode_step<false, true>,
+                 k_decode_step<true, true>}) {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024 - kStaticSmem);
     cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   }
 }
 
-cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, bool multi, cudaStream_t s) {
+cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, bool multi, bool wide, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -1224,7 +1280,11 @@ cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, bool mu
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return multi ? cudaLaunchKernelEx(&cfg, k_decode_step<true>, a) : cudaLaunchKernelEx(&cfg, k_decode_step<false>, a);
+  if (wide)
+    return multi ? cudaLaunchKernelEx(&cfg, k_decode_step<true, true>, a)
+                 : cudaLaunchKernelEx(&cfg, k_decode_step<false, true>, a);
+  return multi ? cudaLaunchKernelEx(&cfg, k_decode_step<true, false>, a)
+               : cudaLaunchKernelEx(&cfg, k_decode_step<false, false>, a);
 }
 
 // ---------------------------------------------------------------------------
@@ -1252,3 +1312,4 @@ void launch_bf16_tile_layout(const bf16* w, int N, int Kp, bf16* out, cudaStream
 }
 
 }  // namespace river
+

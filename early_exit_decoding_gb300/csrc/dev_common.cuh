@@ -41,6 +41,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, long lon
     if (mbar_try(b, parity)) return true;
   return false;
 }
+// Wait on an mbarrier phase for at most `ns` nanoseconds of %globaltimer.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* b, uint32_t parity, unsigned long long ns) {
+  unsigned long long t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try(b, parity)) return true;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > ns) return false;
+  }
+}
 // 16-byte asynchronous copy global -> shared (the load path of ordinary
 // loads: it also reads mapped host memory).
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {

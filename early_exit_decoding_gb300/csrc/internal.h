@@ -420,7 +420,9 @@ enum Tl2Stamp {
 size_t step_smem_bytes(int B, int kmax, int gmax, int* nslot);
 // multi: the instantiation for contexts where a CTA may take several
 // attention chunks (see k_decode_step)
-cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, bool multi, cudaStream_t s);
+// multi: a CTA may take more than one attention chunk; wide: the model has
+// offloaded layers (the producer warp reads them with all its lanes).
+cudaError_t launch_decode_step(const StepArgs& a, int grid, size_t smem, bool multi, bool wide, cudaStream_t s);
 void decode_step_setup();
 int decode_step_occupancy(size_t smem);  // resident CTAs per SM at this shared-memory size
 // Attention chunks per (sequence, KV head) for context `ctx` (identical on host and device).
