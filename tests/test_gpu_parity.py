@@ -182,6 +182,34 @@ def test_step_attention_two_chunks_per_cta(river, tiny, stream, B, prompt):
                   seed=61, max_seq=prompt + 10, path="step")
 
 
+# (d_model, q heads, KV heads, batch, prompt, cache positions) for the step
+# kernel's attention phase, one 128-position chunk or fewer per CTA.
+STEP_ATTN_CASES = [
+    # 8 chunks of 113-114 positions per head group (more chunks than ring
+    # slots in one CTA's ring over the step), the step's own row in the last
+    pytest.param(256, 4, 2, 1, 900, 1000, id="hd64-rep2-8chunks"),
+    # 16 head groups of a single ragged chunk
+    pytest.param(256, 4, 2, 8, 40, 128, id="hd64-rep2-b8"),
+    # head_dim 128 (K and V in separate slots), four query heads per KV head
+    pytest.param(512, 4, 1, 2, 400, 500, id="hd128-rep4"),
+    pytest.param(512, 4, 2, 1, 300, 700, id="hd128-rep2"),
+]
+
+
+@pytest.mark.parametrize("d_model,hq,hkv,B,T,cap", STEP_ATTN_CASES)
+def test_step_attention_shapes(river, stream, d_model, hq, hkv, B, T, cap):
+    """The step kernel's attention at more head dims, GQA ratios, batches and
+    chunk counts (section 三: every layer reads the backbone's K/V slots),
+    forced exits so that both weight paths write and read them."""
+    S = synth.scaled(TINY, d_model=d_model, n_q_heads=hq, n_kv_heads=hkv, n_layers=3, vocab=512)
+    with torch.cuda.stream(stream):
+        m, om, _ = build_pair(S, seed=13, gains="random", stream=stream)
+    sched = [3, 1, 3, 0]
+    res, _ = _run_sequence(river, m, om, stream, _forced(river, sched), B=B, prompt=T, steps=3,
+                           seed=80 + B, max_seq=cap, path="step")
+    assert [int(o["exit_layer"].item()) for o, _ in res] == sched
+
+
 def test_exit_writes_slot_p_of_every_layer(river, tiny, stream):
     """Exit layers write their K/V into the backbone's own slot p (section 三);
     nothing else in any layer's cache changes."""
