@@ -1069,97 +1069,55 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             }
             named_sync(kBarCons, NC * 32);
             const bool merge = s_merge;
-            // The merging CTA keeps this item's slot(s) and stages the head group's
-            // partials there (one bulk copy per head, heads split over the slots)
-            // when they fit; otherwise it reads them from global memory.
-            const int nslot_item = two ? 2 : 1;
-            const int hps = (REP + nslot_item - 1) / nslot_item;  // heads per slot
-            const bool staged = merge && (size_t)hps * npart * PS * 4 <= (size_t)SLOT_B;
-            if (lane == 0 && !staged) {
+            // the partials are in global memory: this item's slot(s) are free
+            if (lane == 0) {
               mbar_arrive(&empty[slot]);
               if (two) mbar_arrive(&empty[slot_v]);
             }
             if (merge) {
+              // every thread merges its own outputs (head h, dim dd) from the
+              // chunks' partials in L2, a round's loads all in flight at once:
+              // no shared memory, no barrier
               const float* hp = a.part + ((size_t)b * Hq + (size_t)hk * REP) * a.part_cap * PS;
-              auto stage_of = [&](int h) -> float* {
-                unsigned char* base = ring + (size_t)(h / hps == 0 ? slot : slot_v) * SLOT_B;
-                return reinterpret_cast<float*>(base) + (size_t)(h % hps) * npart * PS;
-              };
-              if (staged) {
-                if (ct == 0) {
-                  fence_proxy_async();  // the partials were written by generic stores
-                  mbar_expect_tx(&xbar, (uint32_t)(REP * npart * PS * 4));
-                  for (int h = 0; h < REP; ++h)
-                    bulk_g2s(stage_of(h), hp + (size_t)h * a.part_cap * PS, (uint32_t)(npart * PS * 4), &xbar);
-                }
-                if (!mbar_wait(&xbar, xpar, kSpin)) {  // waited for even after an abort
-                  if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
-                  s_abort = 1;
-                }
-                xpar ^= 1u;
-              }
-              // per head: chunk weights exp(m_c - M) / sum_c exp(m_c - M) l_c into mw [h][c]
-              float* mw = redf;
-              for (int i = ct; i < REP * npart; i += NC * 32) {
-                const int h = i / npart, c = i % npart;
-                const float* pc = staged ? stage_of(h) + (size_t)c * PS : hp + ((size_t)h * a.part_cap + c) * PS;
-                mw[2 * i] = staged ? pc[HDC] : __ldcg(pc + HDC);
-                mw[2 * i + 1] = staged ? pc[HDC + 1] : __ldcg(pc + HDC + 1);
-              }
-              named_sync(kBarCons, NC * 32);
-              if (warp < REP) {
-                float* mh = mw + (size_t)warp * npart * 2;
-                float M = -FLT_MAX;
-                for (int c = lane; c < npart; c += 32)
-                  if (mh[2 * c + 1] > 0.f) M = fmaxf(M, mh[2 * c]);
-                M = warp_max(M);
-                float den = 0.f;
-                for (int c = lane; c < npart; c += 32)
-                  if (mh[2 * c + 1] > 0.f) den += __expf(mh[2 * c] - M) * mh[2 * c + 1];
-                den = warp_sum(den);
-                const float inv = den > 0.f ? 1.f / den : 0.f;
-                __syncwarp();
-                for (int c = lane; c < npart; c += 32)
-                  mh[2 * c] = mh[2 * c + 1] > 0.f ? __expf(mh[2 * c] - M) * inv : 0.f;
-              }
-              named_sync(kBarCons, NC * 32);
-              // o = sum_c w_c o_c, chunks in order; each thread owns outputs ct and ct + 256
               constexpr int NOUT = (REP * HDC + NC * 32 - 1) / (NC * 32);
 #pragma unroll
               for (int k = 0; k < NOUT; ++k) {
                 const int i = ct + k * NC * 32;
                 if (i < REP * HDC) {
                   const int h = i / HDC, dd = i % HDC;
-                  const float* wh = mw + (size_t)h * npart * 2;
-                  float acc = 0.f;
-                  if (staged) {
-                    const float* ph = stage_of(h) + dd;
-                    for (int c = 0; c < npart; ++c) acc += wh[2 * c] * ph[(size_t)c * PS];
-                  } else if (kMulti) {
-                    // eight loads in flight at a time (the sum keeps chunk order)
-                    const float* ph = hp + (size_t)h * a.part_cap * PS + dd;
-                    int c = 0;
-                    for (; c + 8 <= npart; c += 8) {
-                      float v[8];
+                  const float* ph = hp + (size_t)h * a.part_cap * PS;
+                  float M = -FLT_MAX, num = 0.f, den = 0.f;
+                  for (int c0 = 0; c0 < npart; c0 += 8) {
+                    float vm[8], vl[8], vo[8];
 #pragma unroll
-                      for (int j = 0; j < 8; ++j) v[j] = __ldcg(ph + (size_t)(c + j) * PS);
-#pragma unroll
-                      for (int j = 0; j < 8; ++j) acc += wh[2 * (c + j)] * v[j];
+                    for (int j = 0; j < 8; ++j) {
+                      const bool in = c0 + j < npart;
+                      const float* pc = ph + (size_t)(c0 + j) * PS;
+                      vm[j] = in ? __ldcg(pc + HDC) : -FLT_MAX;
+                      vl[j] = in ? __ldcg(pc + HDC + 1) : 0.f;
+                      vo[j] = in ? __ldcg(pc + dd) : 0.f;
                     }
-                    for (; c < npart; ++c) acc += wh[2 * c] * __ldcg(ph + (size_t)c * PS);
-                  } else {
-                    const float* ph = hp + (size_t)h * a.part_cap * PS + dd;
-                    for (int c = 0; c < npart; ++c) acc += wh[2 * c] * __ldcg(ph + (size_t)c * PS);
+                    // chunks in order, rescaled to the running maximum
+                    float Mn = M;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                      if (vl[j] > 0.f) Mn = fmaxf(Mn, vm[j]);
+                    const float al = __expf(M - Mn);
+                    num *= al;
+                    den *= al;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                      const float f = vl[j] > 0.f ? __expf(vm[j] - Mn) : 0.f;
+                      num += f * vo[j];
+                      den += f * vl[j];
+                    }
+                    M = Mn;
                   }
-                  D.o_out[(size_t)b * D.ldo_attn + (size_t)(hk * REP + h) * HDC + dd] = __float2bfloat16_rn(acc);
+                  D.o_out[(size_t)b * D.ldo_attn + (size_t)(hk * REP + h) * HDC + dd] =
+                      __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
                 }
               }
               if (ct == 0) a.attn_ticket[b * Hkv + hk] = 0u;  // next step starts from zero
-              named_sync(kBarCons, NC * 32);
-              if (lane == 0 && staged) {
-                mbar_arrive(&empty[slot]);
-                if (two) mbar_arrive(&empty[slot_v]);
-              }
             }
           }
         };
