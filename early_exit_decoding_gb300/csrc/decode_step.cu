@@ -106,17 +106,15 @@ __device__ __forceinline__ void w4_unit(const unsigned char* st, int gi, const u
   const uint32_t* szs = reinterpret_cast<const uint32_t*>(st + 16 * 512);
   const uint32_t s0 = szs[g * 8 + (warp ^ (g >> 2))];
   const uint32_t s1 = szs[(g + 8) * 8 + (warp ^ ((g + 8) >> 2))];
-  float c1[2][4], c2[2][4];
+  float c1[4], c2[4];
 #pragma unroll
-  for (int m = 0; m < 2; ++m)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) c1[m][q] = c2[m][q] = 0.f;
+  for (int q = 0; q < 4; ++q) c1[q] = c2[q] = 0.f;
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const uint32_t va = u4get(wa, m), vb = u4get(wb, m), ha = va >> 8, hb = vb >> 8;
     const uint4 X = *reinterpret_cast<const uint4*>(xrow + (gi * 128 + 32 * m + 8 * t) * 2);
-    mma_f16(c1[m & 1], va & 0x000F000Fu, vb & 0x000F000Fu, ha & 0x000F000Fu, hb & 0x000F000Fu, X.x, X.y);
-    mma_f16(c2[m & 1], va & 0x00F000F0u, vb & 0x00F000F0u, ha & 0x00F000F0u, hb & 0x00F000F0u, X.z, X.w);
+    mma_f16(c1, va & 0x000F000Fu, vb & 0x000F000Fu, ha & 0x000F000Fu, hb & 0x000F000Fu, X.x, X.y);
+    mma_f16(c2, va & 0x00F000F0u, vb & 0x00F000F0u, ha & 0x00F000F0u, hb & 0x00F000F0u, X.z, X.w);
   }
   __half2 h0, h1;
   *reinterpret_cast<uint32_t*>(&h0) = s0;
@@ -130,7 +128,7 @@ __device__ __forceinline__ void w4_unit(const unsigned char* st, int gi, const u
   const float q0 = sz0.x * sz0.y, q1 = sz1.x * sz1.y;
   float av[4];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) av[c] = (c1[0][c] + c1[1][c]) + 0.0625f * (c2[0][c] + c2[1][c]);
+  for (int c = 0; c < 4; ++c) av[c] = c1[c] + 0.0625f * c2[c];
   y[0] = fmaf(p0 * xa.y, av[0], fmaf(-q0, xa.x, y[0]));
   y[1] = fmaf(p0 * xb.y, av[1], fmaf(-q0, xb.x, y[1]));
   y[2] = fmaf(p1 * xa.y, av[2], fmaf(-q1, xa.x, y[2]));
@@ -686,7 +684,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         }
         // MMA column g reads activation row min(g, B-1); columns >= B are dropped
         const unsigned char* xrow = xs + (size_t)(g < B ? g : B - 1) * RSX;
-        const int step_u = w4 ? W4U : 1;
         bool first_w = true;
 
         // epilogue of a batch of nb tiles starting at tile t_first (all consumer threads)
@@ -811,25 +808,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
         int nb = 0, t_first = cta;
         bool first_batch = true;
         for (int tl = cta; tl < ntiles; tl += grid) {
-          float y[4][4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) y[j][i] = 0.f;
-          int uk = 0;
-          for (int i0 = 0; i0 < UPT; i0 += step_u) {
+          // the ring slot of the next unit(s), waited for
+          auto take = [&](bool& ok) -> const unsigned char* {
             const int slot = rc.slot;
-            bool ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
+            ok = s_abort == 0 && mbar_wait(&full[slot], (uint32_t)(rc.round & 1), kSpin);
             if (!ok && s_abort == 0) {
               if (lane == 0) atomicOr(&a.st->err, RL_DEVERR_TIMEOUT);
               s_abort = 1;
             }
             if (first_w && ct == 0) tl2_mark(a.tl2, grid, p, cta, TL2_W);
             first_w = false;
-            const unsigned char* sb = ring + (size_t)slot * SLOT_B;
-            const int ns = min(step_u, UPT - i0);
-            if (w4) {
-              // two units at a time: independent MMA chains interleave
+            return ring + (size_t)slot * SLOT_B;
+          };
+          auto release = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[rc.slot]);
+            rc.next(NS);
+          };
+          float v0, v1, v2, v3;
+          if (w4) {
+            // W4 units, two at a time: independent MMA chains interleave
+            float y[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) y[j][i] = 0.f;
+            for (int uk = 0; uk < UPT; uk += W4U) {
+              bool ok;
+              const unsigned char* sb = take(ok);
+              const int ns = min(W4U, UPT - uk);
               for (int s = 0; s < ns; s += 2) {
                 const int ga = (uk + s) * 8 + warp, gb = ga + 8;
                 const bool on_a = ok && ga < G, on_b = ok && s + 1 < ns && gb < G;
@@ -840,8 +847,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                   w4_unit(sb + (size_t)s * STAGE_W, ga, xrow, xsum, B, G, warp, g, t, y[0]);
                 }
               }
-              uk += ns;
-            } else {
+              release();
+            }
+            v0 = y[0][0] + y[1][0];
+            v1 = y[0][1] + y[1][1];
+            v2 = y[0][2] + y[1][2];
+            v3 = y[0][3] + y[1][3];
+          } else {
+            float y[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) y[j][i] = 0.f;
+            for (int uk = 0; uk < UPT; ++uk) {
+              bool ok;
+              const unsigned char* sb = take(ok);
               // bf16 unit: 16 rows of kn inputs; 16-byte chunk c of row r at
               // c ^ 4 (r & 1): the 8 lanes of a quarter warp (rows 2q, 2q+1,
               // chunks c0..c0+3) hit 8 different 16-byte bank groups
@@ -861,18 +881,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                              u4get(wb, 2 * e + 1), u4get(X, 2 * e), u4get(X, 2 * e + 1));
                 }
               }
-              ++uk;
+              release();
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            rc.next(NS);
+            v0 = (y[0][0] + y[1][0]) + (y[2][0] + y[3][0]);
+            v1 = (y[0][1] + y[1][1]) + (y[2][1] + y[3][1]);
+            v2 = (y[0][2] + y[1][2]) + (y[2][2] + y[3][2]);
+            v3 = (y[0][3] + y[1][3]) + (y[2][3] + y[3][3]);
           }
           // this warp's partial tile -> the batch buffer ([tile][warp][column][row])
           {
-            const float v0 = (y[0][0] + y[1][0]) + (y[2][0] + y[3][0]);
-            const float v1 = (y[0][1] + y[1][1]) + (y[2][1] + y[3][1]);
-            const float v2 = (y[0][2] + y[1][2]) + (y[2][2] + y[3][2]);
-            const float v3 = (y[0][3] + y[1][3]) + (y[2][3] + y[3][3]);
             float* rw = redf + (size_t)(nb * NC + warp) * B * 16;
             if (2 * t < B) {
               rw[(2 * t) * 16 + g] = v0;
