@@ -854,9 +854,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
             v2 = y[0][2] + y[1][2];
             v3 = y[0][3] + y[1][3];
           } else {
-            float y[4][4];
+            float y[2][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
               for (int i = 0; i < 4; ++i) y[j][i] = 0.f;
             for (int uk = 0; uk < UPT; ++uk) {
@@ -877,16 +877,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_step(const __grid_consta
                   const uint4 X = *reinterpret_cast<const uint4*>(xrow + (k0 + cb * 8) * 2);
 #pragma unroll
                   for (int e = 0; e < 2; ++e)
-                    mma_bf16(y[i4], u4get(wa, 2 * e), u4get(wb, 2 * e), u4get(wa, 2 * e + 1),
+                    mma_bf16(y[i4 & 1], u4get(wa, 2 * e), u4get(wb, 2 * e), u4get(wa, 2 * e + 1),
                              u4get(wb, 2 * e + 1), u4get(X, 2 * e), u4get(X, 2 * e + 1));
                 }
               }
               release();
             }
-            v0 = (y[0][0] + y[1][0]) + (y[2][0] + y[3][0]);
-            v1 = (y[0][1] + y[1][1]) + (y[2][1] + y[3][1]);
-            v2 = (y[0][2] + y[1][2]) + (y[2][2] + y[3][2]);
-            v3 = (y[0][3] + y[1][3]) + (y[2][3] + y[3][3]);
+            v0 = y[0][0] + y[1][0];
+            v1 = y[0][1] + y[1][1];
+            v2 = y[0][2] + y[1][2];
+            v3 = y[0][3] + y[1][3];
           }
           // this warp's partial tile -> the batch buffer ([tile][warp][column][row])
           {
