@@ -125,3 +125,22 @@ def test_long_prompts_every_tile_width(river, tiny, stream, B, T):
     res, _ = _run_sequence(river, m, om, stream, _forced(river, sched), B=B, prompt=T,
                            steps=2, seed=50 + T, max_seq=T + 4)
     assert [int(o["exit_layer"].item()) for o, _ in res] == sched
+
+
+@pytest.mark.parametrize("e_pre", [0, 2])
+def test_prompt_long_reduction_split_k(river, stream, e_pre):
+    """A prompt projection with a long reduction (FFN 8192: the down
+    projection has 128 k-blocks of 64 inputs) and few 128-token tiles splits
+    K in two per tile (partial tiles summed by the tile's last CTA): 300
+    tokens (a ragged 44-token tail), on the bf16 backbone (e = 2, full depth)
+    and on the W4 exit river (e = 0, every layer's down projection W4 on the
+    tensor cores)."""
+    S = synth.scaled(TINY, d_model=512, n_q_heads=8, n_kv_heads=2, ffn_dim=8192, n_layers=2,
+                     vocab=512)
+    with torch.cuda.stream(stream):
+        m, om, _ = build_pair(S, seed=9, gains="random", stream=stream)
+    sched = [e_pre, 1, 2]
+    res, _ = _run_sequence(river, m, om, stream, _forced(river, sched), B=1, prompt=300,
+                           steps=2, seed=90 + e_pre, max_seq=320)
+    assert [int(o["exit_layer"].item()) for o, _ in res] == sched
+
